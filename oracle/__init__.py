@@ -1,0 +1,13 @@
+"""fp64 CPU oracle (test infrastructure only; never on the product path)."""
+from .lrkv_oracle import (  # noqa: F401
+    BLOCK,
+    agent_kv,
+    append_pools,
+    apply_rope,
+    attend,
+    base_and_lowrank,
+    decode,
+    gqa_attention,
+    prefill,
+    rope_inv_freq,
+)

@@ -1,0 +1,196 @@
+"""fp64 CPU oracle for LoRA-KV attention over a shared base + shared-A low-rank cache.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path may import this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it. It shares no code with the CUDA library.
+
+What it computes is the plain definition of the method's result, every
+per-agent key and value materialised in full, then textbook softmax attention:
+
+* LRAgent: Efficient KV Cache Sharing for Multi-LoRA LLM Agents (arXiv
+  2602.01053), Abstract: the cache splits into a base part produced by the
+  pretrained weights and an adapter part produced by the LoRA weights; with a
+  shared A, the low-rank part X·A is common to all agents. Reaching the same
+  values as per-agent ("non-shared") caching is the method's accuracy claim, so
+  the reference result is each agent's own full K_i, V_i:
+      K_i = RoPE(X·W_K + (X·A_K)·B_K,i),  V_i = X·W_V + (X·A_V)·B_V,i.
+* PReCache (thelatestinai.com/papers/2609.34054), Abstract and Table 1: the
+  base cache comes from the pretrained weights and the low-rank cache is
+  produced once, when a context segment is first processed (the "append").
+
+Readings where the pages are silent (each listed in the design doc as well):
+row-vector convention X·W; rotate-half RoPE pairing (j, j + d/2) with
+theta_j = base^(-2j/d) and no frequency scaling; LoRA scale folded into B;
+softmax scale 1/sqrt(d); q head m reads kv head floor(m / (Hq/Hkv)); query k of
+a chunk of q_len queries over L keys sits at position L - q_len + k and sees
+keys at positions <= its own; adapter id -1 means B = 0.
+
+All arithmetic is float64. Inputs are the storage-dtype values converted to
+float64; nothing is rounded inside.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BLOCK = 16
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Rotary position embedding (reading: rotate-half pairing, HF Llama family).
+
+def rope_inv_freq(head_dim: int, base: float) -> np.ndarray:
+    """theta_j = base^(-2j/d) for j in [0, d/2)."""
+    j = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(np.float64(base), -2.0 * j / head_dim)
+
+
+def apply_rope(x: np.ndarray, positions: np.ndarray, base: float) -> np.ndarray:
+    """Rotates x [T, H, d] at integer positions [T].
+
+    For pair (j, j + d/2) at position t with angle a = t * theta_j:
+        x'[j]       = x[j] cos a - x[j + d/2] sin a
+        x'[j + d/2] = x[j + d/2] cos a + x[j] sin a
+    """
+    x = _f64(x)
+    d = x.shape[-1]
+    half = d // 2
+    ang = _f64(positions)[:, None] * rope_inv_freq(d, base)[None, :]  # [T, d/2]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# Cache construction.
+
+def base_and_lowrank(X, positions, W_K, W_V, A_K, A_V, n_kv_heads: int, head_dim: int,
+                     base: float):
+    """What one append writes for tokens X [T, h] at the given positions.
+
+    LRAgent, Abstract (base component from the pretrained weights; adapter
+    component kept in its low-rank form, shared when A is shared):
+        K_base = RoPE(X·W_K)  [T, Hkv, d]     V_base = X·W_V  [T, Hkv, d]
+        L_K    = X·A_K        [T, r]          L_V    = X·A_V  [T, r]
+    """
+    X = _f64(X)
+    T = X.shape[0]
+    k_pre = (X @ _f64(W_K)).reshape(T, n_kv_heads, head_dim)
+    v = (X @ _f64(W_V)).reshape(T, n_kv_heads, head_dim)
+    return (apply_rope(k_pre, positions, base), v, X @ _f64(A_K), X @ _f64(A_V))
+
+
+def agent_kv(X, positions, W_K, W_V, A_K, A_V, B_K_i, B_V_i, n_kv_heads: int,
+             head_dim: int, base: float):
+    """One agent's full keys and values, as that agent alone would cache them.
+
+    K_i = RoPE(X·W_K + (X·A_K)·B_K,i),  V_i = X·W_V + (X·A_V)·B_V,i, each
+    [T, Hkv, d]. B_K,i / B_V,i of None stand for B = 0 (base model only).
+    """
+    X = _f64(X)
+    T = X.shape[0]
+    k_pre = X @ _f64(W_K)
+    v = X @ _f64(W_V)
+    if B_K_i is not None:
+        k_pre = k_pre + (X @ _f64(A_K)) @ _f64(B_K_i)
+    if B_V_i is not None:
+        v = v + (X @ _f64(A_V)) @ _f64(B_V_i)
+    k = apply_rope(k_pre.reshape(T, n_kv_heads, head_dim), positions, base)
+    return k, v.reshape(T, n_kv_heads, head_dim)
+
+
+# ---------------------------------------------------------------------------
+# Attention.
+
+def gqa_attention(q, q_positions, K, V, scale: float) -> np.ndarray:
+    """Causal grouped-query softmax attention.
+
+    q [N, Hq, d] at positions [N]; K, V [L, Hkv, d] at positions 0..L-1.
+    Query head m reads kv head m // (Hq / Hkv); key t is visible iff t <= the
+    query's position. Returns [N, Hq, d].
+    """
+    q = _f64(q)
+    K = _f64(K)
+    V = _f64(V)
+    N, Hq, d = q.shape
+    L, Hkv, _ = K.shape
+    g = Hq // Hkv
+    qp = np.asarray(q_positions, dtype=np.int64)
+    visible = np.arange(L)[None, :] <= qp[:, None]  # [N, L]
+    out = np.empty((N, Hq, d), dtype=np.float64)
+    for m in range(Hq):
+        kv = m // g
+        s = (q[:, m, :] @ K[:, kv, :].T) * scale          # [N, L]
+        s = np.where(visible, s, -np.inf)
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, m, :] = p @ V[:, kv, :]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Whole operations, in the library's terms.
+
+def _adapter_B(weights, adapter: int):
+    if adapter < 0:
+        return None, None
+    return weights["B_K"][adapter], weights["B_V"][adapter]
+
+
+def attend(X_seq, adapter: int, q, q_positions, weights, n_kv_heads: int, head_dim: int,
+           base: float, scale: float) -> np.ndarray:
+    """Queries q [N, Hq, d] of one agent over a sequence whose hidden states at
+    positions 0..L-1 are X_seq [L, h]: materialise the agent's K, V, then attend."""
+    L = np.asarray(X_seq).shape[0]
+    B_K, B_V = _adapter_B(weights, adapter)
+    K, V = agent_kv(X_seq, np.arange(L), weights["W_K"], weights["W_V"], weights["A_K"],
+                    weights["A_V"], B_K, B_V, n_kv_heads, head_dim, base)
+    return gqa_attention(q, q_positions, K, V, scale)
+
+
+def decode(X_ctx, q, adapters, weights, n_kv_heads: int, head_dim: int, base: float,
+           scale: float) -> np.ndarray:
+    """Decode queries of several agents on one context X_ctx [L, h]: each query
+    (one per row of q [N, Hq, d], adapter ids [N]) sits at position L - 1."""
+    L = np.asarray(X_ctx).shape[0]
+    out = np.empty(np.asarray(q).shape, dtype=np.float64)
+    for n, a in enumerate(np.asarray(adapters).tolist()):
+        out[n: n + 1] = attend(X_ctx, int(a), np.asarray(q)[n: n + 1], [L - 1], weights,
+                               n_kv_heads, head_dim, base, scale)
+    return out
+
+
+def prefill(X_seq, q_chunk, adapter: int, weights, n_kv_heads: int, head_dim: int,
+            base: float, scale: float) -> np.ndarray:
+    """A chunk of q_len queries at the end of a sequence of L tokens (the chunk's
+    own tokens included): query k sits at position L - q_len + k."""
+    L = np.asarray(X_seq).shape[0]
+    n = np.asarray(q_chunk).shape[0]
+    return attend(X_seq, adapter, q_chunk, np.arange(L - n, L), weights, n_kv_heads,
+                  head_dim, base, scale)
+
+
+def append_pools(base_pool, lr_pool, X, positions, seq_rows, block_tables, W_K, W_V, A_K,
+                 A_V, n_kv_heads: int, head_dim: int, base: float):
+    """Expected pool contents after an append, written in place.
+
+    base_pool [num_blocks, 2, Hkv, 16, d]: plane 0 = K_base, plane 1 = V_base.
+    lr_pool   [num_blocks, 2, 16, r]:      plane 0 = L_K, plane 1 = L_V.
+    Token n goes to block block_tables[seq_rows[n], positions[n] // 16], row
+    positions[n] % 16 (PagedAttention-style block table).
+    """
+    kb, vb, lk, lv = base_and_lowrank(X, positions, W_K, W_V, A_K, A_V, n_kv_heads,
+                                      head_dim, base)
+    for n, (p, s) in enumerate(zip(np.asarray(positions).tolist(), np.asarray(seq_rows).tolist())):
+        blk = int(block_tables[s][p // BLOCK])
+        row = p % BLOCK
+        base_pool[blk, 0, :, row, :] = kb[n]
+        base_pool[blk, 1, :, row, :] = vb[n]
+        lr_pool[blk, 0, row, :] = lk[n]
+        lr_pool[blk, 1, row, :] = lv[n]
+    return base_pool, lr_pool

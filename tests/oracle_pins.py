@@ -1,0 +1,309 @@
+"""Pins for the fp64 oracle: checks against facts fixed outside the oracle itself.
+
+Each ``pin_*`` takes a namespace ``O`` that provides the oracle's functions, so
+the mutation tests can hand in a deliberately broken copy and confirm that some
+pin fails. Pins use: hand-derived closed forms, a library routine
+(``torch.nn.functional.scaled_dot_product_attention`` in float64), brute force
+with Python floats/ints on tiny inputs, and algebraic invariants.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- RoPE pins
+def pin_rope_closed_form(O):
+    """d = 4, base = 100, t = 3, x = [1, 2, 3, 4]: theta = [1, 0.1]; pairs (0, 2)
+    and (1, 3) (rotate-half). Values written out by hand."""
+    x = np.array([[[1.0, 2.0, 3.0, 4.0]]])
+    got = O.apply_rope(x, np.array([3]), 100.0)[0, 0]
+    a0, a1 = 3.0 * 1.0, 3.0 * 0.1
+    want = [1 * math.cos(a0) - 3 * math.sin(a0),
+            2 * math.cos(a1) - 4 * math.sin(a1),
+            3 * math.cos(a0) + 1 * math.sin(a0),
+            4 * math.cos(a1) + 2 * math.sin(a1)]
+    assert np.allclose(got, want, rtol=0, atol=1e-14), (got, want)
+
+
+def pin_rope_frequencies(O):
+    """theta_j = base^(-2j/d): for d = 8, base = 10000 -> 1, 0.1, 0.01, 0.001."""
+    got = O.rope_inv_freq(8, 10000.0)
+    assert np.allclose(got, [1.0, 0.1, 0.01, 0.001], rtol=1e-15, atol=0)
+
+
+def pin_rope_invariants(O):
+    r = _rng(1)
+    x = r.standard_normal((5, 3, 64))
+    pos = np.array([0, 1, 7, 4095, 32767])
+    y = O.apply_rope(x, pos, 10000.0)
+    assert np.array_equal(y[0], x[0])                     # position 0: identity
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+    # scores depend on the position difference only
+    q = r.standard_normal((1, 1, 64))
+    k = r.standard_normal((1, 1, 64))
+    for p, t, c in [(5, 2, 32768 - 5), (100, 0, 1000), (17, 16, 12345)]:
+        s1 = float(np.sum(O.apply_rope(q, np.array([p]), 10000.0) * O.apply_rope(k, np.array([t]), 10000.0)))
+        s2 = float(np.sum(O.apply_rope(q, np.array([p + c]), 10000.0) * O.apply_rope(k, np.array([t + c]), 10000.0)))
+        assert abs(s1 - s2) < 1e-9, (s1, s2)
+
+
+# ----------------------------------------------------------- attention pins
+def _sdpa(q, K, V, causal):
+    """Library routine: torch SDPA in float64 on CPU, GQA handled by torch."""
+    qt = torch.from_numpy(np.ascontiguousarray(q.transpose(1, 0, 2)))[None]   # [1, Hq, N, d]
+    kt = torch.from_numpy(np.ascontiguousarray(K.transpose(1, 0, 2)))[None]
+    vt = torch.from_numpy(np.ascontiguousarray(V.transpose(1, 0, 2)))[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=causal,
+                                                         enable_gqa=True)
+    return o[0].numpy().transpose(1, 0, 2)
+
+
+def pin_attention_sdpa_decode(O):
+    """One query at the last position sees every key: plain SDPA, no mask."""
+    r = _rng(2)
+    L, Hq, Hkv, d = 37, 8, 2, 16
+    K = r.standard_normal((L, Hkv, d))
+    V = r.standard_normal((L, Hkv, d))
+    q = r.standard_normal((1, Hq, d))
+    got = O.gqa_attention(q, [L - 1], K, V, 1 / math.sqrt(d))
+    want = _sdpa(q, K, V, causal=False)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def pin_attention_sdpa_prefill(O):
+    """Full-length causal prefill (queries = keys, square mask) against SDPA's
+    is_causal; then a trailing chunk must equal the last rows of the full run
+    (bottom-right alignment)."""
+    r = _rng(3)
+    L, Hq, Hkv, d = 29, 6, 3, 8
+    K = r.standard_normal((L, Hkv, d))
+    V = r.standard_normal((L, Hkv, d))
+    q = r.standard_normal((L, Hq, d))
+    full = O.gqa_attention(q, np.arange(L), K, V, 1 / math.sqrt(d))
+    assert np.allclose(full, _sdpa(q, K, V, causal=True), rtol=1e-12, atol=1e-13)
+    n = 9
+    chunk = O.gqa_attention(q[-n:], np.arange(L - n, L), K, V, 1 / math.sqrt(d))
+    assert np.allclose(chunk, full[-n:], rtol=1e-13, atol=1e-14)
+
+
+def pin_attention_brute_force(O):
+    """Python floats and math.exp, one loop per term, on a tiny GQA case."""
+    r = _rng(4)
+    L, Hq, Hkv, d = 5, 4, 2, 3
+    K = r.standard_normal((L, Hkv, d))
+    V = r.standard_normal((L, Hkv, d))
+    q = r.standard_normal((2, Hq, d))
+    pos = [2, 4]
+    scale = 0.7
+    got = O.gqa_attention(q, pos, K, V, scale)
+    for n in range(2):
+        for m in range(Hq):
+            kv = m // (Hq // Hkv)
+            sc = [scale * sum(q[n, m, j] * K[t, kv, j] for j in range(d)) for t in range(pos[n] + 1)]
+            mx = max(sc)
+            w = [math.exp(s - mx) for s in sc]
+            z = sum(w)
+            for j in range(d):
+                o = sum(w[t] * V[t, kv, j] for t in range(pos[n] + 1)) / z
+                assert abs(got[n, m, j] - o) < 1e-13
+
+
+def pin_attention_special_cases(O):
+    r = _rng(5)
+    Hq, Hkv, d = 4, 2, 8
+    # one key: the output is that key's value
+    K = r.standard_normal((1, Hkv, d))
+    V = r.standard_normal((1, Hkv, d))
+    q = r.standard_normal((1, Hq, d))
+    o = O.gqa_attention(q, [0], K, V, 1.0)
+    assert np.allclose(o[0], np.repeat(V[0], Hq // Hkv, axis=0), atol=1e-15)
+    # zero query: the mean of the visible values
+    L = 11
+    K = r.standard_normal((L, Hkv, d))
+    V = r.standard_normal((L, Hkv, d))
+    o = O.gqa_attention(np.zeros((1, Hq, d)), [6], K, V, 1.0)
+    assert np.allclose(o[0], np.repeat(V[:7].mean(axis=0), Hq // Hkv, axis=0), atol=1e-14)
+    # one dominant key: its value
+    K = np.zeros((L, Hkv, d))
+    K[3, :, 0] = 1000.0
+    q = np.zeros((1, Hq, d))
+    q[0, :, 0] = 1.0
+    o = O.gqa_attention(q, [L - 1], K, V, 1.0)
+    assert np.allclose(o[0], np.repeat(V[3], Hq // Hkv, axis=0), atol=1e-12)
+
+
+# -------------------------------------------------------- LoRA / cache pins
+def pin_lora_closed_form(O):
+    """h = 1, one kv head, d = 2, r = 1, two tokens X = [[1], [2]] at positions 0, 1.
+    W_K = [[1, 0]], A_K = [[1]], B_K = [[0, 1]] -> K_pre[t] = X[t] * [1, 1];
+    W_V = [[0, 1]], A_V = [[2]], B_V = [[1, 0]] -> V[t] = X[t] * [2, 1].
+    base = 1 so theta_0 = 1. Query q = [1, 0] at position 1, scale 1:
+      K[0] = [1, 1]; K[1] = RoPE_1([2, 2]) = [2cos1 - 2sin1, 2cos1 + 2sin1]
+      s0 = 1, s1 = 2cos1 - 2sin1; o = (e^s0 V[0] + e^s1 V[1]) / (e^s0 + e^s1)."""
+    w = {"W_K": np.array([[1.0, 0.0]]), "W_V": np.array([[0.0, 1.0]]),
+         "A_K": np.array([[1.0]]), "A_V": np.array([[2.0]]),
+         "B_K": np.array([[[0.0, 1.0]]]), "B_V": np.array([[[1.0, 0.0]]])}
+    X = np.array([[1.0], [2.0]])
+    q = np.array([[[1.0, 0.0]]])
+    got = O.attend(X, 0, q, [1], w, 1, 2, 1.0, 1.0)[0, 0]
+    s0, s1 = 1.0, 2 * math.cos(1.0) - 2 * math.sin(1.0)
+    e0, e1 = math.exp(s0), math.exp(s1)
+    want = [(e0 * 2 + e1 * 4) / (e0 + e1), (e0 * 1 + e1 * 2) / (e0 + e1)]
+    assert np.allclose(got, want, rtol=0, atol=1e-14), (got, want)
+    # adapter -1: B = 0 -> K = [1, 0] * X, V = [0, 1] * X
+    got0 = O.attend(X, -1, q, [1], w, 1, 2, 1.0, 1.0)[0, 0]
+    s1b = 2 * math.cos(1.0)
+    e0, e1 = math.exp(1.0), math.exp(s1b)
+    want0 = [0.0, (e0 * 1 + e1 * 2) / (e0 + e1)]
+    assert np.allclose(got0, want0, rtol=0, atol=1e-14), (got0, want0)
+
+
+def _small_weights(r, h=24, Hkv=2, d=8, rank=3, na=3):
+    return {"W_K": r.standard_normal((h, Hkv * d)), "W_V": r.standard_normal((h, Hkv * d)),
+            "A_K": r.standard_normal((h, rank)), "A_V": r.standard_normal((h, rank)),
+            "B_K": r.standard_normal((na, rank, Hkv * d)),
+            "B_V": r.standard_normal((na, rank, Hkv * d))}
+
+
+def pin_merged_weights(O):
+    """Dense per-agent recomputation with merged weights W + A·B_i (one GEMM per
+    projection, the "non-shared" cache of that agent) equals the factored form."""
+    r = _rng(6)
+    w = _small_weights(r)
+    X = r.standard_normal((13, 24))
+    pos = np.arange(13) + 5
+    for i in range(3):
+        k1, v1 = O.agent_kv(X, pos, w["W_K"], w["W_V"], w["A_K"], w["A_V"], w["B_K"][i],
+                            w["B_V"][i], 2, 8, 10000.0)
+        WK = w["W_K"] + w["A_K"] @ w["B_K"][i]
+        WV = w["W_V"] + w["A_V"] @ w["B_V"][i]
+        k2, v2 = O.agent_kv(X, pos, WK, WV, w["A_K"], w["A_V"], None, None, 2, 8, 10000.0)
+        assert np.allclose(k1, k2, rtol=1e-12, atol=1e-12)
+        assert np.allclose(v1, v2, rtol=1e-12, atol=1e-12)
+
+
+def pin_reordered_equals_materialised(O):
+    """The reordered evaluation (what the kernels do) equals the materialised one:
+    K_i = K_base + RoPE(L_K·B_K,i) and P·V_i = P·V_base + (P·L_V)·B_V,i."""
+    r = _rng(7)
+    h, Hq, Hkv, d, rank = 24, 4, 2, 8, 3
+    w = _small_weights(r, h, Hkv, d, rank)
+    L = 21
+    X = r.standard_normal((L, h))
+    pos = np.arange(L)
+    kb, vb, lk, lv = O.base_and_lowrank(X, pos, w["W_K"], w["W_V"], w["A_K"], w["A_V"],
+                                        Hkv, d, 10000.0)
+    q = r.standard_normal((1, Hq, d))
+    scale = 1 / math.sqrt(d)
+    for i in range(3):
+        want = O.attend(X, i, q, [L - 1], w, Hkv, d, 10000.0, scale)[0]
+        adapter_k = O.apply_rope((lk @ w["B_K"][i]).reshape(L, Hkv, d), pos, 10000.0)
+        Ki = kb + adapter_k
+        for m in range(Hq):
+            kv = m // (Hq // Hkv)
+            s = Ki[:, kv, :] @ q[0, m] * scale
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            o = p @ vb[:, kv, :] + (p @ lv) @ w["B_V"][i][:, kv * d:(kv + 1) * d]
+            assert np.allclose(o, want[m], rtol=1e-12, atol=1e-12)
+
+
+def pin_base_equals_ordinary_attention(O):
+    """B = 0 (adapter -1): attend() is ordinary GQA attention over K = RoPE(X·W_K),
+    V = X·W_V, checked against SDPA."""
+    r = _rng(8)
+    h, Hq, Hkv, d = 16, 4, 2, 8
+    w = _small_weights(r, h, Hkv, d, 3)
+    L = 19
+    X = r.standard_normal((L, h))
+    q = r.standard_normal((1, Hq, d))
+    got = O.attend(X, -1, q, [L - 1], w, Hkv, d, 10000.0, 1 / math.sqrt(d))
+    K = O.apply_rope((X @ w["W_K"]).reshape(L, Hkv, d), np.arange(L), 10000.0)
+    V = (X @ w["W_V"]).reshape(L, Hkv, d)
+    assert np.allclose(got, _sdpa(q, K, V, causal=False), rtol=1e-12, atol=1e-13)
+
+
+def pin_append_integer_bruteforce(O):
+    """Integer-valued X and 0/1 weights: the projections are exact integer sums,
+    recomputed with Python ints; position 0 rotation is the identity, so K_base
+    there is exact too. Pool rows land at block_tables[s][p // 16], row p % 16."""
+    r = _rng(9)
+    h, Hkv, d, rank = 12, 2, 4, 2
+    X = r.integers(-3, 4, size=(5, h)).astype(np.float64)
+    WK = r.integers(0, 2, size=(h, Hkv * d)).astype(np.float64)
+    WV = r.integers(0, 2, size=(h, Hkv * d)).astype(np.float64)
+    AK = r.integers(0, 2, size=(h, rank)).astype(np.float64)
+    AV = r.integers(0, 2, size=(h, rank)).astype(np.float64)
+    pos = np.array([0, 17, 3, 40, 0])
+    seqs = np.array([0, 0, 1, 1, 1])
+    bt = np.array([[4, 2, 9], [7, 0, 5]])
+    nb = 10
+    bp = np.full((nb, 2, Hkv, 16, d), np.nan)
+    lp = np.full((nb, 2, 16, rank), np.nan)
+    O.append_pools(bp, lp, X, pos, seqs, bt, WK, WV, AK, AV, Hkv, d, 10000.0)
+
+    def isum(row, W, col):
+        return sum(int(X[row, k]) * int(W[k, col]) for k in range(h))
+
+    written = set()
+    for n in range(5):
+        blk = {(0, 0): 4, (0, 1): 2, (1, 0): 7, (1, 2): 5}[(int(seqs[n]), int(pos[n]) // 16)]
+        row = int(pos[n]) % 16
+        written.add((blk, row))
+        for hh in range(Hkv):
+            for j in range(d):
+                assert bp[blk, 1, hh, row, j] == isum(n, WV, hh * d + j)
+                if pos[n] == 0:
+                    assert bp[blk, 0, hh, row, j] == isum(n, WK, hh * d + j)
+        for k in range(rank):
+            assert lp[blk, 0, row, k] == isum(n, AK, k)
+            assert lp[blk, 1, row, k] == isum(n, AV, k)
+    for blk in range(nb):
+        for row in range(16):
+            if (blk, row) not in written:
+                assert np.isnan(bp[blk, :, :, row]).all() and np.isnan(lp[blk, :, row]).all()
+
+
+def pin_prefill_last_row_equals_decode(O):
+    r = _rng(10)
+    h, Hq, Hkv, d = 16, 4, 2, 8
+    w = _small_weights(r, h, Hkv, d, 3)
+    L = 23
+    X = r.standard_normal((L, h))
+    qc = r.standard_normal((6, Hq, d))
+    pre = O.prefill(X, qc, 1, w, Hkv, d, 10000.0, 0.3)
+    dec = O.decode(X, qc[-1:], [1], w, Hkv, d, 10000.0, 0.3)
+    assert np.allclose(pre[-1], dec[0], rtol=1e-13, atol=1e-14)
+
+
+def pin_multi_agent_batch(O):
+    """Several agents' queries on one context equal the same queries one at a time."""
+    r = _rng(11)
+    h, Hq, Hkv, d = 16, 4, 2, 8
+    w = _small_weights(r, h, Hkv, d, 3)
+    L = 15
+    X = r.standard_normal((L, h))
+    q = r.standard_normal((4, Hq, d))
+    ad = [2, -1, 0, 2]
+    both = O.decode(X, q, ad, w, Hkv, d, 10000.0, 0.5)
+    for n in range(4):
+        one = O.attend(X, ad[n], q[n:n + 1], [L - 1], w, Hkv, d, 10000.0, 0.5)
+        assert np.allclose(both[n], one[0], rtol=1e-14, atol=1e-15)
+    # and adapters really change the result
+    assert not np.allclose(both[0], O.attend(X, -1, q[0:1], [L - 1], w, Hkv, d, 10000.0, 0.5)[0])
+
+
+ALL_PINS = [
+    pin_rope_closed_form, pin_rope_frequencies, pin_rope_invariants,
+    pin_attention_sdpa_decode, pin_attention_sdpa_prefill, pin_attention_brute_force,
+    pin_attention_special_cases, pin_lora_closed_form, pin_merged_weights,
+    pin_reordered_equals_materialised, pin_base_equals_ordinary_attention,
+    pin_append_integer_bruteforce, pin_prefill_last_row_equals_decode, pin_multi_agent_batch,
+]
