@@ -1,0 +1,535 @@
+#!/usr/bin/env python
+"""Benchmark of the LoRA-KV attention hot path on B300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl lrkv|reference]
+
+One step = one pass of the hot path over one batch of the named workload,
+inputs already resident in HBM: for the decode workloads the decode call
+(split-KV attention + combine); for the prefill workload the append of the new
+chunk tokens plus the causal prefill; for the mixed batch append + decode +
+prefill. L2 is flushed (a 512 MiB write) before every step, outside the timed
+events; each step is bracketed by CUDA events on the launching stream and the
+K steps are bracketed by a barrier and a device synchronize. Rank 0 prints one
+JSON line. ``--impl reference`` times the fp64 CPU oracle instead (on the host
+cores, rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "shared_decode_llama8b"
+METRIC = "LoRA-KV attention decode tok/s & GB/s (% of HBM), prefill TFLOP/s (% peak)"
+FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = {"decode": ["decode.cu", "lrkv_device.cuh"], "prefill": ["prefill.cu", "lrkv_device.cuh"],
+                  "append": ["append.cu", "lrkv_device.cuh"]}
+
+
+# ----------------------------------------------------------------- helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def kernel_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        h.update(open(os.path.join(ROOT, "rank_cache_attention_flash_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str, kind: str):
+    """Per-launch DRAM bytes from a committed ncu capture, if the kernel source is
+    unchanged since; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(workload)
+    if not d or d.get("source_sha") != kernel_sha(kind):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def workload_model(case):
+    """Algorithmic bytes and flops of each call of one step (units: bytes, flop)."""
+    sh = case.shape
+    es = 4 if sh.dtype == "fp32" else 2
+    D, R, Hkv, Hq = sh.head_dim, sh.rank, sh.n_kv_heads, sh.n_q_heads
+    out = {}
+    if case.dec_q.shape[0]:
+        qs = case.dec_q_start.tolist()
+        nbytes = flops = 0
+        for c, s in enumerate(case.dec_ctx):
+            L = case.seqs[s].total_len
+            ads = case.dec_adapter[qs[c]:qs[c + 1]].tolist()
+            rows = len(ads) * (Hq // Hkv)
+            distinct = len({a for a in ads if a >= 0})
+            nbytes += L * (Hkv * D * 2 + 2 * R) * es
+            nbytes += distinct * 2 * R * Hkv * D * es
+            nbytes += len(ads) * Hq * D * es * 2
+            flops += L * Hkv * (distinct * 2 * R * D + rows * (4 * D + 2 * R))
+            flops += len([a for a in ads if a >= 0]) * Hq * 2 * R * D
+        out["decode"] = {"bytes": nbytes, "flops": flops, "units": int(case.dec_q.shape[0]),
+                         "unit_name": "query tokens"}
+    if case.pre_seq:
+        qs = case.pre_q_start.tolist()
+        pairs = 0
+        nbytes = flops = 0
+        for p, s in enumerate(case.pre_seq):
+            L = case.seqs[s].total_len
+            n = qs[p + 1] - qs[p]
+            vis = n * (L - n) + n * (n + 1) // 2  # visible (query, key) pairs
+            pairs += vis
+            flops += Hq * vis * (4 * D + 2 * R)          # QK^T + PV + P L_V
+            flops += Hkv * L * 2 * R * D                  # K rebuild (once per key)
+            flops += n * Hq * 2 * R * D                   # O_lr B_V
+            nbytes += L * (Hkv * D * 2 + 2 * R) * es + 2 * n * Hq * D * es
+        out["prefill"] = {"bytes": nbytes, "flops": flops, "units": int(qs[-1]),
+                          "unit_name": "prefill tokens", "pairs": pairs}
+    T = sum(b - a for _, a, b in case.step_appends())
+    if T:
+        N = 2 * Hkv * D + 2 * R
+        out["append"] = {"bytes": (T * sh.hidden + N * sh.hidden + T * N) * es,
+                         "flops": 2 * T * sh.hidden * N, "units": T, "unit_name": "appended tokens"}
+    return out
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running (read only)."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, interval_s: float = 0.002):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.interval = interval_s
+        self._stop = threading.Event()
+        self._h = None
+        try:
+            import pynvml
+
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            try:
+                import torch
+
+                p = torch.cuda.get_device_properties(device_index)
+                bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+                self._h = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+            except Exception:
+                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # NVML missing: report no samples
+            self.error = str(e)
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for bit, name in self.REASONS.items():
+                    if r & bit and bit != 0x1:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.interval)
+
+    def __enter__(self):
+        if self._h is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._h is not None:
+            self._t.join()
+
+    def summary(self):
+        med = statistics.median(self.samples) if self.samples else None
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("internal_api") in ("openblas", "mkl", "blis")]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+# ----------------------------------------------------------- oracle timing
+def oracle_sample(case, budget_s: float, model):
+    """Times the fp64 oracle on a bounded sample of the workload. Returns
+    (value, unit, seconds, description). Decode workloads: whole queries over
+    their full context while the budget lasts (at least one query, or one query
+    over a leading fraction of its context when even one exceeds the budget);
+    prefill workloads: one sequence's chunk rows over the full context."""
+    import numpy as np
+
+    import oracle
+    from tests.parity import weights64
+
+    sh = case.shape
+    w64 = weights64(case)
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    if "decode" in model and "prefill" not in model:
+        qs = case.dec_q_start.tolist()
+        done = 0.0
+        t0 = time.perf_counter()
+        n_full = 0
+        for r in range(case.dec_q.shape[0]):
+            c = next(i for i in range(len(case.dec_ctx)) if qs[i] <= r < qs[i + 1])
+            L_full = case.seqs[case.dec_ctx[c]].total_len
+            X = case.seq_hidden(case.dec_ctx[c]).double().numpy()
+            oracle.decode(X, case.dec_q[r:r + 1].double().numpy(), case.dec_adapter[r:r + 1].numpy(),
+                          w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+            done += 1.0
+            n_full += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return done / dt, "tok/s", dt, f"{n_full} decode queries over their full {L_full}-token contexts"
+    if "prefill" in model and "decode" not in model:
+        p = 0
+        s = case.pre_seq[p]
+        a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
+        n = b - a
+        rows = list(range(0, n, max(1, n // 16)))
+        X = case.seq_hidden(s).double().numpy()
+        L = X.shape[0]
+        t0 = time.perf_counter()
+        oracle.attend(X, int(case.pre_adapter[p]), case.pre_q[a:b][rows].double().numpy(),
+                      np.array([L - n + k for k in rows]), w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+        dt = time.perf_counter() - t0
+        vis = sum(L - n + k + 1 for k in rows)
+        fl = sh.n_q_heads * vis * (4 * sh.head_dim + 2 * sh.rank)
+        return fl / dt / 1e12, "TFLOP/s", dt, f"{len(rows)} prefill rows of sequence 0 over {L} keys"
+    # mixed: one decode query and one prefill sequence's sampled rows, in tokens/s
+    t0 = time.perf_counter()
+    c = 0
+    X = case.seq_hidden(case.dec_ctx[c]).double().numpy()
+    oracle.decode(X, case.dec_q[0:1].double().numpy(), case.dec_adapter[0:1].numpy(), w64, sh.n_kv_heads,
+                  sh.head_dim, sh.rope_base, scale)
+    p = 0
+    s = case.pre_seq[p]
+    a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
+    X = case.seq_hidden(s).double().numpy()
+    oracle.prefill(X, case.pre_q[a:b].double().numpy(), int(case.pre_adapter[p]), w64, sh.n_kv_heads,
+                   sh.head_dim, sh.rope_base, scale)
+    dt = time.perf_counter() - t0
+    return (1 + (b - a)) / dt, "tok/s", dt, f"1 decode query + 1 prefill chunk of {b - a} tokens"
+
+
+def run_reference(args):
+    """The base contract's reference arm: the fp64 CPU oracle as it stands."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from rank_cache_attention_flash_b300 import inputs as I
+
+    case = I.FULL[args.config]()
+    model = workload_model(case)
+    budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    # per-step sample: one query (or chunk rows) over a leading fraction of its
+    # context, sized to the per-step budget; throughput in full-query units
+    import numpy as np
+
+    import oracle
+    from tests.parity import weights64
+
+    sh = case.shape
+    w64 = weights64(case)
+    scale = 1.0 / math.sqrt(sh.head_dim)
+    decode_like = "decode" in model and "prefill" not in model
+    if decode_like:
+        s = case.dec_ctx[0]
+        L_full = case.seqs[s].total_len
+        X_full = case.seq_hidden(s).double().numpy()
+        q = case.dec_q[0:1].double().numpy()
+        ad = case.dec_adapter[0:1].numpy()
+
+        def one(nt):
+            oracle.decode(X_full[:nt], q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+    else:
+        p = 0
+        s = case.pre_seq[p]
+        a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
+        X_full = case.seq_hidden(s).double().numpy()
+        L_full = X_full.shape[0]
+        qrow = case.pre_q[b - 1:b].double().numpy()
+
+        def one(nt):
+            oracle.attend(X_full[:nt], int(case.pre_adapter[p]), qrow, [nt - 1], w64, sh.n_kv_heads,
+                          sh.head_dim, sh.rope_base, scale)
+    # calibrate tokens per step
+    nt = min(L_full, 256)
+    t0 = time.perf_counter()
+    one(nt)
+    per_tok = (time.perf_counter() - t0) / nt
+    nt = int(max(16, min(L_full, budget / max(per_tok, 1e-9))))
+    for _ in range(args.warmup):
+        one(nt)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one(nt)
+    dt = time.perf_counter() - t0
+    units = args.steps * nt / L_full  # fractions of one full query
+    value = units / dt
+    cores = oracle_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.config},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": f"per step: one query over the leading {nt} of its {L_full} keys "
+                                       f"(counted as {nt}/{L_full} of a query)"},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="lrkv", choices=["lrkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from rank_cache_attention_flash_b300 import inputs as I
+    from rank_cache_attention_flash_b300 import lrkv
+    from rank_cache_attention_flash_b300.harness import GpuCase
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lrkv.load()
+
+    case = I.FULL[args.config]()
+    model = workload_model(case)
+    g = GpuCase(case, device=dev)
+    g.setup()
+    if "prefill" in model and "append" in model and "decode" not in model:
+        kinds = ["append", "prefill"]
+    else:
+        kinds = [k for k in ("append", "decode", "prefill") if k in model]
+    dominant = "decode" if "decode" in model else "prefill"
+    launches_per_call = {"append": 1, "decode": 1 if case.shape.dtype == "fp32" else 2, "prefill": 1}
+
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    calls = {"append": g.step_append, "decode": g.decode, "prefill": g.prefill}
+
+    def one_step(evs=None):
+        for k in kinds:
+            if evs is not None:
+                evs[k][0].record(stream)
+            calls[k]()
+            if evs is not None:
+                evs[k][1].record(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        one_step()
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in kinds}
+           for _ in range(K)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    host_t0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            step_ev[i][0].record(stream)
+            one_step(evs[i])
+            step_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    host_dt = time.perf_counter() - host_t0
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    part_ms = {k: [e[k][0].elapsed_time(e[k][1]) for e in evs] for k in kinds}
+    total_ms = torch.tensor([sum(step_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(total_ms, op=dist.ReduceOp.MAX)
+    ms_per_step = float(total_ms.item()) / K
+    status = g.device_status()
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if "decode" in model and "prefill" not in model:
+        q_host = case.dec_q.pin_memory()
+        small = [t.pin_memory() for t in (case.dec_q_start, case.dec_adapter, case.dec_lens())]
+        dsts = [g.dec_q_start, g.dec_adapter, g.dec_lens]
+        out_host = torch.empty(g.dec_out.shape, dtype=g.dec_out.dtype).pin_memory()
+        h2d = q_host.numel() * q_host.element_size() + sum(t.numel() * t.element_size() for t in small)
+        d2h = out_host.numel() * out_host.element_size()
+        e_ms = []
+        for i in range(args.e2e_steps + 5):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.dec_q.copy_(q_host, non_blocking=True)
+            for s_, d_ in zip(small, dsts):
+                d_.copy_(s_, non_blocking=True)
+            g.decode()
+            out_host.copy_(g.dec_out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= 5:
+                e_ms.append(a.elapsed_time(b))
+        e2e_ms = sum(e_ms) / len(e_ms)
+        e2e = {"value": world * model["decode"]["units"] / (e2e_ms / 1e3), "unit": "tok/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    else:
+        # host buffers for the step's new hidden states and queries, outputs back
+        srcs, dsts = [], []
+        if g.n_step_tokens:
+            srcs += [g.step_X.cpu().pin_memory(), g.step_pos.cpu().pin_memory(), g.step_rows.cpu().pin_memory()]
+            dsts += [g.step_X, g.step_pos, g.step_rows]
+        if g.n_dec:
+            srcs.append(case.dec_q.pin_memory())
+            dsts.append(g.dec_q)
+        if g.n_pre:
+            srcs.append(case.pre_q.pin_memory())
+            dsts.append(g.pre_q)
+        outs = [(t, torch.empty(t.shape, dtype=t.dtype).pin_memory())
+                for t in ([g.dec_out] if g.n_dec else []) + ([g.pre_out] if g.n_pre else [])]
+        h2d = sum(t.numel() * t.element_size() for t in srcs)
+        d2h = sum(h.numel() * h.element_size() for _, h in outs)
+        e_ms = []
+        for i in range(min(args.e2e_steps, 50) + 3):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for s_, d_ in zip(srcs, dsts):
+                d_.copy_(s_, non_blocking=True)
+            one_step()
+            for d_, h_ in outs:
+                h_.copy_(d_, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= 3:
+                e_ms.append(a.elapsed_time(b))
+        e2e_ms = sum(e_ms) / len(e_ms)
+
+    pk = peaks()
+    dom_ms = sum(part_ms[dominant]) / K
+    dm = model[dominant]
+    if dominant == "decode":
+        achieved = dm["bytes"] / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
+                "kernel": "lrkv_attn_decode (decode_kernel + combine_kernel)",
+                "algorithmic_bytes_per_launch": dm["bytes"], "launch_ms": dom_ms,
+                "traffic": committed_traffic(args.config, "decode")}
+    else:
+        achieved = dm["flops"] / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"], "peak_source": pk["source"] + " (burst)",
+                "kernel": "lrkv_attn_prefill (prefill_kernel)",
+                "algorithmic_flops_per_launch": dm["flops"], "launch_ms": dom_ms,
+                "traffic": committed_traffic(args.config, "prefill")}
+
+    if dominant == "decode" and "prefill" not in model:
+        unit, value = "tok/s", world * dm["units"] / (ms_per_step / 1e3)
+    elif "decode" not in model:
+        unit = "TFLOP/s"
+        value = world * (model["prefill"]["flops"] + model.get("append", {"flops": 0})["flops"]) / (ms_per_step / 1e3) / 1e12
+    else:
+        unit = "tok/s"
+        value = world * (model["decode"]["units"] + model["prefill"]["units"]) / (ms_per_step / 1e3)
+    if e2e is None:
+        if unit == "TFLOP/s":
+            ev = world * (model["prefill"]["flops"] + model.get("append", {"flops": 0})["flops"]) / (e2e_ms / 1e3) / 1e12
+        else:
+            ev = value * ms_per_step / e2e_ms
+        e2e = {"value": ev, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms}
+
+    sh = case.shape
+    parts = {}
+    for k in kinds:
+        ms = sum(part_ms[k]) / K
+        m = model[k]
+        parts[k] = {"ms": ms, "GB/s": m["bytes"] / (ms / 1e3) / 1e9, "TFLOP/s": m["flops"] / (ms / 1e3) / 1e12,
+                    m["unit_name"]: m["units"]}
+        parts[k]["frac_hbm"] = parts[k]["GB/s"] / pk["hbm_gbs"]
+        parts[k]["frac_tensor"] = parts[k]["TFLOP/s"] / pk["bf16_tflops"]
+    bytes_lrkv = bytes_full = 0
+    es = 4 if sh.dtype == "fp32" else 2
+    if "decode" in model:
+        qs = case.dec_q_start.tolist()
+        for c, s in enumerate(case.dec_ctx):
+            L = case.seqs[s].total_len
+            readers = qs[c + 1] - qs[c]
+            bytes_full += readers * L * sh.n_kv_heads * sh.head_dim * 2 * es
+            bytes_lrkv += L * (sh.n_kv_heads * sh.head_dim * 2 + 2 * sh.rank) * es
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if sh.dtype == "bf16" else "fp32", "data": "synthetic",
+        "config": {"workload": args.config, "hidden": sh.hidden, "n_q_heads": sh.n_q_heads,
+                   "n_kv_heads": sh.n_kv_heads, "head_dim": sh.head_dim, "rank": sh.rank,
+                   "n_adapters": sh.n_adapters, "contexts": len(case.seqs),
+                   "max_len": max(q.total_len for q in case.seqs),
+                   "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"replica x{world} (independent contexts per GPU)"},
+        "roofline": roof, "parts": parts, "e2e": e2e,
+        "gpu_launches": K * sum(launches_per_call[k] for k in kinds),
+        "clocks": clk.summary(), "device_status": status, "host_s": host_dt,
+    }
+    if bytes_full:
+        line["cache_bytes"] = {"lrkv": bytes_lrkv, "per_agent_full": bytes_full,
+                               "saving": bytes_full / bytes_lrkv}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, u, dt, desc = oracle_sample(case, 15.0, model)
+        line["cpu_baseline"] = {"value": v, "unit": u, "cores": oracle_threads(), "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -2,6 +2,7 @@
 from .lrkv_oracle import (  # noqa: F401
     BLOCK,
     agent_kv,
+    agent_kv_from_cache,
     append_pools,
     apply_rope,
     attend,
@@ -10,4 +11,5 @@ from .lrkv_oracle import (  # noqa: F401
     gqa_attention,
     prefill,
     rope_inv_freq,
+    round_bf16,
 )

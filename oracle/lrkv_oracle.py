@@ -26,7 +26,10 @@ a chunk of q_len queries over L keys sits at position L - q_len + k and sees
 keys at positions <= its own; adapter id -1 means B = 0.
 
 All arithmetic is float64. Inputs are the storage-dtype values converted to
-float64; nothing is rounded inside.
+float64; nothing is rounded inside, except in the explicitly named bf16-cache
+variant (agent_kv_from_cache), which rounds the four stored cache components
+to bf16 as a bf16 cache holds them and is used for short-context edge cases
+whose outputs are dominated by that storage rounding.
 """
 from __future__ import annotations
 
@@ -103,6 +106,39 @@ def agent_kv(X, positions, W_K, W_V, A_K, A_V, B_K_i, B_V_i, n_kv_heads: int,
     return k, v.reshape(T, n_kv_heads, head_dim)
 
 
+def round_bf16(x) -> np.ndarray:
+    """Rounds to the nearest bfloat16 (ties to even), returned as float64.
+
+    Used only by the bf16-cache reading below: the value is first rounded to
+    float32, then the low 16 bits of the float32 pattern are rounded away
+    (round half to even on bit 16)."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    u = a.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def agent_kv_from_cache(X, positions, W_K, W_V, A_K, A_V, B_K_i, B_V_i, n_kv_heads: int,
+                        head_dim: int, base: float, cache_dtype: str = "bf16"):
+    """One agent's keys and values when the cache components are STORED in
+    bf16: K_base, V_base, L_K, L_V are computed exactly, rounded to bf16 (what a
+    bf16 cache holds), then combined exactly as the decomposition defines:
+        K_i = K_base + RoPE(L_K B_K,i),   V_i = V_base + L_V B_V,i.
+    (LRAgent, Abstract: base component + low-rank adapter component; RoPE is
+    linear, so RoPE(X W_K + X A_K B_K) = RoPE(X W_K) + RoPE(X A_K B_K).)"""
+    assert cache_dtype == "bf16"
+    kb, vb, lk, lv = base_and_lowrank(X, positions, W_K, W_V, A_K, A_V, n_kv_heads, head_dim, base)
+    kb, vb, lk, lv = round_bf16(kb), round_bf16(vb), round_bf16(lk), round_bf16(lv)
+    T = kb.shape[0]
+    k = kb
+    v = vb
+    if B_K_i is not None:
+        k = k + apply_rope((lk @ _f64(B_K_i)).reshape(T, n_kv_heads, head_dim), positions, base)
+    if B_V_i is not None:
+        v = v + (lv @ _f64(B_V_i)).reshape(T, n_kv_heads, head_dim)
+    return k, v
+
+
 # ---------------------------------------------------------------------------
 # Attention.
 
@@ -143,36 +179,38 @@ def _adapter_B(weights, adapter: int):
 
 
 def attend(X_seq, adapter: int, q, q_positions, weights, n_kv_heads: int, head_dim: int,
-           base: float, scale: float) -> np.ndarray:
+           base: float, scale: float, cache_dtype=None) -> np.ndarray:
     """Queries q [N, Hq, d] of one agent over a sequence whose hidden states at
-    positions 0..L-1 are X_seq [L, h]: materialise the agent's K, V, then attend."""
+    positions 0..L-1 are X_seq [L, h]: materialise the agent's K, V, then attend.
+    cache_dtype="bf16" uses the bf16-stored cache components (agent_kv_from_cache)."""
     L = np.asarray(X_seq).shape[0]
     B_K, B_V = _adapter_B(weights, adapter)
-    K, V = agent_kv(X_seq, np.arange(L), weights["W_K"], weights["W_V"], weights["A_K"],
-                    weights["A_V"], B_K, B_V, n_kv_heads, head_dim, base)
+    make = agent_kv if cache_dtype is None else agent_kv_from_cache
+    K, V = make(X_seq, np.arange(L), weights["W_K"], weights["W_V"], weights["A_K"],
+                weights["A_V"], B_K, B_V, n_kv_heads, head_dim, base)
     return gqa_attention(q, q_positions, K, V, scale)
 
 
 def decode(X_ctx, q, adapters, weights, n_kv_heads: int, head_dim: int, base: float,
-           scale: float) -> np.ndarray:
+           scale: float, cache_dtype=None) -> np.ndarray:
     """Decode queries of several agents on one context X_ctx [L, h]: each query
     (one per row of q [N, Hq, d], adapter ids [N]) sits at position L - 1."""
     L = np.asarray(X_ctx).shape[0]
     out = np.empty(np.asarray(q).shape, dtype=np.float64)
     for n, a in enumerate(np.asarray(adapters).tolist()):
         out[n: n + 1] = attend(X_ctx, int(a), np.asarray(q)[n: n + 1], [L - 1], weights,
-                               n_kv_heads, head_dim, base, scale)
+                               n_kv_heads, head_dim, base, scale, cache_dtype)
     return out
 
 
 def prefill(X_seq, q_chunk, adapter: int, weights, n_kv_heads: int, head_dim: int,
-            base: float, scale: float) -> np.ndarray:
+            base: float, scale: float, cache_dtype=None) -> np.ndarray:
     """A chunk of q_len queries at the end of a sequence of L tokens (the chunk's
     own tokens included): query k sits at position L - q_len + k."""
     L = np.asarray(X_seq).shape[0]
     n = np.asarray(q_chunk).shape[0]
     return attend(X_seq, adapter, q_chunk, np.arange(L - n, L), weights, n_kv_heads,
-                  head_dim, base, scale)
+                  head_dim, base, scale, cache_dtype)
 
 
 def append_pools(base_pool, lr_pool, X, positions, seq_rows, block_tables, W_K, W_V, A_K,

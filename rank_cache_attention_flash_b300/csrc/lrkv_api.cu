@@ -1,0 +1,268 @@
+// C-ABI host layer of liblrkv: argument validation, RoPE frequency table,
+// TMA descriptors over the paged pools, split planning and dispatch to the
+// bf16 (tensor-core) or fp32 kernels. Allocates nothing and keeps no state.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "lrkv.h"
+#include "lrkv_device.cuh"
+#include "lrkv_internal.h"
+
+namespace lrkv {
+
+void rope_freqs(const lrkv_config& cfg, RopeFreqs* f) {
+  std::memset(f, 0, sizeof(*f));
+  const int half = cfg.head_dim / 2;
+  for (int j = 0; j < half && j < 64; ++j) {
+    const double th = std::pow(static_cast<double>(cfg.rope_base), -2.0 * j / cfg.head_dim);
+    const float hi = static_cast<float>(th);
+    f->hi[j] = hi;
+    f->lo[j] = static_cast<float>(th - static_cast<double>(hi));
+  }
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled get_encoder() {
+  static EncodeTiled fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+lrkv_status check_config(const lrkv_config* cfg) {
+  if (cfg == nullptr) return LRKV_ERR_INVALID_ARG;
+  if (cfg->hidden <= 0 || cfg->n_q_heads <= 0 || cfg->n_kv_heads <= 0 || cfg->head_dim <= 0 ||
+      cfg->rank <= 0 || cfg->block_size <= 0 || !(cfg->rope_base > 0.f))
+    return LRKV_ERR_INVALID_ARG;
+  if (cfg->n_q_heads % cfg->n_kv_heads != 0) return LRKV_ERR_INVALID_ARG;
+  if (cfg->dtype != LRKV_BF16 && cfg->dtype != LRKV_FP32) return LRKV_ERR_UNSUPPORTED;
+  if (cfg->block_size != kBlock) return LRKV_ERR_UNSUPPORTED;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return LRKV_ERR_UNSUPPORTED;
+  if (cfg->rank != 8 && cfg->rank != 16 && cfg->rank != 32 && cfg->rank != 64)
+    return LRKV_ERR_UNSUPPORTED;
+  if (cfg->n_q_heads / cfg->n_kv_heads > 16) return LRKV_ERR_UNSUPPORTED;
+  if (cfg->hidden % 64 != 0) return LRKV_ERR_UNSUPPORTED;
+  return LRKV_OK;
+}
+
+// positions must stay below 2^20 (RoPE argument reduction range)
+constexpr int64_t kMaxPositions = int64_t(1) << 20;
+
+lrkv_status check_pool(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
+                       int64_t num_blocks, int max_blocks) {
+  if (base_pool == nullptr || lr_pool == nullptr) return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(base_pool) || !aligned16(lr_pool)) return LRKV_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || max_blocks <= 0) return LRKV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_blocks) * kBlock > kMaxPositions) return LRKV_ERR_UNSUPPORTED;
+  // TMA row coordinates are int32
+  if (num_blocks * 2 * cfg.n_kv_heads * kBlock > INT32_MAX) return LRKV_ERR_UNSUPPORTED;
+  return LRKV_OK;
+}
+
+}  // namespace
+
+bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
+                    int64_t num_blocks, CUtensorMap* base_map, CUtensorMap* lr_map) {
+  EncodeTiled enc = get_encoder();
+  if (enc == nullptr) return false;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cfg.head_dim),
+                                static_cast<cuuint64_t>(num_blocks) * 2 * cfg.n_kv_heads * kBlock};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cfg.head_dim) * 2};
+    const cuuint32_t box[2] = {64, kBlock};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(base_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base_pool), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cfg.rank),
+                                static_cast<cuuint64_t>(num_blocks) * 2 * kBlock};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cfg.rank) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(cfg.rank), kBlock};
+    const cuuint32_t es[2] = {1, 1};
+    CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (cfg.rank == 16) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+    if (cfg.rank == 32) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (cfg.rank == 64) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (enc(lr_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(lr_pool), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+}  // namespace lrkv
+
+using namespace lrkv;
+
+extern "C" {
+
+const char* lrkv_status_string(lrkv_status s) {
+  switch (s) {
+    case LRKV_OK: return "LRKV_OK";
+    case LRKV_ERR_INVALID_ARG: return "LRKV_ERR_INVALID_ARG";
+    case LRKV_ERR_UNSUPPORTED: return "LRKV_ERR_UNSUPPORTED";
+    case LRKV_ERR_CUDA: return "LRKV_ERR_CUDA";
+    case LRKV_ERR_INDEX: return "LRKV_ERR_INDEX";
+    case LRKV_ERR_TIMEOUT: return "LRKV_ERR_TIMEOUT";
+    case LRKV_ERR_WORKSPACE: return "LRKV_ERR_WORKSPACE";
+  }
+  return "LRKV_UNKNOWN_STATUS";
+}
+
+int32_t lrkv_version(void) { return 100; }
+
+lrkv_status lrkv_append(const lrkv_config* cfg, const void* X, int32_t T,
+                        const int32_t* positions, const int32_t* seq_rows,
+                        const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
+                        const void* W_cat, void* base_pool, void* lr_pool, int64_t num_blocks,
+                        int32_t* dev_status, lrkv_stream_t stream) {
+  lrkv_status st = check_config(cfg);
+  if (st != LRKV_OK) return st;
+  if (T < 0 || num_seqs < 0) return LRKV_ERR_INVALID_ARG;
+  if (T == 0) return LRKV_OK;
+  if (X == nullptr || positions == nullptr || seq_rows == nullptr || block_tables == nullptr ||
+      W_cat == nullptr || num_seqs == 0)
+    return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W_cat) || !aligned4(positions) || !aligned4(seq_rows) ||
+      !aligned4(block_tables))
+    return LRKV_ERR_INVALID_ARG;
+  if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->dtype == LRKV_FP32)
+    return launch_append_fp32(*cfg, X, T, positions, seq_rows, block_tables, num_seqs, max_blocks,
+                              W_cat, base_pool, lr_pool, num_blocks, dev_status, s);
+  return launch_append_bf16(*cfg, X, T, positions, seq_rows, block_tables, num_seqs, max_blocks,
+                            W_cat, base_pool, lr_pool, num_blocks, dev_status, s);
+}
+
+size_t lrkv_decode_workspace_bytes(const lrkv_config* cfg, int32_t num_queries, int32_t num_ctx,
+                                   int32_t max_ctx_len, int32_t max_q_per_ctx) {
+  if (check_config(cfg) != LRKV_OK || num_queries < 0 || num_ctx < 0 || max_ctx_len < 0 ||
+      max_q_per_ctx < 0)
+    return 0;
+  if (cfg->dtype == LRKV_FP32 || num_queries == 0 || num_ctx == 0) return 0;
+  DecodePlan plan;
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  if (!plan_decode_bf16(*cfg, num_queries, num_ctx, max_ctx_len, max_q_per_ctx, sms, &plan))
+    return 0;
+  return plan.ws_bytes;
+}
+
+lrkv_status lrkv_attn_decode(const lrkv_config* cfg, const void* q, int32_t num_queries,
+                             const int32_t* ctx_q_start, int32_t num_ctx,
+                             const int32_t* adapter_ids, const int32_t* block_tables,
+                             int32_t max_blocks, const int32_t* ctx_lens, int32_t max_ctx_len,
+                             int32_t max_q_per_ctx, const void* base_pool, const void* lr_pool,
+                             int64_t num_blocks, const void* B_K, const void* B_V,
+                             int32_t n_adapters, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, lrkv_stream_t stream) {
+  lrkv_status st = check_config(cfg);
+  if (st != LRKV_OK) return st;
+  if (num_queries < 0 || num_ctx < 0 || n_adapters < 0 || max_ctx_len < 0 || max_q_per_ctx < 0)
+    return LRKV_ERR_INVALID_ARG;
+  if (num_queries == 0 || num_ctx == 0) return LRKV_OK;
+  if (q == nullptr || ctx_q_start == nullptr || adapter_ids == nullptr || block_tables == nullptr ||
+      ctx_lens == nullptr || out == nullptr)
+    return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(ctx_q_start) || !aligned4(adapter_ids) ||
+      !aligned4(block_tables) || !aligned4(ctx_lens))
+    return LRKV_ERR_INVALID_ARG;
+  if ((B_K != nullptr && !aligned16(B_K)) || (B_V != nullptr && !aligned16(B_V)))
+    return LRKV_ERR_INVALID_ARG;
+  if ((B_K != nullptr || B_V != nullptr) && n_adapters == 0) return LRKV_ERR_INVALID_ARG;
+  if (max_ctx_len < 1 || max_q_per_ctx < 1 || !(scale == scale)) return LRKV_ERR_INVALID_ARG;
+  if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
+  if (static_cast<int64_t>(max_ctx_len) > static_cast<int64_t>(max_blocks) * kBlock)
+    return LRKV_ERR_INVALID_ARG;
+  DecodeArgs a{q, num_queries, ctx_q_start, num_ctx, adapter_ids, block_tables, max_blocks,
+               ctx_lens, max_ctx_len, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters,
+               scale, out, dev_status};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->dtype == LRKV_FP32) return launch_decode_fp32(*cfg, a, max_q_per_ctx, s);
+  const int sms = device_sm_count();
+  if (sms <= 0) return LRKV_ERR_CUDA;
+  DecodePlan plan;
+  if (!plan_decode_bf16(*cfg, num_queries, num_ctx, max_ctx_len, max_q_per_ctx, sms, &plan))
+    return LRKV_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < plan.ws_bytes || !aligned16(workspace))
+    return LRKV_ERR_WORKSPACE;
+  return launch_decode_bf16(*cfg, a, plan, workspace, s);
+}
+
+size_t lrkv_prefill_workspace_bytes(const lrkv_config* cfg, int32_t num_seqs, int32_t total_q,
+                                    int32_t max_q_len, int32_t max_seq_len) {
+  (void)cfg;
+  (void)num_seqs;
+  (void)total_q;
+  (void)max_q_len;
+  (void)max_seq_len;
+  return 0;
+}
+
+lrkv_status lrkv_attn_prefill(const lrkv_config* cfg, const void* q, const int32_t* q_start,
+                              int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                              const int32_t* seq_lens, int32_t max_seq_len,
+                              const int32_t* adapter_ids, const int32_t* block_tables,
+                              int32_t max_blocks, const void* base_pool, const void* lr_pool,
+                              int64_t num_blocks, const void* B_K, const void* B_V,
+                              int32_t n_adapters, float scale, void* out, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, lrkv_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  lrkv_status st = check_config(cfg);
+  if (st != LRKV_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0 || n_adapters < 0)
+    return LRKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return LRKV_OK;
+  if (q == nullptr || q_start == nullptr || seq_lens == nullptr || adapter_ids == nullptr ||
+      block_tables == nullptr || out == nullptr)
+    return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(q_start) || !aligned4(seq_lens) ||
+      !aligned4(adapter_ids) || !aligned4(block_tables))
+    return LRKV_ERR_INVALID_ARG;
+  if ((B_K != nullptr && !aligned16(B_K)) || (B_V != nullptr && !aligned16(B_V)))
+    return LRKV_ERR_INVALID_ARG;
+  if ((B_K != nullptr || B_V != nullptr) && n_adapters == 0) return LRKV_ERR_INVALID_ARG;
+  if (max_q_len < 1 || max_seq_len < max_q_len || !(scale == scale)) return LRKV_ERR_INVALID_ARG;
+  if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * kBlock)
+    return LRKV_ERR_INVALID_ARG;
+  PrefillArgs a{q, q_start, num_seqs, total_q, max_q_len, seq_lens, max_seq_len, adapter_ids,
+                block_tables, max_blocks, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters,
+                scale, out, dev_status};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->dtype == LRKV_FP32) return launch_prefill_fp32(*cfg, a, s);
+  return launch_prefill_bf16(*cfg, a, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// Internal interfaces between the C-ABI host layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "lrkv.h"
+
+namespace lrkv {
+
+struct RopeFreqs;  // lrkv_device.cuh
+
+// Split plan of the bf16 decode kernel; a pure function of the sizes and the
+// device's SM count, so the workspace query and the launch agree.
+struct DecodePlan {
+  int g;             // query heads per kv head
+  int qg_size;       // queries per query group (rows = qg_size * g <= 16)
+  int n_qgroups;     // query groups per context
+  int n_splits;      // splits of each context's blocks
+  int split_blocks;  // blocks per split
+  int64_t n_items;   // num_ctx * n_qgroups * n_splits * Hkv
+  int grid;          // persistent CTAs
+  int nstage;        // pipeline stages
+  int smem_bytes;
+  size_t ws_bytes;   // workspace: split partials
+};
+
+bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int max_ctx_len,
+                      int max_q_per_ctx, int sm_count, DecodePlan* plan);
+
+struct DecodeArgs {
+  const void* q;
+  int num_queries;
+  const int32_t* ctx_q_start;
+  int num_ctx;
+  const int32_t* adapter_ids;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* ctx_lens;
+  int max_ctx_len;
+  const void* base_pool;
+  const void* lr_pool;
+  int64_t num_blocks;
+  const void* B_K;
+  const void* B_V;
+  int n_adapters;
+  float scale;
+  void* out;
+  int32_t* status;
+};
+
+// Host-built RoPE frequency table (theta_j split into two floats).
+void rope_freqs(const lrkv_config& cfg, RopeFreqs* f);
+
+// Tensor maps over the paged pools.
+bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
+                    int64_t num_blocks, CUtensorMap* base_map, CUtensorMap* lr_map);
+
+lrkv_status launch_decode_bf16(const lrkv_config& cfg, const DecodeArgs& a,
+                               const DecodePlan& plan, void* workspace, cudaStream_t stream);
+
+lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X, int T,
+                               const int32_t* positions, const int32_t* seq_rows,
+                               const int32_t* block_tables, int num_seqs, int max_blocks,
+                               const void* W_cat, void* base_pool, void* lr_pool,
+                               int64_t num_blocks, int32_t* status, cudaStream_t stream);
+
+struct PrefillArgs {
+  const void* q;
+  const int32_t* q_start;
+  int num_seqs;
+  int total_q;
+  int max_q_len;
+  const int32_t* seq_lens;
+  int max_seq_len;
+  const int32_t* adapter_ids;
+  const int32_t* block_tables;
+  int max_blocks;
+  const void* base_pool;
+  const void* lr_pool;
+  int64_t num_blocks;
+  const void* B_K;
+  const void* B_V;
+  int n_adapters;
+  float scale;
+  void* out;
+  int32_t* status;
+};
+
+lrkv_status launch_prefill_bf16(const lrkv_config& cfg, const PrefillArgs& a,
+                                cudaStream_t stream);
+
+// fp32 path (plain FMA, no tensor cores).
+lrkv_status launch_append_fp32(const lrkv_config& cfg, const void* X, int T,
+                               const int32_t* positions, const int32_t* seq_rows,
+                               const int32_t* block_tables, int num_seqs, int max_blocks,
+                               const void* W_cat, void* base_pool, void* lr_pool,
+                               int64_t num_blocks, int32_t* status, cudaStream_t stream);
+lrkv_status launch_decode_fp32(const lrkv_config& cfg, const DecodeArgs& a, int max_q_per_ctx,
+                               cudaStream_t stream);
+lrkv_status launch_prefill_fp32(const lrkv_config& cfg, const PrefillArgs& a,
+                                cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace lrkv

@@ -1,0 +1,136 @@
+"""Drives a seeded workload (``inputs.Case``) through the CUDA library.
+
+Uploads the weights and block tables, fills the paged pools with the untimed
+setup appends (the context cached before the step), and runs the step: the
+append of every new token, then decode and prefill attention. Only argument
+preparation happens here; every computation is a library call.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional
+
+import torch
+
+from . import inputs as I
+from . import lrkv
+
+
+class GpuCase:
+    def __init__(self, case: I.Case, device="cuda", pool_fill: Optional[float] = None,
+                 setup_chunk_tokens: int = 1 << 16):
+        self.case = case
+        self.device = torch.device(device)
+        sh = case.shape
+        self.cfg = lrkv.make_config(sh.hidden, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.rank,
+                                    sh.rope_base, sh.torch_dtype)
+        dev = self.device
+        w = case.weights
+        self.W_cat = lrkv.pack_w_cat(w["W_K"], w["W_V"], w["A_K"], w["A_V"]).to(dev)
+        self.B_K = w["B_K"].contiguous().to(dev)
+        self.B_V = w["B_V"].contiguous().to(dev)
+        self.block_tables = case.block_tables.to(dev)
+        self.base_pool, self.lr_pool = lrkv.new_pools(self.cfg, case.num_blocks, dev, pool_fill)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.scale = 1.0 / math.sqrt(sh.head_dim)
+        self.setup_chunk_tokens = setup_chunk_tokens
+        # decode arguments
+        bt = case.block_tables
+        self.n_dec = int(case.dec_q.shape[0])
+        if self.n_dec:
+            self.dec_q = case.dec_q.to(dev)
+            self.dec_q_start = case.dec_q_start.to(dev)
+            self.dec_adapter = case.dec_adapter.to(dev)
+            self.dec_bt = bt[torch.tensor(case.dec_ctx, dtype=torch.long)].contiguous().to(dev)
+            lens = case.dec_lens()
+            self.dec_lens = lens.to(dev)
+            self.dec_max_len = int(lens.max())
+            qs = case.dec_q_start
+            self.dec_max_q = int((qs[1:] - qs[:-1]).max())
+            self.dec_out = torch.empty_like(self.dec_q)
+            self.dec_ws = torch.empty(
+                max(1, lrkv.decode_workspace_bytes(self.cfg, self.n_dec, len(case.dec_ctx),
+                                                   self.dec_max_len, self.dec_max_q)),
+                dtype=torch.uint8, device=dev)
+        # prefill arguments
+        self.n_pre = len(case.pre_seq)
+        if self.n_pre:
+            self.pre_q = case.pre_q.to(dev)
+            self.pre_q_start = case.pre_q_start.to(dev)
+            self.pre_adapter = case.pre_adapter.to(dev)
+            self.pre_bt = bt[torch.tensor(case.pre_seq, dtype=torch.long)].contiguous().to(dev)
+            lens = case.pre_lens()
+            self.pre_lens = lens.to(dev)
+            self.pre_max_len = int(lens.max())
+            qs = case.pre_q_start
+            self.pre_max_q = int((qs[1:] - qs[:-1]).max())
+            self.pre_out = torch.empty_like(self.pre_q)
+        # step append arguments (all new tokens in one call)
+        xs, pos, rows = [], [], []
+        for s, a, b in case.step_appends():
+            xs.append(case.seq_hidden(s, a, b))
+            pos.append(torch.arange(a, b, dtype=torch.int32))
+            rows.append(torch.full((b - a,), s, dtype=torch.int32))
+        self.n_step_tokens = sum(x.shape[0] for x in xs)
+        if xs:
+            self.step_X = torch.cat(xs).to(dev)
+            self.step_pos = torch.cat(pos).to(dev)
+            self.step_rows = torch.cat(rows).to(dev)
+
+    # ------------------------------------------------------------------
+    def setup(self) -> None:
+        """Untimed: append the tokens cached before the step."""
+        case, dev = self.case, self.device
+        pend_x, pend_p, pend_r, n = [], [], [], 0
+
+        def flush():
+            nonlocal pend_x, pend_p, pend_r, n
+            if not pend_x:
+                return
+            X = torch.cat(pend_x).to(dev)
+            P = torch.cat(pend_p).to(dev)
+            Rw = torch.cat(pend_r).to(dev)
+            lrkv.append(self.cfg, X, P, Rw, self.block_tables, self.W_cat, self.base_pool,
+                        self.lr_pool, self.status)
+            pend_x, pend_p, pend_r, n = [], [], [], 0
+
+        for s, a, b in case.setup_appends():
+            for lo in range(a, b, self.setup_chunk_tokens):
+                hi = min(b, lo + self.setup_chunk_tokens)
+                pend_x.append(case.seq_hidden(s, lo, hi))
+                pend_p.append(torch.arange(lo, hi, dtype=torch.int32))
+                pend_r.append(torch.full((hi - lo,), s, dtype=torch.int32))
+                n += hi - lo
+                if n >= self.setup_chunk_tokens:
+                    flush()
+        flush()
+
+    def step_append(self) -> None:
+        if self.n_step_tokens:
+            lrkv.append(self.cfg, self.step_X, self.step_pos, self.step_rows, self.block_tables,
+                        self.W_cat, self.base_pool, self.lr_pool, self.status)
+
+    def decode(self, stream=None) -> Optional[torch.Tensor]:
+        if not self.n_dec:
+            return None
+        return lrkv.attn_decode(self.cfg, self.dec_q, self.dec_q_start, self.dec_adapter,
+                                self.dec_bt, self.dec_lens, self.dec_max_len, self.dec_max_q,
+                                self.base_pool, self.lr_pool, self.B_K, self.B_V, self.scale,
+                                out=self.dec_out, workspace=self.dec_ws, status=self.status,
+                                stream=stream)
+
+    def prefill(self, stream=None) -> Optional[torch.Tensor]:
+        if not self.n_pre:
+            return None
+        return lrkv.attn_prefill(self.cfg, self.pre_q, self.pre_q_start, self.pre_max_q,
+                                 self.pre_lens, self.pre_max_len, self.pre_adapter, self.pre_bt,
+                                 self.base_pool, self.lr_pool, self.B_K, self.B_V, self.scale,
+                                 out=self.pre_out, status=self.status, stream=stream)
+
+    def step(self) -> Dict[str, Optional[torch.Tensor]]:
+        """One pass of the hot path: append the new tokens, then attend."""
+        self.step_append()
+        return {"decode": self.decode(), "prefill": self.prefill()}
+
+    def device_status(self) -> int:
+        return int(self.status.item())

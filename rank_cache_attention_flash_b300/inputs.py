@@ -349,5 +349,5 @@ SMALL = {
     "prefill_chunk_llama8b": lambda seed=0: prefill_chunk(seed, prefix=272, chunk=77),
     "long_decode_ministral8b": lambda seed=0: long_decode(seed, n_seqs=3, n=709),
     "mixed_batch_qwen3_1p7b": lambda seed=0: mixed_batch(seed, n_seqs=6, n_decode=4, chunk=45,
-                                                          lo=17, hi=600),
+                                                          lo=1024, hi=1400),
 }

@@ -1,0 +1,249 @@
+"""Python binding of liblrkv (ctypes). Argument marshalling only: every step of
+the computation runs in the CUDA library; torch provides device memory and
+streams. The library must be built (``python -m rank_cache_attention_flash_b300.build``);
+nothing here falls back to another implementation.
+
+Entry points mirror the C ABI in ``include/lrkv.h``:
+  append, attn_decode, attn_prefill, decode_workspace_bytes,
+  prefill_workspace_bytes, status_string, version.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+BLOCK = 16
+
+STATUS = {0: "LRKV_OK", 1: "LRKV_ERR_INVALID_ARG", 2: "LRKV_ERR_UNSUPPORTED", 3: "LRKV_ERR_CUDA",
+          4: "LRKV_ERR_INDEX", 5: "LRKV_ERR_TIMEOUT", 6: "LRKV_ERR_WORKSPACE"}
+BF16, FP32 = 0, 1
+
+EXPORTS = ("lrkv_append", "lrkv_attn_decode", "lrkv_decode_workspace_bytes", "lrkv_attn_prefill",
+           "lrkv_prefill_workspace_bytes", "lrkv_status_string", "lrkv_version")
+
+
+class LrkvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("rank", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("rope_base", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == BF16 else torch.float32
+
+    @property
+    def n_cols(self) -> int:
+        return 2 * self.n_kv_heads * self.head_dim + 2 * self.rank
+
+
+def make_config(hidden: int, n_q_heads: int, n_kv_heads: int, head_dim: int, rank: int,
+                rope_base: float = 10000.0, dtype: torch.dtype = torch.bfloat16) -> Config:
+    return Config(hidden, n_q_heads, n_kv_heads, head_dim, rank, BLOCK, rope_base,
+                  BF16 if dtype == torch.bfloat16 else FP32)
+
+
+_lib = None
+_P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+
+def load() -> ctypes.CDLL:
+    """Loads liblrkv.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m rank_cache_attention_flash_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    cfgp = ctypes.POINTER(Config)
+    lib.lrkv_append.argtypes = [cfgp, _P, _I32, _P, _P, _P, _I32, _I32, _P, _P, _P, _I64, _P, _P]
+    lib.lrkv_append.restype = ctypes.c_int
+    lib.lrkv_attn_decode.argtypes = [cfgp, _P, _I32, _P, _I32, _P, _P, _I32, _P, _I32, _I32, _P, _P,
+                                     _I64, _P, _P, _I32, _F, _P, _P, _SZ, _P, _P]
+    lib.lrkv_attn_decode.restype = ctypes.c_int
+    lib.lrkv_decode_workspace_bytes.argtypes = [cfgp, _I32, _I32, _I32, _I32]
+    lib.lrkv_decode_workspace_bytes.restype = _SZ
+    lib.lrkv_attn_prefill.argtypes = [cfgp, _P, _P, _I32, _I32, _I32, _P, _I32, _P, _P, _I32, _P,
+                                      _P, _I64, _P, _P, _I32, _F, _P, _P, _SZ, _P, _P]
+    lib.lrkv_attn_prefill.restype = ctypes.c_int
+    lib.lrkv_prefill_workspace_bytes.argtypes = [cfgp, _I32, _I32, _I32, _I32]
+    lib.lrkv_prefill_workspace_bytes.restype = _SZ
+    lib.lrkv_status_string.argtypes = [ctypes.c_int]
+    lib.lrkv_status_string.restype = ctypes.c_char_p
+    lib.lrkv_version.argtypes = []
+    lib.lrkv_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(t: Optional[torch.Tensor], name: str, dtype=None, device=None):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must live on {device}")
+
+
+def _raise(code: int, where: str):
+    if code != 0:
+        raise LrkvError(code, where)
+
+
+def status_string(code: int) -> str:
+    return load().lrkv_status_string(code).decode()
+
+
+def version() -> int:
+    return load().lrkv_version()
+
+
+# ------------------------------------------------------------------ helpers
+def pack_w_cat(W_K: torch.Tensor, W_V: torch.Tensor, A_K: torch.Tensor, A_V: torch.Tensor) -> torch.Tensor:
+    """One-time weight layout for append: [N, h] rows = output columns
+    (nn.Linear layout), in the order K | V | A_K | A_V."""
+    return torch.cat([W_K.t(), W_V.t(), A_K.t(), A_V.t()], 0).contiguous()
+
+
+def new_pools(cfg: Config, num_blocks: int, device, fill: Optional[float] = None
+              ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Allocates (base_pool, lr_pool) for ``num_blocks`` blocks."""
+    dt = cfg.torch_dtype
+    base = torch.empty(num_blocks, 2, cfg.n_kv_heads, BLOCK, cfg.head_dim, dtype=dt, device=device)
+    lr = torch.empty(num_blocks, 2, BLOCK, cfg.rank, dtype=dt, device=device)
+    if fill is not None:
+        base.fill_(fill)
+        lr.fill_(fill)
+    return base, lr
+
+
+# ------------------------------------------------------------- entry points
+def append(cfg: Config, X: torch.Tensor, positions: torch.Tensor, seq_rows: torch.Tensor,
+           block_tables: torch.Tensor, W_cat: torch.Tensor, base_pool: torch.Tensor,
+           lr_pool: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    lib = load()
+    dev = base_pool.device
+    _check(X, "X", cfg.torch_dtype, dev)
+    _check(W_cat, "W_cat", cfg.torch_dtype, dev)
+    for t, n in ((positions, "positions"), (seq_rows, "seq_rows"), (block_tables, "block_tables")):
+        _check(t, n, torch.int32, dev)
+    _check(status, "status", torch.int32, dev)
+    T = X.shape[0]
+    if X.shape != (T, cfg.hidden) or positions.numel() != T or seq_rows.numel() != T:
+        raise ValueError("append: shape mismatch")
+    if W_cat.shape != (cfg.n_cols, cfg.hidden):
+        raise ValueError("append: W_cat must be [2*Hkv*d + 2*r, h]")
+    code = lib.lrkv_append(ctypes.byref(cfg), _ptr(X), T, _ptr(positions), _ptr(seq_rows),
+                           _ptr(block_tables), block_tables.shape[0], block_tables.shape[1],
+                           _ptr(W_cat), _ptr(base_pool), _ptr(lr_pool), base_pool.shape[0],
+                           _ptr(status), _stream(stream))
+    _raise(code, "lrkv_append")
+
+
+def decode_workspace_bytes(cfg: Config, num_queries: int, num_ctx: int, max_ctx_len: int,
+                           max_q_per_ctx: int) -> int:
+    return int(load().lrkv_decode_workspace_bytes(ctypes.byref(cfg), num_queries, num_ctx,
+                                                   max_ctx_len, max_q_per_ctx))
+
+
+def prefill_workspace_bytes(cfg: Config, num_seqs: int, total_q: int, max_q_len: int,
+                            max_seq_len: int) -> int:
+    return int(load().lrkv_prefill_workspace_bytes(ctypes.byref(cfg), num_seqs, total_q, max_q_len,
+                                                    max_seq_len))
+
+
+def attn_decode(cfg: Config, q: torch.Tensor, ctx_q_start: torch.Tensor, adapter_ids: torch.Tensor,
+                block_tables: torch.Tensor, ctx_lens: torch.Tensor, max_ctx_len: int,
+                max_q_per_ctx: int, base_pool: torch.Tensor, lr_pool: torch.Tensor,
+                B_K: Optional[torch.Tensor], B_V: Optional[torch.Tensor],
+                scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    lib = load()
+    dev = base_pool.device
+    _check(q, "q", cfg.torch_dtype, dev)
+    for t, n in ((ctx_q_start, "ctx_q_start"), (adapter_ids, "adapter_ids"),
+                 (block_tables, "block_tables"), (ctx_lens, "ctx_lens")):
+        _check(t, n, torch.int32, dev)
+    _check(B_K, "B_K", cfg.torch_dtype, dev)
+    _check(B_V, "B_V", cfg.torch_dtype, dev)
+    _check(status, "status", torch.int32, dev)
+    nq = q.shape[0]
+    num_ctx = ctx_lens.numel()
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", cfg.torch_dtype, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+    need = decode_workspace_bytes(cfg, nq, num_ctx, max_ctx_len, max_q_per_ctx)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    n_adapters = 0 if B_K is None and B_V is None else (B_K if B_K is not None else B_V).shape[0]
+    code = lib.lrkv_attn_decode(
+        ctypes.byref(cfg), _ptr(q), nq, _ptr(ctx_q_start), num_ctx, _ptr(adapter_ids),
+        _ptr(block_tables), block_tables.shape[1], _ptr(ctx_lens), max_ctx_len, max_q_per_ctx,
+        _ptr(base_pool), _ptr(lr_pool), base_pool.shape[0], _ptr(B_K), _ptr(B_V), n_adapters,
+        float(scale), _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream))
+    _raise(code, "lrkv_attn_decode")
+    return out
+
+
+def attn_prefill(cfg: Config, q: torch.Tensor, q_start: torch.Tensor, max_q_len: int,
+                 seq_lens: torch.Tensor, max_seq_len: int, adapter_ids: torch.Tensor,
+                 block_tables: torch.Tensor, base_pool: torch.Tensor, lr_pool: torch.Tensor,
+                 B_K: Optional[torch.Tensor], B_V: Optional[torch.Tensor],
+                 scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    lib = load()
+    dev = base_pool.device
+    _check(q, "q", cfg.torch_dtype, dev)
+    for t, n in ((q_start, "q_start"), (seq_lens, "seq_lens"), (adapter_ids, "adapter_ids"),
+                 (block_tables, "block_tables")):
+        _check(t, n, torch.int32, dev)
+    _check(B_K, "B_K", cfg.torch_dtype, dev)
+    _check(B_V, "B_V", cfg.torch_dtype, dev)
+    _check(status, "status", torch.int32, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", cfg.torch_dtype, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+    S = seq_lens.numel()
+    n_adapters = 0 if B_K is None and B_V is None else (B_K if B_K is not None else B_V).shape[0]
+    code = lib.lrkv_attn_prefill(
+        ctypes.byref(cfg), _ptr(q), _ptr(q_start), S, q.shape[0], max_q_len, _ptr(seq_lens),
+        max_seq_len, _ptr(adapter_ids), _ptr(block_tables), block_tables.shape[1], _ptr(base_pool),
+        _ptr(lr_pool), base_pool.shape[0], _ptr(B_K), _ptr(B_V), n_adapters, float(scale), _ptr(out),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _raise(code, "lrkv_attn_prefill")
+    return out

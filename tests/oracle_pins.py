@@ -300,10 +300,47 @@ def pin_multi_agent_batch(O):
     assert not np.allclose(both[0], O.attend(X, -1, q[0:1], [L - 1], w, Hkv, d, 10000.0, 0.5)[0])
 
 
+def pin_round_bf16_matches_library(O):
+    """round_bf16 against torch's float32 -> bfloat16 conversion (round to
+    nearest, ties to even), on random values and hand-picked ties."""
+    r = _rng(12)
+    x = np.concatenate([r.standard_normal(4000) * 10.0 ** r.integers(-6, 6, 4000),
+                        [1.00390625, 1.01171875, -1.00390625, 3.0, 0.0, 65504.0, 1e-30]])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.round_bf16(x), want)
+    # ties: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 -> even (1.0); 1 + 3*2^-8 -> 1 + 2^-6
+    assert O.round_bf16(np.array([1.00390625]))[0] == 1.0
+    assert O.round_bf16(np.array([1.01171875]))[0] == 1.015625
+
+
+def pin_bf16_cache_variant_is_exact_on_representable_data(O):
+    """When every cache component is exactly representable in bf16 (small
+    integers), the bf16-cache variant equals the exact materialisation."""
+    r = _rng(13)
+    h, Hkv, d, rank = 16, 2, 8, 2
+    X = r.integers(-2, 3, size=(9, h)).astype(np.float64)
+    W = {k: r.integers(0, 2, size=(h, n)).astype(np.float64)
+         for k, n in (("W_K", Hkv * d), ("W_V", Hkv * d), ("A_K", rank), ("A_V", rank))}
+    BK = r.standard_normal((rank, Hkv * d))
+    BV = r.standard_normal((rank, Hkv * d))
+    pos = np.zeros(9, dtype=int)  # position 0: the rotation is the identity, K_base stays integer
+    k1, v1 = O.agent_kv(X, pos, W["W_K"], W["W_V"], W["A_K"], W["A_V"], BK, BV, Hkv, d, 10000.0)
+    k2, v2 = O.agent_kv_from_cache(X, pos, W["W_K"], W["W_V"], W["A_K"], W["A_V"], BK, BV, Hkv, d, 10000.0)
+    assert np.allclose(k1, k2, rtol=1e-13, atol=1e-13) and np.allclose(v1, v2, rtol=1e-13, atol=1e-13)
+    # and on general data the two differ by about the bf16 spacing
+    Xg = r.standard_normal((9, h))
+    pg = np.arange(9)
+    k1, _ = O.agent_kv(Xg, pg, W["W_K"], W["W_V"], W["A_K"], W["A_V"], BK, BV, Hkv, d, 10000.0)
+    k2, _ = O.agent_kv_from_cache(Xg, pg, W["W_K"], W["W_V"], W["A_K"], W["A_V"], BK, BV, Hkv, d, 10000.0)
+    rel = np.abs(k1 - k2).max() / np.abs(k1).max()
+    assert 1e-5 < rel < 2 ** -7, rel
+
+
 ALL_PINS = [
     pin_rope_closed_form, pin_rope_frequencies, pin_rope_invariants,
     pin_attention_sdpa_decode, pin_attention_sdpa_prefill, pin_attention_brute_force,
     pin_attention_special_cases, pin_lora_closed_form, pin_merged_weights,
     pin_reordered_equals_materialised, pin_base_equals_ordinary_attention,
     pin_append_integer_bruteforce, pin_prefill_last_row_equals_decode, pin_multi_agent_batch,
+    pin_round_bf16_matches_library, pin_bf16_cache_variant_is_exact_on_representable_data,
 ]

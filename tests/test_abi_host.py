@@ -1,0 +1,111 @@
+"""Host-only checks of the C ABI (no GPU needed): the library loads, exports every
+entry point that include/lrkv.h declares, and rejects bad arguments before any
+launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rank_cache_attention_flash_b300 import build as B
+from rank_cache_attention_flash_b300 import lrkv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lrkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return lrkv.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lrkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("lrkv_append", "lrkv_attn_decode", "lrkv_attn_prefill", "lrkv_decode_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in lrkv.h but not exported"
+    assert set(lrkv.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    for code, name in lrkv.STATUS.items():
+        assert lrkv.status_string(code) == name
+    assert lrkv.status_string(77) == "LRKV_UNKNOWN_STATUS"
+    assert lrkv.version() >= 100
+
+
+def _cfg(**kw):
+    base = dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, rank=8, block_size=16,
+                rope_base=10000.0, dtype=0)
+    base.update(kw)
+    return lrkv.Config(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), 2), (dict(rank=12), 2), (dict(block_size=32), 2), (dict(dtype=5), 2),
+    (dict(n_q_heads=5), 1), (dict(hidden=0), 1), (dict(rope_base=0.0), 1), (dict(hidden=100), 2),
+    (dict(n_q_heads=64, n_kv_heads=2), 2),
+])
+def test_bad_config_rejected_before_launch(lib, kw, code):
+    cfg = _cfg(**kw)
+    r = lib.lrkv_append(ctypes.byref(cfg), 16, 1, 16, 16, 16, 1, 1, 16, 16, 16, 1, None, None)
+    assert r == code
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    cfg = _cfg()
+    P = 1 << 20  # a fake, 16-byte aligned address: never dereferenced on these paths
+    # append: null X
+    assert lib.lrkv_append(ctypes.byref(cfg), None, 4, P, P, P, 1, 1, P, P, P, 1, None, None) == 1
+    # append: misaligned X
+    assert lib.lrkv_append(ctypes.byref(cfg), P + 2, 4, P, P, P, 1, 1, P, P, P, 1, None, None) == 1
+    # append: T = 0 is a no-op
+    assert lib.lrkv_append(ctypes.byref(cfg), None, 0, None, None, None, 0, 0, None, None, None, 0,
+                           None, None) == 0
+    # append: negative T
+    assert lib.lrkv_append(ctypes.byref(cfg), P, -1, P, P, P, 1, 1, P, P, P, 1, None, None) == 1
+    # decode: null q
+    args = [ctypes.byref(cfg), None, 2, P, 1, P, P, 4, P, 64, 2, P, P, 8, P, P, 2, 0.125, P, P, 1 << 20,
+            None, None]
+    assert lib.lrkv_attn_decode(*args) == 1
+    # decode: no queries is a no-op
+    args0 = list(args)
+    args0[2] = 0
+    assert lib.lrkv_attn_decode(*args0) == 0
+    # decode: adapters given but n_adapters == 0
+    args2 = list(args)
+    args2[1] = P
+    args2[16] = 0
+    assert lib.lrkv_attn_decode(*args2) == 1
+    # decode: max_ctx_len beyond the block table
+    args3 = list(args)
+    args3[1] = P
+    args3[9] = 4 * 16 + 1
+    assert lib.lrkv_attn_decode(*args3) == 1
+    # prefill: null seq_lens
+    pargs = [ctypes.byref(cfg), P, P, 1, 8, 8, None, 64, P, P, 4, P, P, 8, P, P, 2, 0.125, P, None, 0,
+             None, None]
+    assert lib.lrkv_attn_prefill(*pargs) == 1
+    # prefill: max_seq_len < max_q_len
+    pargs2 = list(pargs)
+    pargs2[6] = P
+    pargs2[7] = 4
+    assert lib.lrkv_attn_prefill(*pargs2) == 1
+
+
+def test_positions_limit_rejected(lib):
+    cfg = _cfg()
+    P = 1 << 20
+    # max_blocks * 16 above 2^20 positions
+    r = lib.lrkv_append(ctypes.byref(cfg), P, 4, P, P, P, 1, (1 << 16) + 1, P, P, P, 10, None, None)
+    assert r == 2

@@ -48,7 +48,7 @@ MUTATIONS = {
     "causal_strict": ("np.arange(L)[None, :] <= qp[:, None]", "np.arange(L)[None, :] < qp[:, None]"),
     "causal_peek_ahead": ("np.arange(L)[None, :] <= qp[:, None]", "np.arange(L)[None, :] <= qp[:, None] + 1"),
     "no_softmax_scale": ("(q[:, m, :] @ K[:, kv, :].T) * scale", "(q[:, m, :] @ K[:, kv, :].T)"),
-    "key_positions_shifted": ("agent_kv(X_seq, np.arange(L),", "agent_kv(X_seq, np.arange(1, L + 1),"),
+    "key_positions_shifted": ("make(X_seq, np.arange(L),", "make(X_seq, np.arange(1, L + 1),"),
     "prefill_positions_shifted": ("np.arange(L - n, L)", "np.arange(L - n - 1, L - 1)"),
     "decode_position_shifted": ("np.asarray(q)[n: n + 1], [L - 1]", "np.asarray(q)[n: n + 1], [L - 2]"),
     "append_row_shifted": ("row = p % BLOCK", "row = (p + 1) % BLOCK"),
@@ -56,6 +56,10 @@ MUTATIONS = {
                            "blk = int(block_tables[s][(p // BLOCK + 1) % len(block_tables[s])])"),
     "adapter_off_by_one": ('return weights["B_K"][adapter], weights["B_V"][adapter]',
                            'return weights["B_K"][adapter - 1], weights["B_V"][adapter - 1]'),
+    "bf16_truncation": ("u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000", "u = u & 0xFFFF0000"),
+    "bf16_ties_away": ("u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000", "u = (u + 0x8000) & 0xFFFF0000"),
+    "cache_variant_drops_rope": ("k = k + apply_rope((lk @ _f64(B_K_i)).reshape(T, n_kv_heads, head_dim), positions, base)",
+                                 "k = k + (lk @ _f64(B_K_i)).reshape(T, n_kv_heads, head_dim)"),
     "swapped_B": ('return weights["B_K"][adapter], weights["B_V"][adapter]',
                   'return weights["B_V"][adapter], weights["B_K"][adapter]'),
 }
