@@ -8,8 +8,11 @@ inputs already resident in HBM: for the decode workloads the decode call
 (split-KV attention + combine); for the prefill workload the append of the new
 chunk tokens plus the causal prefill; for the mixed batch append + decode +
 prefill. L2 is flushed (a 512 MiB write) before every step, outside the timed
-events; each step is bracketed by CUDA events on the launching stream and the
-K steps are bracketed by a barrier and a device synchronize. Rank 0 prints one
+events; each part of the step is captured once into a CUDA graph (the same
+library calls, the same kernels) and replayed, each replay bracketed by CUDA
+events on the launching stream; the K steps are bracketed by a barrier and a
+device synchronize. The e2e figure instead calls the public API directly,
+host buffers and copies included. Rank 0 prints one
 JSON line. ``--impl reference`` times the fp64 CPU oracle instead (on the host
 cores, rank 0 only).
 """
@@ -136,19 +139,21 @@ class ClockSampler:
                 self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
         except Exception as e:  # NVML missing: report no samples
-            self.error = str(e)
+            self.error = f"{type(e).__name__}: {e}"
 
     def _run(self):
         nv = self._nv
+        reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                r = reasons(self._h)
                 for bit, name in self.REASONS.items():
                     if r & bit and bit != 0x1:
                         self.reasons.add(name)
-            except Exception:
-                pass
+            except Exception as e:
+                self.error = f"{type(e).__name__}: {e}"
             time.sleep(self.interval)
 
     def __enter__(self):
@@ -164,8 +169,29 @@ class ClockSampler:
 
     def summary(self):
         med = statistics.median(self.samples) if self.samples else None
-        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        out = {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+               "samples": len(self.samples)}
+        if getattr(self, "error", None):
+            out["error"] = self.error
+        return out
+
+
+def reduce_step_time(total_ms_local: float, steps: int, world: int, device=None) -> float:
+    """Per-step time of the whole job: the max over ranks of each rank's summed
+    step time, divided by the step count (torch.distributed, any backend)."""
+    import torch
+
+    t = torch.tensor([total_ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item()) / steps
+
+
+def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Units processed by all ranks per second (weak scaling: each rank its own replica)."""
+    return world * units_per_rank / (ms_per_step / 1e3)
 
 
 def oracle_threads() -> int:
@@ -356,17 +382,34 @@ def main():
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     calls = {"append": g.step_append, "decode": g.decode, "prefill": g.prefill}
 
-    def one_step(evs=None):
+    def one_step(evs=None, replay=False):
         for k in kinds:
             if evs is not None:
                 evs[k][0].record(stream)
-            calls[k]()
+            if replay:
+                graphs[k].replay()
+            else:
+                calls[k]()
             if evs is not None:
                 evs[k][1].record(stream)
 
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         one_step()
+    torch.cuda.synchronize()
+    # Each part of the step is captured once into a CUDA graph and replayed in
+    # the timed loop: the replay keeps host launch latency out of the device
+    # timings (the kernels and their arguments are exactly the API call's).
+    graphs = {}
+    for k in kinds:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            calls[k]()
+        graphs[k] = gr
+    for i in range(3):
+        flush.fill_(i & 0xFF)
+        for k in kinds:
+            graphs[k].replay()
     torch.cuda.synchronize()
     K = args.steps
     evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in kinds}
@@ -380,7 +423,7 @@ def main():
         for i in range(K):
             flush.fill_(i & 0xFF)
             step_ev[i][0].record(stream)
-            one_step(evs[i])
+            one_step(evs[i], replay=True)
             step_ev[i][1].record(stream)
         torch.cuda.synchronize()
     host_dt = time.perf_counter() - host_t0
@@ -388,10 +431,7 @@ def main():
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     part_ms = {k: [e[k][0].elapsed_time(e[k][1]) for e in evs] for k in kinds}
-    total_ms = torch.tensor([sum(step_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(total_ms, op=dist.ReduceOp.MAX)
-    ms_per_step = float(total_ms.item()) / K
+    ms_per_step = reduce_step_time(sum(step_ms), K, world, dev)
     status = g.device_status()
 
     # ---- end to end through the public API with host buffers
@@ -471,13 +511,13 @@ def main():
                 "traffic": committed_traffic(args.config, "prefill")}
 
     if dominant == "decode" and "prefill" not in model:
-        unit, value = "tok/s", world * dm["units"] / (ms_per_step / 1e3)
+        unit, value = "tok/s", job_throughput(dm["units"], world, ms_per_step)
     elif "decode" not in model:
         unit = "TFLOP/s"
         value = world * (model["prefill"]["flops"] + model.get("append", {"flops": 0})["flops"]) / (ms_per_step / 1e3) / 1e12
     else:
         unit = "tok/s"
-        value = world * (model["decode"]["units"] + model["prefill"]["units"]) / (ms_per_step / 1e3)
+        value = job_throughput(model["decode"]["units"] + model["prefill"]["units"], world, ms_per_step)
     if e2e is None:
         if unit == "TFLOP/s":
             ev = world * (model["prefill"]["flops"] + model.get("append", {"flops": 0})["flops"]) / (e2e_ms / 1e3) / 1e12

@@ -11,16 +11,20 @@
 //     O   += P V_base,  O_lr += P L_V         (the V term reordered: (P L_V) B_V
 //                                              is applied once, after the merge)
 // The kernel is persistent: each CTA walks work items (context, query group,
-// split of the context's blocks, kv head). One producer warp streams the
-// blocks' K/V halves and L_K/L_V tiles with 2-D TMA copies (128-byte swizzle)
-// through a ring of mbarrier-guarded stages; four consumer warps take one
-// block each per stage with legacy warp MMAs (m16n8k16, fp32 accumulators),
-// whose fragments let the rebuilt K stay in registers through RoPE, the base
-// add and the score MMA. Each item ends by merging the warps' (m, l, O, O_lr)
-// and writing an fp32 partial; lrkv_combine merges the splits and applies B_V.
+// split of the context's blocks, kv head; kv head fastest so that concurrent
+// CTAs share the low-rank tiles through L2). Its eight warps take the item's
+// blocks round-robin; each warp streams its own blocks (K/V halves with a
+// 128-byte swizzle, L_K / L_V tiles) through a private two-stage ring of 2-D
+// TMA copies completed on mbarriers, fetching block ids one step ahead and
+// crossing item boundaries without draining. Scores of every adapter
+// accumulate into one fragment: the query fragment is masked to that
+// adapter's rows. Each item ends by merging the warps' (m, l, O, O_lr) in a
+// fixed order and writing an fp32 partial; combine_kernel (launched with
+// programmatic dependent launch) merges the splits and applies B_V.
 #include <math_constants.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "lrkv_device.cuh"
 #include "lrkv_internal.h"
@@ -28,10 +32,11 @@
 namespace lrkv {
 namespace {
 
-constexpr int kNW = 4;                    // consumer warps
-constexpr int kThreads = (kNW + 1) * 32;  // + one producer warp
-constexpr int kMaxRows = 16;              // query rows (queries x heads) per item
-constexpr int kMaxSlots = 4;              // distinct adapters per item
+constexpr int kNW = 8;               // warps per CTA (all consume; lane 0 of each issues its TMA)
+constexpr int kThreads = kNW * 32;
+constexpr int kNST = 2;              // stages per warp
+constexpr int kMaxRows = 16;         // query rows (queries x heads) per item
+constexpr int kMaxSlots = 4;         // distinct adapters per item
 constexpr int kSmemLimit = 227 * 1024;
 
 struct DecodeParams {
@@ -47,7 +52,7 @@ struct DecodeParams {
   int64_t num_blocks;
   int64_t n_items;
   int max_blocks, max_ctx_len, n_adapters, num_ctx, Hq, Hkv, g;
-  int qg_size, n_qgroups, n_splits, split_blocks, nstage;
+  int qg_size, n_qgroups, n_splits, split_blocks;
   int has_bk, has_bv;
   float scale_log2;
   RopeFreqs freqs;
@@ -55,28 +60,29 @@ struct DecodeParams {
 
 // Shared-memory layout (byte offsets from a 1024-aligned base).
 struct Layout {
-  int kv_tile, lr_tile, stage, bk_pitch, bk_slot, d_pitch, acc_pitch;
-  int off_bk, off_dtab, off_btab, off_freq, off_acc, off_ml, off_misc, off_bar, total;
-  __host__ __device__ static Layout make(int D, int R, int nstage, int slots) {
+  int kv_tile, lr_tile, blk, bk_pitch, bk_slot, d_pitch, acc_pitch;
+  int off_bk, off_dtab, off_btab, off_freq, off_ml, off_misc, off_bar, total;
+  __host__ __device__ static Layout make(int D, int R, int slots) {
     Layout L;
     L.kv_tile = 16 * D * 2;
     L.lr_tile = 16 * R * 2;
-    L.stage = kNW * (2 * L.kv_tile + 2 * L.lr_tile);
-    L.bk_pitch = (D + 8) * 2;        // bytes per B_K row in smem (conflict-free ldmatrix)
+    L.blk = ((2 * L.kv_tile + 2 * L.lr_tile) + 1023) & ~1023;  // one block: K, V, L_K, L_V
+    L.bk_pitch = (D + 8) * 2;      // bytes per B_K row in smem (conflict-free ldmatrix)
     L.bk_slot = R * L.bk_pitch;
-    L.d_pitch = (D / 2) * 8 + 64;    // delta-table row: D/2 float2 + pad
-    L.acc_pitch = D + R + 4;         // floats
-    int o = nstage * L.stage;
-    L.off_bk = o;   o += slots * L.bk_slot;
+    L.d_pitch = (D / 2) * 8 + 64;  // delta-table row: D/2 float2 + pad
+    L.acc_pitch = D + R + 4;       // floats (merge accumulator, aliases the B_K slots)
+    int o = kNW * kNST * L.blk;
+    L.off_bk = o;
+    const int bk = slots * L.bk_slot, acc = kMaxRows * L.acc_pitch * 4;
+    o += bk > acc ? bk : acc;
     o = (o + 15) & ~15;
     L.off_dtab = o; o += 16 * L.d_pitch;
     L.off_btab = o; o += kNW * (D / 2) * 8;
     L.off_freq = o; o += 2 * 64 * 4;
-    L.off_acc = o;  o += kMaxRows * L.acc_pitch * 4;
     L.off_ml = o;   o += 2 * kNW * kMaxRows * 4 + 2 * kMaxRows * 4;
     L.off_misc = o; o += 64;
     o = (o + 7) & ~7;
-    L.off_bar = o;  o += 2 * nstage * 8;
+    L.off_bar = o;  o += kNW * kNST * 8;
     L.total = o + 1024;  // alignment slack
     return L;
   }
@@ -111,6 +117,37 @@ __device__ __forceinline__ Item get_item(const DecodeParams& p, int64_t it) {
   return I;
 }
 
+// A warp's walk over its (item, block) pairs: items it = blockIdx.x + k * gridDim.x,
+// blocks kbeg + warp, kbeg + warp + kNW, ... of each active item.
+struct Walk {
+  int64_t it;
+  int kb;
+  Item I;
+  bool more;
+};
+
+__device__ __forceinline__ void walk_next(const DecodeParams& p, int warp, Walk& w) {
+  w.kb += kNW;
+  while (!(w.I.active && w.kb < w.I.kend)) {
+    w.it += gridDim.x;
+    if (w.it >= p.n_items) {
+      w.more = false;
+      return;
+    }
+    w.I = get_item(p, w.it);
+    w.kb = w.I.kbeg + warp;
+  }
+  w.more = true;
+}
+
+__device__ __forceinline__ void walk_init(const DecodeParams& p, int warp, Walk& w) {
+  w.it = static_cast<int64_t>(blockIdx.x) - gridDim.x;
+  w.I.active = false;
+  w.I.kend = 0;
+  w.kb = 0;
+  walk_next(p, warp, w);
+}
+
 template <int D, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p,
@@ -123,191 +160,153 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NLR = R / 8;    // O_lr n-tiles
   constexpr int LR_RB = R * 2;  // low-rank tile row bytes
 
+  // The combine kernel may be scheduled now; it waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const Layout L = Layout::make(D, R, p.nstage, p.qg_size);
+  const Layout L = Layout::make(D, R, p.qg_size);
   const uint32_t sbase = smem_u32(smem);
   float2* dtab = reinterpret_cast<float2*>(smem + L.off_dtab);
   float* freq = reinterpret_cast<float*>(smem + L.off_freq);
-  float* acc = reinterpret_cast<float*>(smem + L.off_acc);
+  float* acc = reinterpret_cast<float*>(smem + L.off_bk);  // merge accumulator (aliases B_K)
   float* sm_m = reinterpret_cast<float*>(smem + L.off_ml);
   float* sm_l = sm_m + kNW * kMaxRows;
   float* sm_M = sm_l + kNW * kMaxRows;
   float* sm_L = sm_M + kMaxRows;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_misc);
-  int* stage_mask = reinterpret_cast<int*>(smem + L.off_misc + 16);  // nstage <= 8
-  const uint32_t bar_full = sbase + L.off_bar;
-  const uint32_t bar_empty = bar_full + 8 * p.nstage;
+  int* slot_ad_s = reinterpret_cast<int*>(smem + L.off_misc + 16);  // [kMaxSlots]
+  int* slot_rn_s = slot_ad_s + kMaxSlots;                             // [kMaxSlots]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, c4 = lane & 3;
+  const uint32_t bar0 = sbase + L.off_bar + warp * kNST * 8;  // this warp's ring barriers
+  const uint32_t ring0 = sbase + warp * kNST * L.blk;           // this warp's ring
 
   // ---- CTA prologue: frequencies, delta table, barriers
   if (tid < HALF) {
     freq[tid] = p.freqs.hi[tid];
     freq[64 + tid] = p.freqs.lo[tid];
   }
-  if (tid == 0) {
-    *abort_flag = 0;
-    for (int s = 0; s < p.nstage; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kNW);
-    }
+  if (tid == 0) *abort_flag = 0;
+  if (lane == 0) {
+    for (int s = 0; s < kNST; ++s) mbar_init(bar0 + 8 * s, 1);
     mbar_fence_init();
   }
   __syncthreads();
   for (int i = tid; i < 16 * HALF; i += kThreads) {
     const int dl = i / HALF, j = i % HALF;
-    float2 cs = rope_cos_sin(dl, freq[j], freq[64 + j]);
-    *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(dtab) + dl * L.d_pitch + j * 8) = cs;
+    *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(dtab) + dl * L.d_pitch + j * 8) =
+        rope_cos_sin(dl, freq[j], freq[64 + j]);
+  }
+  if (lane == 0) {
+    prefetch_tmap(&tm_base);
+    prefetch_tmap(&tm_lr);
   }
   __syncthreads();
 
-  // ======================================================== producer warp
-  if (warp == kNW) {
+  // ---- this warp's TMA ring: issue walk (lane 0 holds the next block id)
+  Walk wi;
+  walk_init(p, warp, wi);
+  int pend_id = -1;
+  if (lane == 0 && wi.more)
+    pend_id = __ldg(p.block_tables + static_cast<int64_t>(wi.I.ctx) * p.max_blocks + wi.kb);
+  uint32_t issued = 0, consumed = 0;
+  uint32_t valid_bits = 0;  // bit s: stage s holds a loaded block
+  const uint32_t lr_bytes = (p.has_bk ? L.lr_tile : 0) + (p.has_bv ? L.lr_tile : 0);
+
+  auto issue_one = [&]() {
+    if (!wi.more) return;
+    const int s = issued % kNST;
+    int ok = 0;
     if (lane == 0) {
-      prefetch_tmap(&tm_base);
-      prefetch_tmap(&tm_lr);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0;  // bit s: stage s ever armed
-      bool ok = true;
-      for (int64_t it = blockIdx.x; ok && it < p.n_items; it += gridDim.x) {
-        const Item I = get_item(p, it);
-        if (!I.active) continue;
-        for (int kb = I.kbeg; kb < I.kend; kb += kNW) {
-          if (*abort_flag || !mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status)) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          int mask = 0;
-          int blks[kNW];
-          uint32_t bytes = 0;
+      const int blk = pend_id;
+      if (blk < 0 || blk >= p.num_blocks) {
+        report(p.status, LRKV_ERR_INDEX);
+        mbar_arrive(bar0 + 8 * s);  // complete this stage's phase without data
+      } else {
+        ok = 1;
+        const uint32_t fb = bar0 + 8 * s;
+        mbar_arrive_expect_tx(fb, 2 * L.kv_tile + lr_bytes);
+        const uint32_t kt = ring0 + s * L.blk, vt = kt + L.kv_tile;
+        const uint32_t lk = kt + 2 * L.kv_tile, lv = lk + L.lr_tile;
+        const int yk = ((blk * 2 + 0) * p.Hkv + wi.I.head) * kBlock;
+        const int yv = ((blk * 2 + 1) * p.Hkv + wi.I.head) * kBlock;
 #pragma unroll
-          for (int w = 0; w < kNW; ++w) {
-            blks[w] = -1;
-            const int b = kb + w;
-            if (b >= I.kend) continue;
-            const int blk = __ldg(p.block_tables + static_cast<int64_t>(I.ctx) * p.max_blocks + b);
-            if (blk < 0 || blk >= p.num_blocks) {
-              report(p.status, LRKV_ERR_INDEX);
-              continue;
-            }
-            blks[w] = blk;
-            mask |= 1 << w;
-            bytes += 2 * L.kv_tile + (p.has_bk ? L.lr_tile : 0) + (p.has_bv ? L.lr_tile : 0);
-          }
-          stage_mask[stage] = mask;
-          const uint32_t fb = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(fb, bytes);
-          issued |= 1u << stage;
-          const uint32_t st = sbase + stage * L.stage;
-#pragma unroll
-          for (int w = 0; w < kNW; ++w) {
-            if (blks[w] < 0) continue;
-            const int blk = blks[w];
-            const int yk = ((blk * 2 + 0) * p.Hkv + I.head) * kBlock;
-            const int yv = ((blk * 2 + 1) * p.Hkv + I.head) * kBlock;
-            const uint32_t kt = st + w * L.kv_tile;
-            const uint32_t vt = st + kNW * L.kv_tile + w * L.kv_tile;
-#pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-              tma_load_2d(kt + h * 2048, &tm_base, 64 * h, yk, fb);
-              tma_load_2d(vt + h * 2048, &tm_base, 64 * h, yv, fb);
-            }
-            const uint32_t lk = st + 2 * kNW * L.kv_tile + w * L.lr_tile;
-            const uint32_t lv = lk + kNW * L.lr_tile;
-            if (p.has_bk) tma_load_2d(lk, &tm_lr, 0, (blk * 2 + 0) * kBlock, fb);
-            if (p.has_bv) tma_load_2d(lv, &tm_lr, 0, (blk * 2 + 1) * kBlock, fb);
-          }
-          if (++stage == p.nstage) {
-            stage = 0;
-            phase ^= 1;
-          }
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_2d(kt + h * 2048, &tm_base, 64 * h, yk, fb);
+          tma_load_2d(vt + h * 2048, &tm_base, 64 * h, yv, fb);
         }
-      }
-      // Drain: never leave the CTA with copies in flight (bounded waits).
-      if (!ok) {
-        for (int s = 0; s < p.nstage; ++s)
-          if (issued >> s & 1) {
-            const uint32_t par = (s < stage) ? phase : (phase ^ 1);
-            mbar_wait(bar_full + 8 * s, par, nullptr, 1u << 16);
-          }
+        if (p.has_bk) tma_load_2d(lk, &tm_lr, 0, (blk * 2 + 0) * kBlock, fb);
+        if (p.has_bv) tma_load_2d(lv, &tm_lr, 0, (blk * 2 + 1) * kBlock, fb);
       }
     }
-    return;
-  }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    valid_bits = ok ? (valid_bits | (1u << s)) : (valid_bits & ~(1u << s));
+    ++issued;
+    walk_next(p, warp, wi);
+    if (lane == 0 && wi.more)
+      pend_id = __ldg(p.block_tables + static_cast<int64_t>(wi.I.ctx) * p.max_blocks + wi.kb);
+  };
+  for (int s = 0; s < kNST; ++s) issue_one();
 
-  // ======================================================= consumer warps
   float2* btab = reinterpret_cast<float2*>(smem + L.off_btab) + warp * HALF;
-  int stage = 0;
-  uint32_t phase = 0;
 
   for (int64_t it = blockIdx.x; it < p.n_items; it += gridDim.x) {
     const Item I = get_item(p, it);
     if (!I.active) continue;
     const int rows = I.nq * p.g;
+
+    __syncthreads();  // previous item's merge finished with the B_K / acc region
+
+    // --- distinct adapters of this query group -> smem (thread 0), per-lane row slots
+    if (tid == 0) {
+      int n = 0, ad[kMaxSlots], rn_mask[kMaxSlots];
+      for (int qi = 0; qi < I.nq; ++qi) {
+        int a = __ldg(p.adapter_ids + I.q0 + qi);
+        if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;  // bad ids: reported by the combine
+        int s = -1;
+        for (int k = 0; k < n; ++k)
+          if (ad[k] == a) s = k;
+        if (s < 0) {
+          s = n++;
+          ad[s] = a;
+          rn_mask[s] = 0;
+        }
+        for (int gi = 0; gi < p.g; ++gi) rn_mask[s] |= 1 << ((qi * p.g + gi) >> 3);
+      }
+      for (int k = 0; k < kMaxSlots; ++k) {
+        slot_ad_s[k] = k < n ? ad[k] : -2;
+        slot_rn_s[k] = k < n ? rn_mask[k] : 0;
+      }
+    }
+    __syncthreads();
+    int nslots = 0;
+    bool any_rebuild = false;
+#pragma unroll
+    for (int k = 0; k < kMaxSlots; ++k) {
+      const int a = slot_ad_s[k];
+      if (a != -2) ++nslots;
+      if (a >= 0) any_rebuild = true;
+    }
+    // slot of the query row held by this lane in the score B fragment: row rn*8 + g8
+    int myslot[2];
+#pragma unroll
+    for (int rn = 0; rn < 2; ++rn) {
+      const int row = rn * 8 + g8;
+      myslot[rn] = -1;
+      if (row < rows) {
+        int a = __ldg(p.adapter_ids + I.q0 + row / p.g);
+        if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;
+#pragma unroll
+        for (int k = 0; k < kMaxSlots; ++k)
+          if (slot_ad_s[k] == a) myslot[rn] = k;
+      }
+    }
     const int RN = rows > 8 ? 2 : 1;
 
-    named_bar_sync(1, kNW * 32);  // previous item's merge finished with smem
-
-    // --- distinct adapters of this query group (warp-uniform)
-    int slot_ad[kMaxSlots];
-    int nslots = 0;
-    int qslot[kMaxSlots];  // slot of query qi (qi < qg_size <= kMaxSlots)
-#pragma unroll
-    for (int i = 0; i < kMaxSlots; ++i) { slot_ad[i] = -1; qslot[i] = 0; }
-#pragma unroll
-    for (int qi = 0; qi < kMaxSlots; ++qi) {
-      if (qi >= I.nq) break;
-      int a = __ldg(p.adapter_ids + I.q0 + qi);
-      if (a < -1 || a >= p.n_adapters) a = -1;  // reported by the combine
-      if (!p.has_bk) a = -1;
-      int s = -1;
-#pragma unroll
-      for (int k = 0; k < kMaxSlots; ++k)
-        if (k < nslots && slot_ad[k] == a) s = k;
-      if (s < 0) {
-        s = nslots++;
-#pragma unroll
-        for (int k = 0; k < kMaxSlots; ++k)
-          if (k == s) slot_ad[k] = a;
-      }
-#pragma unroll
-      for (int k = 0; k < kMaxSlots; ++k)
-        if (k == qi) qslot[k] = s;
-    }
-    // slot of this lane's score columns (rows rn*8 + 2*c4 + e) and per-slot row-tile mask
-    int rslot[2][2];
-    int slot_rn[kMaxSlots];
-#pragma unroll
-    for (int k = 0; k < kMaxSlots; ++k) slot_rn[k] = 0;
-#pragma unroll
-    for (int rn = 0; rn < 2; ++rn)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int row = rn * 8 + 2 * c4 + e;
-        const int qi = row < rows ? row / p.g : 0;
-        int s = 0;
-#pragma unroll
-        for (int k = 0; k < kMaxSlots; ++k)
-          if (k == qi) s = qslot[k];
-        rslot[rn][e] = s;
-      }
-    for (int row = 0; row < rows; ++row) {
-      const int qi = row / p.g;
-      int s = 0;
-#pragma unroll
-      for (int k = 0; k < kMaxSlots; ++k)
-        if (k == qi) s = qslot[k];
-#pragma unroll
-      for (int k = 0; k < kMaxSlots; ++k)
-        if (k == s) slot_rn[k] |= 1 << (row >> 3);
-    }
-
-    // --- query fragments (B operand of S^T = K Q^T), straight from global
+    // --- query fragments (B operand of S^T = K Q^T), fp16, straight from global
     uint32_t qf[2][NKS][2];
 #pragma unroll
     for (int rn = 0; rn < 2; ++rn) {
@@ -322,29 +321,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         qf[rn][ks][1] = ok ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8))) : 0u;
       }
     }
-
     // --- B_K slices of the rebuild slots -> smem [slot][k][D] (padded rows)
     {
-      const int ctid = tid;  // 0 .. kNW*32-1
       constexpr int VPR = D / 8;  // 16-byte vectors per row
       for (int s = 0; s < nslots; ++s) {
-        if (slot_ad[s] < 0) continue;
-        const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(slot_ad[s]) * R * p.Hkv * D +
+        const int a = slot_ad_s[s];
+        if (a < 0) continue;
+        const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(a) * R * p.Hkv * D +
                                    static_cast<int64_t>(I.head) * D;
         uint8_t* dst = smem + L.off_bk + s * L.bk_slot;
-        for (int i = ctid; i < R * VPR; i += kNW * 32) {
+        for (int i = tid; i < R * VPR; i += kThreads) {
           const int k = i / VPR, v = i % VPR;
           const uint4 val = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v);
           *reinterpret_cast<uint4*>(dst + k * L.bk_pitch + v * 16) = val;
         }
       }
     }
-    named_bar_sync(1, kNW * 32);
-
-    bool any_rebuild = false;
-#pragma unroll
-    for (int k = 0; k < kMaxSlots; ++k)
-      if (k < nslots && slot_ad[k] >= 0) any_rebuild = true;
+    __syncthreads();
 
     float O[D / 8][4];
     float Olr[NLR][4];
@@ -358,21 +351,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 2; ++e) { m_run[rn][e] = -CUDART_INF_F; l_run[rn][e] = 0.f; }
 
-    if (I.len == 0 && c4 == 0 && g8 == 0 && warp == 0) report(p.status, LRKV_ERR_INDEX);
+    if (I.len == 0 && tid == 0) report(p.status, LRKV_ERR_INDEX);
 
     // ------------------------------------------------------ block sweep
-    for (int kb = I.kbeg; kb < I.kend; kb += kNW) {
-      bool ok = !(*abort_flag) && mbar_wait(bar_full + 8 * stage, phase, p.status);
-      if (!ok) *abort_flag = 1;
-      const int mask = ok ? stage_mask[stage] : 0;
-      const int b = kb + warp;
-      if (b < I.kend && (mask >> warp & 1)) {
+    for (int b = I.kbeg + warp; b < I.kend; b += kNW) {
+      const int s = consumed % kNST;
+      const uint32_t par = (consumed / kNST) & 1;
+      const bool have = (valid_bits >> s) & 1;
+      // every wait result below is made warp-uniform before any warp-collective use
+      bool ok = have && !__shfl_sync(0xffffffffu, *abort_flag, 0);
+      if (ok) ok = mbar_wait(bar0 + 8 * s, par, p.status);
+      ok = have && __all_sync(0xffffffffu, ok);
+      if (have && !ok) *abort_flag = 1;
+      if (ok) {
         const int t0 = b * kBlock;
-        const uint32_t st = sbase + stage * L.stage;
-        const uint32_t kt = st + warp * L.kv_tile;
-        const uint32_t vt = st + kNW * L.kv_tile + warp * L.kv_tile;
-        const uint32_t lkt = st + 2 * kNW * L.kv_tile + warp * L.lr_tile;
-        const uint32_t lvt = lkt + kNW * L.lr_tile;
+        const uint32_t kt = ring0 + s * L.blk, vt = kt + L.kv_tile;
+        const uint32_t lkt = kt + 2 * L.kv_tile, lvt = lkt + L.lr_tile;
 
         // Rows past the context end may hold stale pool memory: zero their V and
         // L_V rows so that P = 0 there cannot meet a NaN in the PV products.
@@ -388,7 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a = lvt + r * LR_RB + v * 16;
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
           }
-          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
           __syncwarp();
         }
         // base rotation of this block: e^{i t0 theta_j}
@@ -403,25 +396,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < NRT; ++ks) {
               const int mi = lane >> 3;
-              const int tok = (lane & 7) + (mi & 1) * 8;
-              const int byte = (2 * ks + (mi >> 1)) * 16;
-              ldsm_x4(alk[ks], lkt + swz<LR_RB>(tok, byte));
+              ldsm_x4(alk[ks], lkt + swz<LR_RB>((lane & 7) + (mi & 1) * 8, (2 * ks + (mi >> 1)) * 16));
             }
           } else {
             uint32_t t2[2];
-            const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
-            ldsm_x2(t2, lkt + swz<LR_RB>(tok, 0));
+            ldsm_x2(t2, lkt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
             alk[0][0] = t2[0];
             alk[0][1] = t2[1];
             alk[0][2] = alk[0][3] = 0u;
           }
         }
 
-        float sacc[kMaxSlots][2][4];
+        float sacc[2][4];
 #pragma unroll
-        for (int a = 0; a < kMaxSlots; ++a)
-#pragma unroll
-          for (int rn = 0; rn < 2; ++rn) sacc[a][rn][0] = sacc[a][rn][1] = sacc[a][rn][2] = sacc[a][rn][3] = 0.f;
+        for (int rn = 0; rn < 2; ++rn) sacc[rn][0] = sacc[rn][1] = sacc[rn][2] = sacc[rn][3] = 0.f;
 
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
@@ -453,18 +441,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-#pragma unroll
-          for (int a = 0; a < kMaxSlots; ++a) {
-            if (a >= nslots) break;
+#pragma unroll 1
+          for (int a = 0; a < nslots; ++a) {
+            const int ad = slot_ad_s[a];
+            const int rnm = slot_rn_s[a];
             uint32_t A_lo[4], A_hi[4];
-            if (slot_ad[a] >= 0) {
+            if (ad >= 0) {
               float y[4][4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.f;
               const uint32_t bk = sbase + L.off_bk + a * L.bk_slot;
               if constexpr (R >= 16) {
 #pragma unroll
-                for (int ks = 0; ks < NRT; ++ks) {
+                for (int ks = 0; ks < NRT; ++ks)
 #pragma unroll
                   for (int h = 0; h < 2; ++h) {
                     // n-tiles (2cc, 2cc+1) [+ D/16 for the rotation partners]
@@ -476,19 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma16816(y[2 * h + 0], alk[ks], bb[0], bb[1]);
                     mma16816(y[2 * h + 1], alk[ks], bb[2], bb[3]);
                   }
-                }
               } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                  const int krow = lane & 7;
                   const int ncol = 16 * cc + h * HALF + ((lane >> 3) & 1) * 8;
                   uint32_t bb[2];
-                  ldsm_x2_t(bb, bk + krow * L.bk_pitch + ncol * 2);
+                  ldsm_x2_t(bb, bk + (lane & 7) * L.bk_pitch + ncol * 2);
                   mma1688(y[2 * h + 0], alk[0][0], alk[0][1], bb[0]);
                   mma1688(y[2 * h + 1], alk[0][0], alk[0][1], bb[1]);
                 }
               }
-              // rotate the rebuilt pair (j, j + d/2), add K_base, pack bf16
+              // rotate the rebuilt pair (j, j + d/2), add K_base, pack fp16
               float klo[2][4], khi[2][4];
 #pragma unroll
               for (int n = 0; n < 2; ++n)
@@ -496,11 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                   const int tk = i >> 1, e = i & 1;
                   const float x = y[n][i], yy = y[n + 2][i];
-                  const float c = cs[tk][n][e].x, s = cs[tk][n][e].y;
+                  const float c = cs[tk][n][e].x, sn = cs[tk][n][e].y;
                   const float blo = e ? bf16_hi(kbv[n][0][tk]) : bf16_lo(kbv[n][0][tk]);
                   const float bhi = e ? bf16_hi(kbv[n][1][tk]) : bf16_lo(kbv[n][1][tk]);
-                  klo[n][i] = fmaf(x, c, fmaf(-yy, s, blo));
-                  khi[n][i] = fmaf(yy, c, fmaf(x, s, bhi));
+                  klo[n][i] = fmaf(x, c, fmaf(-yy, sn, blo));
+                  khi[n][i] = fmaf(yy, c, fmaf(x, sn, bhi));
                 }
               A_lo[0] = pack_f16(klo[0][0], klo[0][1]);
               A_lo[1] = pack_f16(klo[0][2], klo[0][3]);
@@ -520,28 +507,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               A_hi[2] = bf16x2_to_f16x2(kbv[1][1][0]);
               A_hi[3] = bf16x2_to_f16x2(kbv[1][1][1]);
             }
+            // scores of this adapter's rows only: its query fragment, other rows zeroed
 #pragma unroll
             for (int rn = 0; rn < 2; ++rn) {
-              if (!(slot_rn[a] >> rn & 1)) continue;
-              mma16816_f16(sacc[a][rn], A_lo, qf[rn][cc][0], qf[rn][cc][1]);
-              mma16816_f16(sacc[a][rn], A_hi, qf[rn][cc + NCH][0], qf[rn][cc + NCH][1]);
+              if (!((rnm >> rn) & 1)) continue;
+              const bool mine = myslot[rn] == a;
+              const uint32_t q0 = mine ? qf[rn][cc][0] : 0u, q1 = mine ? qf[rn][cc][1] : 0u;
+              const uint32_t q2 = mine ? qf[rn][cc + NCH][0] : 0u, q3 = mine ? qf[rn][cc + NCH][1] : 0u;
+              mma16816_f16(sacc[rn], A_lo, q0, q1);
+              mma16816_f16(sacc[rn], A_hi, q2, q3);
             }
           }
         }
 
-        // ---- pick each score column from its own adapter's accumulator; mask; scale
-        float s[2][4];
+        // ---- mask and scale
+        float sv[2][4];
 #pragma unroll
         for (int rn = 0; rn < 2; ++rn)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int e = i & 1;
-            float v = sacc[0][rn][i];
-#pragma unroll
-            for (int a = 1; a < kMaxSlots; ++a)
-              if (rslot[rn][e] == a) v = sacc[a][rn][i];
             const int tok = t0 + g8 + 8 * (i >> 1);
-            s[rn][i] = tok < I.len ? v * p.scale_log2 : -CUDART_INF_F;
+            sv[rn][i] = tok < I.len ? sacc[rn][i] * p.scale_log2 : -CUDART_INF_F;
           }
         // ---- online softmax (per score column = query row)
         float alpha[2][2];
@@ -550,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rn = 0; rn < 2; ++rn)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(s[rn][e], s[rn][e + 2]);
+            float mx = fmaxf(sv[rn][e], sv[rn][e + 2]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -560,8 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               al = 1.f; p0 = 0.f; p1 = 0.f;
             } else {
               al = exp2f(m_run[rn][e] - mn);
-              p0 = exp2f(s[rn][e] - mn);
-              p1 = exp2f(s[rn][e + 2] - mn);
+              p0 = exp2f(sv[rn][e] - mn);
+              p1 = exp2f(sv[rn][e + 2] - mn);
             }
             m_run[rn][e] = mn;
             l_run[rn][e] = l_run[rn][e] * al + p0 + p1;
@@ -618,22 +604,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma16816(Olr[2 * np + 1], pa, bb[2], bb[3]);
             }
           } else {
-            const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
             uint32_t bb[2];
-            ldsm_x2_t(bb, lvt + swz<LR_RB>(tok, 0));
+            ldsm_x2_t(bb, lvt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
             mma16816(Olr[0], pa, bb[0], bb[1]);
           }
         }
       }
+      // release the stage and refill it with this warp's next block
+      ++consumed;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
-      if (++stage == p.nstage) {
-        stage = 0;
-        phase ^= 1;
-      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      if (!__shfl_sync(0xffffffffu, *abort_flag, 0)) issue_one();
     }
 
-    // ------------------------------------------------ merge the four warps
+    // ------------------------------------------------ merge the warps
 #pragma unroll
     for (int rn = 0; rn < 2; ++rn)
 #pragma unroll
@@ -654,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sm_l[warp * kMaxRows + row] = l_run[rn][e];
         }
     }
-    named_bar_sync(1, kNW * 32);
+    __syncthreads();  // also: every warp is past its B_K reads; acc may alias them now
     if (tid < kMaxRows) {
       float M = -CUDART_INF_F;
 #pragma unroll
@@ -701,12 +685,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        named_bar_sync(1, kNW * 32);
+        __syncthreads();
       }
     }
-    named_bar_sync(1, kNW * 32);
     // ---- write the partial of each query row
-    for (int i = tid; i < rows * (D + R); i += kNW * 32) {
+    for (int i = tid; i < rows * (D + R); i += kThreads) {
       const int row = i / (D + R), col = i % (D + R);
       const int n = I.q0 + row / p.g, m = I.head * p.g + row % p.g;
       const int64_t rec = (static_cast<int64_t>(n) * p.Hq + m) * p.n_splits + I.split;
@@ -719,11 +702,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.part_ml[rec * 2 + 1] = sm_L[tid];
     }
   }
+  // Drain: never leave the CTA with copies in flight (bounded waits; only after an abort).
+  if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+    for (uint32_t k = consumed; k < issued; ++k) {
+      const int s = k % kNST;
+      if ((valid_bits >> s) & 1) mbar_wait(bar0 + 8 * s, (k / kNST) & 1, nullptr, 1u << 16);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- combine
 // Merges the splits of each (query, head) with log-sum-exp weights, applies
 // the reordered V term O_lr B_V,a once, divides by l and stores bf16.
+// One CTA per (query, head); thread t owns column t of the partial rows.
 struct CombineParams {
   const float* part_ml;
   const float* part_o;
@@ -735,52 +726,63 @@ struct CombineParams {
 };
 
 template <int D, int R>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
-  __shared__ float wsm[8][256];
-  __shared__ float olr[8][R];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t pair = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (pair >= static_cast<int64_t>(p.num_queries) * p.Hq) return;
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
+  constexpr int NCOL = D + R;
+  __shared__ float w_s[256];
+  __shared__ float red[8];
+  __shared__ float olr[R];
+  // wait until the decode grid has finished and its partials are visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int64_t pair = blockIdx.x;
   const int n = static_cast<int>(pair / p.Hq), m = static_cast<int>(pair % p.Hq);
   const int S = p.n_splits;
-  int a = __ldg(p.adapter_ids + n);
-  bool bad = a < -1 || a >= p.n_adapters;
-  if (bad && lane == 0 && m == 0) report(p.status, LRKV_ERR_INDEX);
+  const int a = __ldg(p.adapter_ids + n);
+  const bool bad = a < -1 || a >= p.n_adapters;
+  if (bad && tid == 0 && m == 0) report(p.status, LRKV_ERR_INDEX);
   const float* ml = p.part_ml + pair * S * 2;
+  // max over splits
   float M = -CUDART_INF_F;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, ml[2 * s]);
+  for (int s = tid; s < S; s += 256) M = fmaxf(M, __ldg(ml + 2 * s));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red[wid] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
   float Ls = 0.f;
-  for (int s = lane; s < S; s += 32) {
-    const float ms = ml[2 * s];
+  for (int s = tid; s < S; s += 256) {
+    const float ms = __ldg(ml + 2 * s);
     const float w = (M == -CUDART_INF_F || ms == -CUDART_INF_F) ? 0.f : exp2f(ms - M);
-    wsm[warp][s] = w;
-    Ls += w * ml[2 * s + 1];
+    w_s[s] = w;
+    Ls += w * __ldg(ml + 2 * s + 1);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-  __syncwarp();
-  const float* po = p.part_o + pair * S * (D + R);
+  if (lane == 0) red[wid] = Ls;
+  __syncthreads();
+  Ls = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) Ls += red[w];
   const bool use_lr = p.has_bv && a >= 0 && !bad;
-  for (int k = lane; k < R; k += 32) {
-    float v = 0.f;
-    if (use_lr)
-      for (int s = 0; s < S; ++s) v += wsm[warp][s] * po[static_cast<int64_t>(s) * (D + R) + D + k];
-    olr[warp][k] = v;
-  }
-  __syncwarp();
-  const float inv = (Ls > 0.f && !bad) ? 1.f / Ls : 0.f;
-  const int kvh = m / p.g;
-  for (int j = lane; j < D; j += 32) {
-    float v = 0.f;
-    for (int s = 0; s < S; ++s) v += wsm[warp][s] * po[static_cast<int64_t>(s) * (D + R) + j];
-    if (use_lr) {
-      const __nv_bfloat16* bv = p.B_V + static_cast<int64_t>(a) * R * p.Hkv * D + kvh * D + j;
+  float v = 0.f;
+  if (tid < NCOL) {
+    const float* po = p.part_o + pair * S * NCOL + tid;
 #pragma unroll 8
-      for (int k = 0; k < R; ++k) v += olr[warp][k] * __bfloat162float(bv[static_cast<int64_t>(k) * p.Hkv * D]);
+    for (int s = 0; s < S; ++s) v += w_s[s] * __ldg(po + static_cast<int64_t>(s) * NCOL);
+    if (tid >= D) olr[tid - D] = use_lr ? v : 0.f;
+  }
+  __syncthreads();
+  if (tid < D) {
+    if (use_lr) {
+      const __nv_bfloat16* bv = p.B_V + static_cast<int64_t>(a) * R * p.Hkv * D + (m / p.g) * D + tid;
+#pragma unroll 8
+      for (int k = 0; k < R; ++k) v = fmaf(olr[k], __bfloat162float(bv[static_cast<int64_t>(k) * p.Hkv * D]), v);
     }
-    p.out[pair * D + j] = __float2bfloat16_rn(v * inv);
+    const float inv = (Ls > 0.f && !bad) ? 1.f / Ls : 0.f;
+    p.out[pair * D + tid] = __float2bfloat16_rn(v * inv);
   }
 }
 
@@ -811,7 +813,6 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   p.n_qgroups = plan.n_qgroups;
   p.n_splits = plan.n_splits;
   p.split_blocks = plan.split_blocks;
-  p.nstage = plan.nstage;
   p.has_bk = a.B_K != nullptr;
   p.has_bv = a.B_V != nullptr;
   p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -822,9 +823,13 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
 
   if (plan.n_items > 0) {
     auto kern = decode_kernel<D, R>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes) !=
-        cudaSuccess)
-      return LRKV_ERR_CUDA;
+    static bool attr_set = false;  // idempotent per-process kernel attribute
+    if (!attr_set) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
+          cudaSuccess)
+        return LRKV_ERR_CUDA;
+      attr_set = true;
+    }
     kern<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(p, tb, tl);
     if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
   }
@@ -844,8 +849,17 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   c.has_bv = a.B_V != nullptr;
   const int64_t pairs = static_cast<int64_t>(a.num_queries) * cfg.n_q_heads;
   if (pairs > 0) {
-    combine_kernel<D, R><<<static_cast<unsigned>((pairs + 7) / 8), 256, 0, stream>>>(c);
-    if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(pairs));
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, combine_kernel<D, R>, c) != cudaSuccess) return LRKV_ERR_CUDA;
   }
   return LRKV_OK;
 }
@@ -859,17 +873,16 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   P.g = cfg.n_q_heads / cfg.n_kv_heads;
   if (P.g < 1 || P.g > kMaxRows) return false;
   int qg = std::min(kMaxRows / P.g, kMaxSlots);
-  auto bk_bytes = [&](int slots) { return slots * R * (D + 8) * 2; };
-  while (qg > 1 && bk_bytes(qg) > 40 * 1024) --qg;
+  while (qg > 1 && Layout::make(D, R, qg).total > kSmemLimit) --qg;
+  if (Layout::make(D, R, qg).total > kSmemLimit) return false;
   P.qg_size = qg;
-  const int stage_bytes = Layout::make(D, R, 1, qg).stage;
-  const int fixed = Layout::make(D, R, 0, qg).total;
-  P.nstage = std::min(4, (kSmemLimit - fixed) / stage_bytes);
-  if (P.nstage < 2) return false;
-  P.smem_bytes = Layout::make(D, R, P.nstage, qg).total;
+  P.nstage = kNST;
+  P.smem_bytes = Layout::make(D, R, qg).total;
   P.n_qgroups = std::max(1, (max_q_per_ctx + qg - 1) / qg);
   const int nblk = std::max(1, (max_ctx_len + kBlock - 1) / kBlock);
   const int64_t pairs = static_cast<int64_t>(num_ctx) * P.n_qgroups * cfg.n_kv_heads;
+  // Splits: as many as keep every SM busy in whole waves of items (>= 0.95
+  // efficiency), counting how evenly a split's blocks fall on the kNW warps.
   int best_s = 1;
   double best_eff = -1.0;
   const int smax = std::min(nblk, 256);
@@ -879,7 +892,8 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
     if (ss != s) continue;
     const int64_t items = pairs * s;
     const int64_t waves = (items + sm_count - 1) / sm_count;
-    const double eff = static_cast<double>(items) / static_cast<double>(waves * sm_count);
+    const double rounds = static_cast<double>((sb + kNW - 1) / kNW) * kNW / sb;  // warp balance
+    const double eff = static_cast<double>(items) / static_cast<double>(waves * sm_count) / rounds;
     if (eff > best_eff + 1e-9) {
       best_eff = eff;
       best_s = s;

@@ -259,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
   for (int kt = 0; kt < n_tiles; ++kt) {
-    bool ok = !(*abort_flag) && mbar_wait(bar_full + 8 * stage, phase, p.status);
+    // every wait result is made warp-uniform before any warp-collective use
+    bool ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
+    if (ok) ok = mbar_wait(bar_full + 8 * stage, phase, p.status);
+    ok = __all_sync(0xffffffffu, ok);
     if (!ok) *abort_flag = 1;
     const int mask = ok ? stage_mask[stage] : 0;
     const uint32_t st = sbase + stage * L.stage;
@@ -601,8 +604,13 @@ lrkv_status run(const lrkv_config& cfg, const PrefillArgs& a, cudaStream_t strea
   CUtensorMap tb, tl;
   if (!make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, &tl)) return LRKV_ERR_CUDA;
   auto kern = prefill_kernel<D, R>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return LRKV_ERR_CUDA;
+  static bool attr_set = false;  // idempotent per-process kernel attribute
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
+        cudaSuccess)
+      return LRKV_ERR_CUDA;
+    attr_set = true;
+  }
   const int tiles = (a.max_q_len * p.g + BMQ - 1) / BMQ;
   dim3 grid(tiles, cfg.n_kv_heads, a.num_seqs);
   kern<<<grid, kThreads, smem, stream>>>(p, tb, tl);
