@@ -112,34 +112,40 @@ def workload_model(case):
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while running (read only)."""
+    """Samples the SM clock and clock-event reasons while running (read only):
+    through NVML when the Python binding is present, else by running
+    ``nvidia-smi --query-gpu ... -lms`` for the duration of the region."""
 
-    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-               0x100: "display_clock_setting"}
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index: int, interval_s: float = 0.002):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self.interval = interval_s
+    def __init__(self, device_index: int, interval_ms: int = 20):
+        self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
+        self.interval = interval_ms
         self._stop = threading.Event()
         self._h = None
+        self._proc = None
+        self._bus = None
+        try:
+            import torch
+
+            p = torch.cuda.get_device_properties(device_index)
+            self._bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except Exception as e:
+            self.error = f"bus id: {type(e).__name__}: {e}"
         try:
             import pynvml
 
             pynvml.nvmlInit()
             self._nv = pynvml
-            try:
-                import torch
-
-                p = torch.cuda.get_device_properties(device_index)
-                bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
-                self._h = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
-            except Exception:
-                self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self._h = (pynvml.nvmlDeviceGetHandleByPciBusId(self._bus.encode()) if self._bus
+                       else pynvml.nvmlDeviceGetHandleByIndex(device_index))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # NVML missing: report no samples
-            self.error = f"{type(e).__name__}: {e}"
+        except Exception:
+            self._h = None
 
     def _run(self):
         nv = self._nv
@@ -150,28 +156,63 @@ class ClockSampler:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
                 r = reasons(self._h)
                 for bit, name in self.REASONS.items():
-                    if r & bit and bit != 0x1:
+                    if r & bit:
                         self.reasons.add(name)
             except Exception as e:
                 self.error = f"{type(e).__name__}: {e}"
-            time.sleep(self.interval)
+            time.sleep(self.interval / 1e3)
 
     def __enter__(self):
         if self._h is not None:
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
+        else:
+            import subprocess
+
+            cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                   "-lms", str(self.interval)]
+            if self._bus:
+                cmd += ["-i", self._bus]
+            try:
+                self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+                time.sleep(0.2)  # let the first samples arrive before the region starts
+            except Exception as e:
+                self.error = f"nvidia-smi: {type(e).__name__}: {e}"
         return self
 
     def __exit__(self, *a):
         self._stop.set()
         if self._h is not None:
             self._t.join()
+        elif self._proc is not None:
+            time.sleep(0.05)
+            self._proc.terminate()
+            try:
+                out, err = self._proc.communicate(timeout=5)
+            except Exception:
+                self._proc.kill()
+                out, err = self._proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) != len(self.FIELDS):
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[2:]):
+                    if v.lower().startswith("active"):
+                        self.reasons.add(name)
+            if not self.samples:
+                self.error = (err or "no samples").strip()[:200]
 
     def summary(self):
         med = statistics.median(self.samples) if self.samples else None
         out = {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
                "samples": len(self.samples)}
-        if getattr(self, "error", None):
+        if self.error and not self.samples:
             out["error"] = self.error
         return out
 

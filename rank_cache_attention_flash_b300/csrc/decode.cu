@@ -58,34 +58,29 @@ struct DecodeParams {
   RopeFreqs freqs;
 };
 
-// Shared-memory layout (byte offsets from a 1024-aligned base).
-struct Layout {
-  int kv_tile, lr_tile, blk, bk_pitch, bk_slot, d_pitch, acc_pitch;
-  int off_bk, off_dtab, off_btab, off_freq, off_ml, off_misc, off_bar, total;
-  __host__ __device__ static Layout make(int D, int R, int slots) {
-    Layout L;
-    L.kv_tile = 16 * D * 2;
-    L.lr_tile = 16 * R * 2;
-    L.blk = ((2 * L.kv_tile + 2 * L.lr_tile) + 1023) & ~1023;  // one block: K, V, L_K, L_V
-    L.bk_pitch = (D + 8) * 2;      // bytes per B_K row in smem (conflict-free ldmatrix)
-    L.bk_slot = R * L.bk_pitch;
-    L.d_pitch = (D / 2) * 8 + 64;  // delta-table row: D/2 float2 + pad
-    L.acc_pitch = D + R + 4;       // floats (merge accumulator, aliases the B_K slots)
-    int o = kNW * kNST * L.blk;
-    L.off_bk = o;
-    const int bk = slots * L.bk_slot, acc = kMaxRows * L.acc_pitch * 4;
-    o += bk > acc ? bk : acc;
-    o = (o + 15) & ~15;
-    L.off_dtab = o; o += 16 * L.d_pitch;
-    L.off_btab = o; o += kNW * (D / 2) * 8;
-    L.off_freq = o; o += 2 * 64 * 4;
-    L.off_ml = o;   o += 2 * kNW * kMaxRows * 4 + 2 * kMaxRows * 4;
-    L.off_misc = o; o += 64;
-    o = (o + 7) & ~7;
-    L.off_bar = o;  o += kNW * kNST * 8;
-    L.total = o + 1024;  // alignment slack
-    return L;
-  }
+// Shared-memory layout (byte offsets from a 1024-aligned base), fixed per (D, R).
+// B_K slots: up to four distinct adapters per item (one at rank 64, where the
+// ring of 12 KB blocks leaves room for one 17 KB slice).
+template <int D, int R>
+struct DL {
+  static constexpr int kSlots = R >= 64 ? 1 : kMaxSlots;
+  static constexpr int kv_tile = 16 * D * 2;
+  static constexpr int lr_tile = 16 * R * 2;
+  static constexpr int blk = ((2 * kv_tile + 2 * lr_tile) + 1023) & ~1023;  // K, V, L_K, L_V
+  static constexpr int bk_pitch = (D + 8) * 2;  // bytes per B_K row (conflict-free ldmatrix)
+  static constexpr int bk_slot = R * bk_pitch;
+  static constexpr int d_pitch = (D / 2) * 8 + 64;  // delta-table row: D/2 float2 + pad
+  static constexpr int acc_pitch = D + R + 4;       // floats; the merge accumulator aliases B_K
+  static constexpr int bk_bytes = kSlots * bk_slot;
+  static constexpr int acc_bytes = kMaxRows * acc_pitch * 4;
+  static constexpr int off_bk = kNW * kNST * blk;
+  static constexpr int off_dtab = (off_bk + (bk_bytes > acc_bytes ? bk_bytes : acc_bytes) + 15) & ~15;
+  static constexpr int off_btab = off_dtab + 16 * d_pitch;
+  static constexpr int off_freq = off_btab + kNW * (D / 2) * 8;
+  static constexpr int off_ml = off_freq + 2 * 64 * 4;
+  static constexpr int off_misc = off_ml + 2 * kNW * kMaxRows * 4 + 2 * kMaxRows * 4;
+  static constexpr int off_bar = (off_misc + 64 + 7) & ~7;
+  static constexpr int total = off_bar + kNW * kNST * 8 + 1024;  // + alignment slack
 };
 
 struct Item {
@@ -166,23 +161,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const Layout L = Layout::make(D, R, p.qg_size);
+  using L = DL<D, R>;
   const uint32_t sbase = smem_u32(smem);
-  float2* dtab = reinterpret_cast<float2*>(smem + L.off_dtab);
-  float* freq = reinterpret_cast<float*>(smem + L.off_freq);
-  float* acc = reinterpret_cast<float*>(smem + L.off_bk);  // merge accumulator (aliases B_K)
-  float* sm_m = reinterpret_cast<float*>(smem + L.off_ml);
+  float2* dtab = reinterpret_cast<float2*>(smem + L::off_dtab);
+  float* freq = reinterpret_cast<float*>(smem + L::off_freq);
+  float* acc = reinterpret_cast<float*>(smem + L::off_bk);  // merge accumulator (aliases B_K)
+  float* sm_m = reinterpret_cast<float*>(smem + L::off_ml);
   float* sm_l = sm_m + kNW * kMaxRows;
   float* sm_M = sm_l + kNW * kMaxRows;
   float* sm_L = sm_M + kMaxRows;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_misc);
-  int* slot_ad_s = reinterpret_cast<int*>(smem + L.off_misc + 16);  // [kMaxSlots]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc);
+  int* slot_ad_s = reinterpret_cast<int*>(smem + L::off_misc + 16);  // [kMaxSlots]
   int* slot_rn_s = slot_ad_s + kMaxSlots;                             // [kMaxSlots]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, c4 = lane & 3;
-  const uint32_t bar0 = sbase + L.off_bar + warp * kNST * 8;  // this warp's ring barriers
-  const uint32_t ring0 = sbase + warp * kNST * L.blk;           // this warp's ring
+  const uint32_t bar0 = sbase + L::off_bar + warp * kNST * 8;  // this warp's ring barriers
+  const uint32_t ring0 = sbase + warp * kNST * L::blk;           // this warp's ring
 
   // ---- CTA prologue: frequencies, delta table, barriers
   if (tid < HALF) {
@@ -197,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   for (int i = tid; i < 16 * HALF; i += kThreads) {
     const int dl = i / HALF, j = i % HALF;
-    *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(dtab) + dl * L.d_pitch + j * 8) =
+    *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(dtab) + dl * L::d_pitch + j * 8) =
         rope_cos_sin(dl, freq[j], freq[64 + j]);
   }
   if (lane == 0) {
@@ -214,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pend_id = __ldg(p.block_tables + static_cast<int64_t>(wi.I.ctx) * p.max_blocks + wi.kb);
   uint32_t issued = 0, consumed = 0;
   uint32_t valid_bits = 0;  // bit s: stage s holds a loaded block
-  const uint32_t lr_bytes = (p.has_bk ? L.lr_tile : 0) + (p.has_bv ? L.lr_tile : 0);
+  const uint32_t lr_bytes = (p.has_bk ? L::lr_tile : 0) + (p.has_bv ? L::lr_tile : 0);
 
   auto issue_one = [&]() {
     if (!wi.more) return;
@@ -228,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         ok = 1;
         const uint32_t fb = bar0 + 8 * s;
-        mbar_arrive_expect_tx(fb, 2 * L.kv_tile + lr_bytes);
-        const uint32_t kt = ring0 + s * L.blk, vt = kt + L.kv_tile;
-        const uint32_t lk = kt + 2 * L.kv_tile, lv = lk + L.lr_tile;
+        mbar_arrive_expect_tx(fb, 2 * L::kv_tile + lr_bytes);
+        const uint32_t kt = ring0 + s * L::blk, vt = kt + L::kv_tile;
+        const uint32_t lk = kt + 2 * L::kv_tile, lv = lk + L::lr_tile;
         const int yk = ((blk * 2 + 0) * p.Hkv + wi.I.head) * kBlock;
         const int yv = ((blk * 2 + 1) * p.Hkv + wi.I.head) * kBlock;
 #pragma unroll
@@ -251,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   for (int s = 0; s < kNST; ++s) issue_one();
 
-  float2* btab = reinterpret_cast<float2*>(smem + L.off_btab) + warp * HALF;
+  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab) + warp * HALF;
 
   for (int64_t it = blockIdx.x; it < p.n_items; it += gridDim.x) {
     const Item I = get_item(p, it);
@@ -329,11 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a < 0) continue;
         const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(a) * R * p.Hkv * D +
                                    static_cast<int64_t>(I.head) * D;
-        uint8_t* dst = smem + L.off_bk + s * L.bk_slot;
+        uint8_t* dst = smem + L::off_bk + s * L::bk_slot;
         for (int i = tid; i < R * VPR; i += kThreads) {
           const int k = i / VPR, v = i % VPR;
           const uint4 val = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v);
-          *reinterpret_cast<uint4*>(dst + k * L.bk_pitch + v * 16) = val;
+          *reinterpret_cast<uint4*>(dst + k * L::bk_pitch + v * 16) = val;
         }
       }
     }
@@ -365,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (have && !ok) *abort_flag = 1;
       if (ok) {
         const int t0 = b * kBlock;
-        const uint32_t kt = ring0 + s * L.blk, vt = kt + L.kv_tile;
-        const uint32_t lkt = kt + 2 * L.kv_tile, lvt = lkt + L.lr_tile;
+        const uint32_t kt = ring0 + s * L::blk, vt = kt + L::kv_tile;
+        const uint32_t lkt = kt + 2 * L::kv_tile, lvt = lkt + L::lr_tile;
 
         // Rows past the context end may hold stale pool memory: zero their V and
         // L_V rows so that P = 0 there cannot meet a NaN in the PV products.
@@ -386,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // base rotation of this block: e^{i t0 theta_j}
         if (any_rebuild) {
-          for (int j = lane; j < HALF; j += 32) btab[j] = rope_cos_sin(t0, freq[j], freq[64 + j]);
+          for (int j = lane; j < HALF; j += 32) btab[j] = rope_cos_sin_fast(t0, freq[j], freq[64 + j]);
           __syncwarp();
         }
         // L_K A fragments (tokens x rank)
@@ -413,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
-          // K_base at this lane's fragment positions: [n][h][tk] (bf16 pairs)
-          uint32_t kbv[2][2][2];
+          // K_base at this lane's fragment positions, as fp16 pairs: [n][h][tk]
+          uint32_t kb16[2][2][2];
 #pragma unroll
           for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -423,10 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int tk = 0; tk < 2; ++tk) {
                 const int j = 16 * cc + 8 * n + 2 * c4 + h * HALF;
                 const uint32_t addr = kt + (j / 64) * 2048 + swz<128>(g8 + 8 * tk, (j % 64) * 2);
-                asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(kbv[n][h][tk]) : "r"(addr));
+                uint32_t v;
+                asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+                kb16[n][h][tk] = bf16x2_to_f16x2(v);
               }
-          // rotation factors for (tk, n, e)
-          float2 cs[2][2][2];
+          // rotation factors of this lane's (token, pair) positions as fp16 pairs
+          uint32_t c16[2][2], s16[2][2], ns16[2][2];  // [tk][n]
           if (any_rebuild) {
 #pragma unroll
             for (int n = 0; n < 2; ++n) {
@@ -435,9 +432,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int tk = 0; tk < 2; ++tk) {
                 const float4 dq = *reinterpret_cast<const float4*>(
-                    reinterpret_cast<const uint8_t*>(dtab) + (g8 + 8 * tk) * L.d_pitch + j * 8);
-                cs[tk][n][0] = make_float2(bq.x * dq.x - bq.y * dq.y, bq.y * dq.x + bq.x * dq.y);
-                cs[tk][n][1] = make_float2(bq.z * dq.z - bq.w * dq.w, bq.w * dq.z + bq.z * dq.w);
+                    reinterpret_cast<const uint8_t*>(dtab) + (g8 + 8 * tk) * L::d_pitch + j * 8);
+                const float c0 = bq.x * dq.x - bq.y * dq.y, s0 = bq.y * dq.x + bq.x * dq.y;
+                const float c1 = bq.z * dq.z - bq.w * dq.w, s1 = bq.w * dq.z + bq.z * dq.w;
+                c16[tk][n] = pack_f16(c0, c1);
+                s16[tk][n] = pack_f16(s0, s1);
+                ns16[tk][n] = pack_f16(-s0, -s1);
               }
             }
           }
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float y[4][4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.f;
-              const uint32_t bk = sbase + L.off_bk + a * L.bk_slot;
+              const uint32_t bk = sbase + L::off_bk + a * L::bk_slot;
               if constexpr (R >= 16) {
 #pragma unroll
                 for (int ks = 0; ks < NRT; ++ks)
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int krow = 16 * ks + (lane & 7) + (mi & 1) * 8;
                     const int ncol = 16 * cc + h * HALF + (mi >> 1) * 8;
                     uint32_t bb[4];
-                    ldsm_x4_t(bb, bk + krow * L.bk_pitch + ncol * 2);
+                    ldsm_x4_t(bb, bk + krow * L::bk_pitch + ncol * 2);
                     mma16816(y[2 * h + 0], alk[ks], bb[0], bb[1]);
                     mma16816(y[2 * h + 1], alk[ks], bb[2], bb[3]);
                   }
@@ -470,42 +470,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < 2; ++h) {
                   const int ncol = 16 * cc + h * HALF + ((lane >> 3) & 1) * 8;
                   uint32_t bb[2];
-                  ldsm_x2_t(bb, bk + (lane & 7) * L.bk_pitch + ncol * 2);
+                  ldsm_x2_t(bb, bk + (lane & 7) * L::bk_pitch + ncol * 2);
                   mma1688(y[2 * h + 0], alk[0][0], alk[0][1], bb[0]);
                   mma1688(y[2 * h + 1], alk[0][0], alk[0][1], bb[1]);
                 }
               }
-              // rotate the rebuilt pair (j, j + d/2), add K_base, pack fp16
-              float klo[2][4], khi[2][4];
+              // rotate the rebuilt pair (j, j + d/2) and add K_base, in packed fp16:
+              //   k_lo = K_lo + x cos - y sin,   k_hi = K_hi + y cos + x sin
 #pragma unroll
               for (int n = 0; n < 2; ++n)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int tk = i >> 1, e = i & 1;
-                  const float x = y[n][i], yy = y[n + 2][i];
-                  const float c = cs[tk][n][e].x, sn = cs[tk][n][e].y;
-                  const float blo = e ? bf16_hi(kbv[n][0][tk]) : bf16_lo(kbv[n][0][tk]);
-                  const float bhi = e ? bf16_hi(kbv[n][1][tk]) : bf16_lo(kbv[n][1][tk]);
-                  klo[n][i] = fmaf(x, c, fmaf(-yy, sn, blo));
-                  khi[n][i] = fmaf(yy, c, fmaf(x, sn, bhi));
+                for (int tk = 0; tk < 2; ++tk) {
+                  const uint32_t x = pack_f16(y[n][2 * tk], y[n][2 * tk + 1]);
+                  const uint32_t yy = pack_f16(y[n + 2][2 * tk], y[n + 2][2 * tk + 1]);
+                  const uint32_t lo = hfma2_u32(x, c16[tk][n], hfma2_u32(yy, ns16[tk][n], kb16[n][0][tk]));
+                  const uint32_t hi = hfma2_u32(yy, c16[tk][n], hfma2_u32(x, s16[tk][n], kb16[n][1][tk]));
+                  A_lo[2 * n + tk] = lo;
+                  A_hi[2 * n + tk] = hi;
                 }
-              A_lo[0] = pack_f16(klo[0][0], klo[0][1]);
-              A_lo[1] = pack_f16(klo[0][2], klo[0][3]);
-              A_lo[2] = pack_f16(klo[1][0], klo[1][1]);
-              A_lo[3] = pack_f16(klo[1][2], klo[1][3]);
-              A_hi[0] = pack_f16(khi[0][0], khi[0][1]);
-              A_hi[1] = pack_f16(khi[0][2], khi[0][3]);
-              A_hi[2] = pack_f16(khi[1][0], khi[1][1]);
-              A_hi[3] = pack_f16(khi[1][2], khi[1][3]);
             } else {
-              A_lo[0] = bf16x2_to_f16x2(kbv[0][0][0]);
-              A_lo[1] = bf16x2_to_f16x2(kbv[0][0][1]);
-              A_lo[2] = bf16x2_to_f16x2(kbv[1][0][0]);
-              A_lo[3] = bf16x2_to_f16x2(kbv[1][0][1]);
-              A_hi[0] = bf16x2_to_f16x2(kbv[0][1][0]);
-              A_hi[1] = bf16x2_to_f16x2(kbv[0][1][1]);
-              A_hi[2] = bf16x2_to_f16x2(kbv[1][1][0]);
-              A_hi[3] = bf16x2_to_f16x2(kbv[1][1][1]);
+#pragma unroll
+              for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int tk = 0; tk < 2; ++tk) {
+                  A_lo[2 * n + tk] = kb16[n][0][tk];
+                  A_hi[2 * n + tk] = kb16[n][1][tk];
+                }
             }
             // scores of this adapter's rows only: its query fragment, other rows zeroed
 #pragma unroll
@@ -564,10 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float a11 = __shfl_sync(0xffffffffu, alpha[1][1], src);
           const float ar0 = (g8 & 1) ? a01 : a00;
           const float ar1 = (g8 & 1) ? a11 : a10;
+          if (__any_sync(0xffffffffu, ar0 != 1.f || ar1 != 1.f)) {
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) { O[i][0] *= ar0; O[i][1] *= ar0; O[i][2] *= ar1; O[i][3] *= ar1; }
+            for (int i = 0; i < D / 8; ++i) { O[i][0] *= ar0; O[i][1] *= ar0; O[i][2] *= ar1; O[i][3] *= ar1; }
 #pragma unroll
-          for (int i = 0; i < NLR; ++i) { Olr[i][0] *= ar0; Olr[i][1] *= ar0; Olr[i][2] *= ar1; Olr[i][3] *= ar1; }
+            for (int i = 0; i < NLR; ++i) { Olr[i][0] *= ar0; Olr[i][1] *= ar0; Olr[i][2] *= ar1; Olr[i][3] *= ar1; }
+          }
         }
         // ---- P (rows x tokens) A fragment via register transposes
         uint32_t pa[4];
@@ -668,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (h == 1 && RN == 1) break;
-            float* arow = acc + (g8 + 8 * h) * L.acc_pitch;
+            float* arow = acc + (g8 + 8 * h) * L::acc_pitch;
 #pragma unroll
             for (int nt = 0; nt < D / 8; ++nt) {
               float2* d2 = reinterpret_cast<float2*>(arow + 8 * nt + 2 * c4);
@@ -693,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = i / (D + R), col = i % (D + R);
       const int n = I.q0 + row / p.g, m = I.head * p.g + row % p.g;
       const int64_t rec = (static_cast<int64_t>(n) * p.Hq + m) * p.n_splits + I.split;
-      p.part_o[rec * (D + R) + col] = acc[row * L.acc_pitch + col];
+      p.part_o[rec * (D + R) + col] = acc[row * L::acc_pitch + col];
     }
     if (tid < rows) {
       const int n = I.q0 + tid / p.g, m = I.head * p.g + tid % p.g;
@@ -872,12 +864,17 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   DecodePlan P{};
   P.g = cfg.n_q_heads / cfg.n_kv_heads;
   if (P.g < 1 || P.g > kMaxRows) return false;
-  int qg = std::min(kMaxRows / P.g, kMaxSlots);
-  while (qg > 1 && Layout::make(D, R, qg).total > kSmemLimit) --qg;
-  if (Layout::make(D, R, qg).total > kSmemLimit) return false;
+  int slots = 0, total = 0;
+#define LRKV_L(d, r) \
+  if (D == d && R == r) { slots = DL<d, r>::kSlots; total = DL<d, r>::total; }
+  LRKV_L(128, 8) LRKV_L(128, 16) LRKV_L(128, 32) LRKV_L(128, 64)
+  LRKV_L(64, 8) LRKV_L(64, 16) LRKV_L(64, 32) LRKV_L(64, 64)
+#undef LRKV_L
+  if (slots == 0 || total > kSmemLimit) return false;
+  const int qg = std::min(kMaxRows / P.g, slots);
   P.qg_size = qg;
   P.nstage = kNST;
-  P.smem_bytes = Layout::make(D, R, qg).total;
+  P.smem_bytes = total;
   P.n_qgroups = std::max(1, (max_q_per_ctx + qg - 1) / qg);
   const int nblk = std::max(1, (max_ctx_len + kBlock - 1) / kBlock);
   const int64_t pairs = static_cast<int64_t>(num_ctx) * P.n_qgroups * cfg.n_kv_heads;

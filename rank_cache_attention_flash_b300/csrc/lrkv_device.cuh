@@ -192,6 +192,32 @@ __device__ __forceinline__ float2 rope_cos_sin(int32_t t, float th_hi, float th_
   return make_float2(c, s);
 }
 
+// Same reduction, then the hardware sine/cosine approximation (absolute error
+// near 2^-21 on [-pi, pi]); used where the result feeds fp16 arithmetic.
+__device__ __forceinline__ float2 rope_cos_sin_fast(int32_t t, float th_hi, float th_lo) {
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  constexpr float kC1 = static_cast<float>(kTwoPi);
+  constexpr float kC2 = static_cast<float>(kTwoPi - static_cast<double>(kC1));
+  constexpr float kInv = static_cast<float>(1.0 / kTwoPi);
+  const float tf = static_cast<float>(t);
+  const float p = tf * th_hi;
+  float e = fmaf(tf, th_hi, -p);
+  e = fmaf(tf, th_lo, e);
+  const float n = rintf(p * kInv);
+  float r = fmaf(-n, kC1, p);
+  r = fmaf(-n, kC2, r);
+  r += e;
+  float s, c;
+  __sincosf(r, &s, &c);
+  return make_float2(c, s);
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // Per-launch RoPE frequencies theta_j = base^(-2j/d), j < d/2, split hi/lo.
 struct RopeFreqs {
   float hi[64];

@@ -1,12 +1,14 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
 
 Small workloads (every layer shape of the five workloads, several tiles and a
-ragged tail) are compared element by element with the literal oracle; pools
-are pre-filled with NaN so that any read of an unwritten slot shows up.
-Short-context edge cases (a few to a few hundred keys, where one key can carry
-half of the softmax mass) are compared with the oracle's bf16-cache variant:
-there the rounding of the stored cache alone can move an output by more than
-the absolute bound, for any implementation that stores the cache in bf16.
+ragged tail) and edge cases are compared element by element with the oracle's
+bf16-cache variant (the oracle rounds its own fp64 cache components to bf16,
+as the stored cache holds them), which isolates the kernels' own error from the
+storage format's: on short contexts, or on the Qwen-shaped layer, the bf16
+rounding of the cache alone reaches the stated bounds (rel-Frobenius 4.8e-3
+measured on the small mixed batch). The five workloads at their stated sizes
+are checked against the literal oracle in test_gpu_full.py. Pools are
+pre-filled with NaN so that any read of an unwritten slot shows up.
 """
 import math
 
@@ -37,11 +39,13 @@ def test_small_workload_parity(cuda_lib, name):
     g, res = _run(case)
     assert g.device_status() == 0
     tol = tol_for(case)
+    cache = None if case.shape.dtype == "fp32" else "bf16"
     if g.n_dec:
-        assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case), tol, f"{name} decode")
+        assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case, cache=cache), tol,
+                     f"{name} decode")
     w64 = weights64(case)
     for p in range(g.n_pre):
-        rows, want = oracle_prefill_seq(case, p, w64=w64)
+        rows, want = oracle_prefill_seq(case, p, w64=w64, cache=cache)
         assert_close(res["prefill"][rows].double().cpu().numpy(), want, tol, f"{name} prefill seq {p}")
 
 
