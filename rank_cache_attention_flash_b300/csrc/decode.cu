@@ -79,7 +79,7 @@ struct DL {
   static constexpr int off_freq = off_btab + kNW * (D / 2) * 8;
   static constexpr int off_ml = off_freq + 2 * 64 * 4;
   static constexpr int off_misc = off_ml + 2 * kNW * kMaxRows * 4 + 2 * kMaxRows * 4;
-  static constexpr int off_bar = (off_misc + 64 + 7) & ~7;
+  static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
   static constexpr int total = off_bar + kNW * kNST * 8 + 1024;  // + alignment slack
 };
 
@@ -143,7 +143,7 @@ __device__ __forceinline__ void walk_init(const DecodeParams& p, int warp, Walk&
   walk_next(p, warp, w);
 }
 
-template <int D, int R>
+template <int D, int R, int RN>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p,
                   const __grid_constant__ CUtensorMap tm_base,
@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NCH = D / 32;   // dim chunks: each covers 16 dims + their RoPE partners
   constexpr int NKS = D / 16;   // k-slices of the score MMA
   constexpr int NRT = R >= 16 ? R / 16 : 1;  // rank k-steps of the rebuild
-  constexpr int NLR = R / 8;    // O_lr n-tiles
+  constexpr int NMT = D / 16;   // m-tiles of O^T (head dims)
+  constexpr int NLM = R >= 16 ? R / 16 : 1;  // m-tiles of O_lr^T (rank)
   constexpr int LR_RB = R * 2;  // low-rank tile row bytes
 
   // The combine kernel may be scheduled now; it waits for this grid to finish.
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc);
   int* slot_ad_s = reinterpret_cast<int*>(smem + L::off_misc + 16);  // [kMaxSlots]
   int* slot_rn_s = slot_ad_s + kMaxSlots;                             // [kMaxSlots]
+  int* q_ad_s = slot_rn_s + kMaxSlots;                                // [kMaxSlots]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, c4 = lane & 3;
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = tid; i < 16 * HALF; i += kThreads) {
     const int dl = i / HALF, j = i % HALF;
     *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(dtab) + dl * L::d_pitch + j * 8) =
-        rope_cos_sin(dl, freq[j], freq[64 + j]);
+        rope_cos_sin_fast(dl, freq[j], freq[64 + j]);
   }
   if (lane == 0) {
     prefetch_tmap(&tm_base);
@@ -251,60 +253,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int64_t it = blockIdx.x; it < p.n_items; it += gridDim.x) {
     const Item I = get_item(p, it);
     if (!I.active) continue;
-    const int rows = I.nq * p.g;
+    const int rows = I.nq * p.g;  // <= 8 * RN by the plan
 
-    __syncthreads();  // previous item's merge finished with the B_K / acc region
-
-    // --- distinct adapters of this query group -> smem (thread 0), per-lane row slots
-    if (tid == 0) {
-      int n = 0, ad[kMaxSlots], rn_mask[kMaxSlots];
-      for (int qi = 0; qi < I.nq; ++qi) {
-        int a = __ldg(p.adapter_ids + I.q0 + qi);
-        if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;  // bad ids: reported by the combine
-        int s = -1;
-        for (int k = 0; k < n; ++k)
-          if (ad[k] == a) s = k;
-        if (s < 0) {
-          s = n++;
-          ad[s] = a;
-          rn_mask[s] = 0;
-        }
-        for (int gi = 0; gi < p.g; ++gi) rn_mask[s] |= 1 << ((qi * p.g + gi) >> 3);
-      }
-      for (int k = 0; k < kMaxSlots; ++k) {
-        slot_ad_s[k] = k < n ? ad[k] : -2;
-        slot_rn_s[k] = k < n ? rn_mask[k] : 0;
-      }
+    __syncthreads();  // previous item's merge finished with the B_K / acc / slot smem
+    // --- adapter ids of the group's queries (one load per query, in parallel)
+    if (tid < I.nq) {
+      int a = __ldg(p.adapter_ids + I.q0 + tid);
+      if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;  // bad ids: reported by the combine
+      q_ad_s[tid] = a;
     }
     __syncthreads();
-    int nslots = 0;
-    bool any_rebuild = false;
+    // distinct adapters (slots), computed redundantly by every thread
+    int nslots = 0, qslot[kMaxSlots], sad[kMaxSlots], srn[kMaxSlots];
 #pragma unroll
-    for (int k = 0; k < kMaxSlots; ++k) {
-      const int a = slot_ad_s[k];
-      if (a != -2) ++nslots;
-      if (a >= 0) any_rebuild = true;
-    }
-    // slot of the query row held by this lane in the score B fragment: row rn*8 + g8
-    int myslot[2];
+    for (int k = 0; k < kMaxSlots; ++k) { qslot[k] = 0; sad[k] = -2; srn[k] = 0; }
 #pragma unroll
-    for (int rn = 0; rn < 2; ++rn) {
-      const int row = rn * 8 + g8;
-      myslot[rn] = -1;
-      if (row < rows) {
-        int a = __ldg(p.adapter_ids + I.q0 + row / p.g);
-        if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;
+    for (int qi = 0; qi < kMaxSlots; ++qi) {
+      if (qi < I.nq) {
+        const int a = q_ad_s[qi];
+        int sl = nslots;
 #pragma unroll
         for (int k = 0; k < kMaxSlots; ++k)
-          if (slot_ad_s[k] == a) myslot[rn] = k;
+          if (k < nslots && sad[k] == a) sl = k;
+        if (sl == nslots) {
+#pragma unroll
+          for (int k = 0; k < kMaxSlots; ++k)
+            if (k == sl) sad[k] = a;
+          ++nslots;
+        }
+        int m = 0;
+        for (int gi = 0; gi < p.g; ++gi) m |= 1 << ((qi * p.g + gi) >> 3);
+#pragma unroll
+        for (int k = 0; k < kMaxSlots; ++k) {
+          if (k == sl) srn[k] |= m;
+          if (k == qi) qslot[k] = sl;
+        }
       }
     }
-    const int RN = rows > 8 ? 2 : 1;
+    bool any_rebuild = false;
+#pragma unroll
+    for (int k = 0; k < kMaxSlots; ++k) any_rebuild |= sad[k] >= 0;
+    if (tid == 0) {
+#pragma unroll
+      for (int k = 0; k < kMaxSlots; ++k) {
+        slot_ad_s[k] = sad[k];
+        slot_rn_s[k] = srn[k];
+      }
+    }
+    // slot of the query row held by this lane in the score B fragment: row rn*8 + g8
+    int myslot[RN];
+#pragma unroll
+    for (int rn = 0; rn < RN; ++rn) {
+      const int row = rn * 8 + g8;
+      int sl = -1;
+#pragma unroll
+      for (int k = 0; k < kMaxSlots; ++k)
+        if (row < rows && k == row / p.g) sl = qslot[k];
+      myslot[rn] = sl;
+    }
 
     // --- query fragments (B operand of S^T = K Q^T), fp16, straight from global
-    uint32_t qf[2][NKS][2];
+    uint32_t qf[RN][NKS][2];
 #pragma unroll
-    for (int rn = 0; rn < 2; ++rn) {
+    for (int rn = 0; rn < RN; ++rn) {
       const int row = rn * 8 + g8;
       const bool ok = row < rows;
       const __nv_bfloat16* qrow =
@@ -316,33 +327,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         qf[rn][ks][1] = ok ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8))) : 0u;
       }
     }
-    // --- B_K slices of the rebuild slots -> smem [slot][k][D] (padded rows)
+    // --- B_K slices of the rebuild slots -> smem [slot][k][D] (padded rows), async copies
     {
       constexpr int VPR = D / 8;  // 16-byte vectors per row
-      for (int s = 0; s < nslots; ++s) {
-        const int a = slot_ad_s[s];
+#pragma unroll
+      for (int s = 0; s < L::kSlots; ++s) {
+        const int a = sad[s];
         if (a < 0) continue;
         const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(a) * R * p.Hkv * D +
                                    static_cast<int64_t>(I.head) * D;
-        uint8_t* dst = smem + L::off_bk + s * L::bk_slot;
+        const uint32_t dst = sbase + L::off_bk + s * L::bk_slot;
         for (int i = tid; i < R * VPR; i += kThreads) {
           const int k = i / VPR, v = i % VPR;
-          const uint4 val = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v);
-          *reinterpret_cast<uint4*>(dst + k * L::bk_pitch + v * 16) = val;
+          const void* g = reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + k * L::bk_pitch + v * 16),
+                       "l"(g) : "memory");
         }
       }
+      asm volatile("cp.async.commit_group;\n" ::: "memory");
+      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     }
     __syncthreads();
 
-    float O[D / 8][4];
-    float Olr[NLR][4];
+    // O^T [head dims x query rows] and O_lr^T [rank x query rows] accumulators
+    float OT[NMT][RN][4];
+    float OlrT[NLM][RN][4];
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+    for (int i = 0; i < NMT; ++i)
 #pragma unroll
-    for (int i = 0; i < NLR; ++i) Olr[i][0] = Olr[i][1] = Olr[i][2] = Olr[i][3] = 0.f;
-    float m_run[2][2], l_run[2][2];
+      for (int rn = 0; rn < RN; ++rn) OT[i][rn][0] = OT[i][rn][1] = OT[i][rn][2] = OT[i][rn][3] = 0.f;
 #pragma unroll
-    for (int rn = 0; rn < 2; ++rn)
+    for (int i = 0; i < NLM; ++i)
+#pragma unroll
+      for (int rn = 0; rn < RN; ++rn) OlrT[i][rn][0] = OlrT[i][rn][1] = OlrT[i][rn][2] = OlrT[i][rn][3] = 0.f;
+    float m_run[RN][2], l_run[RN][2];
+#pragma unroll
+    for (int rn = 0; rn < RN; ++rn)
 #pragma unroll
       for (int e = 0; e < 2; ++e) { m_run[rn][e] = -CUDART_INF_F; l_run[rn][e] = 0.f; }
 
@@ -402,9 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
-        float sacc[2][4];
+        // two independent score accumulators (low / high head-dim halves) keep the
+        // MMA dependency chain short
+        float sacc[2][RN][4];
 #pragma unroll
-        for (int rn = 0; rn < 2; ++rn) sacc[rn][0] = sacc[rn][1] = sacc[rn][2] = sacc[rn][3] = 0.f;
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int rn = 0; rn < RN; ++rn)
+            sacc[hh][rn][0] = sacc[hh][rn][1] = sacc[hh][rn][2] = sacc[hh][rn][3] = 0.f;
 
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
@@ -483,10 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int tk = 0; tk < 2; ++tk) {
                   const uint32_t x = pack_f16(y[n][2 * tk], y[n][2 * tk + 1]);
                   const uint32_t yy = pack_f16(y[n + 2][2 * tk], y[n + 2][2 * tk + 1]);
-                  const uint32_t lo = hfma2_u32(x, c16[tk][n], hfma2_u32(yy, ns16[tk][n], kb16[n][0][tk]));
-                  const uint32_t hi = hfma2_u32(yy, c16[tk][n], hfma2_u32(x, s16[tk][n], kb16[n][1][tk]));
-                  A_lo[2 * n + tk] = lo;
-                  A_hi[2 * n + tk] = hi;
+                  A_lo[2 * n + tk] = hfma2_u32(x, c16[tk][n], hfma2_u32(yy, ns16[tk][n], kb16[n][0][tk]));
+                  A_hi[2 * n + tk] = hfma2_u32(yy, c16[tk][n], hfma2_u32(x, s16[tk][n], kb16[n][1][tk]));
                 }
             } else {
 #pragma unroll
@@ -499,31 +522,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // scores of this adapter's rows only: its query fragment, other rows zeroed
 #pragma unroll
-            for (int rn = 0; rn < 2; ++rn) {
+            for (int rn = 0; rn < RN; ++rn) {
               if (!((rnm >> rn) & 1)) continue;
               const bool mine = myslot[rn] == a;
               const uint32_t q0 = mine ? qf[rn][cc][0] : 0u, q1 = mine ? qf[rn][cc][1] : 0u;
               const uint32_t q2 = mine ? qf[rn][cc + NCH][0] : 0u, q3 = mine ? qf[rn][cc + NCH][1] : 0u;
-              mma16816_f16(sacc[rn], A_lo, q0, q1);
-              mma16816_f16(sacc[rn], A_hi, q2, q3);
+              mma16816_f16(sacc[0][rn], A_lo, q0, q1);
+              mma16816_f16(sacc[1][rn], A_hi, q2, q3);
             }
           }
         }
 
-        // ---- mask and scale
-        float sv[2][4];
+        // ---- mask and scale (S^T: tokens g8, g8 + 8 x query rows rn*8 + 2*c4 + e)
+        float sv[RN][4];
 #pragma unroll
-        for (int rn = 0; rn < 2; ++rn)
+        for (int rn = 0; rn < RN; ++rn)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int tok = t0 + g8 + 8 * (i >> 1);
-            sv[rn][i] = tok < I.len ? sacc[rn][i] * p.scale_log2 : -CUDART_INF_F;
+            sv[rn][i] = tok < I.len ? (sacc[0][rn][i] + sacc[1][rn][i]) * p.scale_log2 : -CUDART_INF_F;
           }
         // ---- online softmax (per score column = query row)
-        float alpha[2][2];
-        float pr[2][4];
+        float alpha[RN][2];
+        float pr[RN][4];
+        bool moved = false;
 #pragma unroll
-        for (int rn = 0; rn < 2; ++rn)
+        for (int rn = 0; rn < RN; ++rn)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             float mx = fmaxf(sv[rn][e], sv[rn][e + 2]);
@@ -539,66 +563,66 @@ __global__ void __launch_bounds__(kThreads, 1)
               p0 = exp2f(sv[rn][e] - mn);
               p1 = exp2f(sv[rn][e + 2] - mn);
             }
+            moved |= al != 1.f;
             m_run[rn][e] = mn;
             l_run[rn][e] = l_run[rn][e] * al + p0 + p1;
             alpha[rn][e] = al;
             pr[rn][e] = p0;
             pr[rn][e + 2] = p1;
           }
-        // ---- rescale accumulators (rows g8 and g8 + 8 in the PV layout)
-        {
-          const int src = g8 >> 1;
-          const float a00 = __shfl_sync(0xffffffffu, alpha[0][0], src);
-          const float a01 = __shfl_sync(0xffffffffu, alpha[0][1], src);
-          const float a10 = __shfl_sync(0xffffffffu, alpha[1][0], src);
-          const float a11 = __shfl_sync(0xffffffffu, alpha[1][1], src);
-          const float ar0 = (g8 & 1) ? a01 : a00;
-          const float ar1 = (g8 & 1) ? a11 : a10;
-          if (__any_sync(0xffffffffu, ar0 != 1.f || ar1 != 1.f)) {
+        // ---- rescale accumulators: this lane's O^T columns are its own score rows
+        if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) { O[i][0] *= ar0; O[i][1] *= ar0; O[i][2] *= ar1; O[i][3] *= ar1; }
+          for (int rn = 0; rn < RN; ++rn) {
 #pragma unroll
-            for (int i = 0; i < NLR; ++i) { Olr[i][0] *= ar0; Olr[i][1] *= ar0; Olr[i][2] *= ar1; Olr[i][3] *= ar1; }
+            for (int i = 0; i < NMT; ++i) {
+              OT[i][rn][0] *= alpha[rn][0]; OT[i][rn][1] *= alpha[rn][1];
+              OT[i][rn][2] *= alpha[rn][0]; OT[i][rn][3] *= alpha[rn][1];
+            }
+#pragma unroll
+            for (int i = 0; i < NLM; ++i) {
+              OlrT[i][rn][0] *= alpha[rn][0]; OlrT[i][rn][1] *= alpha[rn][1];
+              OlrT[i][rn][2] *= alpha[rn][0]; OlrT[i][rn][3] *= alpha[rn][1];
+            }
           }
         }
-        // ---- P (rows x tokens) A fragment via register transposes
-        uint32_t pa[4];
-        pa[0] = movm_t(pack_bf16(pr[0][0], pr[0][1]));
-        pa[2] = movm_t(pack_bf16(pr[0][2], pr[0][3]));
-        if (RN > 1) {
-          pa[1] = movm_t(pack_bf16(pr[1][0], pr[1][1]));
-          pa[3] = movm_t(pack_bf16(pr[1][2], pr[1][3]));
-        } else {
-          pa[1] = pa[3] = 0u;
-        }
-        // ---- O += P V_base
+        // ---- P^T (tokens x rows) B fragments via register transposes
+        uint32_t pb[RN][2];
 #pragma unroll
-        for (int np = 0; np < D / 16; ++np) {
-          const int mi = lane >> 3;
-          const int tok = (lane & 7) + (mi & 1) * 8;
-          const int dim = 16 * np + (mi >> 1) * 8;
-          uint32_t bb[4];
-          ldsm_x4_t(bb, vt + (dim / 64) * 2048 + swz<128>(tok, (dim % 64) * 2));
-          mma16816(O[2 * np], pa, bb[0], bb[1]);
-          mma16816(O[2 * np + 1], pa, bb[2], bb[3]);
+        for (int rn = 0; rn < RN; ++rn) {
+          pb[rn][0] = movm_t(pack_bf16(pr[rn][0], pr[rn][1]));
+          pb[rn][1] = movm_t(pack_bf16(pr[rn][2], pr[rn][3]));
         }
-        // ---- O_lr += P L_V
+        // ---- O^T += V_base^T P^T (M = head dims, N = query rows, K = tokens)
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+          const int mi = lane >> 3;
+          const int tok = (lane & 7) + (mi >> 1) * 8;
+          const int dim = 16 * mt + (mi & 1) * 8;
+          uint32_t av[4];
+          ldsm_x4_t(av, vt + (dim / 64) * 2048 + swz<128>(tok, (dim % 64) * 2));
+#pragma unroll
+          for (int rn = 0; rn < RN; ++rn) mma16816(OT[mt][rn], av, pb[rn][0], pb[rn][1]);
+        }
+        // ---- O_lr^T += L_V^T P^T
         if (p.has_bv) {
           if constexpr (R >= 16) {
 #pragma unroll
-            for (int np = 0; np < R / 16; ++np) {
+            for (int mt = 0; mt < NLM; ++mt) {
               const int mi = lane >> 3;
-              const int tok = (lane & 7) + (mi & 1) * 8;
-              const int col = 16 * np + (mi >> 1) * 8;
-              uint32_t bb[4];
-              ldsm_x4_t(bb, lvt + swz<LR_RB>(tok, col * 2));
-              mma16816(Olr[2 * np], pa, bb[0], bb[1]);
-              mma16816(Olr[2 * np + 1], pa, bb[2], bb[3]);
+              const int tok = (lane & 7) + (mi >> 1) * 8;
+              const int col = 16 * mt + (mi & 1) * 8;
+              uint32_t av[4];
+              ldsm_x4_t(av, lvt + swz<LR_RB>(tok, col * 2));
+#pragma unroll
+              for (int rn = 0; rn < RN; ++rn) mma16816(OlrT[mt][rn], av, pb[rn][0], pb[rn][1]);
             }
           } else {
-            uint32_t bb[2];
-            ldsm_x2_t(bb, lvt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
-            mma16816(Olr[0], pa, bb[0], bb[1]);
+            uint32_t t2[2];
+            ldsm_x2_t(t2, lvt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
+            const uint32_t av[4] = {t2[0], 0u, t2[1], 0u};  // rank rows 8..15 do not exist
+#pragma unroll
+            for (int rn = 0; rn < RN; ++rn) mma16816(OlrT[0][rn], av, pb[rn][0], pb[rn][1]);
           }
         }
       }
@@ -611,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------ merge the warps
 #pragma unroll
-    for (int rn = 0; rn < 2; ++rn)
+    for (int rn = 0; rn < RN; ++rn)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         float l = l_run[rn][e];
@@ -622,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     if (g8 == 0) {
 #pragma unroll
-      for (int rn = 0; rn < 2; ++rn)
+      for (int rn = 0; rn < RN; ++rn)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int row = rn * 8 + 2 * c4 + e;
@@ -631,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();  // also: every warp is past its B_K reads; acc may alias them now
-    if (tid < kMaxRows) {
+    if (tid < RN * 8) {
       float M = -CUDART_INF_F;
 #pragma unroll
       for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * kMaxRows + tid]);
@@ -644,38 +668,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       sm_L[tid] = Ls;
     }
     {
-      float f[2];
+      // per-row weight of this warp's partial: exp2(m_w - max over warps)
+      float f[RN][2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = g8 + 8 * h;
-        float M = -CUDART_INF_F;
+      for (int rn = 0; rn < RN; ++rn)
 #pragma unroll
-        for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * kMaxRows + row]);
-        const float mw = sm_m[warp * kMaxRows + row];
-        f[h] = (M == -CUDART_INF_F || mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
-      }
-      // fixed-order accumulation (warp 0 writes, warps 1.. add): reproducible bits
+        for (int e = 0; e < 2; ++e) {
+          const int row = rn * 8 + 2 * c4 + e;
+          float M = -CUDART_INF_F;
+#pragma unroll
+          for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * kMaxRows + row]);
+          const float mw = m_run[rn][e];
+          f[rn][e] = (M == -CUDART_INF_F || mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+        }
+      // fixed-order accumulation (warp 0 writes, warps 1.. add): reproducible bits.
+      // acc[row][col]: col = head dim 16*mt + g8 (+8), or D + rank index.
       for (int w = 0; w < kNW; ++w) {
         if (warp == w) {
+          float cur[NMT + NLM][RN][4];
+          if (w > 0) {  // all loads first, then all stores
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (h == 1 && RN == 1) break;
-            float* arow = acc + (g8 + 8 * h) * L::acc_pitch;
+            for (int i = 0; i < NMT + NLM; ++i)
 #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-              float2* d2 = reinterpret_cast<float2*>(arow + 8 * nt + 2 * c4);
-              const float2 v = make_float2(f[h] * O[nt][2 * h], f[h] * O[nt][2 * h + 1]);
-              if (w == 0) *d2 = v;
-              else { float2 o = *d2; o.x += v.x; o.y += v.y; *d2 = o; }
-            }
+              for (int rn = 0; rn < RN; ++rn)
 #pragma unroll
-            for (int nt = 0; nt < NLR; ++nt) {
-              float2* d2 = reinterpret_cast<float2*>(arow + D + 8 * nt + 2 * c4);
-              const float2 v = make_float2(f[h] * Olr[nt][2 * h], f[h] * Olr[nt][2 * h + 1]);
-              if (w == 0) *d2 = v;
-              else { float2 o = *d2; o.x += v.x; o.y += v.y; *d2 = o; }
-            }
+                for (int v = 0; v < 4; ++v) {
+                  const int row = rn * 8 + 2 * c4 + (v & 1);
+                  const int col = (i < NMT ? 16 * i : D + 16 * (i - NMT)) + g8 + 8 * (v >> 1);
+                  cur[i][rn][v] = (i >= NMT && 16 * (i - NMT) + g8 + 8 * (v >> 1) >= R)
+                                      ? 0.f : acc[row * L::acc_pitch + col];
+                }
           }
+#pragma unroll
+          for (int i = 0; i < NMT + NLM; ++i)
+#pragma unroll
+            for (int rn = 0; rn < RN; ++rn)
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int row = rn * 8 + 2 * c4 + (v & 1);
+                const int k = (i < NMT ? 16 * i : 16 * (i - NMT)) + g8 + 8 * (v >> 1);
+                if (i >= NMT && k >= R) continue;
+                const int col = (i < NMT ? 0 : D) + k;
+                const float x = f[rn][v & 1] * (i < NMT ? OT[i][rn][v] : OlrT[i - NMT][rn][v]);
+                acc[row * L::acc_pitch + col] = (w > 0 ? cur[i][rn][v] : 0.f) + x;
+              }
         }
         __syncthreads();
       }
@@ -778,7 +814,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   }
 }
 
-template <int D, int R>
+template <int D, int R, int RN>
 lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& plan,
                 void* workspace, cudaStream_t stream) {
   DecodeParams p{};
@@ -814,7 +850,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   if (!make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, &tl)) return LRKV_ERR_CUDA;
 
   if (plan.n_items > 0) {
-    auto kern = decode_kernel<D, R>;
+    auto kern = decode_kernel<D, R, RN>;
     static bool attr_set = false;  // idempotent per-process kernel attribute
     if (!attr_set) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
@@ -873,6 +909,7 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   if (slots == 0 || total > kSmemLimit) return false;
   const int qg = std::min(kMaxRows / P.g, slots);
   P.qg_size = qg;
+  P.rn = qg * P.g > 8 ? 2 : 1;
   P.nstage = kNST;
   P.smem_bytes = total;
   P.n_qgroups = std::max(1, (max_q_per_ctx + qg - 1) / qg);
@@ -910,8 +947,10 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
 lrkv_status launch_decode_bf16(const lrkv_config& cfg, const DecodeArgs& a,
                                const DecodePlan& plan, void* workspace, cudaStream_t stream) {
   const int D = cfg.head_dim, R = cfg.rank;
-#define LRKV_DEC(d, r) \
-  if (D == d && R == r) return run<d, r>(cfg, a, plan, workspace, stream);
+#define LRKV_DEC(d, r)                                                          \
+  if (D == d && R == r)                                                         \
+    return plan.rn == 1 ? run<d, r, 1>(cfg, a, plan, workspace, stream)         \
+                        : run<d, r, 2>(cfg, a, plan, workspace, stream);
   LRKV_DEC(128, 8) LRKV_DEC(128, 16) LRKV_DEC(128, 32) LRKV_DEC(128, 64)
   LRKV_DEC(64, 8) LRKV_DEC(64, 16) LRKV_DEC(64, 32) LRKV_DEC(64, 64)
 #undef LRKV_DEC

@@ -17,6 +17,7 @@ struct RopeFreqs;  // lrkv_device.cuh
 struct DecodePlan {
   int g;             // query heads per kv head
   int qg_size;       // queries per query group (rows = qg_size * g <= 16)
+  int rn;            // 8-row tiles of query rows (1 or 2)
   int n_qgroups;     // query groups per context
   int n_splits;      // splits of each context's blocks
   int split_blocks;  // blocks per split
