@@ -209,6 +209,44 @@ lrkv_status lrkv_attn_prefill(const lrkv_config* cfg, const void* q, const int32
 size_t lrkv_prefill_workspace_bytes(const lrkv_config* cfg, int32_t num_seqs, int32_t total_q,
                                     int32_t max_q_len, int32_t max_seq_len);
 
+/*
+ * lrkv_attn_decode_noalloc -- lrkv_attn_decode for callers that cannot
+ * allocate device memory.
+ *
+ * The paper has no counterpart: this is a library convenience. Some callers
+ * cannot call cudaMalloc (or any routine that allocates) where they run
+ * decode, e.g. a runtime whose device memory is reserved once at start-up, or
+ * a serving loop that forbids allocation; they cannot supply the workspace of
+ * lrkv_attn_decode. This entry point takes the same arguments minus the
+ * workspace and uses instead a fixed scratch array of
+ * LRKV_NOALLOC_SCRATCH_BYTES held in the library's own device memory (every
+ * GPU that loads the library keeps it until the process exits). It allocates
+ * nothing.
+ *
+ * - Result: identical to lrkv_attn_decode with a workspace of its own.
+ * - Limit: sizes for which lrkv_decode_workspace_bytes(...) exceeds
+ *   LRKV_NOALLOC_SCRATCH_BYTES return LRKV_ERR_WORKSPACE before any launch.
+ * - First call on a device: resolves the array's device address for that
+ *   device (with that device current) and caches it; make that first call
+ *   before any stream capture on the device.
+ * - Sharing: every call on a device uses the same array. Nothing in it needs
+ *   to start at zero (it holds split partials that are written before they
+ *   are read), but calls whose kernels overlap on the GPU (on different
+ *   streams, or from several threads) race on it and give wrong results;
+ *   order them on one stream or with events.
+ * Other arguments, errors and dev_status: as lrkv_attn_decode.
+ */
+#define LRKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+lrkv_status lrkv_attn_decode_noalloc(const lrkv_config* cfg, const void* q, int32_t num_queries,
+                                     const int32_t* ctx_q_start, int32_t num_ctx,
+                                     const int32_t* adapter_ids, const int32_t* block_tables,
+                                     int32_t max_blocks, const int32_t* ctx_lens,
+                                     int32_t max_ctx_len, int32_t max_q_per_ctx,
+                                     const void* base_pool, const void* lr_pool,
+                                     int64_t num_blocks, const void* B_K, const void* B_V,
+                                     int32_t n_adapters, float scale, void* out,
+                                     int32_t* dev_status, lrkv_stream_t stream);
+
 /* Static string naming a status code. */
 const char* lrkv_status_string(lrkv_status status);
 

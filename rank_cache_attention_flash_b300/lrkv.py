@@ -5,7 +5,7 @@ nothing here falls back to another implementation.
 
 Entry points mirror the C ABI in ``include/lrkv.h``:
   append, attn_decode, attn_prefill, decode_workspace_bytes,
-  prefill_workspace_bytes, status_string, version.
+  prefill_workspace_bytes, status_string, version, attn_decode_noalloc.
 """
 from __future__ import annotations
 
@@ -26,7 +26,9 @@ STATUS = {0: "LRKV_OK", 1: "LRKV_ERR_INVALID_ARG", 2: "LRKV_ERR_UNSUPPORTED", 3:
 BF16, FP32 = 0, 1
 
 EXPORTS = ("lrkv_append", "lrkv_attn_decode", "lrkv_decode_workspace_bytes", "lrkv_attn_prefill",
-           "lrkv_prefill_workspace_bytes", "lrkv_status_string", "lrkv_version")
+           "lrkv_prefill_workspace_bytes", "lrkv_status_string", "lrkv_version",
+           "lrkv_attn_decode_noalloc")
+NOALLOC_SCRATCH_BYTES = 16 << 20  # LRKV_NOALLOC_SCRATCH_BYTES in lrkv.h
 
 
 class LrkvError(RuntimeError):
@@ -82,6 +84,9 @@ def load() -> ctypes.CDLL:
     lib.lrkv_attn_prefill.restype = ctypes.c_int
     lib.lrkv_prefill_workspace_bytes.argtypes = [cfgp, _I32, _I32, _I32, _I32]
     lib.lrkv_prefill_workspace_bytes.restype = _SZ
+    lib.lrkv_attn_decode_noalloc.argtypes = [cfgp, _P, _I32, _P, _I32, _P, _P, _I32, _P, _I32, _I32,
+                                             _P, _P, _I64, _P, _P, _I32, _F, _P, _P, _P]
+    lib.lrkv_attn_decode_noalloc.restype = ctypes.c_int
     lib.lrkv_status_string.argtypes = [ctypes.c_int]
     lib.lrkv_status_string.restype = ctypes.c_char_p
     lib.lrkv_version.argtypes = []
@@ -246,4 +251,36 @@ def attn_prefill(cfg: Config, q: torch.Tensor, q_start: torch.Tensor, max_q_len:
         _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream))
     _raise(code, "lrkv_attn_prefill")
+    return out
+
+
+def attn_decode_noalloc(cfg: Config, q: torch.Tensor, ctx_q_start: torch.Tensor,
+                        adapter_ids: torch.Tensor, block_tables: torch.Tensor, ctx_lens: torch.Tensor,
+                        max_ctx_len: int, max_q_per_ctx: int, base_pool: torch.Tensor,
+                        lr_pool: torch.Tensor, B_K: Optional[torch.Tensor], B_V: Optional[torch.Tensor],
+                        out: torch.Tensor, scale: Optional[float] = None,
+                        status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """lrkv_attn_decode_noalloc: decode without a caller workspace, for callers
+    that cannot allocate device memory (the library keeps a fixed scratch array
+    of NOALLOC_SCRATCH_BYTES per device). ``out`` is required: this wrapper
+    allocates nothing either."""
+    lib = load()
+    dev = base_pool.device
+    _check(q, "q", cfg.torch_dtype, dev)
+    for t, n in ((ctx_q_start, "ctx_q_start"), (adapter_ids, "adapter_ids"),
+                 (block_tables, "block_tables"), (ctx_lens, "ctx_lens")):
+        _check(t, n, torch.int32, dev)
+    _check(B_K, "B_K", cfg.torch_dtype, dev)
+    _check(B_V, "B_V", cfg.torch_dtype, dev)
+    _check(status, "status", torch.int32, dev)
+    _check(out, "out", cfg.torch_dtype, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+    n_adapters = 0 if B_K is None and B_V is None else (B_K if B_K is not None else B_V).shape[0]
+    code = lib.lrkv_attn_decode_noalloc(
+        ctypes.byref(cfg), _ptr(q), q.shape[0], _ptr(ctx_q_start), ctx_lens.numel(), _ptr(adapter_ids),
+        _ptr(block_tables), block_tables.shape[1], _ptr(ctx_lens), max_ctx_len, max_q_per_ctx,
+        _ptr(base_pool), _ptr(lr_pool), base_pool.shape[0], _ptr(B_K), _ptr(B_V), n_adapters,
+        float(scale), _ptr(out), _ptr(status), _stream(stream))
+    _raise(code, "lrkv_attn_decode_noalloc")
     return out
