@@ -101,6 +101,7 @@ bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* l
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
+  if (lr_map == nullptr) return true;
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cfg.rank),
                                 static_cast<cuuint64_t>(num_blocks) * 2 * kBlock};
@@ -117,6 +118,26 @@ bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* l
       return false;
   }
   return true;
+}
+
+// Low-rank pool map whose box is `box_cols` wide (>= rank): the columns past
+// the rank read as zero (out-of-bounds fill), so a rank-8 tile lands in smem
+// as a 16-column tile; rows of box_cols * 2 bytes with the matching swizzle.
+bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks, int box_cols,
+                 CUtensorMap* lr_map) {
+  EncodeTiled enc = get_encoder();
+  if (enc == nullptr || box_cols < cfg.rank) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cfg.rank),
+                              static_cast<cuuint64_t>(num_blocks) * 2 * kBlock};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cfg.rank) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), kBlock};
+  const cuuint32_t es[2] = {1, 1};
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  if (box_cols == 32) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (box_cols == 64) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  return enc(lr_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(lr_pool), dims, strides,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace lrkv

@@ -55,9 +55,12 @@ struct DecodeArgs {
 // Host-built RoPE frequency table (theta_j split into two floats).
 void rope_freqs(const lrkv_config& cfg, RopeFreqs* f);
 
-// Tensor maps over the paged pools.
+// Tensor maps over the paged pools (lr_map may be NULL: base map only).
 bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
                     int64_t num_blocks, CUtensorMap* base_map, CUtensorMap* lr_map);
+// Low-rank pool map with a box of box_cols (>= rank) columns, zero-filled past the rank.
+bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks, int box_cols,
+                 CUtensorMap* lr_map);
 
 lrkv_status launch_decode_bf16(const lrkv_config& cfg, const DecodeArgs& a,
                                const DecodePlan& plan, void* workspace, cudaStream_t stream);

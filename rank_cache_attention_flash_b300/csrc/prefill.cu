@@ -1,34 +1,53 @@
-// Causal prefill attention over the paged base + shared-A low-rank cache (bf16).
+// Causal prefill attention over the paged base + shared-A low-rank cache (bf16),
+// on the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // LRAgent (arXiv 2602.01053), Abstract (Flash-LoRA-Attention): each agent's
 // K adapter term L_K B_K is rebuilt per key tile on chip, rotated and added to
 // K_base; the V term is reordered as (P L_V) B_V. PReCache, Abstract: a new
 // turn attends over the context cached by earlier agents plus its own chunk.
 //
-// One CTA per (sequence, kv head, tile of 64 query rows); rows are
-// (query, head-in-group) pairs so the g query heads sharing a kv head share
-// every key tile. A producer warp streams 64-key tiles (4 paged blocks: K/V
-// halves and L_K/L_V) with 2-D TMA copies into an mbarrier ring; each of the
-// four consumer warps rebuilds one block of K_a = K_base + RoPE(L_K B_K,a)
-// into a shared, swizzled fp16 tile, then all four compute S = Q K_a^T (fp16
-// operands, fp32 accumulation), the causal
-// mask (bottom-right aligned), the online softmax, O += P V_base and
-// O_lr += P L_V with legacy warp MMAs. The epilogue applies O_lr B_V,a and 1/l.
+// One CTA per (sequence, kv head, tile of 128 query rows); rows are
+// (query, head-in-group) pairs so that the g query heads sharing a kv head
+// share every key tile. Per stage of 128 keys (8 paged blocks):
+//   Y    = L_K B_K                    tcgen05, 128 keys x d, K = rank  -> TMEM
+//   K_a  = K_base + RoPE(Y)           rebuild warpgroup, in place in the
+//                                     stage's K tile (fp16, never stored to HBM)
+//   S    = Q K_a^T                    tcgen05, Q read from TMEM, two halves of
+//                                     64 keys (double-buffered in TMEM)
+//   P    = online softmax(S)          softmax warpgroup, thread = query row,
+//                                     P written back over S as bf16
+//   O   += P V_base, O_lr += P L_V    tcgen05, P read from TMEM
+// and at the end out = (O + O_lr B_V) / l.
+//
+// Warp roles (320 threads): warp 0 streams K, V, L_K, L_V tiles with 2-D TMA
+// copies into an mbarrier ring; warp 1 owns the tensor memory and one of its
+// lanes issues every MMA (in-order, so a TMEM region is only rewritten after
+// the MMAs reading it were issued); warps 2-5 run the softmax; warps 6-9
+// rebuild K_a. Tensor-memory columns: Q [0, d/2) packed, S0 [64, 128),
+// S1 [128, 192), O [192, 192+d), O_lr [192+d, 192+d+r'), Y [384, 384+d).
+// Every wait is bounded: a wait that gives up stores LRKV_ERR_TIMEOUT, sets a
+// CTA-wide abort flag, and every role leaves its loop; no MMA or copy is left
+// in flight when the tensor memory is released.
 #include <math_constants.h>
 
 #include <algorithm>
 
 #include "lrkv_device.cuh"
 #include "lrkv_internal.h"
+#include "tcgen05.cuh"
 
 namespace lrkv {
 namespace {
 
-constexpr int kNW = 4;
-constexpr int kThreads = (kNW + 1) * 32;
-constexpr int BMQ = 64;   // query rows per CTA (16 per consumer warp)
-constexpr int BKEY = 64;  // keys per tile (kNW blocks)
+constexpr int kThreads = 320;
+constexpr int BM = 128;   // query rows per CTA (= TMEM lanes)
+constexpr int BN = 128;   // keys per stage (8 paged blocks)
+constexpr int HN = 64;    // keys per score half-tile
 constexpr int kSmemLimit = 227 * 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr int Q_COL = 0, S_COL0 = 64, O_COL = 192, Y_COL = 384;
+constexpr int kSmWarp0 = 2, kRbWarp0 = 6;  // first softmax / rebuild warp
+constexpr float kRescaleLog2 = 8.0f;       // rescale O only when the row max grows by > 2^8
 
 struct PrefillParams {
   const __nv_bfloat16* q;
@@ -41,79 +60,109 @@ struct PrefillParams {
   __nv_bfloat16* out;
   int32_t* status;
   int64_t num_blocks;
-  int num_seqs, max_blocks, max_seq_len, n_adapters, Hq, Hkv, g, nstage;
+  int num_seqs, max_blocks, max_seq_len, n_adapters, Hq, Hkv, g;
   int has_bk, has_bv;
   float scale_log2;
   RopeFreqs freqs;
 };
 
-struct PLayout {
-  int kv_tile, lr_tile, stage, ki_buf, bk_pitch, d_pitch;
-  int off_ki, off_bk, off_bv, off_olr, off_dtab, off_btab, off_freq, off_misc, off_bar, total;
-  __host__ __device__ static PLayout make(int D, int R, int nstage) {
-    PLayout L;
-    L.kv_tile = 16 * D * 2;
-    L.lr_tile = 16 * R * 2;
-    L.stage = kNW * (2 * L.kv_tile + 2 * L.lr_tile);
-    L.ki_buf = BKEY * D * 2;
-    L.bk_pitch = (D + 8) * 2;
-    L.d_pitch = (D / 2) * 8 + 64;
-    int o = nstage * L.stage;
-    L.off_ki = o;   o += 2 * L.ki_buf;
-    L.off_bk = o;   o += R * L.bk_pitch;
-    o = (o + 15) & ~15;
-    L.off_bv = o;   o += R * D * 4;
-    L.off_olr = o;  o += BMQ * (R + 4) * 4;
-    L.off_dtab = o; o += 16 * L.d_pitch;
-    L.off_btab = o; o += kNW * (D / 2) * 8;
-    L.off_freq = o; o += 2 * 64 * 4;
-    L.off_misc = o; o += 64;
-    o = (o + 7) & ~7;
-    L.off_bar = o;  o += 2 * nstage * 8;
-    L.total = o + 1024;
-    return L;
-  }
+// Shared-memory layout (byte offsets from a 1024-aligned base).
+template <int D, int R>
+struct PL {
+  static constexpr int RP = R < 16 ? 16 : R;      // rank padded to the MMA granularity
+  static constexpr int LSPAN = RP * 2;            // bytes per low-rank row (32 / 64 / 128)
+  static constexpr int KV = BN * D * 2;           // K or V tile
+  static constexpr int LT = BN * LSPAN;           // L_K or L_V tile
+  static constexpr int STAGE = 2 * KV + 2 * LT;
+  static constexpr int BKB = D * LSPAN;           // B_K^T tile [d][r'], K-major
+  static constexpr int BTAB = 8 * (D / 2) * 8;    // per-stage block start angles (cos, sin)
+  static constexpr int MISC = 256;
+  static constexpr int FIXED = BKB + BTAB + MISC + 1024;
+  static constexpr int NST_FIT = (kSmemLimit - FIXED) / STAGE;
+  static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
+  static constexpr int off_k = 0, off_v = KV, off_lk = 2 * KV, off_lv = 2 * KV + LT;
+  static constexpr int off_bk = NST * STAGE;
+  static constexpr int off_btab = off_bk + BKB;
+  static constexpr int off_misc = off_btab + BTAB;
+  static constexpr int total = off_misc + MISC + 1024;  // + alignment slack
+  static_assert(NST >= 2, "two pipeline stages must fit");
+  static_assert(total <= kSmemLimit, "shared memory");
+  static_assert(192 + D + RP <= Y_COL, "tensor-memory columns");
 };
+
+// Barrier slots inside the misc area (8 bytes each).
+enum : int {
+  B_FULL = 0,    // [4] TMA -> consumers (one phase per stage use)
+  B_EMPTY = 4,   // [4] MMA commit -> producer
+  B_KA = 8,      // [4] rebuild warpgroup -> MMA (K_a written)
+  B_YFULL = 12,  // MMA commit -> rebuild (Y in TMEM)
+  B_YFREE = 13,  // rebuild -> MMA (Y read)
+  B_SFULL = 14,  // [2] MMA commit -> softmax (S half-tile in TMEM)
+  B_PFULL = 16,  // [2] softmax -> MMA (P written, O rescaled)
+  B_OBAR = 18,   // MMA commit after each P V
+  B_DRAIN = 19,  // MMA commit on abort: every issued MMA has completed
+  B_COUNT = 20
+};
+
+__device__ __forceinline__ bool try_wait_parity(uint32_t bar, uint32_t parity) {
+  return mbar_try_wait(bar, parity);
+}
+
+// Named barrier over `count` threads that also ORs a predicate across them:
+// every participant gets the same answer, so a group can leave a loop together.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 template <int D, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p,
                    const __grid_constant__ CUtensorMap tm_base,
                    const __grid_constant__ CUtensorMap tm_lr) {
+  using L = PL<D, R>;
   constexpr int HALF = D / 2;
-  constexpr int NCH = D / 32;
-  constexpr int NKS = D / 16;
-  constexpr int NRT = R >= 16 ? R / 16 : 1;
-  constexpr int NLR = R / 8;
-  constexpr int LR_RB = R * 2;
+  constexpr int RP = L::RP;
+  constexpr int LSPAN = L::LSPAN;
+  constexpr int NST = L::NST;
+  constexpr int OLR_COL = O_COL + D;
+  constexpr uint32_t SW_LR = tc::swizzle_code(LSPAN);
+  constexpr uint32_t kIdY = tc::idesc_f16(128, D, true, false, false);
+  constexpr uint32_t kIdS16 = tc::idesc_f16(128, HN, false, false, false);  // fp16 Q, K_a
+  constexpr uint32_t kIdSbf = tc::idesc_f16(128, HN, true, false, false);   // bf16 Q, K_base
+  constexpr uint32_t kIdPV = tc::idesc_f16(128, D, true, false, true);
+  constexpr uint32_t kIdPLV = tc::idesc_f16(128, RP, true, false, true);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const PLayout L = PLayout::make(D, R, p.nstage);
   const uint32_t sbase = smem_u32(smem);
-  float2* dtab = reinterpret_cast<float2*>(smem + L.off_dtab);
-  float* freq = reinterpret_cast<float*>(smem + L.off_freq);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_misc);
-  int* stage_mask = reinterpret_cast<int*>(smem + L.off_misc + 16);
-  const uint32_t bar_full = sbase + L.off_bar;
-  const uint32_t bar_empty = bar_full + 8 * p.nstage;
+  const uint32_t bars = sbase + L::off_misc;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_misc + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc + 8 * B_COUNT + 4);
+  int* stage_mask = reinterpret_cast<int*>(smem + L::off_misc + 8 * B_COUNT + 8);  // [NST]
+  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab);                  // [8][HALF]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g8 = lane >> 2, c4 = lane & 3;
-  const int s = blockIdx.z, head = blockIdx.y, tile = blockIdx.x;
-
-  const int qs = __ldg(p.q_start + s), qe = __ldg(p.q_start + s + 1);
+  const int s_row = blockIdx.z, head = blockIdx.y;
+  const int qs = __ldg(p.q_start + s_row), qe = __ldg(p.q_start + s_row + 1);
   const int q_len = qe - qs;
-  int Ls = __ldg(p.seq_lens + s);
+  const int Ls = __ldg(p.seq_lens + s_row);
   const int g = p.g;
-  const int row0 = tile * BMQ;             // first (query, head) row of this CTA
-  if (row0 >= q_len * g) return;           // whole CTA beyond this sequence's chunk
-  if (Ls < q_len || Ls > p.max_seq_len) {  // inconsistent lengths: skip, report
+  const int row0 = blockIdx.x * BM;
+  if (q_len <= 0 || row0 >= q_len * g) return;  // whole CTA beyond this sequence's chunk
+  if (Ls < q_len || Ls > p.max_seq_len) {       // inconsistent lengths: skip, report
     if (tid == 0) report(p.status, LRKV_ERR_INDEX);
     return;
   }
-  int adapter = __ldg(p.adapter_ids + s);
+  int adapter = __ldg(p.adapter_ids + s_row);
   if (adapter < -1 || adapter >= p.n_adapters) {
     if (tid == 0) report(p.status, LRKV_ERR_INDEX);
     adapter = -1;
@@ -121,453 +170,514 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool rebuild = p.has_bk && adapter >= 0;
   const bool use_lr = p.has_bv && adapter >= 0;
   const int k_first = row0 / g;
-  const int k_last = min(q_len, (row0 + BMQ + g - 1) / g) - 1;
+  const int k_last = min(q_len, (row0 + BM + g - 1) / g) - 1;
   const int pos_min = Ls - q_len + k_first;
   const int pos_max = Ls - q_len + k_last;
-  const int n_tiles = (pos_max + BKEY) / BKEY;  // keys 0 .. pos_max
+  const int U = (pos_max + HN) / HN;     // score half-tiles covering keys 0 .. pos_max
+  const int n_st = (U + 1) / 2;          // stages of 128 keys
 
-  // ---- prologue
-  if (tid < HALF) {
-    freq[tid] = p.freqs.hi[tid];
-    freq[64 + tid] = p.freqs.lo[tid];
-  }
+  // ---------------------------------------------------------------- setup
   if (tid == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < p.nstage; ++i) {
-      mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, kNW);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(B_FULL + i), 1);
+      mbar_init(bar(B_EMPTY + i), 1);
+      mbar_init(bar(B_KA + i), 128);
     }
+    mbar_init(bar(B_YFULL), 1);
+    mbar_init(bar(B_YFREE), 128);
+    mbar_init(bar(B_SFULL + 0), 1);
+    mbar_init(bar(B_SFULL + 1), 1);
+    mbar_init(bar(B_PFULL + 0), 128);
+    mbar_init(bar(B_PFULL + 1), 128);
+    mbar_init(bar(B_OBAR), 1);
+    mbar_init(bar(B_DRAIN), 1);
     mbar_fence_init();
   }
+  if (warp == 1) tc::alloc(smem_u32(tmem_slot), kTmemCols);
+  tc::fence_before();
   __syncthreads();
-  for (int i = tid; i < 16 * HALF; i += kThreads) {
-    const int dl = i / HALF, j = i % HALF;
-    *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(dtab) + dl * L.d_pitch + j * 8) =
-        rope_cos_sin(dl, freq[j], freq[64 + j]);
-  }
-  if (rebuild) {
-    const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
-    for (int i = tid; i < R * (D / 8); i += kThreads) {
-      const int k = i / (D / 8), v = i % (D / 8);
-      *reinterpret_cast<uint4*>(smem + L.off_bk + k * L.bk_pitch + v * 16) =
-          __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v);
+  tc::fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;  // this warp's TMEM lanes
+
+  // Rebuild warpgroup state: per-row RoPE delta factors cos/sin(r * theta_j),
+  // r = key % 16, packed (cos, sin) as fp16 pairs.
+  uint32_t dl[HALF];
+  const int rb_i = 32 * (warp & 3) + lane;  // key row (rebuild) or query row (softmax) in the tile
+  if (warp >= kRbWarp0) {
+    const int r = rb_i & 15;
+#pragma unroll
+    for (int j = 0; j < HALF; ++j) {
+      const float2 cs = rope_cos_sin(r, p.freqs.hi[j], p.freqs.lo[j]);
+      dl[j] = pack_f16(cs.x, cs.y);
+    }
+    if (rebuild) {
+      // B_K^T [d][r'] (K-major, swizzled like the L_K tiles), zero beyond rank R
+      const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
+      const int rt = tid - kRbWarp0 * 32;
+      for (int e = rt; e < D * (RP / 2); e += 128) {
+        const int n = e % D, k2 = e / D;
+        const int k0 = 2 * k2;
+        const uint32_t lo = k0 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0) * p.Hkv * D + n]) : 0u;
+        const uint32_t hi = k0 + 1 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0 + 1) * p.Hkv * D + n]) : 0u;
+        *reinterpret_cast<uint32_t*>(smem + L::off_bk + swz<LSPAN>(n, 4 * k2)) = lo | (hi << 16);
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     }
   }
-  if (use_lr) {
-    const __nv_bfloat16* src = p.B_V + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
-    float* bv = reinterpret_cast<float*>(smem + L.off_bv);
-    for (int i = tid; i < R * D; i += kThreads)
-      bv[i] = __bfloat162float(src[static_cast<int64_t>(i / D) * p.Hkv * D + i % D]);
+  // Softmax warpgroup: its query row into TMEM (fp16 when K_a is fp16, else bf16).
+  const int sm_r = row0 + rb_i;
+  const int sm_k = sm_r / g;
+  const bool sm_valid = sm_k < q_len;
+  const int sm_pos = Ls - q_len + (sm_valid ? sm_k : 0);
+  if (warp >= kSmWarp0 && warp < kRbWarp0) {
+    const __nv_bfloat16* qrow =
+        p.q + (static_cast<int64_t>(qs + (sm_valid ? sm_k : 0)) * p.Hq + head * g + sm_r % g) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[16];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        uint4 u = sm_valid ? __ldg(reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * x)) : make_uint4(0, 0, 0, 0);
+        v[4 * x + 0] = rebuild ? bf16x2_to_f16x2(u.x) : u.x;
+        v[4 * x + 1] = rebuild ? bf16x2_to_f16x2(u.y) : u.y;
+        v[4 * x + 2] = rebuild ? bf16x2_to_f16x2(u.z) : u.z;
+        v[4 * x + 3] = rebuild ? bf16x2_to_f16x2(u.w) : u.w;
+      }
+      tc::st_x16(tbase + lane_off + Q_COL + 16 * c, v);
+    }
+    tc::wait_st();
   }
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
 
-  const int nblk_seq = (Ls + kBlock - 1) / kBlock;
-
-  // ======================================================== producer warp
-  if (warp == kNW) {
+  // ============================================================ producer
+  if (warp == 0) {
     if (lane == 0) {
       prefetch_tmap(&tm_base);
       prefetch_tmap(&tm_lr);
-      int stage = 0;
-      uint32_t phase = 0, issued = 0;
-      bool ok = true;
-      for (int kt = 0; kt < n_tiles; ++kt) {
-        if (*abort_flag || !mbar_wait(bar_empty + 8 * stage, phase ^ 1, p.status)) {
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        int mask = 0, blks[kNW];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) {
-          blks[w] = -1;
-          const int b = kt * kNW + w;
-          if (b >= nblk_seq) continue;
-          const int blk = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks + b);
-          if (blk < 0 || blk >= p.num_blocks) {
-            report(p.status, LRKV_ERR_INDEX);
-            continue;
-          }
-          blks[w] = blk;
-          mask |= 1 << w;
-          bytes += 2 * L.kv_tile + (rebuild ? L.lr_tile : 0) + (use_lr ? L.lr_tile : 0);
-        }
-        stage_mask[stage] = mask;
-        const uint32_t fb = bar_full + 8 * stage;
-        mbar_arrive_expect_tx(fb, bytes);
-        issued |= 1u << stage;
-        const uint32_t st = sbase + stage * L.stage;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) {
-          if (blks[w] < 0) continue;
-          const int blk = blks[w];
-          const int yk = ((blk * 2 + 0) * p.Hkv + head) * kBlock;
-          const int yv = ((blk * 2 + 1) * p.Hkv + head) * kBlock;
-          const uint32_t kt_s = st + w * L.kv_tile;
-          const uint32_t vt_s = st + kNW * L.kv_tile + w * L.kv_tile;
-#pragma unroll
-          for (int h = 0; h < D / 64; ++h) {
-            tma_load_2d(kt_s + h * 2048, &tm_base, 64 * h, yk, fb);
-            tma_load_2d(vt_s + h * 2048, &tm_base, 64 * h, yv, fb);
-          }
-          const uint32_t lk = st + 2 * kNW * L.kv_tile + w * L.lr_tile;
-          if (rebuild) tma_load_2d(lk, &tm_lr, 0, (blk * 2 + 0) * kBlock, fb);
-          if (use_lr) tma_load_2d(lk + kNW * L.lr_tile, &tm_lr, 0, (blk * 2 + 1) * kBlock, fb);
-        }
-        if (++stage == p.nstage) {
-          stage = 0;
-          phase ^= 1;
-        }
+    }
+    const int nblk_vis = pos_max / kBlock + 1;  // blocks holding a key some row sees
+    const uint32_t per_blk = 2u * kBlock * D * 2 + (rebuild ? kBlock * LSPAN : 0) +
+                             (use_lr ? kBlock * LSPAN : 0);
+    int issued = 0;
+    for (int j = 0; j < n_st; ++j) {
+      const int s = j % NST;
+      int ok = 1;
+      if (lane == 0) {
+        if (*abort_flag) ok = 0;
+        else if (j >= NST && !mbar_wait(bar(B_EMPTY + s), ((j / NST) - 1) & 1, p.status)) ok = 0;
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
-        for (int i = 0; i < p.nstage; ++i)
-          if (issued >> i & 1) mbar_wait(bar_full + 8 * i, (i < stage) ? phase : (phase ^ 1), nullptr, 1u << 16);
+        *abort_flag = 1;
+        break;
       }
+      int blk = -1;
+      const int bi = j * 8 + lane;
+      if (lane < 8 && bi < nblk_vis) {
+        const int b = __ldg(p.block_tables + static_cast<int64_t>(s_row) * p.max_blocks + bi);
+        if (b >= 0 && b < p.num_blocks) blk = b;
+        else report(p.status, LRKV_ERR_INDEX);
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, blk >= 0);
+      if (lane == 0) {
+        stage_mask[s] = static_cast<int>(mask);
+        mbar_arrive_expect_tx(bar(B_FULL + s), __popc(mask) * per_blk);
+      }
+      __syncwarp();
+      if (blk >= 0) {
+        const uint32_t st = sbase + s * L::STAGE;
+        const uint32_t fb = bar(B_FULL + s);
+        const int yk = ((blk * 2 + 0) * p.Hkv + head) * kBlock;
+        const int yv = ((blk * 2 + 1) * p.Hkv + head) * kBlock;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_2d(st + L::off_k + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yk, fb);
+          tma_load_2d(st + L::off_v + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yv, fb);
+        }
+        if (rebuild) tma_load_2d(st + L::off_lk + lane * kBlock * LSPAN, &tm_lr, 0, (blk * 2 + 0) * kBlock, fb);
+        if (use_lr) tma_load_2d(st + L::off_lv + lane * kBlock * LSPAN, &tm_lr, 0, (blk * 2 + 1) * kBlock, fb);
+      }
+      ++issued;
     }
-    return;
+    // after an abort, never leave copies in flight (bounded waits)
+    if (lane == 0 && *abort_flag) {
+      for (int j = max(0, issued - NST); j < issued; ++j)
+        mbar_wait(bar(B_FULL + j % NST), (j / NST) & 1, nullptr, 1u << 16);
+    }
   }
 
-  // ======================================================= consumer warps
-  float2* btab = reinterpret_cast<float2*>(smem + L.off_btab) + warp * HALF;
-  // Q A fragments: rows (16*warp + g8, + 8), straight from global
-  uint32_t qa[NKS][4];
-  int rpos[2];
-  bool rvalid[2];
+  // ================================================================= MMA
+  if (warp == 1 && lane == 0) {
+    const uint32_t idS = rebuild ? kIdS16 : kIdSbf;
+    int u_s = 0, u_p = 0, j_y = 0;
+    uint32_t idle = 0;
+    while (u_p < U) {
+      bool progress = false;
+      if (*abort_flag) break;
+      // Y(j) = L_K B_K for the next stage (needs its tiles and the Y buffer)
+      if (rebuild && j_y < n_st && (j_y == 0 || try_wait_parity(bar(B_YFREE), (j_y - 1) & 1)) &&
+          try_wait_parity(bar(B_FULL + j_y % NST), (j_y / NST) & 1)) {
+        tc::fence_after();
+        const uint32_t st = sbase + (j_y % NST) * L::STAGE;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = row0 + 16 * warp + g8 + 8 * h;
-    const int k = r / g;
-    rvalid[h] = k < q_len;
-    rpos[h] = Ls - q_len + (rvalid[h] ? k : 0);
-    const __nv_bfloat16* qrow =
-        p.q + (static_cast<int64_t>(qs + (rvalid[h] ? k : 0)) * p.Hq + head * g + r % g) * D;
+        for (int kk = 0; kk < RP / 16; ++kk) {
+          const uint64_t a = tc::sdesc(st + L::off_lk + kk * 32, 16, 8 * LSPAN, SW_LR);
+          const uint64_t b = tc::sdesc(sbase + L::off_bk + kk * 32, 16, 8 * LSPAN, SW_LR);
+          tc::mma_ss(tbase + Y_COL, a, b, kIdY, kk > 0);
+        }
+        tc::commit(bar(B_YFULL));
+        ++j_y;
+        progress = true;
+      }
+      // S(u) = Q K_a^T for the next half-tile (its buffer was last read by P V(u-2))
+      if (u_s < U && u_p >= u_s - 1 &&
+          ((u_s & 1) || try_wait_parity(bar(B_KA + (u_s >> 1) % NST), ((u_s >> 1) / NST) & 1))) {
+        tc::fence_after();
+        const uint32_t kt = sbase + ((u_s >> 1) % NST) * L::STAGE + L::off_k + (u_s & 1) * HN * 128;
+        const uint32_t dcol = tbase + S_COL0 + 64 * (u_s & 1);
 #pragma unroll
-    for (int ks = 0; ks < NKS; ++ks) {
-      qa[ks][h] = rvalid[h] ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4))) : 0u;
-      qa[ks][h + 2] = rvalid[h] ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c4))) : 0u;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t b = tc::sdesc(kt + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024, 2);
+          tc::mma_ts(dcol, tbase + Q_COL + ks * 8, b, idS, ks > 0);
+        }
+        tc::commit(bar(B_SFULL + (u_s & 1)));
+        ++u_s;
+        progress = true;
+      }
+      // O += P V_base, O_lr += P L_V for the oldest half-tile whose P is ready
+      if (u_p < u_s && try_wait_parity(bar(B_PFULL + (u_p & 1)), (u_p >> 1) & 1)) {
+        tc::fence_after();
+        const int s = (u_p >> 1) % NST;
+        const uint32_t st = sbase + s * L::STAGE;
+        const uint32_t pcol = tbase + S_COL0 + 64 * (u_p & 1);
+        const uint32_t vt = st + L::off_v + (u_p & 1) * HN * 128;
+#pragma unroll
+        for (int kk = 0; kk < HN / 16; ++kk) {
+          const uint64_t b = tc::sdesc(vt + kk * 16 * 128, BN * 128, 1024, 2);
+          tc::mma_ts(tbase + O_COL, pcol + kk * 8, b, kIdPV, (u_p > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (use_lr) {
+          const uint32_t lvt = st + L::off_lv + (u_p & 1) * HN * LSPAN;
+#pragma unroll
+          for (int kk = 0; kk < HN / 16; ++kk) {
+            const uint64_t b = tc::sdesc(lvt + kk * 16 * LSPAN, BN * LSPAN, 8 * LSPAN, SW_LR);
+            tc::mma_ts(tbase + OLR_COL, pcol + kk * 8, b, kIdPLV, (u_p > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        tc::commit(bar(B_OBAR));
+        if ((u_p & 1) || u_p == U - 1) tc::commit(bar(B_EMPTY + s));
+        ++u_p;
+        progress = true;
+      }
+      if (progress) {
+        idle = 0;
+      } else if (++idle > (1u << 24)) {
+        report(p.status, LRKV_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      } else if (idle > 256) {
+        __nanosleep(32);
+      }
+    }
+    // drain: every MMA issued so far completes before the tensor memory is released
+    if (*abort_flag) {
+      tc::commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0, nullptr, 1u << 16);
     }
   }
-  float O[D / 8][4];
-  float Olr[NLR][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
-#pragma unroll
-  for (int i = 0; i < NLR; ++i) Olr[i][0] = Olr[i][1] = Olr[i][2] = Olr[i][3] = 0.f;
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.f, 0.f};
 
-  int stage = 0;
-  uint32_t phase = 0;
-  for (int kt = 0; kt < n_tiles; ++kt) {
-    // every wait result is made warp-uniform before any warp-collective use
-    bool ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
-    if (ok) ok = mbar_wait(bar_full + 8 * stage, phase, p.status);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) *abort_flag = 1;
-    const int mask = ok ? stage_mask[stage] : 0;
-    const uint32_t st = sbase + stage * L.stage;
-    const uint32_t ki = sbase + L.off_ki + (kt & 1) * L.ki_buf;
-
-    // ---- this warp's block: K_a = K_base + RoPE(L_K B_K) -> ki (swizzled)
-    {
-      const int b = kt * kNW + warp;
-      const int t0 = b * kBlock;
-      const uint32_t kts = st + warp * L.kv_tile;
-      const uint32_t lkt = st + 2 * kNW * L.kv_tile + warp * L.lr_tile;
-      const bool have = (mask >> warp) & 1;
-      // Rows past the sequence end may hold stale pool memory: zero their V and
-      // L_V rows so that P = 0 there cannot meet a NaN in the PV products.
-      if (have && t0 + kBlock > Ls) {
-        const uint32_t vts = st + kNW * L.kv_tile + warp * L.kv_tile;
-        const uint32_t lvts = lkt + kNW * L.lr_tile;
-        const int r0 = Ls - t0;
-        for (int i = lane; i < (kBlock - r0) * (D / 8); i += 32) {
-          const int r = r0 + i / (D / 8), v = i % (D / 8);
-          const uint32_t a = vts + (v / 8) * 2048 + r * 128 + (v % 8) * 16;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
-        }
-        for (int i = lane; i < (kBlock - r0) * (R / 8); i += 32) {
-          const int r = r0 + i / (R / 8), v = i % (R / 8);
-          const uint32_t a = lvts + r * LR_RB + v * 16;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
-        }
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        __syncwarp();
+  // ============================================================ softmax
+  if (warp >= kSmWarp0 && warp < kRbWarp0) {
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    const float sc = p.scale_log2;
+    int u = 0;
+    for (; u < U; ++u) {
+      const int b = u & 1;
+      bool ok = !*abort_flag && mbar_wait(bar(B_SFULL + b), (u >> 1) & 1, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        break;
       }
-      if (rebuild && have) {
-        for (int j = lane; j < HALF; j += 32) btab[j] = rope_cos_sin(t0, freq[j], freq[64 + j]);
-        __syncwarp();
-      }
-      uint32_t alk[NRT][4];
-      if (rebuild && have) {
-        if constexpr (R >= 16) {
+      tc::fence_after();
+      uint32_t sv[64];
+      {
+        uint32_t a[32], c[32];
+        tc::ld_x32(tbase + lane_off + S_COL0 + 64 * b, a);
+        tc::ld_x32(tbase + lane_off + S_COL0 + 64 * b + 32, c);
+        tc::wait_ld();
 #pragma unroll
-          for (int ks = 0; ks < NRT; ++ks) {
-            const int mi = lane >> 3;
-            ldsm_x4(alk[ks], lkt + swz<LR_RB>((lane & 7) + (mi & 1) * 8, (2 * ks + (mi >> 1)) * 16));
-          }
-        } else {
-          uint32_t t2[2];
-          ldsm_x2(t2, lkt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
-          alk[0][0] = t2[0];
-          alk[0][1] = t2[1];
-          alk[0][2] = alk[0][3] = 0u;
+        for (int e = 0; e < 32; ++e) {
+          sv[e] = a[e];
+          sv[32 + e] = c[e];
         }
       }
-#pragma unroll
-      for (int cc = 0; cc < NCH; ++cc) {
-        uint32_t kbv[2][2][2];
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int tk = 0; tk < 2; ++tk) {
-              const int j = 16 * cc + 8 * n + 2 * c4 + h * HALF;
-              uint32_t v = 0u;
-              if (have) {
-                const uint32_t addr = kts + (j / 64) * 2048 + swz<128>(g8 + 8 * tk, (j % 64) * 2);
-                asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
-              }
-              kbv[n][h][tk] = v;
-            }
-        uint32_t outv[2][2][2];
-        if (rebuild && have) {
-          float2 cs[2][2][2];
-#pragma unroll
-          for (int n = 0; n < 2; ++n) {
-            const int j = 16 * cc + 8 * n + 2 * c4;
-            const float4 bq = *reinterpret_cast<const float4*>(btab + j);
-#pragma unroll
-            for (int tk = 0; tk < 2; ++tk) {
-              const float4 dq = *reinterpret_cast<const float4*>(
-                  reinterpret_cast<const uint8_t*>(dtab) + (g8 + 8 * tk) * L.d_pitch + j * 8);
-              cs[tk][n][0] = make_float2(bq.x * dq.x - bq.y * dq.y, bq.y * dq.x + bq.x * dq.y);
-              cs[tk][n][1] = make_float2(bq.z * dq.z - bq.w * dq.w, bq.w * dq.z + bq.z * dq.w);
-            }
-          }
-          float y[4][4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.f;
-          const uint32_t bk = sbase + L.off_bk;
-          if constexpr (R >= 16) {
-#pragma unroll
-            for (int ks = 0; ks < NRT; ++ks)
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int mi = lane >> 3;
-                const int krow = 16 * ks + (lane & 7) + (mi & 1) * 8;
-                const int ncol = 16 * cc + h * HALF + (mi >> 1) * 8;
-                uint32_t bb[4];
-                ldsm_x4_t(bb, bk + krow * L.bk_pitch + ncol * 2);
-                mma16816(y[2 * h + 0], alk[ks], bb[0], bb[1]);
-                mma16816(y[2 * h + 1], alk[ks], bb[2], bb[3]);
-              }
-          } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int ncol = 16 * cc + h * HALF + ((lane >> 3) & 1) * 8;
-              uint32_t bb[2];
-              ldsm_x2_t(bb, bk + (lane & 7) * L.bk_pitch + ncol * 2);
-              mma1688(y[2 * h + 0], alk[0][0], alk[0][1], bb[0]);
-              mma1688(y[2 * h + 1], alk[0][0], alk[0][1], bb[1]);
-            }
-          }
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int tk = 0; tk < 2; ++tk) {
-              float lo2[2], hi2[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int i = 2 * tk + e;
-                const float x = y[n][i], yy = y[n + 2][i];
-                const float c = cs[tk][n][e].x, sn = cs[tk][n][e].y;
-                const float blo = e ? bf16_hi(kbv[n][0][tk]) : bf16_lo(kbv[n][0][tk]);
-                const float bhi = e ? bf16_hi(kbv[n][1][tk]) : bf16_lo(kbv[n][1][tk]);
-                lo2[e] = fmaf(x, c, fmaf(-yy, sn, blo));
-                hi2[e] = fmaf(yy, c, fmaf(x, sn, bhi));
-              }
-              outv[n][0][tk] = pack_f16(lo2[0], lo2[1]);
-              outv[n][1][tk] = pack_f16(hi2[0], hi2[1]);
-            }
-        } else {
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int tk = 0; tk < 2; ++tk) outv[n][h][tk] = bf16x2_to_f16x2(kbv[n][h][tk]);
-        }
-        // store into ki: [D/64 halves][64 keys][64 dims], 128-byte swizzle
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int tk = 0; tk < 2; ++tk) {
-              const int j = 16 * cc + 8 * n + 2 * c4 + h * HALF;
-              const int key = 16 * warp + g8 + 8 * tk;
-              const uint32_t addr = ki + (j / 64) * (BKEY * 128) + swz<128>(key, (j % 64) * 2);
-              asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(addr), "r"(outv[n][h][tk]) : "memory");
-            }
-      }
-    }
-    named_bar_sync(1, kNW * 32);
-
-    // ---- S = Q K_a^T for this warp's 16 rows x 64 keys
-    float sacc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < NKS; ++ks)
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int mi = lane >> 3;
-        const int key = 16 * np + (lane & 7) + (mi >> 1) * 8;
-        const int dim = 16 * ks + (mi & 1) * 8;
-        uint32_t bb[4];
-        ldsm_x4(bb, ki + (dim / 64) * (BKEY * 128) + swz<128>(key, (dim % 64) * 2));
-        mma16816_f16(sacc[2 * np], qa[ks], bb[0], bb[1]);
-        mma16816_f16(sacc[2 * np + 1], qa[ks], bb[2], bb[3]);
-      }
-    // ---- mask, online softmax (rows g8, g8 + 8)
-    const int key0 = kt * BKEY;
-    const bool need_mask = key0 + BKEY - 1 > pos_min;
-    float alpha[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+      const int key0 = u * HN;
+      const int bm = (stage_mask[(u >> 1) % NST] >> (4 * (u & 1))) & 0xF;
+      const bool need_mask = (key0 + HN - 1 > pos_min) || bm != 0xF || !sm_valid;
       float mx = -CUDART_INF_F;
+      if (need_mask) {
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = key0 + 8 * nt + 2 * c4 + e;
-          const int blkw = (8 * nt + 2 * c4 + e) >> 4;
-          float v = sacc[nt][2 * h + e] * p.scale_log2;
-          const bool vis = ((mask >> blkw) & 1) && (!need_mask || key <= rpos[h]) && rvalid[h];
-          v = vis ? v : -CUDART_INF_F;
-          sacc[nt][2 * h + e] = v;
+        for (int c = 0; c < HN; ++c) {
+          const bool vis = sm_valid && (key0 + c <= sm_pos) && ((bm >> (c >> 4)) & 1);
+          const float v = vis ? __uint_as_float(sv[c]) : -CUDART_INF_F;
+          sv[c] = __float_as_uint(v);
           mx = fmaxf(mx, v);
         }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float mn = fmaxf(m_run[h], mx);
-      float sum = 0.f;
-      if (mn == -CUDART_INF_F) {
-        alpha[h] = 1.f;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) sacc[nt][2 * h] = sacc[nt][2 * h + 1] = 0.f;
       } else {
-        alpha[h] = exp2f(m_run[h] - mn);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float pv = exp2f(sacc[nt][2 * h + e] - mn);
-            sacc[nt][2 * h + e] = pv;
-            sum += pv;
-          }
+        for (int c = 0; c < HN; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
       }
-      m_run[h] = mn;
-      l_run[h] = l_run[h] * alpha[h] + sum;
+      const float mt = mx * sc;  // -inf stays -inf
+      bool resc = false;
+      float alpha = 1.f;
+      if (mt > m_run) {
+        if (m_run == -CUDART_INF_F) {
+          m_run = mt;  // first visible key of this row: O and O_lr rows are still zero
+        } else if (mt > m_run + kRescaleLog2) {
+          alpha = exp2f(m_run - mt);
+          m_run = mt;
+          resc = true;
+        }
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // O and O_lr must not be in use by P V(u-1): wait for it, then rescale
+        bool okw = mbar_wait(bar(B_OBAR), (u - 1) & 1, p.status);
+        okw = __all_sync(0xffffffffu, okw);
+        if (!okw) {
+          *abort_flag = 1;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tc::ld_x32(tbase + lane_off + O_COL + 32 * c, v);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tc::st_x32(tbase + lane_off + O_COL + 32 * c, v);
+        }
+        if (use_lr) {
+#pragma unroll
+          for (int c = 0; c < RP / 16; ++c) {
+            uint32_t v[16];
+            tc::ld_x16(tbase + lane_off + OLR_COL + 16 * c, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tc::st_x16(tbase + lane_off + OLR_COL + 16 * c, v);
+          }
+        }
+        l_run *= alpha;
+      }
+      uint32_t pk[32];
+      float sum = 0.f;
+      if (m_run == -CUDART_INF_F) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = 0u;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = exp2f(fmaf(__uint_as_float(sv[2 * c]), sc, -m_run));
+          const float p1 = exp2f(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -m_run));
+          sum += p0 + p1;
+          pk[c] = pack_bf16(p0, p1);
+        }
+      }
+      l_run += sum;
+      tc::st_x32(tbase + lane_off + S_COL0 + 64 * b, pk);
+      tc::wait_st();
+      tc::fence_before();
+      mbar_arrive(bar(B_PFULL + b));
     }
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) { O[i][0] *= alpha[0]; O[i][1] *= alpha[0]; O[i][2] *= alpha[1]; O[i][3] *= alpha[1]; }
-#pragma unroll
-    for (int i = 0; i < NLR; ++i) { Olr[i][0] *= alpha[0]; Olr[i][1] *= alpha[0]; Olr[i][2] *= alpha[1]; Olr[i][3] *= alpha[1]; }
-
-    // ---- O += P V_base, O_lr += P L_V (one 16-key block per k-step)
-#pragma unroll
-    for (int kk = 0; kk < kNW; ++kk) {
-      if (!((mask >> kk) & 1)) continue;
-      uint32_t pa[4];
-      pa[0] = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
-      pa[1] = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
-      pa[2] = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-      pa[3] = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-      const uint32_t vt = st + kNW * L.kv_tile + kk * L.kv_tile;
-#pragma unroll
-      for (int np = 0; np < D / 16; ++np) {
-        const int mi = lane >> 3;
-        const int tok = (lane & 7) + (mi & 1) * 8;
-        const int dim = 16 * np + (mi >> 1) * 8;
-        uint32_t bb[4];
-        ldsm_x4_t(bb, vt + (dim / 64) * 2048 + swz<128>(tok, (dim % 64) * 2));
-        mma16816(O[2 * np], pa, bb[0], bb[1]);
-        mma16816(O[2 * np + 1], pa, bb[2], bb[3]);
+    // ---- epilogue: out = (O + O_lr B_V) / l
+    bool ok = (u == U) && !*abort_flag && mbar_wait(bar(B_OBAR), (U - 1) & 1, p.status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) *abort_flag = 1;
+    // B_V [R][d] (bf16) into the first stage's buffers: all MMAs have completed
+    const bool ep_lr = ok && use_lr;
+    if (ep_lr) {
+      const __nv_bfloat16* src = p.B_V + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
+      for (int e = rb_i; e < R * (D / 8); e += 128) {
+        const int k = e / (D / 8), v8 = e % (D / 8);
+        *reinterpret_cast<uint4*>(smem + k * D * 2 + v8 * 16) =
+            __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v8);
       }
-      if (use_lr) {
-        const uint32_t lvt = st + 2 * kNW * L.kv_tile + kNW * L.lr_tile + kk * L.lr_tile;
-        if constexpr (R >= 16) {
+    }
+    named_bar_sync(2, 128);
+    if (ok) {
+      tc::fence_after();
+      float olr[RP];
+      if (ep_lr) {
 #pragma unroll
-          for (int np = 0; np < R / 16; ++np) {
-            const int mi = lane >> 3;
-            const int tok = (lane & 7) + (mi & 1) * 8;
-            const int col = 16 * np + (mi >> 1) * 8;
-            uint32_t bb[4];
-            ldsm_x4_t(bb, lvt + swz<LR_RB>(tok, col * 2));
-            mma16816(Olr[2 * np], pa, bb[0], bb[1]);
-            mma16816(Olr[2 * np + 1], pa, bb[2], bb[3]);
+        for (int c = 0; c < RP / 16; ++c) {
+          uint32_t v[16];
+          tc::ld_x16(tbase + lane_off + OLR_COL + 16 * c, v);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) olr[16 * c + e] = __uint_as_float(v[e]);
+        }
+      }
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      __nv_bfloat16* orow = p.out + (static_cast<int64_t>(qs + (sm_valid ? sm_k : 0)) * p.Hq + head * g + sm_r % g) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tc::ld_x32(tbase + lane_off + O_COL + 32 * c, v);
+        tc::wait_ld();
+        float o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]);
+        if (ep_lr) {
+#pragma unroll 4
+          for (int k = 0; k < R; ++k) {
+            const float a = olr[k];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const uint4 w = *reinterpret_cast<const uint4*>(smem + k * D * 2 + (32 * c + 8 * x) * 2);
+              o[8 * x + 0] = fmaf(a, bf16_lo(w.x), o[8 * x + 0]);
+              o[8 * x + 1] = fmaf(a, bf16_hi(w.x), o[8 * x + 1]);
+              o[8 * x + 2] = fmaf(a, bf16_lo(w.y), o[8 * x + 2]);
+              o[8 * x + 3] = fmaf(a, bf16_hi(w.y), o[8 * x + 3]);
+              o[8 * x + 4] = fmaf(a, bf16_lo(w.z), o[8 * x + 4]);
+              o[8 * x + 5] = fmaf(a, bf16_hi(w.z), o[8 * x + 5]);
+              o[8 * x + 6] = fmaf(a, bf16_lo(w.w), o[8 * x + 6]);
+              o[8 * x + 7] = fmaf(a, bf16_hi(w.w), o[8 * x + 7]);
+            }
           }
-        } else {
-          uint32_t bb[2];
-          ldsm_x2_t(bb, lvt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
-          mma16816(Olr[0], pa, bb[0], bb[1]);
+        }
+        if (sm_valid) {
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            uint4 w;
+            w.x = pack_bf16(o[8 * x + 0] * inv, o[8 * x + 1] * inv);
+            w.y = pack_bf16(o[8 * x + 2] * inv, o[8 * x + 3] * inv);
+            w.z = pack_bf16(o[8 * x + 4] * inv, o[8 * x + 5] * inv);
+            w.w = pack_bf16(o[8 * x + 6] * inv, o[8 * x + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * x) = w;
+          }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
-    if (++stage == p.nstage) {
-      stage = 0;
-      phase ^= 1;
+  }
+
+  // ============================================================ rebuild
+  if (warp >= kRbWarp0) {
+    const int i = rb_i;       // key row within the stage
+    const int bb = i >> 4;    // block within the stage
+    // Every exit from this loop is decided by a barrier vote of the whole
+    // warpgroup (bar.red.or), so no warp is left waiting at a named barrier.
+    for (int j = 0; j < n_st; ++j) {
+      const int s = j % NST;
+      const uint32_t st = sbase + s * L::STAGE;
+      // the previous stage's readers of btab are done past this barrier
+      if (named_bar_or(3, 128, *abort_flag != 0)) break;
+      if (rebuild) {  // block start angles of this stage
+        for (int e = i; e < 8 * HALF; e += 128) {
+          const int b2 = e / HALF, jj = e % HALF;
+          btab[e] = rope_cos_sin_fast(j * BN + kBlock * b2, p.freqs.hi[jj], p.freqs.lo[jj]);
+        }
+      }
+      const bool ok = mbar_wait(bar(B_FULL + s), (j / NST) & 1, p.status);
+      if (named_bar_or(3, 128, !ok)) {  // also publishes btab to the warpgroup
+        *abort_flag = 1;
+        break;
+      }
+      const int mask = stage_mask[s];
+      const int t = j * BN + i;
+      const bool key_ok = ((mask >> bb) & 1) && t < Ls;
+      if (rebuild) {
+        const bool oky = mbar_wait(bar(B_YFULL), j & 1, p.status);
+        if (named_bar_or(3, 128, !oky)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc::fence_after();
+        const float2* bt = btab + bb * HALF;
+#pragma unroll
+        for (int grp = 0; grp < HALF / 16; ++grp) {
+          uint32_t ylo[16], yhi[16];
+          tc::ld_x16(tbase + lane_off + Y_COL + 16 * grp, ylo);
+          tc::ld_x16(tbase + lane_off + Y_COL + HALF + 16 * grp, yhi);
+          tc::wait_ld();
+          if (key_ok) {
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {  // 8 pairs per 16-byte chunk
+              const int dlo = 16 * grp + 8 * hc, dhi = dlo + HALF;
+              const uint32_t alo = st + L::off_k + (dlo / 64) * (BN * 128) + swz<128>(i, (dlo % 64) * 2);
+              const uint32_t ahi = st + L::off_k + (dhi / 64) * (BN * 128) + swz<128>(i, (dhi % 64) * 2);
+              uint4 klo, khi;
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                           : "=r"(klo.x), "=r"(klo.y), "=r"(klo.z), "=r"(klo.w) : "r"(alo));
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                           : "=r"(khi.x), "=r"(khi.y), "=r"(khi.z), "=r"(khi.w) : "r"(ahi));
+              const uint32_t kl[4] = {klo.x, klo.y, klo.z, klo.w};
+              const uint32_t kh[4] = {khi.x, khi.y, khi.z, khi.w};
+              uint32_t olo[4], ohi[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                float rl[2], rh[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int pp = 8 * hc + 2 * w + e;  // pair index within the group
+                  const int jj = 16 * grp + pp;
+                  const float2 b2 = bt[jj];
+                  const float cd = __half2float(__ushort_as_half(static_cast<unsigned short>(dl[jj] & 0xffffu)));
+                  const float sd = __half2float(__ushort_as_half(static_cast<unsigned short>(dl[jj] >> 16)));
+                  const float c = b2.x * cd - b2.y * sd;
+                  const float sn = b2.y * cd + b2.x * sd;
+                  const float yl = __uint_as_float(ylo[pp]), yh = __uint_as_float(yhi[pp]);
+                  const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
+                  const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
+                  rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
+                  rh[e] = fmaf(yh, c, fmaf(yl, sn, bh));
+                }
+                olo[w] = pack_f16(rl[0], rl[1]);
+                ohi[w] = pack_f16(rh[0], rh[1]);
+              }
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(alo), "r"(olo[0]), "r"(olo[1]),
+                           "r"(olo[2]), "r"(olo[3]) : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(ahi), "r"(ohi[0]), "r"(ohi[1]),
+                           "r"(ohi[2]), "r"(ohi[3]) : "memory");
+            }
+          }
+        }
+        tc::fence_before();
+        mbar_arrive(bar(B_YFREE));
+      }
+      // Keys past the sequence end or in a block that was not loaded: zero their
+      // V and L_V rows, so that P = 0 there cannot meet stale (NaN) data.
+      if (!key_ok) {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint32_t a = st + L::off_v + (c / 8) * (BN * 128) + swz<128>(i, (c % 8) * 16);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
+        }
+        if (use_lr) {
+#pragma unroll
+          for (int c = 0; c < LSPAN / 16; ++c) {
+            const uint32_t a = st + L::off_lv + swz<LSPAN>(i, c * 16);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
+          }
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      mbar_arrive(bar(B_KA + s));
     }
   }
 
-  // ---- epilogue: out = (O + O_lr B_V) / l
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float l = l_run[h];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    l_run[h] = l;
-  }
-  float* olr = reinterpret_cast<float*>(smem + L.off_olr);
-  const float* bv = reinterpret_cast<const float*>(smem + L.off_bv);
-  if (use_lr) {
-#pragma unroll
-    for (int nt = 0; nt < NLR; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = 16 * warp + g8 + 8 * h;
-        olr[r * (R + 4) + 8 * nt + 2 * c4] = Olr[nt][2 * h];
-        olr[r * (R + 4) + 8 * nt + 2 * c4 + 1] = Olr[nt][2 * h + 1];
-      }
-    __syncwarp();
-  }
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    if (!rvalid[h]) continue;
-    const int rl = 16 * warp + g8 + 8 * h;
-    const int r = row0 + rl;
-    const int k = r / g;
-    const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
-    __nv_bfloat16* orow = p.out + (static_cast<int64_t>(qs + k) * p.Hq + head * g + r % g) * D;
-#pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      const int j = 8 * nt + 2 * c4;
-      float v0 = O[nt][2 * h], v1 = O[nt][2 * h + 1];
-      if (use_lr) {
-#pragma unroll 8
-        for (int kr = 0; kr < R; ++kr) {
-          const float ol = olr[rl * (R + 4) + kr];
-          v0 = fmaf(ol, bv[kr * D + j], v0);
-          v1 = fmaf(ol, bv[kr * D + j + 1], v1);
-        }
-      }
-      *reinterpret_cast<uint32_t*>(orow + j) = pack_bf16(v0 * inv, v1 * inv);
-    }
+  // ------------------------------------------------------------ teardown
+  __syncwarp();
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tbase, kTmemCols);
   }
 }
 
@@ -596,22 +706,18 @@ lrkv_status run(const lrkv_config& cfg, const PrefillArgs& a, cudaStream_t strea
   p.has_bv = a.B_V != nullptr;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   rope_freqs(cfg, &p.freqs);
-  const int stage_bytes = PLayout::make(D, R, 1).stage;
-  const int fixed = PLayout::make(D, R, 0).total;
-  p.nstage = std::min(4, (kSmemLimit - fixed) / stage_bytes);
-  if (p.nstage < 2) return LRKV_ERR_UNSUPPORTED;
-  const int smem = PLayout::make(D, R, p.nstage).total;
   CUtensorMap tb, tl;
-  if (!make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, &tl)) return LRKV_ERR_CUDA;
+  if (!make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
+  if (!make_lr_map(cfg, a.lr_pool, a.num_blocks, PL<D, R>::RP, &tl)) return LRKV_ERR_CUDA;
   auto kern = prefill_kernel<D, R>;
+  constexpr int smem = PL<D, R>::total;
   static bool attr_set = false;  // idempotent per-process kernel attribute
   if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return LRKV_ERR_CUDA;
     attr_set = true;
   }
-  const int tiles = (a.max_q_len * p.g + BMQ - 1) / BMQ;
+  const int tiles = (a.max_q_len * p.g + BM - 1) / BM;
   dim3 grid(tiles, cfg.n_kv_heads, a.num_seqs);
   kern<<<grid, kThreads, smem, stream>>>(p, tb, tl);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
