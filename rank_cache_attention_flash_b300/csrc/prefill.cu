@@ -66,6 +66,10 @@ struct PrefillParams {
   RopeFreqs freqs;
 };
 
+// Y = L_K B_K is produced in column groups of 32: group g holds the 16 dims
+// 16g.. and their RoPE partners d/2 + 16g.. (B_K^T is staged with its rows in
+// that order), so each group can be rotated on its own and its TMEM columns
+// refilled for the next stage as soon as they have been read.
 // Shared-memory layout (byte offsets from a 1024-aligned base).
 template <int D, int R>
 struct PL {
@@ -76,7 +80,7 @@ struct PL {
   static constexpr int STAGE = 2 * KV + 2 * LT;
   static constexpr int BKB = D * LSPAN;           // B_K^T tile [d][r'], K-major
   static constexpr int BTAB = 8 * (D / 2) * 8;    // per-stage block start angles (cos, sin)
-  static constexpr int MISC = 256;
+  static constexpr int MISC = 512;
   static constexpr int FIXED = BKB + BTAB + MISC + 1024;
   static constexpr int NST_FIT = (kSmemLimit - FIXED) / STAGE;
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
@@ -95,17 +99,53 @@ enum : int {
   B_FULL = 0,    // [4] TMA -> consumers (one phase per stage use)
   B_EMPTY = 4,   // [4] MMA commit -> producer
   B_KA = 8,      // [4] rebuild warpgroup -> MMA (K_a written)
-  B_YFULL = 12,  // MMA commit -> rebuild (Y in TMEM)
-  B_YFREE = 13,  // rebuild -> MMA (Y read)
-  B_SFULL = 14,  // [2] MMA commit -> softmax (S half-tile in TMEM)
-  B_PFULL = 16,  // [2] softmax -> MMA (P written, O rescaled)
-  B_OBAR = 18,   // MMA commit after each P V
-  B_DRAIN = 19,  // MMA commit on abort: every issued MMA has completed
-  B_COUNT = 20
+  B_YFULL = 12,  // [4] MMA commit -> rebuild (column group of Y in TMEM)
+  B_YFREE = 16,  // [4] rebuild -> MMA (column group of Y read)
+  B_SFULL = 20,  // [2] MMA commit -> softmax (S half-tile in TMEM)
+  B_PFULL = 22,  // [2] softmax -> MMA (P written, O rescaled)
+  B_OBAR = 24,   // MMA commit after each P V
+  B_DRAIN = 25,  // MMA commit on abort: every issued MMA has completed
+  B_EPI = 26,    // softmax -> MMA: fp16(O_lr / l) in TMEM and B_V in smem
+  B_ZFULL = 27,  // MMA commit -> softmax: Z = fp16(O_lr / l) B_V in TMEM
+  B_COUNT = 28
 };
 
-__device__ __forceinline__ bool try_wait_parity(uint32_t bar, uint32_t parity) {
-  return mbar_try_wait(bar, parity);
+// Non-blocking test of an mbarrier phase (the MMA issuer polls several).
+__device__ __forceinline__ bool test_parity(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr long long kWaitCycles = 1ll << 31;  // ~1 s: a wait this long has failed
+
+// 2^x by the hardware approximation (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Waits for an mbarrier phase with try_wait (which suspends until the phase
+// completes or a short hardware time limit), without sleeping in between;
+// gives up after kWaitCycles, stores LRKV_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_t* st) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) {
+      report(st, LRKV_ERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Named barrier over `count` threads that also ORs a predicate across them:
@@ -133,11 +173,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NST = L::NST;
   constexpr int OLR_COL = O_COL + D;
   constexpr uint32_t SW_LR = tc::swizzle_code(LSPAN);
-  constexpr uint32_t kIdY = tc::idesc_f16(128, D, true, false, false);
+  constexpr int NG = HALF / 16;  // Y column groups
+  constexpr uint32_t kIdY = tc::idesc_f16(128, 32, true, false, false);
   constexpr uint32_t kIdS16 = tc::idesc_f16(128, HN, false, false, false);  // fp16 Q, K_a
   constexpr uint32_t kIdSbf = tc::idesc_f16(128, HN, true, false, false);   // bf16 Q, K_base
   constexpr uint32_t kIdPV = tc::idesc_f16(128, D, true, false, true);
   constexpr uint32_t kIdPLV = tc::idesc_f16(128, RP, true, false, true);
+  constexpr uint32_t kIdZ = tc::idesc_f16(128, D, false, false, true);  // fp16 O_lr/l x B_V
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -183,15 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FULL + i), 1);
       mbar_init(bar(B_EMPTY + i), 1);
       mbar_init(bar(B_KA + i), 128);
+      mbar_init(bar(B_YFULL + i), 1);
+      mbar_init(bar(B_YFREE + i), 128);
     }
-    mbar_init(bar(B_YFULL), 1);
-    mbar_init(bar(B_YFREE), 128);
     mbar_init(bar(B_SFULL + 0), 1);
     mbar_init(bar(B_SFULL + 1), 1);
     mbar_init(bar(B_PFULL + 0), 128);
     mbar_init(bar(B_PFULL + 1), 128);
     mbar_init(bar(B_OBAR), 1);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_EPI), 128);
+    mbar_init(bar(B_ZFULL), 1);
     mbar_fence_init();
   }
   if (warp == 1) tc::alloc(smem_u32(tmem_slot), kTmemCols);
@@ -213,15 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       dl[j] = pack_f16(cs.x, cs.y);
     }
     if (rebuild) {
-      // B_K^T [d][r'] (K-major, swizzled like the L_K tiles), zero beyond rank R
+      // B_K^T [d][r'] (K-major, swizzled like the L_K tiles), zero beyond rank
+      // R; row 32g + t holds dim 16g + t (t < 16) or d/2 + 16g + t - 16
       const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
       const int rt = tid - kRbWarp0 * 32;
       for (int e = rt; e < D * (RP / 2); e += 128) {
-        const int n = e % D, k2 = e / D;
+        const int row = e % D, k2 = e / D;
+        const int t = row & 31;
+        const int n = t < 16 ? 16 * (row >> 5) + t : HALF + 16 * (row >> 5) + t - 16;
         const int k0 = 2 * k2;
         const uint32_t lo = k0 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0) * p.Hkv * D + n]) : 0u;
         const uint32_t hi = k0 + 1 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0 + 1) * p.Hkv * D + n]) : 0u;
-        *reinterpret_cast<uint32_t*>(smem + L::off_bk + swz<LSPAN>(n, 4 * k2)) = lo | (hi << 16);
+        *reinterpret_cast<uint32_t*>(smem + L::off_bk + swz<LSPAN>(row, 4 * k2)) = lo | (hi << 16);
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     }
@@ -268,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ok = 1;
       if (lane == 0) {
         if (*abort_flag) ok = 0;
-        else if (j >= NST && !mbar_wait(bar(B_EMPTY + s), ((j / NST) - 1) & 1, p.status)) ok = 0;
+        else if (j >= NST && !wait_phase(bar(B_EMPTY + s), ((j / NST) - 1) & 1, p.status)) ok = 0;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -311,82 +358,96 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ================================================================= MMA
-  if (warp == 1 && lane == 0) {
+  // Fixed issue order S(0); then per half-tile u: S(u+1), P V(u). S(u+1)
+  // overwrites the score buffer of u-1, whose P V was issued one step earlier
+  // (MMAs execute in issue order). The whole warp runs the sequence in
+  // lockstep, every decision taken from lane 0; one elected lane issues.
+  if (warp == 1) {
     const uint32_t idS = rebuild ? kIdS16 : kIdSbf;
-    int u_s = 0, u_p = 0, j_y = 0;
-    uint32_t idle = 0;
-    while (u_p < U) {
-      bool progress = false;
-      if (*abort_flag) break;
-      // Y(j) = L_K B_K for the next stage (needs its tiles and the Y buffer)
-      if (rebuild && j_y < n_st && (j_y == 0 || try_wait_parity(bar(B_YFREE), (j_y - 1) & 1)) &&
-          try_wait_parity(bar(B_FULL + j_y % NST), (j_y / NST) & 1)) {
-        tc::fence_after();
-        const uint32_t st = sbase + (j_y % NST) * L::STAGE;
-#pragma unroll
-        for (int kk = 0; kk < RP / 16; ++kk) {
-          const uint64_t a = tc::sdesc(st + L::off_lk + kk * 32, 16, 8 * LSPAN, SW_LR);
-          const uint64_t b = tc::sdesc(sbase + L::off_bk + kk * 32, 16, 8 * LSPAN, SW_LR);
-          tc::mma_ss(tbase + Y_COL, a, b, kIdY, kk > 0);
-        }
-        tc::commit(bar(B_YFULL));
-        ++j_y;
-        progress = true;
-      }
-      // S(u) = Q K_a^T for the next half-tile (its buffer was last read by P V(u-2))
-      if (u_s < U && u_p >= u_s - 1 &&
-          ((u_s & 1) || try_wait_parity(bar(B_KA + (u_s >> 1) % NST), ((u_s >> 1) / NST) & 1))) {
-        tc::fence_after();
-        const uint32_t kt = sbase + ((u_s >> 1) % NST) * L::STAGE + L::off_k + (u_s & 1) * HN * 128;
-        const uint32_t dcol = tbase + S_COL0 + 64 * (u_s & 1);
+    auto uni = [&](bool c) { return __shfl_sync(0xffffffffu, static_cast<int>(c), 0) != 0; };
+    auto wait_u = [&](uint32_t b, uint32_t par) { return uni(wait_phase(b, par, p.status)); };
+    auto issue_S = [&](int u) {
+      tc::fence_after();
+      const uint32_t kt = sbase + ((u >> 1) % NST) * L::STAGE + L::off_k + (u & 1) * HN * 128;
+      const uint32_t dcol = tbase + S_COL0 + 64 * (u & 1);
+      if (tc::elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t b = tc::sdesc(kt + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024, 2);
           tc::mma_ts(dcol, tbase + Q_COL + ks * 8, b, idS, ks > 0);
         }
-        tc::commit(bar(B_SFULL + (u_s & 1)));
-        ++u_s;
-        progress = true;
+        tc::commit(bar(B_SFULL + (u & 1)));
       }
-      // O += P V_base, O_lr += P L_V for the oldest half-tile whose P is ready
-      if (u_p < u_s && try_wait_parity(bar(B_PFULL + (u_p & 1)), (u_p >> 1) & 1)) {
-        tc::fence_after();
-        const int s = (u_p >> 1) % NST;
-        const uint32_t st = sbase + s * L::STAGE;
-        const uint32_t pcol = tbase + S_COL0 + 64 * (u_p & 1);
-        const uint32_t vt = st + L::off_v + (u_p & 1) * HN * 128;
+      __syncwarp();
+    };
+    auto issue_PV = [&](int u) {
+      tc::fence_after();
+      const int s = (u >> 1) % NST;
+      const uint32_t st = sbase + s * L::STAGE;
+      const uint32_t pcol = tbase + S_COL0 + 64 * (u & 1);
+      const uint32_t vt = st + L::off_v + (u & 1) * HN * 128;
+      if (tc::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < HN / 16; ++kk) {
           const uint64_t b = tc::sdesc(vt + kk * 16 * 128, BN * 128, 1024, 2);
-          tc::mma_ts(tbase + O_COL, pcol + kk * 8, b, kIdPV, (u_p > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_ts(tbase + O_COL, pcol + kk * 8, b, kIdPV, (u > 0 || kk > 0) ? 1u : 0u);
         }
         if (use_lr) {
-          const uint32_t lvt = st + L::off_lv + (u_p & 1) * HN * LSPAN;
+          const uint32_t lvt = st + L::off_lv + (u & 1) * HN * LSPAN;
 #pragma unroll
           for (int kk = 0; kk < HN / 16; ++kk) {
             const uint64_t b = tc::sdesc(lvt + kk * 16 * LSPAN, BN * LSPAN, 8 * LSPAN, SW_LR);
-            tc::mma_ts(tbase + OLR_COL, pcol + kk * 8, b, kIdPLV, (u_p > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_ts(tbase + OLR_COL, pcol + kk * 8, b, kIdPLV, (u > 0 || kk > 0) ? 1u : 0u);
           }
         }
         tc::commit(bar(B_OBAR));
-        if ((u_p & 1) || u_p == U - 1) tc::commit(bar(B_EMPTY + s));
-        ++u_p;
-        progress = true;
+        if ((u & 1) || u == U - 1) tc::commit(bar(B_EMPTY + s));
       }
-      if (progress) {
-        idle = 0;
-      } else if (++idle > (1u << 24)) {
-        report(p.status, LRKV_ERR_TIMEOUT);
-        *abort_flag = 1;
+      __syncwarp();
+    };
+    bool ok = !uni(*abort_flag != 0) && wait_u(bar(B_KA + 0), 0);
+    if (ok) issue_S(0);
+    for (int u = 0; ok && u < U; ++u) {
+      if (u + 1 < U) {
+        const int j1 = (u + 1) >> 1;
+        if (!((u + 1) & 1) && !wait_u(bar(B_KA + j1 % NST), (j1 / NST) & 1)) {
+          ok = false;
+          break;
+        }
+        issue_S(u + 1);
+      }
+      if (!wait_u(bar(B_PFULL + (u & 1)), (u >> 1) & 1)) {
+        ok = false;
         break;
-      } else if (idle > 256) {
-        __nanosleep(32);
+      }
+      issue_PV(u);
+      if (uni(*abort_flag != 0)) ok = false;
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
+    // Z = fp16(O_lr / l) B_V into the score buffers (free once every P V is issued)
+    if (ok && use_lr) {
+      if (wait_u(bar(B_EPI), 0)) {
+        tc::fence_after();
+        if (tc::elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < RP / 16; ++kk) {
+            const uint64_t b = tc::sdesc(sbase + kk * 16 * 128, RP * 128, 1024, 2);
+            tc::mma_ts(tbase + S_COL0, tbase + Q_COL + kk * 8, b, kIdZ, kk > 0);
+          }
+          tc::commit(bar(B_ZFULL));
+        }
+        __syncwarp();
+      } else if (lane == 0) {
+        *abort_flag = 1;
       }
     }
     // drain: every MMA issued so far completes before the tensor memory is released
-    if (*abort_flag) {
-      tc::commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, nullptr, 1u << 16);
+    if (uni(*abort_flag != 0)) {
+      if (tc::elect_one()) {
+        tc::commit(bar(B_DRAIN));
+        mbar_wait(bar(B_DRAIN), 0, nullptr, 1u << 16);
+      }
+      __syncwarp();
     }
   }
 
@@ -397,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int u = 0;
     for (; u < U; ++u) {
       const int b = u & 1;
-      bool ok = !*abort_flag && mbar_wait(bar(B_SFULL + b), (u >> 1) & 1, p.status);
+      bool ok = !*abort_flag && wait_phase(bar(B_SFULL + b), (u >> 1) & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         *abort_flag = 1;
@@ -419,19 +480,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key0 = u * HN;
       const int bm = (stage_mask[(u >> 1) % NST] >> (4 * (u & 1))) & 0xF;
       const bool need_mask = (key0 + HN - 1 > pos_min) || bm != 0xF || !sm_valid;
-      float mx = -CUDART_INF_F;
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < HN; ++c) {
           const bool vis = sm_valid && (key0 + c <= sm_pos) && ((bm >> (c >> 4)) & 1);
-          const float v = vis ? __uint_as_float(sv[c]) : -CUDART_INF_F;
-          sv[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          sv[c] = vis ? sv[c] : __float_as_uint(-CUDART_INF_F);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < HN; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
       }
+      // row max as a tree of 8 independent chains
+      float mxs[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mxs[k] = __uint_as_float(sv[k]);
+#pragma unroll
+      for (int c = 8; c < HN; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], __uint_as_float(sv[c]));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mxs[k] = fmaxf(mxs[k], mxs[k + 4]);
+      const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
       const float mt = mx * sc;  // -inf stays -inf
       bool resc = false;
       float alpha = 1.f;
@@ -439,14 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (m_run == -CUDART_INF_F) {
           m_run = mt;  // first visible key of this row: O and O_lr rows are still zero
         } else if (mt > m_run + kRescaleLog2) {
-          alpha = exp2f(m_run - mt);
+          alpha = ex2(m_run - mt);
           m_run = mt;
           resc = true;
         }
       }
       if (__any_sync(0xffffffffu, resc)) {
         // O and O_lr must not be in use by P V(u-1): wait for it, then rescale
-        bool okw = mbar_wait(bar(B_OBAR), (u - 1) & 1, p.status);
+        bool okw = wait_phase(bar(B_OBAR), (u - 1) & 1, p.status);
         okw = __all_sync(0xffffffffu, okw);
         if (!okw) {
           *abort_flag = 1;
@@ -476,89 +540,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= alpha;
       }
       uint32_t pk[32];
-      float sum = 0.f;
-      if (m_run == -CUDART_INF_F) {
+      float sums[8];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = 0u;
-      } else {
+      for (int k = 0; k < 8; ++k) sums[k] = 0.f;
+      // m_run = -inf only while no key of this row was visible: every s is -inf
+      // then, and the offset 0 keeps ex2(-inf) = 0 instead of NaN
+      const float moff = m_run == -CUDART_INF_F ? 0.f : m_run;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = exp2f(fmaf(__uint_as_float(sv[2 * c]), sc, -m_run));
-          const float p1 = exp2f(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -m_run));
-          sum += p0 + p1;
-          pk[c] = pack_bf16(p0, p1);
-        }
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), sc, -moff));
+        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -moff));
+        sums[c & 7] += p0 + p1;
+        pk[c] = pack_bf16(p0, p1);
       }
-      l_run += sum;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sums[k] += sums[k + 4];
+      l_run += (sums[0] + sums[1]) + (sums[2] + sums[3]);
       tc::st_x32(tbase + lane_off + S_COL0 + 64 * b, pk);
       tc::wait_st();
       tc::fence_before();
       mbar_arrive(bar(B_PFULL + b));
     }
-    // ---- epilogue: out = (O + O_lr B_V) / l
-    bool ok = (u == U) && !*abort_flag && mbar_wait(bar(B_OBAR), (U - 1) & 1, p.status);
+    // ---- epilogue: out = O / l + Z,  Z = fp16(O_lr / l) B_V  (one small MMA)
+    bool ok = (u == U) && !*abort_flag && wait_phase(bar(B_OBAR), (U - 1) & 1, p.status);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) *abort_flag = 1;
-    // B_V [R][d] (bf16) into the first stage's buffers: all MMAs have completed
-    const bool ep_lr = ok && use_lr;
-    if (ep_lr) {
-      const __nv_bfloat16* src = p.B_V + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
-      for (int e = rb_i; e < R * (D / 8); e += 128) {
-        const int k = e / (D / 8), v8 = e % (D / 8);
-        *reinterpret_cast<uint4*>(smem + k * D * 2 + v8 * 16) =
-            __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v8);
-      }
-    }
-    named_bar_sync(2, 128);
-    if (ok) {
-      tc::fence_after();
-      float olr[RP];
-      if (ep_lr) {
-#pragma unroll
-        for (int c = 0; c < RP / 16; ++c) {
-          uint32_t v[16];
-          tc::ld_x16(tbase + lane_off + OLR_COL + 16 * c, v);
-          tc::wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) olr[16 * c + e] = __uint_as_float(v[e]);
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    if (ok) tc::fence_after();
+    if (use_lr) {
+      if (ok) {
+        // B_V [R][d] -> fp16, MN-major with 128-byte swizzle, into stage 0 (idle:
+        // every MMA has completed); rows R .. r'-1 are zero
+        const __nv_bfloat16* src = p.B_V + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
+        for (int e = rb_i; e < RP * (D / 8); e += 128) {
+          const int k = e / (D / 8), v8 = e % (D / 8);
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (k < R) {
+            w = __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v8);
+            w.x = bf16x2_to_f16x2(w.x);
+            w.y = bf16x2_to_f16x2(w.y);
+            w.z = bf16x2_to_f16x2(w.z);
+            w.w = bf16x2_to_f16x2(w.w);
+          }
+          *reinterpret_cast<uint4*>(smem + (v8 / 8) * (RP * 128) + swz<128>(k, (v8 % 8) * 16)) = w;
         }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        // fp16(O_lr / l) as the A operand, over the (no longer needed) Q columns
+#pragma unroll
+        for (int c = 0; c < RP / 32 + (RP % 32 ? 1 : 0); ++c) {
+          uint32_t v[16];
+          uint32_t f[16];
+          tc::ld_x16(tbase + lane_off + OLR_COL + 32 * c, v);
+          if (RP - 32 * c > 16) tc::ld_x16(tbase + lane_off + OLR_COL + 32 * c + 16, f);
+          tc::wait_ld();
+          uint32_t a[16];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            a[e] = pack_f16(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            a[8 + e] = (RP - 32 * c > 16) ? pack_f16(__uint_as_float(f[2 * e]) * inv, __uint_as_float(f[2 * e + 1]) * inv) : 0u;
+          tc::st_x16(tbase + lane_off + Q_COL + 16 * c, a);
+        }
+        tc::wait_st();
+        tc::fence_before();
       }
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      mbar_arrive(bar(B_EPI));
+      bool okz = ok && wait_phase(bar(B_ZFULL), 0, p.status);
+      okz = __all_sync(0xffffffffu, okz);
+      if (!okz) *abort_flag = 1;
+      ok = okz;
+      if (ok) tc::fence_after();
+    }
+    if (ok) {
       __nv_bfloat16* orow = p.out + (static_cast<int64_t>(qs + (sm_valid ? sm_k : 0)) * p.Hq + head * g + sm_r % g) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
+        uint32_t v[32], z[32];
         tc::ld_x32(tbase + lane_off + O_COL + 32 * c, v);
+        if (use_lr) tc::ld_x32(tbase + lane_off + S_COL0 + 32 * c, z);
         tc::wait_ld();
-        float o[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(v[e]);
-        if (ep_lr) {
-#pragma unroll 4
-          for (int k = 0; k < R; ++k) {
-            const float a = olr[k];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const uint4 w = *reinterpret_cast<const uint4*>(smem + k * D * 2 + (32 * c + 8 * x) * 2);
-              o[8 * x + 0] = fmaf(a, bf16_lo(w.x), o[8 * x + 0]);
-              o[8 * x + 1] = fmaf(a, bf16_hi(w.x), o[8 * x + 1]);
-              o[8 * x + 2] = fmaf(a, bf16_lo(w.y), o[8 * x + 2]);
-              o[8 * x + 3] = fmaf(a, bf16_hi(w.y), o[8 * x + 3]);
-              o[8 * x + 4] = fmaf(a, bf16_lo(w.z), o[8 * x + 4]);
-              o[8 * x + 5] = fmaf(a, bf16_hi(w.z), o[8 * x + 5]);
-              o[8 * x + 6] = fmaf(a, bf16_lo(w.w), o[8 * x + 6]);
-              o[8 * x + 7] = fmaf(a, bf16_hi(w.w), o[8 * x + 7]);
-            }
-          }
-        }
         if (sm_valid) {
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o[e] = __uint_as_float(v[8 * x + e]) * inv + (use_lr ? __uint_as_float(z[8 * x + e]) : 0.f);
             uint4 w;
-            w.x = pack_bf16(o[8 * x + 0] * inv, o[8 * x + 1] * inv);
-            w.y = pack_bf16(o[8 * x + 2] * inv, o[8 * x + 3] * inv);
-            w.z = pack_bf16(o[8 * x + 4] * inv, o[8 * x + 5] * inv);
-            w.w = pack_bf16(o[8 * x + 6] * inv, o[8 * x + 7] * inv);
+            w.x = pack_bf16(o[0], o[1]);
+            w.y = pack_bf16(o[2], o[3]);
+            w.z = pack_bf16(o[4], o[5]);
+            w.w = pack_bf16(o[6], o[7]);
             *reinterpret_cast<uint4*>(orow + 32 * c + 8 * x) = w;
           }
         }
@@ -571,20 +644,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = rb_i;       // key row within the stage
     const int bb = i >> 4;    // block within the stage
     // Every exit from this loop is decided by a barrier vote of the whole
-    // warpgroup (bar.red.or), so no warp is left waiting at a named barrier.
+    // warpgroup (bar.red.or), so no warp is left waiting at a named barrier;
+    // a warp whose wait failed skips its work until the next vote.
+    // The warpgroup issues its own Y MMAs (one elected lane of its first
+    // warp; commits track each issuing thread separately): Y(j+1) as soon as
+    // every thread has read Y(j) and stage j+1 has landed, else right after
+    // stage j+1's tiles are seen.
+    bool failed = false;
+    bool y_next = false;  // Y of the coming stage already issued (issuing warp only)
+    const bool y_warp = warp == kRbWarp0;
+    auto issue_Y = [&](int jj) {
+      tc::fence_after();
+      const uint32_t stj = sbase + (jj % NST) * L::STAGE;
+      if (tc::elect_one()) {
+#pragma unroll
+        for (int gy = 0; gy < NG; ++gy) {
+#pragma unroll
+          for (int kk = 0; kk < RP / 16; ++kk) {
+            const uint64_t a = tc::sdesc(stj + L::off_lk + kk * 32, 16, 8 * LSPAN, SW_LR);
+            const uint64_t b = tc::sdesc(sbase + L::off_bk + 32 * gy * LSPAN + kk * 32, 16, 8 * LSPAN, SW_LR);
+            tc::mma_ss(tbase + Y_COL + 32 * gy, a, b, kIdY, kk > 0);
+          }
+          tc::commit(bar(B_YFULL + gy));
+        }
+      }
+      __syncwarp();
+    };
     for (int j = 0; j < n_st; ++j) {
       const int s = j % NST;
       const uint32_t st = sbase + s * L::STAGE;
       // the previous stage's readers of btab are done past this barrier
-      if (named_bar_or(3, 128, *abort_flag != 0)) break;
+      if (named_bar_or(3, 128, failed || *abort_flag != 0)) break;
       if (rebuild) {  // block start angles of this stage
         for (int e = i; e < 8 * HALF; e += 128) {
           const int b2 = e / HALF, jj = e % HALF;
           btab[e] = rope_cos_sin_fast(j * BN + kBlock * b2, p.freqs.hi[jj], p.freqs.lo[jj]);
         }
       }
-      const bool ok = mbar_wait(bar(B_FULL + s), (j / NST) & 1, p.status);
-      if (named_bar_or(3, 128, !ok)) {  // also publishes btab to the warpgroup
+      failed = !wait_phase(bar(B_FULL + s), (j / NST) & 1, p.status);
+      if (named_bar_or(3, 128, failed)) {  // also publishes btab to the warpgroup
         *abort_flag = 1;
         break;
       }
@@ -592,18 +690,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = j * BN + i;
       const bool key_ok = ((mask >> bb) & 1) && t < Ls;
       if (rebuild) {
-        const bool oky = mbar_wait(bar(B_YFULL), j & 1, p.status);
-        if (named_bar_or(3, 128, !oky)) {
-          *abort_flag = 1;
-          break;
-        }
-        tc::fence_after();
+        if (y_warp && !y_next) issue_Y(j);
         const float2* bt = btab + bb * HALF;
 #pragma unroll
-        for (int grp = 0; grp < HALF / 16; ++grp) {
-          uint32_t ylo[16], yhi[16];
-          tc::ld_x16(tbase + lane_off + Y_COL + 16 * grp, ylo);
-          tc::ld_x16(tbase + lane_off + Y_COL + HALF + 16 * grp, yhi);
+        for (int grp = 0; grp < NG; ++grp) {
+          bool oky = !failed && wait_phase(bar(B_YFULL + grp), j & 1, p.status);
+          oky = __all_sync(0xffffffffu, oky);
+          if (!oky) {
+            failed = true;
+            *abort_flag = 1;
+          }
+          if (failed) continue;
+          tc::fence_after();
+          uint32_t y[32];  // [0, 16): dims 16 grp + e; [16, 32): their partners
+          tc::ld_x32(tbase + lane_off + Y_COL + 32 * grp, y);
           tc::wait_ld();
           if (key_ok) {
 #pragma unroll
@@ -631,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float sd = __half2float(__ushort_as_half(static_cast<unsigned short>(dl[jj] >> 16)));
                   const float c = b2.x * cd - b2.y * sd;
                   const float sn = b2.y * cd + b2.x * sd;
-                  const float yl = __uint_as_float(ylo[pp]), yh = __uint_as_float(yhi[pp]);
+                  const float yl = __uint_as_float(y[pp]), yh = __uint_as_float(y[16 + pp]);
                   const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
                   const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
                   rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
@@ -647,9 +747,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // every thread has read Y(j): issue Y(j+1) now if its tiles are there
         tc::fence_before();
-        mbar_arrive(bar(B_YFREE));
+        if (named_bar_or(3, 128, failed)) {
+          *abort_flag = 1;
+          break;
+        }
+        y_next = false;
+        if (y_warp && j + 1 < n_st &&
+            __shfl_sync(0xffffffffu, static_cast<int>(test_parity(bar(B_FULL + (j + 1) % NST), ((j + 1) / NST) & 1)), 0)) {
+          issue_Y(j + 1);
+          y_next = true;
+        }
       }
+      if (failed) continue;
       // Keys past the sequence end or in a block that was not loaded: zero their
       // V and L_V rows, so that P = 0 there cannot meet stale (NaN) data.
       if (!key_ok) {
