@@ -140,6 +140,46 @@ bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D maps that load a run of `nb` consecutive blocks of one (K|V, kv head)
+// chunk, or of one low-rank plane, in a single copy. Base pool dims: (d,
+// 16 rows, 2 * Hkv chunks of a block, blocks), box {64, 16, 1, nb}; low-rank
+// pool dims: (r, 16 rows, 2 planes, blocks), box {lr_cols, 16, 1, nb}. The
+// copy lands as nb * 16 consecutive rows in shared memory, swizzled like the
+// per-block maps.
+bool make_run_maps(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
+                   int64_t num_blocks, int nb, int lr_cols, CUtensorMap* base_map,
+                   CUtensorMap* lr_map) {
+  EncodeTiled enc = get_encoder();
+  if (enc == nullptr || lr_cols < cfg.rank) return false;
+  const cuuint64_t d = static_cast<cuuint64_t>(cfg.head_dim);
+  {
+    const cuuint64_t dims[4] = {d, kBlock, static_cast<cuuint64_t>(2 * cfg.n_kv_heads),
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {d * 2, d * 2 * kBlock, d * 2 * kBlock * 2 * cfg.n_kv_heads};
+    const cuuint32_t box[4] = {64, kBlock, 1, static_cast<cuuint32_t>(nb)};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(base_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base_pool), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    const cuuint64_t r = static_cast<cuuint64_t>(cfg.rank);
+    const cuuint64_t dims[4] = {r, kBlock, 2, static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[3] = {r * 2, r * 2 * kBlock, r * 2 * kBlock * 2};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(lr_cols), kBlock, 1, static_cast<cuuint32_t>(nb)};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_32B;
+    if (lr_cols == 32) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (lr_cols == 64) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (enc(lr_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(lr_pool), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 }  // namespace lrkv
 
 using namespace lrkv;

@@ -61,6 +61,12 @@ bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* l
 // Low-rank pool map with a box of box_cols (>= rank) columns, zero-filled past the rank.
 bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks, int box_cols,
                  CUtensorMap* lr_map);
+// 4-D maps copying a run of nb consecutive blocks per copy (base: one K|V
+// chunk of one kv head; low-rank: one plane), box width lr_cols for the
+// low-rank pool.
+bool make_run_maps(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
+                   int64_t num_blocks, int nb, int lr_cols, CUtensorMap* base_map,
+                   CUtensorMap* lr_map);
 
 lrkv_status launch_decode_bf16(const lrkv_config& cfg, const DecodeArgs& a,
                                const DecodePlan& plan, void* workspace, cudaStream_t stream);

@@ -8,23 +8,29 @@
 //
 // One CTA per (sequence, kv head, tile of 128 query rows); rows are
 // (query, head-in-group) pairs so that the g query heads sharing a kv head
-// share every key tile. Per stage of 128 keys (8 paged blocks):
-//   Y    = L_K B_K                    tcgen05, 128 keys x d, K = rank  -> TMEM
-//   K_a  = K_base + RoPE(Y)           rebuild warpgroup, in place in the
-//                                     stage's K tile (fp16, never stored to HBM)
-//   S    = Q K_a^T                    tcgen05, Q read from TMEM, two halves of
-//                                     64 keys (double-buffered in TMEM)
-//   P    = online softmax(S)          softmax warpgroup, thread = query row,
-//                                     P written back over S as bf16
-//   O   += P V_base, O_lr += P L_V    tcgen05, P read from TMEM
-// and at the end out = (O + O_lr B_V) / l.
+// share every key tile. Per tile of BN keys (BN / 16 paged blocks):
+//   Y         = L_K B_K               tcgen05 (rebuild warpgroup)   -> TMEM
+//   K_a       = K_base + RoPE(Y)      rebuild warpgroup, in place in the tile's
+//                                     K buffer (fp16, never stored to HBM)
+//   S         = Q K_a^T               tcgen05, Q read from TMEM       -> TMEM
+//   P         = online softmax(S)     softmax warpgroup, thread = query row,
+//                                     P (bf16) to its own TMEM columns
+//   O += P V_base, O_lr += P L_V      tcgen05, P read from TMEM
+// and at the end out = O / l + fp16(O_lr / l) B_V (one more small MMA).
 //
-// Warp roles (320 threads): warp 0 streams K, V, L_K, L_V tiles with 2-D TMA
-// copies into an mbarrier ring; warp 1 owns the tensor memory and one of its
-// lanes issues every MMA (in-order, so a TMEM region is only rewritten after
-// the MMAs reading it were issued); warps 2-5 run the softmax; warps 6-9
-// rebuild K_a. Tensor-memory columns: Q [0, d/2) packed, S0 [64, 128),
-// S1 [128, 192), O [192, 192+d), O_lr [192+d, 192+d+r'), Y [384, 384+d).
+// A tcgen05.mma takes about as long to issue from one warp as the tensor
+// pipe needs for a 128 x 192 x 16 product, so every MMA is made as wide as
+// the data allows and the independent streams are issued by different
+// warps: S by warp 1, P V by warp 2, P L_V by warp 3, Y by the rebuild
+// warpgroup. Y is produced in quarters of 16 RoPE pairs (B_K^T is staged
+// with its rows in that order) into two TMEM buffers, so the next quarters
+// compute while the current one is rotated.
+// Warp roles (384 threads): warp 0 streams K, V, L_V, L_K tiles with 2-D TMA
+// copies into an mbarrier ring; warp 1 owns the tensor memory and issues S;
+// warps 2 and 3 issue P V and P L_V; warps 4-7 run the softmax; warps 8-11
+// rebuild K_a. Tensor-memory columns: Q [0, d/2) (packed 16-bit),
+// S [64, 64 + BN), P [192, 192 + BN/2) (packed bf16), O [256, 256 + d),
+// O_lr [256 + d, 256 + d + r'), Y [448, 512) (two buffers of 32 columns).
 // Every wait is bounded: a wait that gives up stores LRKV_ERR_TIMEOUT, sets a
 // CTA-wide abort flag, and every role leaves its loop; no MMA or copy is left
 // in flight when the tensor memory is released.
@@ -39,15 +45,17 @@
 namespace lrkv {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int BM = 128;   // query rows per CTA (= TMEM lanes)
-constexpr int BN = 128;   // keys per stage (8 paged blocks)
-constexpr int HN = 64;    // keys per score half-tile
+constexpr int kThreads = 512;
+constexpr int BM = 128;  // query rows per CTA (= TMEM lanes)
 constexpr int kSmemLimit = 227 * 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr int Q_COL = 0, S_COL0 = 64, O_COL = 192, Y_COL = 384;
-constexpr int kSmWarp0 = 2, kRbWarp0 = 6;  // first softmax / rebuild warp
+constexpr int Q_COL = 0, S_COL = 64, P_COL = 192, O_COL = 256, Y_COL = 448;
+constexpr int kSmWarp0 = 4, kRbWarp0 = 8;  // first softmax / rebuild warp
 constexpr float kRescaleLog2 = 8.0f;       // rescale O only when the row max grows by > 2^8
+constexpr int kYWarp = 12;                 // Y issuer (warps 13-15 idle)
+constexpr int kLaunchRegs = 128;           // 65536 / 512
+constexpr int kLowRegs = 40, kHighRegs = 216;
+static_assert(256 * kLowRegs + 256 * kHighRegs == kThreads * kLaunchRegs, "register split");
 
 struct PrefillParams {
   const __nv_bfloat16* q;
@@ -66,51 +74,83 @@ struct PrefillParams {
   RopeFreqs freqs;
 };
 
-// Y = L_K B_K is produced in column groups of 32: group g holds the 16 dims
-// 16g.. and their RoPE partners d/2 + 16g.. (B_K^T is staged with its rows in
-// that order), so each group can be rotated on its own and its TMEM columns
-// refilled for the next stage as soon as they have been read.
-// Shared-memory layout (byte offsets from a 1024-aligned base).
+// Shared-memory layout (byte offsets from a 1024-aligned base). A stage holds
+// one key tile: K (rebuilt in place), V, L_V, L_K. The tile is the widest
+// multiple of 16 keys up to 128 that leaves room for three stages.
+constexpr int pl_stage(int D, int R, int bn) { return 2 * bn * D * 2 + 2 * bn * (R < 16 ? 32 : 2 * R); }
+constexpr int pl_fixed(int D, int R, int bn) {
+  return D * (R < 16 ? 32 : 2 * R) + (bn / 16) * (D / 2) * 8 + 16 * ((D / 2) * 8 + 16) + 512 + 1024;
+}
+constexpr int pl_bn(int D, int R) {
+  int bn = 128;
+  while (bn > 64 && (kSmemLimit - pl_fixed(D, R, bn)) / pl_stage(D, R, bn) < 3) bn -= 16;
+  return bn;
+}
 template <int D, int R>
 struct PL {
   static constexpr int RP = R < 16 ? 16 : R;      // rank padded to the MMA granularity
   static constexpr int LSPAN = RP * 2;            // bytes per low-rank row (32 / 64 / 128)
+  static constexpr int BN = pl_bn(D, R);          // keys per tile
+  static constexpr int NB = BN / 16;              // paged blocks per tile
   static constexpr int KV = BN * D * 2;           // K or V tile
-  static constexpr int LT = BN * LSPAN;           // L_K or L_V tile
+  static constexpr int LT = BN * LSPAN;           // L_V or L_K tile
   static constexpr int STAGE = 2 * KV + 2 * LT;
   static constexpr int BKB = D * LSPAN;           // B_K^T tile [d][r'], K-major
-  static constexpr int BTAB = 8 * (D / 2) * 8;    // per-stage block start angles (cos, sin)
+  static constexpr int BTAB = NB * (D / 2) * 8;   // per-tile block start angles (cos, sin)
+  static constexpr int DPITCH = (D / 2) * 8 + 16; // delta-table row: d/2 (cos, sin) + pad
+  static constexpr int DTAB = 16 * DPITCH;        // cos / sin(r theta_j), r < 16
   static constexpr int MISC = 512;
-  static constexpr int FIXED = BKB + BTAB + MISC + 1024;
+  static constexpr int FIXED = BKB + BTAB + DTAB + MISC + 1024;
   static constexpr int NST_FIT = (kSmemLimit - FIXED) / STAGE;
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
-  static constexpr int off_k = 0, off_v = KV, off_lk = 2 * KV, off_lv = 2 * KV + LT;
+  static constexpr int off_k = 0, off_v = KV, off_lv = 2 * KV, off_lk = 2 * KV + LT;
   static constexpr int off_bk = NST * STAGE;
   static constexpr int off_btab = off_bk + BKB;
-  static constexpr int off_misc = off_btab + BTAB;
+  static constexpr int off_dtab = off_btab + BTAB;
+  static constexpr int off_misc = off_dtab + DTAB;
+  static_assert(FIXED == pl_fixed(D, R, BN) && STAGE == pl_stage(D, R, BN), "layout");
+  static_assert(KV % 1024 == 0 && LT % 256 == 0 && (2 * KV + LT) % (8 * LSPAN) == 0, "atom alignment");
   static constexpr int total = off_misc + MISC + 1024;  // + alignment slack
   static_assert(NST >= 2, "two pipeline stages must fit");
   static_assert(total <= kSmemLimit, "shared memory");
-  static_assert(192 + D + RP <= Y_COL, "tensor-memory columns");
+  static_assert(S_COL + BN <= P_COL && P_COL + BN / 2 <= O_COL && O_COL + D + RP <= Y_COL &&
+                    Y_COL + 64 <= 512, "tensor-memory columns");
+
+  static_assert(RP * D * 2 <= KV, "B_V staging fits the first K buffer");
 };
 
 // Barrier slots inside the misc area (8 bytes each).
 enum : int {
   B_FULL = 0,    // [4] TMA -> consumers (one phase per stage use)
-  B_EMPTY = 4,   // [4] MMA commit -> producer
-  B_KA = 8,      // [4] rebuild warpgroup -> MMA (K_a written)
-  B_YFULL = 12,  // [4] MMA commit -> rebuild (column group of Y in TMEM)
-  B_YFREE = 16,  // [4] rebuild -> MMA (column group of Y read)
-  B_SFULL = 20,  // [2] MMA commit -> softmax (S half-tile in TMEM)
-  B_PFULL = 22,  // [2] softmax -> MMA (P written, O rescaled)
-  B_OBAR = 24,   // MMA commit after each P V
-  B_DRAIN = 25,  // MMA commit on abort: every issued MMA has completed
-  B_EPI = 26,    // softmax -> MMA: fp16(O_lr / l) in TMEM and B_V in smem
-  B_ZFULL = 27,  // MMA commit -> softmax: Z = fp16(O_lr / l) B_V in TMEM
+  B_EMPTY = 4,   // [4] P V and P L_V issuer commits -> producer
+  B_KA = 8,      // [4] rebuild warpgroup -> S issuer (K_a written)
+  B_YFULL = 24,  // [2] Y issuer commit -> rebuild warpgroup (per Y buffer)
+  B_YFREE = 26,  // [2] rebuild warpgroup -> Y issuer (quarter read from the buffer)
+  B_SFULL = 13,  // S issuer commit -> softmax
+  B_SFREE = 14,  // softmax -> S issuer (S loaded into registers)
+  B_PFULL = 15,  // softmax -> P V / P L_V issuers (P in TMEM, O rescaled)
+  B_OBAR = 16,   // P V issuer commit after each tile
+  B_LBAR = 17,   // P L_V issuer commit after each tile
+  B_EPI = 18,    // softmax -> P V issuer: fp16(O_lr / l) in TMEM, B_V in smem
+  B_ZFULL = 19,  // P V issuer commit -> softmax
+  B_DRAIN = 20,  // [4] per issuer, on abort: every MMA it issued has completed
   B_COUNT = 28
 };
 
-// Non-blocking test of an mbarrier phase (the MMA issuer polls several).
+// Named barrier over `count` threads that also ORs a predicate across them:
+// every participant gets the same answer, so a group can leave a loop together.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool test_parity(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -123,13 +163,6 @@ __device__ __forceinline__ bool test_parity(uint32_t bar, uint32_t parity) {
 }
 
 constexpr long long kWaitCycles = 1ll << 31;  // ~1 s: a wait this long has failed
-
-// 2^x by the hardware approximation (flush-to-zero; 2^-inf = 0).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Waits for an mbarrier phase with try_wait (which suspends until the phase
 // completes or a short hardware time limit), without sleeping in between;
@@ -148,49 +181,47 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_
   }
 }
 
-// Named barrier over `count` threads that also ORs a predicate across them:
-// every participant gets the same answer, so a group can leave a loop together.
-__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
+// 2^x by the hardware approximation (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int D, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p,
                    const __grid_constant__ CUtensorMap tm_base,
-                   const __grid_constant__ CUtensorMap tm_lr) {
+                   const __grid_constant__ CUtensorMap tm_lk,
+                   const __grid_constant__ CUtensorMap tm_base_run,
+                   const __grid_constant__ CUtensorMap tm_lr_run) {
   using L = PL<D, R>;
   constexpr int HALF = D / 2;
   constexpr int RP = L::RP;
   constexpr int LSPAN = L::LSPAN;
   constexpr int NST = L::NST;
-  constexpr int OLR_COL = O_COL + D;
-  constexpr uint32_t SW_LR = tc::swizzle_code(LSPAN);
-  constexpr int NG = HALF / 16;  // Y column groups
+  constexpr int BN = L::BN;
+  constexpr int NB = L::NB;
+  constexpr uint32_t SW_LK = tc::swizzle_code(LSPAN);
+  constexpr int NQ = HALF / 16;  // Y quarters of 16 RoPE pairs per tile
   constexpr uint32_t kIdY = tc::idesc_f16(128, 32, true, false, false);
-  constexpr uint32_t kIdS16 = tc::idesc_f16(128, HN, false, false, false);  // fp16 Q, K_a
-  constexpr uint32_t kIdSbf = tc::idesc_f16(128, HN, true, false, false);   // bf16 Q, K_base
+  constexpr uint32_t kIdS16 = tc::idesc_f16(128, BN, false, false, false);  // fp16 Q, K_a
+  constexpr uint32_t kIdSbf = tc::idesc_f16(128, BN, true, false, false);   // bf16 Q, K_base
   constexpr uint32_t kIdPV = tc::idesc_f16(128, D, true, false, true);
   constexpr uint32_t kIdPLV = tc::idesc_f16(128, RP, true, false, true);
   constexpr uint32_t kIdZ = tc::idesc_f16(128, D, false, false, true);  // fp16 O_lr/l x B_V
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned base, offset from the shared array itself so that the
+  // compiler keeps every access through it in the shared address space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + L::off_misc;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_misc + 8 * B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc + 8 * B_COUNT + 4);
   int* stage_mask = reinterpret_cast<int*>(smem + L::off_misc + 8 * B_COUNT + 8);  // [NST]
-  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab);                  // [8][HALF]
+  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab);                  // [NB][HALF]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s_row = blockIdx.z, head = blockIdx.y;
@@ -215,25 +246,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k_last = min(q_len, (row0 + BM + g - 1) / g) - 1;
   const int pos_min = Ls - q_len + k_first;
   const int pos_max = Ls - q_len + k_last;
-  const int U = (pos_max + HN) / HN;     // score half-tiles covering keys 0 .. pos_max
-  const int n_st = (U + 1) / 2;          // stages of 128 keys
+  const int U = (pos_max + BN) / BN;  // key tiles covering keys 0 .. pos_max
 
   // ---------------------------------------------------------------- setup
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(B_FULL + i), 1);
-      mbar_init(bar(B_EMPTY + i), 1);
+      mbar_init(bar(B_EMPTY + i), use_lr ? 2 : 1);
       mbar_init(bar(B_KA + i), 128);
-      mbar_init(bar(B_YFULL + i), 1);
-      mbar_init(bar(B_YFREE + i), 128);
+      mbar_init(bar(B_DRAIN + i), 1);
     }
-    mbar_init(bar(B_SFULL + 0), 1);
-    mbar_init(bar(B_SFULL + 1), 1);
-    mbar_init(bar(B_PFULL + 0), 128);
-    mbar_init(bar(B_PFULL + 1), 128);
+    mbar_init(bar(B_YFULL + 0), 1);
+    mbar_init(bar(B_YFULL + 1), 1);
+    mbar_init(bar(B_YFREE + 0), 128);
+    mbar_init(bar(B_YFREE + 1), 128);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFREE), 128);
+    mbar_init(bar(B_PFULL), 128);
     mbar_init(bar(B_OBAR), 1);
-    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_LBAR), 1);
     mbar_init(bar(B_EPI), 128);
     mbar_init(bar(B_ZFULL), 1);
     mbar_fence_init();
@@ -244,27 +276,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tbase = *tmem_slot;
   const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;  // this warp's TMEM lanes
-
-  // Rebuild warpgroup state: per-row RoPE delta factors cos/sin(r * theta_j),
-  // r = key % 16, packed (cos, sin) as fp16 pairs.
-  uint32_t dl[HALF];
   const int rb_i = 32 * (warp & 3) + lane;  // key row (rebuild) or query row (softmax) in the tile
+
+  // Rebuild warpgroup: B_K^T staged in smem (the RoPE delta factors are set
+  // up once the warpgroup has its larger register share, below).
   if (warp >= kRbWarp0) {
-    const int r = rb_i & 15;
-#pragma unroll
-    for (int j = 0; j < HALF; ++j) {
-      const float2 cs = rope_cos_sin(r, p.freqs.hi[j], p.freqs.lo[j]);
-      dl[j] = pack_f16(cs.x, cs.y);
-    }
     if (rebuild) {
       // B_K^T [d][r'] (K-major, swizzled like the L_K tiles), zero beyond rank
-      // R; row 32g + t holds dim 16g + t (t < 16) or d/2 + 16g + t - 16
+      // R; row 32 q + t holds dim 16 q + t (t < 16) or d/2 + 16 q + t - 16
       const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
-      const int rt = tid - kRbWarp0 * 32;
-      for (int e = rt; e < D * (RP / 2); e += 128) {
+      for (int e = rb_i; e < D * (RP / 2); e += 128) {
         const int row = e % D, k2 = e / D;
-        const int t = row & 31;
-        const int n = t < 16 ? 16 * (row >> 5) + t : HALF + 16 * (row >> 5) + t - 16;
+        const int q = row / 32, t = row % 32;
+        const int n = t < 16 ? 16 * q + t : HALF + 16 * q + t - 16;
         const int k0 = 2 * k2;
         const uint32_t lo = k0 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0) * p.Hkv * D + n]) : 0u;
         const uint32_t hi = k0 + 1 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0 + 1) * p.Hkv * D + n]) : 0u;
@@ -299,19 +323,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  // Register split: the launch gives every thread kLaunchRegs; warpgroup 0
+  // (producer and MMA issuers) hands registers to the softmax and rebuild
+  // warpgroups (128 * kLowRegs + 256 * kHighRegs = 384 * kLaunchRegs), each
+  // warpgroup at the top of its own branch below.
+  auto uni = [&](bool c) { return __shfl_sync(0xffffffffu, static_cast<int>(c), 0) != 0; };
 
+  if (warp < kSmWarp0) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kLowRegs));
   // ============================================================ producer
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tmap(&tm_base);
-      prefetch_tmap(&tm_lr);
+      prefetch_tmap(&tm_lk);
+      prefetch_tmap(&tm_base_run);
+      prefetch_tmap(&tm_lr_run);
     }
     const int nblk_vis = pos_max / kBlock + 1;  // blocks holding a key some row sees
-    const uint32_t per_blk = 2u * kBlock * D * 2 + (rebuild ? kBlock * LSPAN : 0) +
-                             (use_lr ? kBlock * LSPAN : 0);
+    const uint32_t per_blk = 2u * kBlock * D * 2 + (use_lr ? kBlock * LSPAN : 0) +
+                             (rebuild ? kBlock * LSPAN : 0);
+    const int32_t* bt_row = p.block_tables + static_cast<int64_t>(s_row) * p.max_blocks;
+    // block ids of the next tile are fetched one tile ahead (lane b: block b)
+    int id_next = (lane < NB && lane < nblk_vis) ? __ldg(bt_row + lane) : -1;
     int issued = 0;
-    for (int j = 0; j < n_st; ++j) {
+    for (int j = 0; j < U; ++j) {
       const int s = j % NST;
+      const int id = id_next;
+      const int bn = (j + 1) * NB + lane;
+      id_next = (lane < NB && bn < nblk_vis) ? __ldg(bt_row + bn) : -1;
       int ok = 1;
       if (lane == 0) {
         if (*abort_flag) ok = 0;
@@ -323,21 +362,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       int blk = -1;
-      const int bi = j * 8 + lane;
-      if (lane < 8 && bi < nblk_vis) {
-        const int b = __ldg(p.block_tables + static_cast<int64_t>(s_row) * p.max_blocks + bi);
-        if (b >= 0 && b < p.num_blocks) blk = b;
+      if (lane < NB && j * NB + lane < nblk_vis) {
+        if (id >= 0 && id < p.num_blocks) blk = id;
         else report(p.status, LRKV_ERR_INDEX);
       }
       const uint32_t mask = __ballot_sync(0xffffffffu, blk >= 0);
+      // one copy per plane when the tile's blocks are consecutive in the pool
+      const int blk0 = __shfl_sync(0xffffffffu, blk, 0);
+      const bool run = mask == (1u << NB) - 1 && __all_sync(0xffffffffu, lane >= NB || blk == blk0 + lane);
       if (lane == 0) {
         stage_mask[s] = static_cast<int>(mask);
         mbar_arrive_expect_tx(bar(B_FULL + s), __popc(mask) * per_blk);
       }
       __syncwarp();
-      if (blk >= 0) {
-        const uint32_t st = sbase + s * L::STAGE;
-        const uint32_t fb = bar(B_FULL + s);
+      const uint32_t st = sbase + s * L::STAGE;
+      const uint32_t fb = bar(B_FULL + s);
+      if (run) {
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_4d(st + L::off_k + h * (BN * 128), &tm_base_run, 64 * h, 0, head, blk0, fb);
+            tma_load_4d(st + L::off_v + h * (BN * 128), &tm_base_run, 64 * h, 0, p.Hkv + head, blk0, fb);
+          }
+          if (use_lr) tma_load_4d(st + L::off_lv, &tm_lr_run, 0, 0, 1, blk0, fb);
+          if (rebuild) tma_load_4d(st + L::off_lk, &tm_lr_run, 0, 0, 0, blk0, fb);
+        }
+      } else if (blk >= 0) {
         const int yk = ((blk * 2 + 0) * p.Hkv + head) * kBlock;
         const int yv = ((blk * 2 + 1) * p.Hkv + head) * kBlock;
 #pragma unroll
@@ -345,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(st + L::off_k + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yk, fb);
           tma_load_2d(st + L::off_v + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yv, fb);
         }
-        if (rebuild) tma_load_2d(st + L::off_lk + lane * kBlock * LSPAN, &tm_lr, 0, (blk * 2 + 0) * kBlock, fb);
-        if (use_lr) tma_load_2d(st + L::off_lv + lane * kBlock * LSPAN, &tm_lr, 0, (blk * 2 + 1) * kBlock, fb);
+        if (use_lr) tma_load_2d(st + L::off_lv + lane * kBlock * LSPAN, &tm_lk, 0, (blk * 2 + 1) * kBlock, fb);
+        if (rebuild) tma_load_2d(st + L::off_lk + lane * kBlock * LSPAN, &tm_lk, 0, (blk * 2 + 0) * kBlock, fb);
       }
       ++issued;
     }
@@ -357,82 +407,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ================================================================= MMA
-  // Fixed issue order S(0); then per half-tile u: S(u+1), P V(u). S(u+1)
-  // overwrites the score buffer of u-1, whose P V was issued one step earlier
-  // (MMAs execute in issue order). The whole warp runs the sequence in
-  // lockstep, every decision taken from lane 0; one elected lane issues.
+  // ============================================================ S issuer
+  // S(u) = Q K_a(u)^T into the single score buffer, once the rebuild has
+  // written K_a(u) and the softmax has loaded S(u-1).
   if (warp == 1) {
     const uint32_t idS = rebuild ? kIdS16 : kIdSbf;
-    auto uni = [&](bool c) { return __shfl_sync(0xffffffffu, static_cast<int>(c), 0) != 0; };
-    auto wait_u = [&](uint32_t b, uint32_t par) { return uni(wait_phase(b, par, p.status)); };
-    auto issue_S = [&](int u) {
-      tc::fence_after();
-      const uint32_t kt = sbase + ((u >> 1) % NST) * L::STAGE + L::off_k + (u & 1) * HN * 128;
-      const uint32_t dcol = tbase + S_COL0 + 64 * (u & 1);
-      if (tc::elect_one()) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t b = tc::sdesc(kt + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024, 2);
-          tc::mma_ts(dcol, tbase + Q_COL + ks * 8, b, idS, ks > 0);
-        }
-        tc::commit(bar(B_SFULL + (u & 1)));
-      }
-      __syncwarp();
-    };
-    auto issue_PV = [&](int u) {
-      tc::fence_after();
-      const int s = (u >> 1) % NST;
-      const uint32_t st = sbase + s * L::STAGE;
-      const uint32_t pcol = tbase + S_COL0 + 64 * (u & 1);
-      const uint32_t vt = st + L::off_v + (u & 1) * HN * 128;
-      if (tc::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < HN / 16; ++kk) {
-          const uint64_t b = tc::sdesc(vt + kk * 16 * 128, BN * 128, 1024, 2);
-          tc::mma_ts(tbase + O_COL, pcol + kk * 8, b, kIdPV, (u > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (use_lr) {
-          const uint32_t lvt = st + L::off_lv + (u & 1) * HN * LSPAN;
-#pragma unroll
-          for (int kk = 0; kk < HN / 16; ++kk) {
-            const uint64_t b = tc::sdesc(lvt + kk * 16 * LSPAN, BN * LSPAN, 8 * LSPAN, SW_LR);
-            tc::mma_ts(tbase + OLR_COL, pcol + kk * 8, b, kIdPLV, (u > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-        tc::commit(bar(B_OBAR));
-        if ((u & 1) || u == U - 1) tc::commit(bar(B_EMPTY + s));
-      }
-      __syncwarp();
-    };
-    bool ok = !uni(*abort_flag != 0) && wait_u(bar(B_KA + 0), 0);
-    if (ok) issue_S(0);
-    for (int u = 0; ok && u < U; ++u) {
-      if (u + 1 < U) {
-        const int j1 = (u + 1) >> 1;
-        if (!((u + 1) & 1) && !wait_u(bar(B_KA + j1 % NST), (j1 / NST) & 1)) {
-          ok = false;
-          break;
-        }
-        issue_S(u + 1);
-      }
-      if (!wait_u(bar(B_PFULL + (u & 1)), (u >> 1) & 1)) {
+    const uint64_t bdesc0 = tc::sdesc(sbase + L::off_k, 16, 1024, 2);
+    bool ok = true;
+    for (int u = 0; u < U; ++u) {
+      const int s = u % NST;
+      if (uni(*abort_flag != 0) || !uni(wait_phase(bar(B_KA + s), (u / NST) & 1, p.status)) ||
+          (u > 0 && !uni(wait_phase(bar(B_SFREE), (u - 1) & 1, p.status)))) {
         ok = false;
         break;
       }
-      issue_PV(u);
-      if (uni(*abort_flag != 0)) ok = false;
+      tc::fence_after();
+      if (tc::elect_one()) {
+        const uint64_t bd = bdesc0 + ((s * L::STAGE) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc::mma_ts(tbase + S_COL, tbase + Q_COL + ks * 8, bd + (((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4),
+                     idS, ks > 0);
+        tc::commit(bar(B_SFULL));
+      }
+      __syncwarp();
     }
     if (!ok && lane == 0) *abort_flag = 1;
-    // Z = fp16(O_lr / l) B_V into the score buffers (free once every P V is issued)
-    if (ok && use_lr) {
-      if (wait_u(bar(B_EPI), 0)) {
+    if (uni(*abort_flag != 0)) {
+      if (tc::elect_one()) {
+        tc::commit(bar(B_DRAIN + 1));
+        mbar_wait(bar(B_DRAIN + 1), 0, nullptr, 1u << 16);
+      }
+      __syncwarp();
+    }
+  }
+
+  // ================================================== P V / P L_V issuers
+  // O += P(u) V (warp 2) and O_lr += P(u) L_V (warp 3) once the softmax has
+  // written P(u); each commit releases the stage (two arrivals when both run).
+  // At the end warp 2 also computes Z = fp16(O_lr / l) B_V.
+  if (warp == 2 || (warp == 3 && use_lr)) {
+    const bool lv = warp == 3;
+    const uint64_t bdesc0 = lv ? tc::sdesc(sbase + L::off_lv, BN * LSPAN, 8 * LSPAN, SW_LK)
+                               : tc::sdesc(sbase + L::off_v, BN * 128, 1024, 2);
+    const uint32_t dcol = tbase + (lv ? O_COL + D : O_COL);
+    const uint32_t idPV = lv ? kIdPLV : kIdPV;
+    const uint32_t row_bytes = lv ? LSPAN : 128;
+    bool ok = true;
+    for (int u = 0; u < U; ++u) {
+      const int s = u % NST;
+      if (uni(*abort_flag != 0) || !uni(wait_phase(bar(B_PFULL), u & 1, p.status))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      if (tc::elect_one()) {
+        const uint64_t bd = bdesc0 + ((s * L::STAGE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc::mma_ts(dcol, tbase + P_COL + kk * 8, bd + ((kk * 16 * row_bytes) >> 4), idPV,
+                     (u > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(bar(lv ? B_LBAR : B_OBAR));
+        tc::commit(bar(B_EMPTY + s));
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
+    if (!lv && ok && use_lr) {
+      if (uni(wait_phase(bar(B_EPI), 0, p.status))) {
         tc::fence_after();
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < RP / 16; ++kk) {
             const uint64_t b = tc::sdesc(sbase + kk * 16 * 128, RP * 128, 1024, 2);
-            tc::mma_ts(tbase + S_COL0, tbase + Q_COL + kk * 8, b, kIdZ, kk > 0);
+            tc::mma_ts(tbase + S_COL, tbase + Q_COL + kk * 8, b, kIdZ, kk > 0);
           }
           tc::commit(bar(B_ZFULL));
         }
@@ -441,48 +489,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
     }
-    // drain: every MMA issued so far completes before the tensor memory is released
     if (uni(*abort_flag != 0)) {
       if (tc::elect_one()) {
-        tc::commit(bar(B_DRAIN));
-        mbar_wait(bar(B_DRAIN), 0, nullptr, 1u << 16);
+        tc::commit(bar(B_DRAIN + warp));
+        mbar_wait(bar(B_DRAIN + warp), 0, nullptr, 1u << 16);
       }
       __syncwarp();
     }
   }
-
+  }  // warpgroup 0
   // ============================================================ softmax
-  if (warp >= kSmWarp0 && warp < kRbWarp0) {
+  else if (warp < kRbWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kHighRegs));
     float m_run = -CUDART_INF_F, l_run = 0.f;
     const float sc = p.scale_log2;
     int u = 0;
     for (; u < U; ++u) {
-      const int b = u & 1;
-      bool ok = !*abort_flag && wait_phase(bar(B_SFULL + b), (u >> 1) & 1, p.status);
+      bool ok = !*abort_flag && wait_phase(bar(B_SFULL), u & 1, p.status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         *abort_flag = 1;
         break;
       }
       tc::fence_after();
-      uint32_t sv[64];
-      {
-        uint32_t a[32], c[32];
-        tc::ld_x32(tbase + lane_off + S_COL0 + 64 * b, a);
-        tc::ld_x32(tbase + lane_off + S_COL0 + 64 * b + 32, c);
-        tc::wait_ld();
+      uint32_t sv[BN];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[e] = a[e];
-          sv[32 + e] = c[e];
-        }
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t a[16];
+        tc::ld_x16(tbase + lane_off + S_COL + 16 * c, a);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sv[16 * c + e] = a[e];
       }
-      const int key0 = u * HN;
-      const int bm = (stage_mask[(u >> 1) % NST] >> (4 * (u & 1))) & 0xF;
-      const bool need_mask = (key0 + HN - 1 > pos_min) || bm != 0xF || !sm_valid;
+      tc::wait_ld();
+      tc::fence_before();
+      mbar_arrive(bar(B_SFREE));  // the score buffer may take S(u+1)
+      const int key0 = u * BN;
+      const int bm = stage_mask[u % NST];
+      const bool need_mask = (key0 + BN - 1 > pos_min) || bm != (1 << NB) - 1 || !sm_valid;
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < HN; ++c) {
+        for (int c = 0; c < BN; ++c) {
           const bool vis = sm_valid && (key0 + c <= sm_pos) && ((bm >> (c >> 4)) & 1);
           sv[c] = vis ? sv[c] : __float_as_uint(-CUDART_INF_F);
         }
@@ -492,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxs[k] = __uint_as_float(sv[k]);
 #pragma unroll
-      for (int c = 8; c < HN; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], __uint_as_float(sv[c]));
+      for (int c = 8; c < BN; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], __uint_as_float(sv[c]));
 #pragma unroll
       for (int k = 0; k < 4; ++k) mxs[k] = fmaxf(mxs[k], mxs[k + 4]);
       const float mx = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
@@ -508,17 +554,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           resc = true;
         }
       }
-      if (__any_sync(0xffffffffu, resc)) {
-        // O and O_lr must not be in use by P V(u-1): wait for it, then rescale
+      // P(u-1) V and P(u-1) L_V must have completed: they read the P columns
+      // and write O, O_lr
+      if (u > 0) {
         bool okw = wait_phase(bar(B_OBAR), (u - 1) & 1, p.status);
+        if (use_lr) okw = okw && wait_phase(bar(B_LBAR), (u - 1) & 1, p.status);
         okw = __all_sync(0xffffffffu, okw);
         if (!okw) {
           *abort_flag = 1;
           break;
         }
         tc::fence_after();
+      }
+      if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < (D + RP + 31) / 32; ++c) {
           uint32_t v[32];
           tc::ld_x32(tbase + lane_off + O_COL + 32 * c, v);
           tc::wait_ld();
@@ -526,20 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           tc::st_x32(tbase + lane_off + O_COL + 32 * c, v);
         }
-        if (use_lr) {
-#pragma unroll
-          for (int c = 0; c < RP / 16; ++c) {
-            uint32_t v[16];
-            tc::ld_x16(tbase + lane_off + OLR_COL + 16 * c, v);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tc::st_x16(tbase + lane_off + OLR_COL + 16 * c, v);
-          }
-        }
         l_run *= alpha;
       }
-      uint32_t pk[32];
+      // P = 2^(s * scale - m) as packed bf16 into the P columns of this row
       float sums[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sums[k] = 0.f;
@@ -547,30 +586,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // then, and the offset 0 keeps ex2(-inf) = 0 instead of NaN
       const float moff = m_run == -CUDART_INF_F ? 0.f : m_run;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), sc, -moff));
-        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), sc, -moff));
-        sums[c & 7] += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
+      for (int c16 = 0; c16 < BN / 16; ++c16) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[16 * c16 + 2 * e]), sc, -moff));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[16 * c16 + 2 * e + 1]), sc, -moff));
+          sums[e] += p0 + p1;
+          w[e] = pack_bf16(p0, p1);
+        }
+        tc::st_x8(tbase + lane_off + P_COL + 8 * c16, w);
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) sums[k] += sums[k + 4];
       l_run += (sums[0] + sums[1]) + (sums[2] + sums[3]);
-      tc::st_x32(tbase + lane_off + S_COL0 + 64 * b, pk);
       tc::wait_st();
       tc::fence_before();
-      mbar_arrive(bar(B_PFULL + b));
+      mbar_arrive(bar(B_PFULL));
     }
     // ---- epilogue: out = O / l + Z,  Z = fp16(O_lr / l) B_V  (one small MMA)
-    bool ok = (u == U) && !*abort_flag && wait_phase(bar(B_OBAR), (U - 1) & 1, p.status);
+    bool ok = (u == U) && !*abort_flag && wait_phase(bar(B_OBAR), (U - 1) & 1, p.status) &&
+              (!use_lr || wait_phase(bar(B_LBAR), (U - 1) & 1, p.status));
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) *abort_flag = 1;
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
     if (ok) tc::fence_after();
     if (use_lr) {
       if (ok) {
-        // B_V [R][d] -> fp16, MN-major with 128-byte swizzle, into stage 0 (idle:
-        // every MMA has completed); rows R .. r'-1 are zero
+        // B_V [R][d] -> fp16, MN-major with 128-byte swizzle, into stage 0's K
+        // buffer (idle: every MMA has completed); rows R .. r'-1 are zero
         const __nv_bfloat16* src = p.B_V + static_cast<int64_t>(adapter) * R * p.Hkv * D + head * D;
         for (int e = rb_i; e < RP * (D / 8); e += 128) {
           const int k = e / (D / 8), v8 = e % (D / 8);
@@ -587,11 +631,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         // fp16(O_lr / l) as the A operand, over the (no longer needed) Q columns
 #pragma unroll
-        for (int c = 0; c < RP / 32 + (RP % 32 ? 1 : 0); ++c) {
+        for (int c = 0; c < (RP + 31) / 32; ++c) {
           uint32_t v[16];
           uint32_t f[16];
-          tc::ld_x16(tbase + lane_off + OLR_COL + 32 * c, v);
-          if (RP - 32 * c > 16) tc::ld_x16(tbase + lane_off + OLR_COL + 32 * c + 16, f);
+          tc::ld_x16(tbase + lane_off + O_COL + D + 32 * c, v);
+          if (RP - 32 * c > 16) tc::ld_x16(tbase + lane_off + O_COL + D + 32 * c + 16, f);
           tc::wait_ld();
           uint32_t a[16];
 #pragma unroll
@@ -618,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32], z[32];
         tc::ld_x32(tbase + lane_off + O_COL + 32 * c, v);
-        if (use_lr) tc::ld_x32(tbase + lane_off + S_COL0 + 32 * c, z);
+        if (use_lr) tc::ld_x32(tbase + lane_off + S_COL + 32 * c, z);
         tc::wait_ld();
         if (sm_valid) {
 #pragma unroll
@@ -640,45 +684,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ============================================================ rebuild
-  if (warp >= kRbWarp0) {
-    const int i = rb_i;       // key row within the stage
-    const int bb = i >> 4;    // block within the stage
-    // Every exit from this loop is decided by a barrier vote of the whole
-    // warpgroup (bar.red.or), so no warp is left waiting at a named barrier;
-    // a warp whose wait failed skips its work until the next vote.
-    // The warpgroup issues its own Y MMAs (one elected lane of its first
-    // warp; commits track each issuing thread separately): Y(j+1) as soon as
-    // every thread has read Y(j) and stage j+1 has landed, else right after
-    // stage j+1's tiles are seen.
+  else if (warp < kYWarp) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kHighRegs));
+    // RoPE delta table cos / sin(r * theta_j), r < 16, in smem (padded rows:
+    // the 16 rows a warp reads at once fall in distinct banks); kept out of
+    // registers so that the rotation loop stays rolled (small code)
+    for (int e = rb_i; e < 16 * HALF; e += 128) {
+      const int r = e / HALF, j = e % HALF;
+      *reinterpret_cast<float2*>(smem + L::off_dtab + r * L::DPITCH + j * 8) =
+          rope_cos_sin(r, p.freqs.hi[j], p.freqs.lo[j]);
+    }
+    named_bar_sync(3, 128);
+    const float* drow = reinterpret_cast<const float*>(smem + L::off_dtab + (rb_i & 15) * L::DPITCH);
+    const int i = rb_i;     // key row within the tile (rows >= BN idle)
+    const int bb = i >> 4;  // block within the tile
+    const bool row_in = i < BN;
+    // Block start angles: this thread keeps the entries e = i + 128 k of the
+    // table [NB][d/2] (all with pair jj = i % (d/2)) and advances them by the
+    // angle BN * theta_jj per tile (a complex product), recomputing them
+    // exactly every kAnchor tiles.
+    constexpr int NE = (NB * HALF + 127) / 128;
+    constexpr int kAnchor = 32;
+    const int jj_own = i % HALF;
+    const float2 rot = rope_cos_sin(BN, p.freqs.hi[jj_own], p.freqs.lo[jj_own]);
+    float bc[NE], bs[NE];
+    // Y arrives in quarters of 16 RoPE pairs from the Y issuer (warp 12):
+    // quarter g of the loop in TMEM buffer g & 1, phase g >> 1 of
+    // YFULL[g & 1]; each thread signals YFREE[g & 1] once it has the quarter
+    // in registers. Every exit from this loop is decided by a barrier vote of
+    // the whole warpgroup (bar.red.or), so no warp is left waiting at a named
+    // barrier; a warp whose wait failed skips its work until the next vote.
     bool failed = false;
-    bool y_next = false;  // Y of the coming stage already issued (issuing warp only)
-    const bool y_warp = warp == kRbWarp0;
-    auto issue_Y = [&](int jj) {
-      tc::fence_after();
-      const uint32_t stj = sbase + (jj % NST) * L::STAGE;
-      if (tc::elect_one()) {
-#pragma unroll
-        for (int gy = 0; gy < NG; ++gy) {
-#pragma unroll
-          for (int kk = 0; kk < RP / 16; ++kk) {
-            const uint64_t a = tc::sdesc(stj + L::off_lk + kk * 32, 16, 8 * LSPAN, SW_LR);
-            const uint64_t b = tc::sdesc(sbase + L::off_bk + 32 * gy * LSPAN + kk * 32, 16, 8 * LSPAN, SW_LR);
-            tc::mma_ss(tbase + Y_COL + 32 * gy, a, b, kIdY, kk > 0);
-          }
-          tc::commit(bar(B_YFULL + gy));
-        }
-      }
-      __syncwarp();
-    };
-    for (int j = 0; j < n_st; ++j) {
+    for (int j = 0; j < U; ++j) {
       const int s = j % NST;
-      const uint32_t st = sbase + s * L::STAGE;
-      // the previous stage's readers of btab are done past this barrier
+      // the previous tile's readers of btab are done past this barrier
       if (named_bar_or(3, 128, failed || *abort_flag != 0)) break;
-      if (rebuild) {  // block start angles of this stage
-        for (int e = i; e < 8 * HALF; e += 128) {
-          const int b2 = e / HALF, jj = e % HALF;
-          btab[e] = rope_cos_sin_fast(j * BN + kBlock * b2, p.freqs.hi[jj], p.freqs.lo[jj]);
+      if (rebuild) {  // block start angles of this tile
+#pragma unroll
+        for (int k = 0; k < NE; ++k) {
+          if (i + 128 * k >= NB * HALF) break;
+          if (j % kAnchor == 0) {
+            const float2 cs = rope_cos_sin_fast(j * BN + kBlock * ((i + 128 * k) / HALF), p.freqs.hi[jj_own],
+                                                p.freqs.lo[jj_own]);
+            bc[k] = cs.x;
+            bs[k] = cs.y;
+          } else {
+            const float c = bc[k] * rot.x - bs[k] * rot.y;
+            bs[k] = bs[k] * rot.x + bc[k] * rot.y;
+            bc[k] = c;
+          }
+          btab[i + 128 * k] = make_float2(bc[k], bs[k]);
         }
       }
       failed = !wait_phase(bar(B_FULL + s), (j / NST) & 1, p.status);
@@ -688,34 +743,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int mask = stage_mask[s];
       const int t = j * BN + i;
-      const bool key_ok = ((mask >> bb) & 1) && t < Ls;
+      const bool key_ok = row_in && ((mask >> bb) & 1) && t < Ls;
+      uint8_t* kbuf = smem + s * L::STAGE + L::off_k;  // this tile's K buffer
       if (rebuild) {
-        if (y_warp && !y_next) issue_Y(j);
         const float2* bt = btab + bb * HALF;
-#pragma unroll
-        for (int grp = 0; grp < NG; ++grp) {
-          bool oky = !failed && wait_phase(bar(B_YFULL + grp), j & 1, p.status);
+#pragma unroll 1
+        for (int q = 0; q < NQ; ++q) {
+          const int g = j * NQ + q;
+          bool oky = !failed && wait_phase(bar(B_YFULL + (g & 1)), (g >> 1) & 1, p.status);
           oky = __all_sync(0xffffffffu, oky);
-          if (!oky) {
+          if (!oky && !failed) {
             failed = true;
             *abort_flag = 1;
           }
           if (failed) continue;
+          uint32_t ylo[16], yhi[16];  // pairs 16 q + e: low dim, its partner
           tc::fence_after();
-          uint32_t y[32];  // [0, 16): dims 16 grp + e; [16, 32): their partners
-          tc::ld_x32(tbase + lane_off + Y_COL + 32 * grp, y);
+          tc::ld_x16(tbase + lane_off + Y_COL + 32 * (g & 1), ylo);
+          tc::ld_x16(tbase + lane_off + Y_COL + 32 * (g & 1) + 16, yhi);
           tc::wait_ld();
+          tc::fence_before();
+          mbar_arrive(bar(B_YFREE + (g & 1)));  // the buffer may take quarter g + 2
           if (key_ok) {
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {  // 8 pairs per 16-byte chunk
-              const int dlo = 16 * grp + 8 * hc, dhi = dlo + HALF;
-              const uint32_t alo = st + L::off_k + (dlo / 64) * (BN * 128) + swz<128>(i, (dlo % 64) * 2);
-              const uint32_t ahi = st + L::off_k + (dhi / 64) * (BN * 128) + swz<128>(i, (dhi % 64) * 2);
-              uint4 klo, khi;
-              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                           : "=r"(klo.x), "=r"(klo.y), "=r"(klo.z), "=r"(klo.w) : "r"(alo));
-              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                           : "=r"(khi.x), "=r"(khi.y), "=r"(khi.z), "=r"(khi.w) : "r"(ahi));
+              const int dlo = 16 * q + 8 * hc, dhi = dlo + HALF;
+              // this thread's own K row: plain shared accesses the compiler may schedule
+              uint4* plo = reinterpret_cast<uint4*>(kbuf + (dlo / 64) * (BN * 128) + swz<128>(i, (dlo % 64) * 2));
+              uint4* phi = reinterpret_cast<uint4*>(kbuf + (dhi / 64) * (BN * 128) + swz<128>(i, (dhi % 64) * 2));
+              const uint4 klo = *plo, khi = *phi;
               const uint32_t kl[4] = {klo.x, klo.y, klo.z, klo.w};
               const uint32_t kh[4] = {khi.x, khi.y, khi.z, khi.w};
               uint32_t olo[4], ohi[4];
@@ -724,14 +780,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float rl[2], rh[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                  const int pp = 8 * hc + 2 * w + e;  // pair index within the group
-                  const int jj = 16 * grp + pp;
+                  const int pp = 8 * hc + 2 * w + e;  // pair index within the quarter
+                  const int jj = 16 * q + pp;
                   const float2 b2 = bt[jj];
-                  const float cd = __half2float(__ushort_as_half(static_cast<unsigned short>(dl[jj] & 0xffffu)));
-                  const float sd = __half2float(__ushort_as_half(static_cast<unsigned short>(dl[jj] >> 16)));
+                  const float cd = drow[2 * jj], sd = drow[2 * jj + 1];
                   const float c = b2.x * cd - b2.y * sd;
                   const float sn = b2.y * cd + b2.x * sd;
-                  const float yl = __uint_as_float(y[pp]), yh = __uint_as_float(y[16 + pp]);
+                  const float yl = __uint_as_float(ylo[pp]), yh = __uint_as_float(yhi[pp]);
                   const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
                   const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
                   rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
@@ -740,45 +795,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                 olo[w] = pack_f16(rl[0], rl[1]);
                 ohi[w] = pack_f16(rh[0], rh[1]);
               }
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(alo), "r"(olo[0]), "r"(olo[1]),
-                           "r"(olo[2]), "r"(olo[3]) : "memory");
-              asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(ahi), "r"(ohi[0]), "r"(ohi[1]),
-                           "r"(ohi[2]), "r"(ohi[3]) : "memory");
+              *plo = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+              *phi = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
             }
           }
-        }
-        // every thread has read Y(j): issue Y(j+1) now if its tiles are there
-        tc::fence_before();
-        if (named_bar_or(3, 128, failed)) {
-          *abort_flag = 1;
-          break;
-        }
-        y_next = false;
-        if (y_warp && j + 1 < n_st &&
-            __shfl_sync(0xffffffffu, static_cast<int>(test_parity(bar(B_FULL + (j + 1) % NST), ((j + 1) / NST) & 1)), 0)) {
-          issue_Y(j + 1);
-          y_next = true;
         }
       }
       if (failed) continue;
       // Keys past the sequence end or in a block that was not loaded: zero their
       // V and L_V rows, so that P = 0 there cannot meet stale (NaN) data.
-      if (!key_ok) {
+      if (row_in && !key_ok) {
+        uint8_t* vbuf = smem + s * L::STAGE + L::off_v;
+        uint8_t* lvbuf = smem + s * L::STAGE + L::off_lv;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint32_t a = st + L::off_v + (c / 8) * (BN * 128) + swz<128>(i, (c % 8) * 16);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
-        }
+        for (int c = 0; c < D / 8; ++c)
+          *reinterpret_cast<uint4*>(vbuf + (c / 8) * (BN * 128) + swz<128>(i, (c % 8) * 16)) = make_uint4(0, 0, 0, 0);
         if (use_lr) {
 #pragma unroll
-          for (int c = 0; c < LSPAN / 16; ++c) {
-            const uint32_t a = st + L::off_lv + swz<LSPAN>(i, c * 16);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
-          }
+          for (int c = 0; c < LSPAN / 16; ++c)
+            *reinterpret_cast<uint4*>(lvbuf + swz<LSPAN>(i, c * 16)) = make_uint4(0, 0, 0, 0);
         }
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_arrive(bar(B_KA + s));
+    }
+  }
+  // ============================================================ Y issuer
+  // Quarter g = L_K(tile g / NQ) B_K^T[rows 32 (g % NQ) ..] into Y buffer
+  // g & 1, once the tile has landed and every rebuild thread has read
+  // quarter g - 2 from that buffer.
+  else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kLowRegs));
+    if (warp == kYWarp && rebuild) {
+      bool ok = true;
+      for (int g = 0; g < NQ * U; ++g) {
+        const int jj = g / NQ, q = g % NQ;
+        if (uni(*abort_flag != 0) ||
+            (g >= 2 && !uni(wait_phase(bar(B_YFREE + (g & 1)), ((g - 2) >> 1) & 1, p.status))) ||
+            (q == 0 && !uni(wait_phase(bar(B_FULL + jj % NST), (jj / NST) & 1, p.status)))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        const uint32_t stj = sbase + (jj % NST) * L::STAGE;
+        if (tc::elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < RP / 16; ++kk) {
+            const uint64_t a = tc::sdesc(stj + L::off_lk + kk * 32, 16, 8 * LSPAN, SW_LK);
+            const uint64_t b = tc::sdesc(sbase + L::off_bk + 32 * q * LSPAN + kk * 32, 16, 8 * LSPAN, SW_LK);
+            tc::mma_ss(tbase + Y_COL + 32 * (g & 1), a, b, kIdY, kk > 0);
+          }
+          tc::commit(bar(B_YFULL + (g & 1)));
+        }
+        __syncwarp();
+      }
+      if (!ok && lane == 0) *abort_flag = 1;
+      if (uni(*abort_flag != 0)) {
+        if (tc::elect_one()) {
+          tc::commit(bar(B_DRAIN + 0));
+          mbar_wait(bar(B_DRAIN + 0), 0, nullptr, 1u << 16);
+        }
+        __syncwarp();
+      }
     }
   }
 
@@ -817,9 +895,11 @@ lrkv_status run(const lrkv_config& cfg, const PrefillArgs& a, cudaStream_t strea
   p.has_bv = a.B_V != nullptr;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   rope_freqs(cfg, &p.freqs);
-  CUtensorMap tb, tl;
+  CUtensorMap tb, tlk, tbr, tlr;
   if (!make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
-  if (!make_lr_map(cfg, a.lr_pool, a.num_blocks, PL<D, R>::RP, &tl)) return LRKV_ERR_CUDA;
+  if (!make_lr_map(cfg, a.lr_pool, a.num_blocks, PL<D, R>::RP, &tlk)) return LRKV_ERR_CUDA;
+  if (!make_run_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, PL<D, R>::NB, PL<D, R>::RP, &tbr, &tlr))
+    return LRKV_ERR_CUDA;
   auto kern = prefill_kernel<D, R>;
   constexpr int smem = PL<D, R>::total;
   static bool attr_set = false;  // idempotent per-process kernel attribute
@@ -830,7 +910,7 @@ lrkv_status run(const lrkv_config& cfg, const PrefillArgs& a, cudaStream_t strea
   }
   const int tiles = (a.max_q_len * p.g + BM - 1) / BM;
   dim3 grid(tiles, cfg.n_kv_heads, a.num_seqs);
-  kern<<<grid, kThreads, smem, stream>>>(p, tb, tl);
+  kern<<<grid, kThreads, smem, stream>>>(p, tb, tlk, tbr, tlr);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
 

@@ -127,6 +127,11 @@ __device__ __forceinline__ void ld_x32(uint32_t taddr, uint32_t (&v)[32]) {
       : LRKV_R8(v, 0), LRKV_R8(v, 8), LRKV_R8(v, 16), LRKV_R8(v, 24)
       : "r"(taddr));
 }
+__device__ __forceinline__ void st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+               LRKV_W8(v, 0)
+               : "memory");
+}
 __device__ __forceinline__ void st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),

@@ -74,6 +74,22 @@ def test_prefill_ranks(cuda_lib, rank):
         assert_close(res["prefill"][rows].double().cpu().numpy(), want, BF16_TOL, f"r={rank} seq {p}")
 
 
+@pytest.mark.parametrize("rank", [16, 64])
+def test_head_dim_64_prefill_and_decode(cuda_lib, rank):
+    """head_dim 64 (one 64-column swizzle atom per K / V row), with a ragged
+    chunk: prefill and decode against the oracle."""
+    sh = I.Shape(1024, 8, 2, 64, rank, 2, 10000.0, "bf16", 1.0, 1 / math.sqrt(1024), 1 / math.sqrt(1024),
+                 1 / math.sqrt(rank), 1.0)
+    seqs = [I.Seq(0, 144, 1 + a, 144, 37, a, "prefill") for a in range(2)]
+    case = I._build("head_dim_64", sh, 0, seqs, [], [0, 1], False)
+    g, res = _run(case)
+    assert g.device_status() == 0
+    w64 = weights64(case)
+    for p in range(g.n_pre):
+        rows, want = oracle_prefill_seq(case, p, w64=w64, cache="bf16")
+        assert_close(res["prefill"][rows].double().cpu().numpy(), want, BF16_TOL, f"d=64 r={rank} seq {p}")
+
+
 def test_decode_many_agents_one_context(cuda_lib):
     """More queries on one context than one sweep serves (several query groups),
     with repeated and base-only adapters."""
@@ -130,6 +146,24 @@ def test_permuted_block_table_is_bitwise_identical(cuda_lib):
     bt2 = torch.where(g.dec_bt >= 0, perm[g.dec_bt.long().clamp(min=0)].int(), g.dec_bt)
     out2 = cuda_lib.attn_decode(g.cfg, g.dec_q, g.dec_q_start, g.dec_adapter, bt2, g.dec_lens,
                                 g.dec_max_len, g.dec_max_q, base2, lr2, g.B_K, g.B_V, g.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_prefill_permuted_block_table_is_bitwise_identical(cuda_lib):
+    """Contiguous block tables take the run-of-blocks copies, a permuted pool the
+    per-block copies: both must land the same tiles, bit for bit."""
+    case = I.prefill_chunk(prefix=304, chunk=70, n_agents=2)
+    g, res = _run(case, pool_fill=0.0)
+    out1 = res["prefill"].clone()
+    perm = torch.randperm(case.num_blocks, generator=torch.Generator().manual_seed(11)).to(g.device)
+    base2 = torch.empty_like(g.base_pool)
+    lr2 = torch.empty_like(g.lr_pool)
+    base2[perm.long()] = g.base_pool
+    lr2[perm.long()] = g.lr_pool
+    bt2 = torch.where(g.pre_bt >= 0, perm[g.pre_bt.long().clamp(min=0)].int(), g.pre_bt)
+    out2 = cuda_lib.attn_prefill(g.cfg, g.pre_q, g.pre_q_start, g.pre_max_q, g.pre_lens, g.pre_max_len,
+                                 g.pre_adapter, bt2, base2, lr2, g.B_K, g.B_V, g.scale)
     torch.cuda.synchronize()
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
