@@ -1,26 +1,44 @@
-// Decode attention over the paged base + shared-A low-rank cache (bf16).
+// Decode attention over the paged base + shared-A low-rank cache (bf16), on
+// the 5th-generation tensor cores.
 //
 // LRAgent (arXiv 2602.01053), Abstract: one cached context serves every agent;
 // each agent's adapter contribution is rebuilt from the low-rank cache at
 // attention time, never expanded to full width in memory (Flash-LoRA-
-// Attention). Here, per 16-token block and per distinct adapter a of the
-// queries reading the block:
-//     K_a = K_base + RoPE(L_K B_K,a)          rebuilt in registers, never stored
-//     S^T = K_a Q^T * scale                   (tokens x query rows; fp16 operands)
-//     online softmax over tokens, per row
-//     O   += P V_base,  O_lr += P L_V         (the V term reordered: (P L_V) B_V
-//                                              is applied once, after the merge)
-// The kernel is persistent: each CTA walks work items (context, query group,
-// split of the context's blocks, kv head; kv head fastest so that concurrent
-// CTAs share the low-rank tiles through L2). Its eight warps take the item's
-// blocks round-robin; each warp streams its own blocks (K/V halves with a
-// 128-byte swizzle, L_K / L_V tiles) through a private two-stage ring of 2-D
-// TMA copies completed on mbarriers, fetching block ids one step ahead and
-// crossing item boundaries without draining. Scores of every adapter
-// accumulate into one fragment: the query fragment is masked to that
-// adapter's rows. Each item ends by merging the warps' (m, l, O, O_lr) in a
-// fixed order and writing an fp32 partial; combine_kernel (launched with
-// programmatic dependent launch) merges the splits and applies B_V.
+// Attention). The V term is reordered as (P L_V) B_V and applied once, after
+// the splits are merged.
+//
+// The K term. For a query row q (query n, head m, adapter a) and key token t
+// with low-rank entry l(t) = L_K[t] (rank r), RoPE turns the pairs
+// (j, j + d/2) by the angle t * theta_j, so the adapter part of the score is
+//   q . RoPE_t(B_K,a^T l(t))
+//     = sum_k l_k(t) sum_j [ cos(t theta_j) G_{k,j} + sin(t theta_j) G_{k,d/2+j} ]
+//   G_{k,j}       = q_j B_{k,j} + q_{j+d/2} B_{k,j+d/2}
+//   G_{k,d/2+j}   = q_{j+d/2} B_{k,j} - q_j B_{k,j+d/2}          (j < d/2)
+// (the same sum as rotating the rebuilt row and taking the dot product, in
+// another association order). G depends only on the query row and its
+// adapter, so it is built once per work item; u(t) = [cos t theta, sin t theta]
+// depends only on the position. Per 128-token tile the kernel then computes
+//   W   = U G^T        (tokens x rows*r, tcgen05, fp16 operands)
+//   S_b = K_base Q^T   (tokens x rows,   tcgen05, bf16)
+//   s(t, row) = S_b(t, row) + sum_k l_k(t) W(t, row*r + k)     (one thread per token)
+//   online softmax over tokens, P^T (bf16) to shared memory
+//   O^T += V^T P^T,  O_lr^T += L_V^T P^T                        (tcgen05, bf16)
+// so every agent's rows of one kv head share one pass over each base and
+// low-rank tile, and the full-width adapter K is never formed.
+//
+// Work item: (context, chunk of <= 16 query rows of one kv head, split of the
+// context's blocks, kv head), kv head fastest so that the items running
+// together share the low-rank tiles through L2. One CTA per item:
+//   warp 0      TMA producer: K_base + L_K tiles and V_base + L_V tiles of 8
+//               blocks (per-block 2-D copies) into two rings
+//   warp 1      issues W = U G^T (U from tensor memory)
+//   warp 2      issues S_b = K_base Q^T
+//   warp 3      issues O^T += V^T P^T and O_lr^T += L_V^T P^T
+//   warps 4-7   one thread per token of the tile: U for the next tile, scores,
+//               online softmax (rescale decided by a block-wide vote), P^T,
+//               and at the end the split partial (m, l, O, O_lr)
+// combine_kernel (programmatic dependent launch) merges the splits and
+// applies B_V.
 #include <math_constants.h>
 
 #include <algorithm>
@@ -28,16 +46,27 @@
 
 #include "lrkv_device.cuh"
 #include "lrkv_internal.h"
+#include "tcgen05.cuh"
 
 namespace lrkv {
 namespace {
 
-constexpr int kNW = 8;               // warps per CTA (all consume; lane 0 of each issues its TMA)
-constexpr int kThreads = kNW * 32;
-constexpr int kNST = 2;              // stages per warp
-constexpr int kMaxRows = 16;         // query rows (queries x heads) per item
-constexpr int kMaxSlots = 4;         // distinct adapters per item
+constexpr int kThreads = 256;
+constexpr int kBT = 128;                   // tokens per tile (tcgen05 M)
+constexpr int kTileBlocks = kBT / kBlock;  // 8 blocks per tile
+constexpr int kMaxRows = 16;               // query rows per item (tcgen05 N of S_b, O^T)
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMinSmem = 120 * 1024;       // keeps one CTA (and one TMEM owner) per SM
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns
+constexpr uint32_t W_COL = 0;     // [<=256] W = U G^T, fp32
+constexpr uint32_t DT_COL = 256;  // [d]    e^{i delta theta_j} of this lane's token offset, fp32
+constexpr uint32_t U_COL = 384;   // [d/2]  U (fp16 pairs), operand A of W
+constexpr uint32_t S_COL = 448;   // [16]   S_b
+constexpr uint32_t OT_COL = 464;  // [16]   O^T  (lane = head dim)
+constexpr uint32_t OL_COL = 480;  // [16]   O_lr^T (lane = rank index)
+constexpr float kRescaleLog2 = 8.f;         // lazy rescale threshold (log2 units)
+constexpr long long kWaitCycles = 1ll << 31;  // ~1 s: a wait this long has failed
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -50,692 +79,713 @@ struct DecodeParams {
   float* part_o;   // [Nq*Hq][S][D + R]
   int32_t* status;
   int64_t num_blocks;
-  int64_t n_items;
-  int max_blocks, max_ctx_len, n_adapters, num_ctx, Hq, Hkv, g;
-  int qg_size, n_qgroups, n_splits, split_blocks;
+  int max_blocks, max_ctx_len, n_adapters, num_queries, Hq, Hkv, g;
+  int rpi, n_chunks, n_splits, split_blocks;
   int has_bk, has_bv;
   float scale_log2;
   RopeFreqs freqs;
 };
 
-// Shared-memory layout (byte offsets from a 1024-aligned base), fixed per (D, R).
-// B_K slots: up to four distinct adapters per item (one at rank 64, where the
-// ring of 12 KB blocks leaves room for one 17 KB slice).
+// Shared-memory layout (byte offsets from a 1024-aligned base), fixed per (d, r).
+// A stage holds one tile of one operand pair: [low-rank 128 x RP][base atoms
+// 64 dims x 128 tokens, 128-byte swizzle]. NK stages of K_base + L_K, NV of
+// V_base + L_V.
 template <int D, int R>
 struct DL {
-  static constexpr int kSlots = R >= 64 ? 1 : kMaxSlots;
-  static constexpr int kv_tile = 16 * D * 2;
-  static constexpr int lr_tile = 16 * R * 2;
-  static constexpr int blk = ((2 * kv_tile + 2 * lr_tile) + 1023) & ~1023;  // K, V, L_K, L_V
-  static constexpr int bk_pitch = (D + 8) * 2;  // bytes per B_K row (conflict-free ldmatrix)
-  static constexpr int bk_slot = R * bk_pitch;
-  static constexpr int d_pitch = (D / 2) * 8 + 64;  // delta-table row: D/2 float2 + pad
-  static constexpr int acc_pitch = D + R + 4;       // floats; the merge accumulator aliases B_K
-  static constexpr int bk_bytes = kSlots * bk_slot;
-  static constexpr int acc_bytes = kMaxRows * acc_pitch * 4;
-  static constexpr int off_bk = kNW * kNST * blk;
-  static constexpr int off_dtab = (off_bk + (bk_bytes > acc_bytes ? bk_bytes : acc_bytes) + 15) & ~15;
-  static constexpr int off_btab = off_dtab + 16 * d_pitch;
-  static constexpr int off_freq = off_btab + kNW * (D / 2) * 8;
-  static constexpr int off_ml = off_freq + 2 * 64 * 4;
-  static constexpr int off_misc = off_ml + 2 * kNW * kMaxRows * 4 + 2 * kMaxRows * 4;
-  static constexpr int off_bar = (off_misc + 128 + 7) & ~7;
-  static constexpr int total = off_bar + kNW * kNST * 8 + 1024;  // + alignment slack
+  static constexpr int HALF = D / 2;
+  static constexpr int RP = R < 16 ? 16 : R;  // low-rank tile columns (zero past R)
+  static constexpr int LSPAN = RP * 2;        // bytes per low-rank row
+  static constexpr uint32_t SW_LR = tc::swizzle_code(LSPAN);
+  static constexpr int RPI = (256 / R) < kMaxRows ? 256 / R : kMaxRows;  // rows per item
+  static constexpr int NW_MAX = RPI * R;      // W columns (<= 256)
+  static constexpr int KATOMS = D / 64;
+  static constexpr int ATOM = kBT * 128;
+  static constexpr int LR_TILE = kBT * LSPAN;
+  static constexpr int STAGE = LR_TILE + KATOMS * ATOM;
+  static constexpr int GAMMA_ATOM = NW_MAX * 128;
+  static constexpr int GAMMA = KATOMS * GAMMA_ATOM;
+  static constexpr int QB = KATOMS * kMaxRows * 128;
+  static constexpr int PB = 2 * kMaxRows * 128;  // P^T [16 rows][128 tokens] bf16
+  static constexpr int BTAB = 2 * HALF * 8;
+  static constexpr int TAIL = GAMMA + QB + 2 * PB + BTAB + 512 + 512;
+  static constexpr int NK = (4 * STAGE + TAIL + 1024 <= kSmemLimit) ? 2 : 1;
+  static constexpr int NV = 2;
+  static constexpr int off_k = 0;
+  static constexpr int off_v = NK * STAGE;
+  static constexpr int off_g = off_v + NV * STAGE;
+  static constexpr int off_q = off_g + GAMMA;
+  static constexpr int off_p = off_q + QB;
+  static constexpr int off_btab = off_p + 2 * PB;
+  static constexpr int off_misc = off_btab + BTAB;
+  static constexpr int off_bar = off_misc + 512;
+  static constexpr int used = off_bar + 512;
+  static constexpr int total = used + 1024;  // + alignment slack
+  static_assert(total <= kSmemLimit, "decode tile does not fit in shared memory");
+  static_assert(NW_MAX <= 256 && NW_MAX % 16 == 0, "W must be a legal tcgen05 N");
+  // The M = 128 operands V^T (d = 64) and L_V^T (r < 128) read whole 128-row
+  // spans; the rows past the tile land in the following buffers (never past
+  // the allocation) and only feed accumulator lanes that are never read.
+  static_assert(off_v + (NV - 1) * STAGE + LR_TILE + 2 * ATOM <= used, "V^T span");
+  static_assert(off_v + (NV - 1) * STAGE + 7 * 16 * LSPAN + (128 / RP - 1) * LR_TILE +
+                        16 * LSPAN <= used, "L_V^T span");
 };
 
-struct Item {
-  int ctx, qg, split, head;
-  int q0, nq;      // first query row and count in this group
-  int kbeg, kend;  // block range [kbeg, kend)
-  int len;
-  bool active;
+enum : int {
+  B_FK = 0,     // [2] K_base + L_K stage full (TMA bytes)
+  B_EK = 2,     // [2] K stage consumed (token warps, after S_b completed)
+  B_FV = 4,     // [2] V_base + L_V stage full (TMA bytes)
+  B_EV = 6,     // [2] V stage consumed (commit of the O^T / O_lr^T MMAs)
+  B_UF = 8,     // U of the next tile written (token warps)
+  B_WF = 9,     // W complete (commit)
+  B_SF = 10,    // S_b complete (commit)
+  B_WR = 11,    // W and S_b read out (token warps)
+  B_PF = 12,    // [2] P^T written, O rescaled (token warps)
+  B_PR = 14,    // [2] P V of that buffer complete (commit)
+  B_DRAIN = 16, // [4] per MMA warp, on abort: its MMAs have completed
+  B_COUNT = 20
 };
 
-__device__ __forceinline__ Item get_item(const DecodeParams& p, int64_t it) {
-  Item I;
-  I.head = static_cast<int>(it % p.Hkv);
-  int64_t r = it / p.Hkv;
-  I.split = static_cast<int>(r % p.n_splits);
-  r /= p.n_splits;
-  I.qg = static_cast<int>(r % p.n_qgroups);
-  I.ctx = static_cast<int>(r / p.n_qgroups);
-  const int qs = __ldg(p.ctx_q_start + I.ctx), qe = __ldg(p.ctx_q_start + I.ctx + 1);
-  I.q0 = qs + I.qg * p.qg_size;
-  I.nq = min(p.qg_size, qe - I.q0);
-  I.active = I.nq > 0;
-  int len = __ldg(p.ctx_lens + I.ctx);
-  if (len < 1 || len > p.max_ctx_len) len = 0;
-  I.len = len;
-  const int nblk = (len + kBlock - 1) / kBlock;
-  I.kbeg = I.split * p.split_blocks;
-  I.kend = min(I.kbeg + p.split_blocks, nblk);
-  return I;
+__device__ __forceinline__ uint32_t bar_count(int i) {
+  if (i == B_EK || i == B_EK + 1 || i == B_UF || i == B_WR || i == B_PF || i == B_PF + 1) return 4;
+  return 1;
 }
 
-// A warp's walk over its (item, block) pairs: items it = blockIdx.x + k * gridDim.x,
-// blocks kbeg + warp, kbeg + warp + kNW, ... of each active item.
-struct Walk {
-  int64_t it;
-  int kb;
-  Item I;
-  bool more;
-};
+// Named barrier over `count` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
-__device__ __forceinline__ void walk_next(const DecodeParams& p, int warp, Walk& w) {
-  w.kb += kNW;
-  while (!(w.I.active && w.kb < w.I.kend)) {
-    w.it += gridDim.x;
-    if (w.it >= p.n_items) {
-      w.more = false;
-      return;
+// Waits for an mbarrier phase; gives up (LRKV_ERR_TIMEOUT, false) after
+// kWaitCycles, or early once another role has raised the CTA's abort flag.
+__device__ __forceinline__ bool wait_ab(uint32_t bar, uint32_t parity, int32_t* st,
+                                        const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag != 0) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      report(st, LRKV_ERR_TIMEOUT);
+      return false;
     }
-    w.I = get_item(p, w.it);
-    w.kb = w.I.kbeg + warp;
   }
-  w.more = true;
 }
 
-__device__ __forceinline__ void walk_init(const DecodeParams& p, int warp, Walk& w) {
-  w.it = static_cast<int64_t>(blockIdx.x) - gridDim.x;
-  w.I.active = false;
-  w.I.kend = 0;
-  w.kb = 0;
-  walk_next(p, warp, w);
+// 2^x by the hardware approximation (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
-template <int D, int R, int RN>
+__device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
+
+template <int D, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p,
                   const __grid_constant__ CUtensorMap tm_base,
                   const __grid_constant__ CUtensorMap tm_lr) {
+  using L = DL<D, R>;
   constexpr int HALF = D / 2;
-  constexpr int NCH = D / 32;   // dim chunks: each covers 16 dims + their RoPE partners
-  constexpr int NKS = D / 16;   // k-slices of the score MMA
-  constexpr int NRT = R >= 16 ? R / 16 : 1;  // rank k-steps of the rebuild
-  constexpr int NMT = D / 16;   // m-tiles of O^T (head dims)
-  constexpr int NLM = R >= 16 ? R / 16 : 1;  // m-tiles of O_lr^T (rank)
-  constexpr int LR_RB = R * 2;  // low-rank tile row bytes
+  constexpr int KS = D / 16;  // k-steps over the head dims (and over u)
+  constexpr int LSPAN = L::LSPAN;
+  constexpr int NK = L::NK, NV = L::NV;
 
   // The combine kernel may be scheduled now; it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  using L = DL<D, R>;
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  float2* dtab = reinterpret_cast<float2*>(smem + L::off_dtab);
-  float* freq = reinterpret_cast<float*>(smem + L::off_freq);
-  float* acc = reinterpret_cast<float*>(smem + L::off_bk);  // merge accumulator (aliases B_K)
-  float* sm_m = reinterpret_cast<float*>(smem + L::off_ml);
-  float* sm_l = sm_m + kNW * kMaxRows;
-  float* sm_M = sm_l + kNW * kMaxRows;
-  float* sm_L = sm_M + kMaxRows;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc);
-  int* slot_ad_s = reinterpret_cast<int*>(smem + L::off_misc + 16);  // [kMaxSlots]
-  int* slot_rn_s = slot_ad_s + kMaxSlots;                             // [kMaxSlots]
-  int* q_ad_s = slot_rn_s + kMaxSlots;                                // [kMaxSlots]
+  auto bar = [&](int i) -> uint32_t { return sbase + L::off_bar + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc + 4);
+  int* kmask = reinterpret_cast<int*>(smem + L::off_misc + 8);          // [2] loaded blocks per K stage
+  int* row_ad = reinterpret_cast<int*>(smem + L::off_misc + 16);        // [16]
+  float* red = reinterpret_cast<float*>(smem + L::off_misc + 128);      // [4][16]
+  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab);         // [2][HALF]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g8 = lane >> 2, c4 = lane & 3;
-  const uint32_t bar0 = sbase + L::off_bar + warp * kNST * 8;  // this warp's ring barriers
-  const uint32_t ring0 = sbase + warp * kNST * L::blk;           // this warp's ring
 
-  // ---- CTA prologue: frequencies, delta table, barriers
-  if (tid < HALF) {
-    freq[tid] = p.freqs.hi[tid];
-    freq[64 + tid] = p.freqs.lo[tid];
+  // ---- the work item (uniform across the CTA)
+  int64_t rest = blockIdx.x;
+  const int head = static_cast<int>(rest % p.Hkv);
+  rest /= p.Hkv;
+  const int split = static_cast<int>(rest % p.n_splits);
+  rest /= p.n_splits;
+  const int chunk = static_cast<int>(rest % p.n_chunks);
+  const int ctx = static_cast<int>(rest / p.n_chunks);
+  const int qs = __ldg(p.ctx_q_start + ctx), qe = __ldg(p.ctx_q_start + ctx + 1);
+  if (qs < 0 || qe > p.num_queries) {
+    if (tid == 0) report(p.status, LRKV_ERR_INDEX);
+    return;
   }
-  if (tid == 0) *abort_flag = 0;
-  if (lane == 0) {
-    for (int s = 0; s < kNST; ++s) mbar_init(bar0 + 8 * s, 1);
+  const int row0 = chunk * p.rpi;
+  const int nrows = min(p.rpi, (qe - qs) * p.g - row0);
+  if (nrows <= 0) return;
+  int len = __ldg(p.ctx_lens + ctx);
+  if (len < 1 || len > p.max_ctx_len) {
+    if (tid == 0) report(p.status, LRKV_ERR_INDEX);
+    len = 0;
+  }
+  const int nblk = (len + kBlock - 1) / kBlock;
+  const int kbeg = split * p.split_blocks;
+  const int kend = min(kbeg + p.split_blocks, nblk);
+  const int ntiles = kend > kbeg ? (kend - kbeg + kTileBlocks - 1) / kTileBlocks : 0;
+  auto rec_of = [&](int r) -> int64_t {
+    const int gr = row0 + r;
+    const int n = qs + gr / p.g, m = head * p.g + gr % p.g;
+    return (static_cast<int64_t>(n) * p.Hq + m) * p.n_splits + split;
+  };
+  if (ntiles == 0) {
+    // An empty split still leaves a neutral partial (m = -inf, l = 0, O = 0).
+    for (int i = tid; i < nrows * (D + R); i += kThreads)
+      p.part_o[rec_of(i / (D + R)) * (D + R) + i % (D + R)] = 0.f;
+    if (tid < nrows) {
+      p.part_ml[2 * rec_of(tid)] = -CUDART_INF_F;
+      p.part_ml[2 * rec_of(tid) + 1] = 0.f;
+    }
+    return;
+  }
+
+  // ---- barriers, tensor memory
+  if (tid == 0) {
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count(i));
+    *abort_flag = 0;
     mbar_fence_init();
   }
-  __syncthreads();
-  for (int i = tid; i < 16 * HALF; i += kThreads) {
-    const int dl = i / HALF, j = i % HALF;
-    *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(dtab) + dl * L::d_pitch + j * 8) =
-        rope_cos_sin_fast(dl, freq[j], freq[64 + j]);
-  }
-  if (lane == 0) {
+  if (warp == 1) tc::alloc(smem_u32(tmem_slot), kTmemCols);
+  if (tid == 0) {
     prefetch_tmap(&tm_base);
     prefetch_tmap(&tm_lr);
   }
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tmem_slot;
 
-  // ---- this warp's TMA ring: issue walk (lane 0 holds the next block id)
-  Walk wi;
-  walk_init(p, warp, wi);
-  int pend_id = -1;
-  if (lane == 0 && wi.more)
-    pend_id = __ldg(p.block_tables + static_cast<int64_t>(wi.I.ctx) * p.max_blocks + wi.kb);
-  uint32_t issued = 0, consumed = 0;
-  uint32_t valid_bits = 0;  // bit s: stage s holds a loaded block
-  const uint32_t lr_bytes = (p.has_bk ? L::lr_tile : 0) + (p.has_bv ? L::lr_tile : 0);
-
-  auto issue_one = [&]() {
-    if (!wi.more) return;
-    const int s = issued % kNST;
-    int ok = 0;
-    if (lane == 0) {
-      const int blk = pend_id;
-      if (blk < 0 || blk >= p.num_blocks) {
+  // ============================================================ producer
+  if (warp == 0) {
+    const int32_t* bt = p.block_tables + static_cast<int64_t>(ctx) * p.max_blocks;
+    auto load_id = [&](int j) -> int {
+      const int kb = kbeg + j * kTileBlocks + lane;
+      return (lane < kTileBlocks && j < ntiles && kb < kend) ? __ldg(bt + kb) : INT_MIN;
+    };
+    const uint32_t kbytes = L::KATOMS * 2048 + (p.has_bk ? 16 * LSPAN : 0);
+    const uint32_t vbytes = L::KATOMS * 2048 + (p.has_bv ? 16 * LSPAN : 0);
+    int id_cur = load_id(0);
+    bool ok = true;
+    int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;  // last tile issued per stage
+    for (int j = 0; j < ntiles; ++j) {
+      const int id_nxt = load_id(j + 1);
+      bool valid = id_cur != INT_MIN;
+      if (valid && (id_cur < 0 || id_cur >= p.num_blocks)) {
         report(p.status, LRKV_ERR_INDEX);
-        mbar_arrive(bar0 + 8 * s);  // complete this stage's phase without data
-      } else {
-        ok = 1;
-        const uint32_t fb = bar0 + 8 * s;
-        mbar_arrive_expect_tx(fb, 2 * L::kv_tile + lr_bytes);
-        const uint32_t kt = ring0 + s * L::blk, vt = kt + L::kv_tile;
-        const uint32_t lk = kt + 2 * L::kv_tile, lv = lk + L::lr_tile;
-        const int yk = ((blk * 2 + 0) * p.Hkv + wi.I.head) * kBlock;
-        const int yv = ((blk * 2 + 1) * p.Hkv + wi.I.head) * kBlock;
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_2d(kt + h * 2048, &tm_base, 64 * h, yk, fb);
-          tma_load_2d(vt + h * 2048, &tm_base, 64 * h, yv, fb);
-        }
-        if (p.has_bk) tma_load_2d(lk, &tm_lr, 0, (blk * 2 + 0) * kBlock, fb);
-        if (p.has_bv) tma_load_2d(lv, &tm_lr, 0, (blk * 2 + 1) * kBlock, fb);
+        valid = false;
       }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    valid_bits = ok ? (valid_bits | (1u << s)) : (valid_bits & ~(1u << s));
-    ++issued;
-    walk_next(p, warp, wi);
-    if (lane == 0 && wi.more)
-      pend_id = __ldg(p.block_tables + static_cast<int64_t>(wi.I.ctx) * p.max_blocks + wi.kb);
-  };
-  for (int s = 0; s < kNST; ++s) issue_one();
-
-  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab) + warp * HALF;
-
-  for (int64_t it = blockIdx.x; it < p.n_items; it += gridDim.x) {
-    const Item I = get_item(p, it);
-    if (!I.active) continue;
-    const int rows = I.nq * p.g;  // <= 8 * RN by the plan
-
-    __syncthreads();  // previous item's merge finished with the B_K / acc / slot smem
-    // --- adapter ids of the group's queries (one load per query, in parallel)
-    if (tid < I.nq) {
-      int a = __ldg(p.adapter_ids + I.q0 + tid);
-      if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;  // bad ids: reported by the combine
-      q_ad_s[tid] = a;
-    }
-    __syncthreads();
-    // distinct adapters (slots), computed redundantly by every thread
-    int nslots = 0, qslot[kMaxSlots], sad[kMaxSlots], srn[kMaxSlots];
-#pragma unroll
-    for (int k = 0; k < kMaxSlots; ++k) { qslot[k] = 0; sad[k] = -2; srn[k] = 0; }
-#pragma unroll
-    for (int qi = 0; qi < kMaxSlots; ++qi) {
-      if (qi < I.nq) {
-        const int a = q_ad_s[qi];
-        int sl = nslots;
-#pragma unroll
-        for (int k = 0; k < kMaxSlots; ++k)
-          if (k < nslots && sad[k] == a) sl = k;
-        if (sl == nslots) {
-#pragma unroll
-          for (int k = 0; k < kMaxSlots; ++k)
-            if (k == sl) sad[k] = a;
-          ++nslots;
-        }
-        int m = 0;
-        for (int gi = 0; gi < p.g; ++gi) m |= 1 << ((qi * p.g + gi) >> 3);
-#pragma unroll
-        for (int k = 0; k < kMaxSlots; ++k) {
-          if (k == sl) srn[k] |= m;
-          if (k == qi) qslot[k] = sl;
-        }
+      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+      const uint32_t nv = __popc(vm);
+      const int s = j % NK, v = j % NV;
+      if (j >= NK) ok = warp_all(wait_ab(bar(B_EK + s), ((j / NK) - 1) & 1, p.status, abort_flag));
+      if (!ok) break;
+      const uint32_t kst = sbase + L::off_k + s * L::STAGE;
+      if (lane == 0) {
+        kmask[s] = static_cast<int>(vm);  // published by the arrive (release) below
+        mbar_arrive_expect_tx(bar(B_FK + s), nv * kbytes);
       }
-    }
-    bool any_rebuild = false;
-#pragma unroll
-    for (int k = 0; k < kMaxSlots; ++k) any_rebuild |= sad[k] >= 0;
-    if (tid == 0) {
-#pragma unroll
-      for (int k = 0; k < kMaxSlots; ++k) {
-        slot_ad_s[k] = sad[k];
-        slot_rn_s[k] = srn[k];
-      }
-    }
-    // slot of the query row held by this lane in the score B fragment: row rn*8 + g8
-    int myslot[RN];
-#pragma unroll
-    for (int rn = 0; rn < RN; ++rn) {
-      const int row = rn * 8 + g8;
-      int sl = -1;
-#pragma unroll
-      for (int k = 0; k < kMaxSlots; ++k)
-        if (row < rows && k == row / p.g) sl = qslot[k];
-      myslot[rn] = sl;
-    }
-
-    // --- query fragments (B operand of S^T = K Q^T), fp16, straight from global
-    uint32_t qf[RN][NKS][2];
-#pragma unroll
-    for (int rn = 0; rn < RN; ++rn) {
-      const int row = rn * 8 + g8;
-      const bool ok = row < rows;
-      const __nv_bfloat16* qrow =
-          p.q + (static_cast<int64_t>(I.q0 + (ok ? row / p.g : 0)) * p.Hq + I.head * p.g +
-                 (ok ? row % p.g : 0)) * D;
-#pragma unroll
-      for (int ks = 0; ks < NKS; ++ks) {
-        qf[rn][ks][0] = ok ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4))) : 0u;
-        qf[rn][ks][1] = ok ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c4 + 8))) : 0u;
-      }
-    }
-    // --- B_K slices of the rebuild slots -> smem [slot][k][D] (padded rows), async copies
-    {
-      constexpr int VPR = D / 8;  // 16-byte vectors per row
-#pragma unroll
-      for (int s = 0; s < L::kSlots; ++s) {
-        const int a = sad[s];
-        if (a < 0) continue;
-        const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(a) * R * p.Hkv * D +
-                                   static_cast<int64_t>(I.head) * D;
-        const uint32_t dst = sbase + L::off_bk + s * L::bk_slot;
-        for (int i = tid; i < R * VPR; i += kThreads) {
-          const int k = i / VPR, v = i % VPR;
-          const void* g = reinterpret_cast<const uint4*>(src + static_cast<int64_t>(k) * p.Hkv * D) + v;
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + k * L::bk_pitch + v * 16),
-                       "l"(g) : "memory");
-        }
-      }
-      asm volatile("cp.async.commit_group;\n" ::: "memory");
-      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    }
-    __syncthreads();
-
-    // O^T [head dims x query rows] and O_lr^T [rank x query rows] accumulators
-    float OT[NMT][RN][4];
-    float OlrT[NLM][RN][4];
-#pragma unroll
-    for (int i = 0; i < NMT; ++i)
-#pragma unroll
-      for (int rn = 0; rn < RN; ++rn) OT[i][rn][0] = OT[i][rn][1] = OT[i][rn][2] = OT[i][rn][3] = 0.f;
-#pragma unroll
-    for (int i = 0; i < NLM; ++i)
-#pragma unroll
-      for (int rn = 0; rn < RN; ++rn) OlrT[i][rn][0] = OlrT[i][rn][1] = OlrT[i][rn][2] = OlrT[i][rn][3] = 0.f;
-    float m_run[RN][2], l_run[RN][2];
-#pragma unroll
-    for (int rn = 0; rn < RN; ++rn)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) { m_run[rn][e] = -CUDART_INF_F; l_run[rn][e] = 0.f; }
-
-    if (I.len == 0 && tid == 0) report(p.status, LRKV_ERR_INDEX);
-
-    // ------------------------------------------------------ block sweep
-    for (int b = I.kbeg + warp; b < I.kend; b += kNW) {
-      const int s = consumed % kNST;
-      const uint32_t par = (consumed / kNST) & 1;
-      const bool have = (valid_bits >> s) & 1;
-      // every wait result below is made warp-uniform before any warp-collective use
-      bool ok = have && !__shfl_sync(0xffffffffu, *abort_flag, 0);
-      if (ok) ok = mbar_wait(bar0 + 8 * s, par, p.status);
-      ok = have && __all_sync(0xffffffffu, ok);
-      if (have && !ok) *abort_flag = 1;
-      if (ok) {
-        const int t0 = b * kBlock;
-        const uint32_t kt = ring0 + s * L::blk, vt = kt + L::kv_tile;
-        const uint32_t lkt = kt + 2 * L::kv_tile, lvt = lkt + L::lr_tile;
-
-        // Rows past the context end may hold stale pool memory: zero their V and
-        // L_V rows so that P = 0 there cannot meet a NaN in the PV products.
-        if (t0 + kBlock > I.len) {
-          const int r0 = I.len - t0;
-          for (int i = lane; i < (kBlock - r0) * (D / 8); i += 32) {
-            const int r = r0 + i / (D / 8), v = i % (D / 8);
-            const uint32_t a = vt + (v / 8) * 2048 + r * 128 + (v % 8) * 16;
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
-          }
-          for (int i = lane; i < (kBlock - r0) * (R / 8); i += 32) {
-            const int r = r0 + i / (R / 8), v = i % (R / 8);
-            const uint32_t a = lvt + r * LR_RB + v * 16;
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};\n" ::"r"(a), "r"(0u) : "memory");
-          }
-          __syncwarp();
-        }
-        // base rotation of this block: e^{i t0 theta_j}
-        if (any_rebuild) {
-          for (int j = lane; j < HALF; j += 32) btab[j] = rope_cos_sin_fast(t0, freq[j], freq[64 + j]);
-          __syncwarp();
-        }
-        // L_K A fragments (tokens x rank)
-        uint32_t alk[NRT][4];
-        if (any_rebuild) {
-          if constexpr (R >= 16) {
-#pragma unroll
-            for (int ks = 0; ks < NRT; ++ks) {
-              const int mi = lane >> 3;
-              ldsm_x4(alk[ks], lkt + swz<LR_RB>((lane & 7) + (mi & 1) * 8, (2 * ks + (mi >> 1)) * 16));
-            }
-          } else {
-            uint32_t t2[2];
-            ldsm_x2(t2, lkt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
-            alk[0][0] = t2[0];
-            alk[0][1] = t2[1];
-            alk[0][2] = alk[0][3] = 0u;
-          }
-        }
-
-        // two independent score accumulators (low / high head-dim halves) keep the
-        // MMA dependency chain short
-        float sacc[2][RN][4];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int rn = 0; rn < RN; ++rn)
-            sacc[hh][rn][0] = sacc[hh][rn][1] = sacc[hh][rn][2] = sacc[hh][rn][3] = 0.f;
-
-#pragma unroll
-        for (int cc = 0; cc < NCH; ++cc) {
-          // K_base at this lane's fragment positions, as fp16 pairs: [n][h][tk]
-          uint32_t kb16[2][2][2];
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int tk = 0; tk < 2; ++tk) {
-                const int j = 16 * cc + 8 * n + 2 * c4 + h * HALF;
-                const uint32_t addr = kt + (j / 64) * 2048 + swz<128>(g8 + 8 * tk, (j % 64) * 2);
-                uint32_t v;
-                asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
-                kb16[n][h][tk] = bf16x2_to_f16x2(v);
-              }
-          // rotation factors of this lane's (token, pair) positions as fp16 pairs
-          uint32_t c16[2][2], s16[2][2], ns16[2][2];  // [tk][n]
-          if (any_rebuild) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-              const int j = 16 * cc + 8 * n + 2 * c4;
-              const float4 bq = *reinterpret_cast<const float4*>(btab + j);
-#pragma unroll
-              for (int tk = 0; tk < 2; ++tk) {
-                const float4 dq = *reinterpret_cast<const float4*>(
-                    reinterpret_cast<const uint8_t*>(dtab) + (g8 + 8 * tk) * L::d_pitch + j * 8);
-                const float c0 = bq.x * dq.x - bq.y * dq.y, s0 = bq.y * dq.x + bq.x * dq.y;
-                const float c1 = bq.z * dq.z - bq.w * dq.w, s1 = bq.w * dq.z + bq.z * dq.w;
-                c16[tk][n] = pack_f16(c0, c1);
-                s16[tk][n] = pack_f16(s0, s1);
-                ns16[tk][n] = pack_f16(-s0, -s1);
-              }
-            }
-          }
-#pragma unroll 1
-          for (int a = 0; a < nslots; ++a) {
-            const int ad = slot_ad_s[a];
-            const int rnm = slot_rn_s[a];
-            uint32_t A_lo[4], A_hi[4];
-            if (ad >= 0) {
-              float y[4][4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.f;
-              const uint32_t bk = sbase + L::off_bk + a * L::bk_slot;
-              if constexpr (R >= 16) {
-#pragma unroll
-                for (int ks = 0; ks < NRT; ++ks)
-#pragma unroll
-                  for (int h = 0; h < 2; ++h) {
-                    // n-tiles (2cc, 2cc+1) [+ D/16 for the rotation partners]
-                    const int mi = lane >> 3;
-                    const int krow = 16 * ks + (lane & 7) + (mi & 1) * 8;
-                    const int ncol = 16 * cc + h * HALF + (mi >> 1) * 8;
-                    uint32_t bb[4];
-                    ldsm_x4_t(bb, bk + krow * L::bk_pitch + ncol * 2);
-                    mma16816(y[2 * h + 0], alk[ks], bb[0], bb[1]);
-                    mma16816(y[2 * h + 1], alk[ks], bb[2], bb[3]);
-                  }
-              } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int ncol = 16 * cc + h * HALF + ((lane >> 3) & 1) * 8;
-                  uint32_t bb[2];
-                  ldsm_x2_t(bb, bk + (lane & 7) * L::bk_pitch + ncol * 2);
-                  mma1688(y[2 * h + 0], alk[0][0], alk[0][1], bb[0]);
-                  mma1688(y[2 * h + 1], alk[0][0], alk[0][1], bb[1]);
-                }
-              }
-              // rotate the rebuilt pair (j, j + d/2) and add K_base, in packed fp16:
-              //   k_lo = K_lo + x cos - y sin,   k_hi = K_hi + y cos + x sin
-#pragma unroll
-              for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int tk = 0; tk < 2; ++tk) {
-                  const uint32_t x = pack_f16(y[n][2 * tk], y[n][2 * tk + 1]);
-                  const uint32_t yy = pack_f16(y[n + 2][2 * tk], y[n + 2][2 * tk + 1]);
-                  A_lo[2 * n + tk] = hfma2_u32(x, c16[tk][n], hfma2_u32(yy, ns16[tk][n], kb16[n][0][tk]));
-                  A_hi[2 * n + tk] = hfma2_u32(yy, c16[tk][n], hfma2_u32(x, s16[tk][n], kb16[n][1][tk]));
-                }
-            } else {
-#pragma unroll
-              for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int tk = 0; tk < 2; ++tk) {
-                  A_lo[2 * n + tk] = kb16[n][0][tk];
-                  A_hi[2 * n + tk] = kb16[n][1][tk];
-                }
-            }
-            // scores of this adapter's rows only: its query fragment, other rows zeroed
-#pragma unroll
-            for (int rn = 0; rn < RN; ++rn) {
-              if (!((rnm >> rn) & 1)) continue;
-              const bool mine = myslot[rn] == a;
-              const uint32_t q0 = mine ? qf[rn][cc][0] : 0u, q1 = mine ? qf[rn][cc][1] : 0u;
-              const uint32_t q2 = mine ? qf[rn][cc + NCH][0] : 0u, q3 = mine ? qf[rn][cc + NCH][1] : 0u;
-              mma16816_f16(sacc[0][rn], A_lo, q0, q1);
-              mma16816_f16(sacc[1][rn], A_hi, q2, q3);
-            }
-          }
-        }
-
-        // ---- mask and scale (S^T: tokens g8, g8 + 8 x query rows rn*8 + 2*c4 + e)
-        float sv[RN][4];
-#pragma unroll
-        for (int rn = 0; rn < RN; ++rn)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int tok = t0 + g8 + 8 * (i >> 1);
-            sv[rn][i] = tok < I.len ? (sacc[0][rn][i] + sacc[1][rn][i]) * p.scale_log2 : -CUDART_INF_F;
-          }
-        // ---- online softmax (per score column = query row)
-        float alpha[RN][2];
-        float pr[RN][4];
-        bool moved = false;
-#pragma unroll
-        for (int rn = 0; rn < RN; ++rn)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float mx = fmaxf(sv[rn][e], sv[rn][e + 2]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float mn = fmaxf(m_run[rn][e], mx);
-            float al, p0, p1;
-            if (mn == -CUDART_INF_F) {
-              al = 1.f; p0 = 0.f; p1 = 0.f;
-            } else {
-              al = exp2f(m_run[rn][e] - mn);
-              p0 = exp2f(sv[rn][e] - mn);
-              p1 = exp2f(sv[rn][e + 2] - mn);
-            }
-            moved |= al != 1.f;
-            m_run[rn][e] = mn;
-            l_run[rn][e] = l_run[rn][e] * al + p0 + p1;
-            alpha[rn][e] = al;
-            pr[rn][e] = p0;
-            pr[rn][e + 2] = p1;
-          }
-        // ---- rescale accumulators: this lane's O^T columns are its own score rows
-        if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-          for (int rn = 0; rn < RN; ++rn) {
-#pragma unroll
-            for (int i = 0; i < NMT; ++i) {
-              OT[i][rn][0] *= alpha[rn][0]; OT[i][rn][1] *= alpha[rn][1];
-              OT[i][rn][2] *= alpha[rn][0]; OT[i][rn][3] *= alpha[rn][1];
-            }
-#pragma unroll
-            for (int i = 0; i < NLM; ++i) {
-              OlrT[i][rn][0] *= alpha[rn][0]; OlrT[i][rn][1] *= alpha[rn][1];
-              OlrT[i][rn][2] *= alpha[rn][0]; OlrT[i][rn][3] *= alpha[rn][1];
-            }
-          }
-        }
-        // ---- P^T (tokens x rows) B fragments via register transposes
-        uint32_t pb[RN][2];
-#pragma unroll
-        for (int rn = 0; rn < RN; ++rn) {
-          pb[rn][0] = movm_t(pack_bf16(pr[rn][0], pr[rn][1]));
-          pb[rn][1] = movm_t(pack_bf16(pr[rn][2], pr[rn][3]));
-        }
-        // ---- O^T += V_base^T P^T (M = head dims, N = query rows, K = tokens)
-#pragma unroll
-        for (int mt = 0; mt < NMT; ++mt) {
-          const int mi = lane >> 3;
-          const int tok = (lane & 7) + (mi >> 1) * 8;
-          const int dim = 16 * mt + (mi & 1) * 8;
-          uint32_t av[4];
-          ldsm_x4_t(av, vt + (dim / 64) * 2048 + swz<128>(tok, (dim % 64) * 2));
-#pragma unroll
-          for (int rn = 0; rn < RN; ++rn) mma16816(OT[mt][rn], av, pb[rn][0], pb[rn][1]);
-        }
-        // ---- O_lr^T += L_V^T P^T
-        if (p.has_bv) {
-          if constexpr (R >= 16) {
-#pragma unroll
-            for (int mt = 0; mt < NLM; ++mt) {
-              const int mi = lane >> 3;
-              const int tok = (lane & 7) + (mi >> 1) * 8;
-              const int col = 16 * mt + (mi & 1) * 8;
-              uint32_t av[4];
-              ldsm_x4_t(av, lvt + swz<LR_RB>(tok, col * 2));
-#pragma unroll
-              for (int rn = 0; rn < RN; ++rn) mma16816(OlrT[mt][rn], av, pb[rn][0], pb[rn][1]);
-            }
-          } else {
-            uint32_t t2[2];
-            ldsm_x2_t(t2, lvt + swz<LR_RB>((lane & 7) + ((lane >> 3) & 1) * 8, 0));
-            const uint32_t av[4] = {t2[0], 0u, t2[1], 0u};  // rank rows 8..15 do not exist
-#pragma unroll
-            for (int rn = 0; rn < RN; ++rn) mma16816(OlrT[0][rn], av, pb[rn][0], pb[rn][1]);
-          }
-        }
-      }
-      // release the stage and refill it with this warp's next block
-      ++consumed;
       __syncwarp();
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      if (!__shfl_sync(0xffffffffu, *abort_flag, 0)) issue_one();
+      if (s == 0) last_k0 = j; else last_k1 = j;
+      if (valid) {
+        const int yk = ((id_cur * 2 + 0) * p.Hkv + head) * kBlock;
+#pragma unroll
+        for (int a = 0; a < L::KATOMS; ++a)
+          tma_load_2d(kst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, yk, bar(B_FK + s));
+        if (p.has_bk) tma_load_2d(kst + lane * 16 * LSPAN, &tm_lr, 0, (id_cur * 2 + 0) * kBlock, bar(B_FK + s));
+      }
+      if (j >= NV) ok = warp_all(wait_ab(bar(B_EV + v), ((j / NV) - 1) & 1, p.status, abort_flag));
+      if (!ok) break;
+      const uint32_t vst = sbase + L::off_v + v * L::STAGE;
+      if (lane == 0) mbar_arrive_expect_tx(bar(B_FV + v), nv * vbytes);
+      __syncwarp();
+      if (v == 0) last_v0 = j; else last_v1 = j;
+      if (valid) {
+        const int yv = ((id_cur * 2 + 1) * p.Hkv + head) * kBlock;
+#pragma unroll
+        for (int a = 0; a < L::KATOMS; ++a)
+          tma_load_2d(vst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, yv, bar(B_FV + v));
+        if (p.has_bv) tma_load_2d(vst + lane * 16 * LSPAN, &tm_lr, 0, (id_cur * 2 + 1) * kBlock, bar(B_FV + v));
+      }
+      id_cur = id_nxt;
     }
+    if (!ok && lane == 0) *abort_flag = 1;
+    // No copy may still be landing when the CTA leaves.
+    if (last_k0 >= 0) wait_ab(bar(B_FK + 0), (last_k0 / NK) & 1, p.status, nullptr);
+    if (last_k1 >= 0) wait_ab(bar(B_FK + 1), (last_k1 / NK) & 1, p.status, nullptr);
+    if (last_v0 >= 0) wait_ab(bar(B_FV + 0), (last_v0 / NV) & 1, p.status, nullptr);
+    if (last_v1 >= 0) wait_ab(bar(B_FV + 1), (last_v1 / NV) & 1, p.status, nullptr);
+  } else {
+    // ================================================ prologue (warps 1-7)
+    // Row adapters and Q (bf16, K-major, 128-byte swizzle; zero past nrows)
+    // by warps 1-3; the token warps meanwhile fill their rotation tables.
+    const int tt = tid - 128;  // token warps: token row of the tile = TMEM lane
+    const uint32_t tl = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    float th_hi = 0.f, th_lo = 0.f;
+    if (warp >= 4 && tt < HALF) {
+      th_hi = p.freqs.hi[tt];
+      th_lo = p.freqs.lo[tt];
+    }
+    if (warp < 4) {
+      const int pt = tid - 32;  // 0..95
+      if (pt < kMaxRows) {
+        int a = -2;
+        if (pt < nrows) {
+          a = __ldg(p.adapter_ids + qs + (row0 + pt) / p.g);
+          if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;  // bad ids: reported by the combine
+        }
+        row_ad[pt] = a;
+      }
+      constexpr int QCH = kMaxRows * (D / 8);
+      constexpr int QIT = (QCH + 95) / 96;
+      uint4 qv[QIT];
+#pragma unroll
+      for (int u = 0; u < QIT; ++u) {
+        const int i = pt + 96 * u;
+        const int r = i / (D / 8), c = i % (D / 8);
+        qv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < QCH && r < nrows) {
+          const int gr = row0 + r;
+          const __nv_bfloat16* src =
+              p.q + (static_cast<int64_t>(qs + gr / p.g) * p.Hq + head * p.g + gr % p.g) * D + 8 * c;
+          qv[u] = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < QIT; ++u) {
+        const int i = pt + 96 * u;
+        const int r = i / (D / 8), c = i % (D / 8);
+        if (i < QCH)
+          *reinterpret_cast<uint4*>(smem + L::off_q + (c >> 3) * (kMaxRows * 128) + r * 128 +
+                                    (((c & 7) ^ (r & 7)) << 4)) = qv[u];
+      }
+    } else {
+      // e^{i delta theta_j} for this lane's token offset delta = tt, in TMEM
+#pragma unroll
+      for (int q4 = 0; q4 < HALF / 16; ++q4) {
+        uint32_t dv[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 cs = rope_cos_sin_fast(tt, p.freqs.hi[16 * q4 + i], p.freqs.lo[16 * q4 + i]);
+          dv[2 * i] = __float_as_uint(cs.x);
+          dv[2 * i + 1] = __float_as_uint(cs.y);
+        }
+        tc::st_x32(tl + DT_COL + 32 * q4, dv);
+      }
+      tc::wait_st();
+      // base angles e^{i t0 theta_j} of tiles 0 and 1
+      const int t00 = kbeg * kBlock;
+      if (tt < HALF) btab[tt] = rope_cos_sin_fast(t00, th_hi, th_lo);
+      else if (tt < 2 * HALF && ntiles > 1)
+        btab[tt] = rope_cos_sin_fast(t00 + kBT, p.freqs.hi[tt - HALF], p.freqs.lo[tt - HALF]);
+    }
+    named_bar_sync(1, 224);
+    bool use_w = false;
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) use_w |= row_ad[r] >= 0;
+    const int nw = ((nrows * R + 15) / 16) * 16;
 
-    // ------------------------------------------------ merge the warps
+    // G (fp16, K-major over u, 128-byte swizzle) for rows n = row * R + k < nw
+    if (use_w) {
+      for (int n = tid - 32; n < nw; n += 224) {
+        const int r = n / R, k = n % R;
+        const int a = row_ad[r];
+        uint8_t* grow = smem + L::off_g + n * 128;
+        if (a >= 0) {
+          const uint4* brow = reinterpret_cast<const uint4*>(
+              p.B_K + ((static_cast<int64_t>(a) * R + k) * p.Hkv + head) * D);
+          uint4 bv[D / 8];
 #pragma unroll
-    for (int rn = 0; rn < RN; ++rn)
+          for (int c = 0; c < D / 8; ++c) bv[c] = __ldg(brow + c);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float l = l_run[rn][e];
-        l += __shfl_xor_sync(0xffffffffu, l, 4);
-        l += __shfl_xor_sync(0xffffffffu, l, 8);
-        l += __shfl_xor_sync(0xffffffffu, l, 16);
-        l_run[rn][e] = l;
-      }
-    if (g8 == 0) {
+          for (int jc = 0; jc < HALF / 8; ++jc) {
+            const int c2 = HALF / 8 + jc;
+            const uint4 q1 = *reinterpret_cast<const uint4*>(
+                smem + L::off_q + (jc >> 3) * (kMaxRows * 128) + r * 128 + (((jc & 7) ^ (r & 7)) << 4));
+            const uint4 q2 = *reinterpret_cast<const uint4*>(
+                smem + L::off_q + (c2 >> 3) * (kMaxRows * 128) + r * 128 + (((c2 & 7) ^ (r & 7)) << 4));
+            const uint32_t qa[4] = {q1.x, q1.y, q1.z, q1.w}, qb[4] = {q2.x, q2.y, q2.z, q2.w};
+            const uint32_t ba[4] = {bv[jc].x, bv[jc].y, bv[jc].z, bv[jc].w};
+            const uint32_t bb[4] = {bv[c2].x, bv[c2].y, bv[c2].z, bv[c2].w};
+            uint32_t gc[4], gs[4];
 #pragma unroll
-      for (int rn = 0; rn < RN; ++rn)
+            for (int e = 0; e < 4; ++e) {
+              const float q1l = bf16_lo(qa[e]), q1h = bf16_hi(qa[e]);
+              const float q2l = bf16_lo(qb[e]), q2h = bf16_hi(qb[e]);
+              const float b1l = bf16_lo(ba[e]), b1h = bf16_hi(ba[e]);
+              const float b2l = bf16_lo(bb[e]), b2h = bf16_hi(bb[e]);
+              gc[e] = pack_f16(fmaf(q1l, b1l, q2l * b2l), fmaf(q1h, b1h, q2h * b2h));
+              gs[e] = pack_f16(fmaf(q2l, b1l, -(q1l * b2l)), fmaf(q2h, b1h, -(q1h * b2h)));
+            }
+            *reinterpret_cast<uint4*>(grow + (jc >> 3) * L::GAMMA_ATOM + (((jc & 7) ^ (n & 7)) << 4)) =
+                make_uint4(gc[0], gc[1], gc[2], gc[3]);
+            *reinterpret_cast<uint4*>(grow + (c2 >> 3) * L::GAMMA_ATOM + (((c2 & 7) ^ (n & 7)) << 4)) =
+                make_uint4(gs[0], gs[1], gs[2], gs[3]);
+          }
+        } else {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = rn * 8 + 2 * c4 + e;
-          sm_m[warp * kMaxRows + row] = m_run[rn][e];
-          sm_l[warp * kMaxRows + row] = l_run[rn][e];
+          for (int c = 0; c < D / 8; ++c)
+            *reinterpret_cast<uint4*>(grow + (c >> 3) * L::GAMMA_ATOM + (((c & 7) ^ (n & 7)) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
-    }
-    __syncthreads();  // also: every warp is past its B_K reads; acc may alias them now
-    if (tid < RN * 8) {
-      float M = -CUDART_INF_F;
-#pragma unroll
-      for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * kMaxRows + tid]);
-      float Ls = 0.f;
-      if (M != -CUDART_INF_F) {
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) Ls += sm_l[w * kMaxRows + tid] * exp2f(sm_m[w * kMaxRows + tid] - M);
       }
-      sm_M[tid] = M;
-      sm_L[tid] = Ls;
     }
-    {
-      // per-row weight of this warp's partial: exp2(m_w - max over warps)
-      float f[RN][2];
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // Q, G -> MMA operands
+    named_bar_sync(1, 224);
+
+    if (warp == 1) {
+      // ======================================================= W issuer
+      bool ok = true;
+      int issued = 0;
+      if (use_w) {
+        const uint32_t idw = tc::idesc_f16(128, nw, false, false, false);
+        const uint64_t gdesc = tc::sdesc(sbase + L::off_g, 16, 1024, 2);
+        for (int j = 0; j < ntiles; ++j) {
+          ok = warp_all(wait_ab(bar(B_UF), j & 1, p.status, abort_flag));
+          if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
+          if (!ok) break;
+          tc::fence_after();
+          if (tc::elect_one()) {
 #pragma unroll
-      for (int rn = 0; rn < RN; ++rn)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = rn * 8 + 2 * c4 + e;
-          float M = -CUDART_INF_F;
-#pragma unroll
-          for (int w = 0; w < kNW; ++w) M = fmaxf(M, sm_m[w * kMaxRows + row]);
-          const float mw = m_run[rn][e];
-          f[rn][e] = (M == -CUDART_INF_F || mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+            for (int k = 0; k < KS; ++k)
+              tc::mma_ts(tbase + W_COL, tbase + U_COL + 8 * k,
+                         gdesc + (((k >> 2) * L::GAMMA_ATOM + (k & 3) * 32) >> 4), idw, k > 0 ? 1u : 0u);
+            tc::commit(bar(B_WF));
+          }
+          __syncwarp();
+          ++issued;
         }
-      // fixed-order accumulation (warp 0 writes, warps 1.. add): reproducible bits.
-      // acc[row][col]: col = head dim 16*mt + g8 (+8), or D + rank index.
-      for (int w = 0; w < kNW; ++w) {
-        if (warp == w) {
-          float cur[NMT + NLM][RN][4];
-          if (w > 0) {  // all loads first, then all stores
+      }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        if (issued > 0) {
+          if (tc::elect_one()) tc::commit(bar(B_DRAIN + 1));
+          __syncwarp();
+          wait_ab(bar(B_DRAIN + 1), 0, p.status, nullptr);
+        }
+      }
+    } else if (warp == 2) {
+      // ===================================================== S_b issuer
+      const uint32_t ids = tc::idesc_f16(128, kMaxRows, true, false, false);
+      const uint64_t qdesc = tc::sdesc(sbase + L::off_q, 16, 1024, 2);
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % NK;
+        ok = warp_all(wait_ab(bar(B_FK + s), (j / NK) & 1, p.status, abort_flag));
+        if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after();
+        if (tc::elect_one()) {
+          const uint64_t kdesc = tc::sdesc(sbase + L::off_k + s * L::STAGE + L::LR_TILE, 16, 1024, 2);
 #pragma unroll
-            for (int i = 0; i < NMT + NLM; ++i)
+          for (int k = 0; k < KS; ++k)
+            tc::mma_ss(tbase + S_COL, kdesc + (((k >> 2) * L::ATOM + (k & 3) * 32) >> 4),
+                       qdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ids, k > 0 ? 1u : 0u);
+          tc::commit(bar(B_SF));
+        }
+        __syncwarp();
+        ++issued;
+      }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        if (issued > 0) {
+          if (tc::elect_one()) tc::commit(bar(B_DRAIN + 2));
+          __syncwarp();
+          wait_ab(bar(B_DRAIN + 2), 0, p.status, nullptr);
+        }
+      }
+    } else if (warp == 3) {
+      // ======================================= O^T / O_lr^T issuer
+      const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int v = j % NV, b = j & 1;
+        ok = warp_all(wait_ab(bar(B_FV + v), (j / NV) & 1, p.status, abort_flag));
+        if (ok) ok = warp_all(wait_ab(bar(B_PF + b), (j >> 1) & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after();
+        if (tc::elect_one()) {
+          const uint32_t vst = sbase + L::off_v + v * L::STAGE;
+          // V^T: M = head dims (MN-major; 64-dim atoms ATOM bytes apart), K = tokens
+          const uint64_t vdesc = tc::sdesc(vst + L::LR_TILE, L::ATOM, 1024, 2);
+          // L_V^T: M = rank (MN-major, swizzled by the row span), K = tokens
+          const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
+          const uint64_t pdesc = tc::sdesc(sbase + L::off_p + b * L::PB, 16, 1024, 2);
 #pragma unroll
-              for (int rn = 0; rn < RN; ++rn)
+          for (int k = 0; k < kBT / 16; ++k) {
+            const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+            const uint64_t pk = pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4);
+            tc::mma_ss(tbase + OT_COL, vdesc + ((k * 16 * 128) >> 4), pk, ido, acc);
+            if (p.has_bv) tc::mma_ss(tbase + OL_COL, lvdesc + ((k * 16 * LSPAN) >> 4), pk, ido, acc);
+          }
+          tc::commit(bar(B_PR + b));
+          tc::commit(bar(B_EV + v));
+        }
+        __syncwarp();
+        ++issued;
+      }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        if (issued > 0) {
+          if (tc::elect_one()) tc::commit(bar(B_DRAIN + 3));
+          __syncwarp();
+          wait_ab(bar(B_DRAIN + 3), 0, p.status, nullptr);
+        }
+      }
+    } else {
+      // ================================================== token warps
+      // U(t) = e^{i t0 theta} e^{i delta theta}, packed fp16 pairs:
+      // columns [0, HALF/2) hold cos, [HALF/2, HALF) hold sin.
+      auto build_u = [&](int bb) {
+        const float2* bt = btab + bb * HALF;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  const int row = rn * 8 + 2 * c4 + (v & 1);
-                  const int col = (i < NMT ? 16 * i : D + 16 * (i - NMT)) + g8 + 8 * (v >> 1);
-                  cur[i][rn][v] = (i >= NMT && 16 * (i - NMT) + g8 + 8 * (v >> 1) >= R)
-                                      ? 0.f : acc[row * L::acc_pitch + col];
+        for (int q4 = 0; q4 < HALF / 16; ++q4) {
+          uint32_t dv[32];
+          tc::ld_x32(tl + DT_COL + 32 * q4, dv);
+          tc::wait_ld();
+          uint32_t uc[8], us[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 b2 = *reinterpret_cast<const float4*>(bt + 16 * q4 + 2 * i);
+            const float cd0 = __uint_as_float(dv[4 * i]), sd0 = __uint_as_float(dv[4 * i + 1]);
+            const float cd1 = __uint_as_float(dv[4 * i + 2]), sd1 = __uint_as_float(dv[4 * i + 3]);
+            uc[i] = pack_f16(fmaf(b2.x, cd0, -(b2.y * sd0)), fmaf(b2.z, cd1, -(b2.w * sd1)));
+            us[i] = pack_f16(fmaf(b2.y, cd0, b2.x * sd0), fmaf(b2.w, cd1, b2.z * sd1));
+          }
+          tc::st_x8(tl + U_COL + 8 * q4, uc);
+          tc::st_x8(tl + U_COL + HALF / 2 + 8 * q4, us);
+        }
+        tc::wait_st();
+      };
+      if (use_w) {
+        build_u(0);
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_UF));
+      }
+
+      float m_run[kMaxRows], l_run[kMaxRows];
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        m_run[r] = -CUDART_INF_F;
+        l_run[r] = 0.f;
+      }
+      bool failed = false;
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % NK, v = j % NV, b = j & 1;
+        const int t0 = (kbeg + j * kTileBlocks) * kBlock;
+        // ---- scores of this lane's token
+        if (!failed && use_w) failed = !wait_ab(bar(B_WF), j & 1, p.status, abort_flag);
+        if (!failed) failed = !wait_ab(bar(B_SF), j & 1, p.status, abort_flag);
+        if (!failed) failed = !wait_ab(bar(B_FK + s), (j / NK) & 1, p.status, abort_flag);
+        tc::fence_after();
+        const int vmask = kmask[s];  // blocks of this tile that were loaded (valid ids inside the split)
+        float sc[kMaxRows];
+        {
+          uint32_t sv[16];
+          tc::ld_x16(tl + S_COL, sv);
+          float slr[kMaxRows];
+#pragma unroll
+          for (int r = 0; r < kMaxRows; ++r) slr[r] = 0.f;
+          if (use_w) {
+            float lk[R];
+            const uint8_t* lrow = smem + L::off_k + s * L::STAGE;
+#pragma unroll
+            for (int c = 0; c < (R + 7) / 8; ++c) {
+              const uint4 x = *reinterpret_cast<const uint4*>(lrow + swz<LSPAN>(tt, 16 * c));
+              const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (8 * c + 2 * e < R) lk[8 * c + 2 * e] = bf16_lo(xs[e]);
+                if (8 * c + 2 * e + 1 < R) lk[8 * c + 2 * e + 1] = bf16_hi(xs[e]);
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < L::NW_MAX / 32; ++c) {
+              if (32 * c < nw) {
+                uint32_t w[32];
+                tc::ld_x32(tl + W_COL + 32 * c, w);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const int n = 32 * c + i;
+                  slr[n / R] = fmaf(lk[n % R], __uint_as_float(w[i]), slr[n / R]);
                 }
+              }
+            }
+          }
+          tc::wait_ld();
+#pragma unroll
+          for (int r = 0; r < kMaxRows; ++r) sc[r] = __uint_as_float(sv[r]) + slr[r];
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_WR));
+          mbar_arrive(bar(B_EK + s));
+        }
+        // ---- U of the next tile, base angles of the one after
+        if (use_w && j + 1 < ntiles) {
+          build_u((j + 1) & 1);
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_UF));
+        }
+        if (tt < HALF && j + 2 < ntiles) btab[b * HALF + tt] = rope_cos_sin_fast(t0 + 2 * kBT, th_hi, th_lo);
+
+        // ---- online softmax over the tile's tokens (log2 units)
+        const bool tok_ok = ((vmask >> (tt >> 4)) & 1) != 0 && t0 + tt < len;
+        bool need = false;
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          sc[r] = tok_ok ? sc[r] * p.scale_log2 : -CUDART_INF_F;
+          need |= sc[r] > m_run[r] + kRescaleLog2;
+        }
+        if (*abort_flag != 0) failed = true;
+        if (named_bar_or(2, 128, need || failed)) {  // also publishes btab
+          if (named_bar_or(2, 128, failed)) {
+            failed = true;
+            break;
           }
 #pragma unroll
-          for (int i = 0; i < NMT + NLM; ++i)
+          for (int r = 0; r < kMaxRows; ++r) {
+            float x = sc[r];
 #pragma unroll
-            for (int rn = 0; rn < RN; ++rn)
+            for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+            if (lane == 0) red[(warp & 3) * kMaxRows + r] = x;
+          }
+          named_bar_sync(2, 128);
+          float alpha[kMaxRows];
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const int row = rn * 8 + 2 * c4 + (v & 1);
-                const int k = (i < NMT ? 16 * i : 16 * (i - NMT)) + g8 + 8 * (v >> 1);
-                if (i >= NMT && k >= R) continue;
-                const int col = (i < NMT ? 0 : D) + k;
-                const float x = f[rn][v & 1] * (i < NMT ? OT[i][rn][v] : OlrT[i - NMT][rn][v]);
-                acc[row * L::acc_pitch + col] = (w > 0 ? cur[i][rn][v] : 0.f) + x;
-              }
+          for (int r = 0; r < kMaxRows; ++r) {
+            const float mx = fmaxf(fmaxf(red[r], red[kMaxRows + r]),
+                                   fmaxf(red[2 * kMaxRows + r], red[3 * kMaxRows + r]));
+            const float mn = fmaxf(m_run[r], mx);
+            alpha[r] = mn == -CUDART_INF_F ? 1.f : ex2(m_run[r] - mn);
+            m_run[r] = mn;
+            l_run[r] *= alpha[r];
+          }
+          if (j > 0) {
+            // the P V of the previous tile must have landed before O is rescaled
+            if (!failed) failed = !wait_ab(bar(B_PR + ((j - 1) & 1)), ((j - 1) >> 1) & 1, p.status, abort_flag);
+            tc::fence_after();
+            uint32_t o[16];
+            tc::ld_x16(tl + OT_COL, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+            tc::st_x16(tl + OT_COL, o);
+            if (p.has_bv) {
+              tc::ld_x16(tl + OL_COL, o);
+              tc::wait_ld();
+#pragma unroll
+              for (int r = 0; r < kMaxRows; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+              tc::st_x16(tl + OL_COL, o);
+            }
+            tc::wait_st();
+          }
         }
-        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          const float pr = ex2(sc[r] - (m_run[r] == -CUDART_INF_F ? 0.f : m_run[r]));
+          l_run[r] += pr;
+          sc[r] = pr;
+        }
+        // ---- P^T (bf16, K-major over tokens) once the P V two tiles back has read the buffer
+        if (j >= 2 && !failed) failed = !wait_ab(bar(B_PR + b), ((j >> 1) - 1) & 1, p.status, abort_flag);
+        {
+          uint8_t* pb = smem + L::off_p + b * L::PB + (tt >> 6) * (kMaxRows * 128) + ((tt & 7) << 1);
+          const int ch = (tt & 63) >> 3;
+#pragma unroll
+          for (int r = 0; r < kMaxRows; ++r)
+            *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((ch ^ (r & 7)) << 4)) = __float2bfloat16_rn(sc[r]);
+        }
+        // rows of tokens outside the context or the split, or of blocks with a
+        // bad id, hold stale memory: zero their V and L_V rows so that P = 0
+        // there cannot meet a NaN
+        if (vmask != (1 << kTileBlocks) - 1 || t0 + kBT > len) {
+          if (!failed) failed = !wait_ab(bar(B_FV + v), (j / NV) & 1, p.status, abort_flag);
+          if (!tok_ok) {
+            uint8_t* vst = smem + L::off_v + v * L::STAGE;
+#pragma unroll
+            for (int a = 0; a < L::KATOMS; ++a)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(vst + L::LR_TILE + a * L::ATOM + tt * 128 + 16 * c) =
+                    make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < LSPAN / 16; ++c)
+              *reinterpret_cast<uint4*>(vst + tt * LSPAN + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PF + b));
       }
-    }
-    // ---- write the partial of each query row
-    for (int i = tid; i < rows * (D + R); i += kThreads) {
-      const int row = i / (D + R), col = i % (D + R);
-      const int n = I.q0 + row / p.g, m = I.head * p.g + row % p.g;
-      const int64_t rec = (static_cast<int64_t>(n) * p.Hq + m) * p.n_splits + I.split;
-      p.part_o[rec * (D + R) + col] = acc[row * L::acc_pitch + col];
-    }
-    if (tid < rows) {
-      const int n = I.q0 + tid / p.g, m = I.head * p.g + tid % p.g;
-      const int64_t rec = (static_cast<int64_t>(n) * p.Hq + m) * p.n_splits + I.split;
-      p.part_ml[rec * 2 + 0] = sm_M[tid];
-      p.part_ml[rec * 2 + 1] = sm_L[tid];
+
+      // ---- split partial: m, l, O, O_lr of each row
+      bool aborted = named_bar_or(3, 128, failed);
+      if (!aborted) {
+        const bool okp = wait_ab(bar(B_PR + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, p.status, abort_flag);
+        aborted = named_bar_or(3, 128, !okp);
+      }
+      if (aborted) {
+        if (tt == 0) *abort_flag = 1;
+      } else {
+        tc::fence_after();
+        uint32_t o[16], ol[16];
+        tc::ld_x16(tl + OT_COL, o);
+        tc::ld_x16(tl + OL_COL, ol);
+        tc::wait_ld();
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          float x = l_run[r];
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o2);
+          if (lane == 0) red[(warp & 3) * kMaxRows + r] = x;
+        }
+        named_bar_sync(3, 128);
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          if (r < nrows) {
+            const int64_t rec = rec_of(r);
+            float* po = p.part_o + rec * (D + R);
+            if (tt < D) po[tt] = __uint_as_float(o[r]);
+            if (tt < R) po[D + tt] = p.has_bv ? __uint_as_float(ol[r]) : 0.f;
+            if (tt == r) {
+              p.part_ml[2 * rec] = m_run[r];
+              p.part_ml[2 * rec + 1] = red[r] + red[kMaxRows + r] + red[2 * kMaxRows + r] + red[3 * kMaxRows + r];
+            }
+          }
+        }
+      }
     }
   }
-  // Drain: never leave the CTA with copies in flight (bounded waits; only after an abort).
-  if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
-    for (uint32_t k = consumed; k < issued; ++k) {
-      const int s = k % kNST;
-      if ((valid_bits >> s) & 1) mbar_wait(bar0 + 8 * s, (k / kNST) & 1, nullptr, 1u << 16);
-    }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tbase, kTmemCols);
   }
 }
 
@@ -814,9 +864,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   }
 }
 
-template <int D, int R, int RN>
+template <int D, int R>
 lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& plan,
                 void* workspace, cudaStream_t stream) {
+  using L = DL<D, R>;
   DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.ctx_q_start = a.ctx_q_start;
@@ -829,16 +880,15 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   p.part_o = p.part_ml + ((nrec * 2 + 63) / 64) * 64;
   p.status = a.status;
   p.num_blocks = a.num_blocks;
-  p.n_items = plan.n_items;
   p.max_blocks = a.max_blocks;
   p.max_ctx_len = a.max_ctx_len;
   p.n_adapters = a.n_adapters;
-  p.num_ctx = a.num_ctx;
+  p.num_queries = a.num_queries;
   p.Hq = cfg.n_q_heads;
   p.Hkv = cfg.n_kv_heads;
   p.g = plan.g;
-  p.qg_size = plan.qg_size;
-  p.n_qgroups = plan.n_qgroups;
+  p.rpi = plan.rows_per_item;
+  p.n_chunks = plan.n_chunks;
   p.n_splits = plan.n_splits;
   p.split_blocks = plan.split_blocks;
   p.has_bk = a.B_K != nullptr;
@@ -847,18 +897,19 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   rope_freqs(cfg, &p.freqs);
 
   CUtensorMap tb, tl;
-  if (!make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, &tl)) return LRKV_ERR_CUDA;
+  if (!make_pool_maps(cfg, a.base_pool, nullptr, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
+  if (!make_lr_map(cfg, a.lr_pool, a.num_blocks, L::RP, &tl)) return LRKV_ERR_CUDA;
 
   if (plan.n_items > 0) {
-    auto kern = decode_kernel<D, R, RN>;
+    auto kern = decode_kernel<D, R>;
     static bool attr_set = false;  // idempotent per-process kernel attribute
     if (!attr_set) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes) !=
           cudaSuccess)
         return LRKV_ERR_CUDA;
       attr_set = true;
     }
-    kern<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(p, tb, tl);
+    kern<<<static_cast<unsigned>(plan.n_items), kThreads, plan.smem_bytes, stream>>>(p, tb, tl);
     if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
   }
   CombineParams c{};
@@ -900,44 +951,39 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   DecodePlan P{};
   P.g = cfg.n_q_heads / cfg.n_kv_heads;
   if (P.g < 1 || P.g > kMaxRows) return false;
-  int slots = 0, total = 0;
+  int rpi = 0, total = 0;
 #define LRKV_L(d, r) \
-  if (D == d && R == r) { slots = DL<d, r>::kSlots; total = DL<d, r>::total; }
+  if (D == d && R == r) { rpi = DL<d, r>::RPI; total = DL<d, r>::total; }
   LRKV_L(128, 8) LRKV_L(128, 16) LRKV_L(128, 32) LRKV_L(128, 64)
   LRKV_L(64, 8) LRKV_L(64, 16) LRKV_L(64, 32) LRKV_L(64, 64)
 #undef LRKV_L
-  if (slots == 0 || total > kSmemLimit) return false;
-  const int qg = std::min(kMaxRows / P.g, slots);
-  P.qg_size = qg;
-  P.rn = qg * P.g > 8 ? 2 : 1;
-  P.nstage = kNST;
-  P.smem_bytes = total;
-  P.n_qgroups = std::max(1, (max_q_per_ctx + qg - 1) / qg);
+  if (rpi == 0) return false;
+  P.rows_per_item = rpi;
+  P.smem_bytes = std::max(total, kMinSmem);
+  P.n_chunks = std::max(1, (max_q_per_ctx * P.g + rpi - 1) / rpi);
   const int nblk = std::max(1, (max_ctx_len + kBlock - 1) / kBlock);
-  const int64_t pairs = static_cast<int64_t>(num_ctx) * P.n_qgroups * cfg.n_kv_heads;
-  // Splits: as many as keep every SM busy in whole waves of items (>= 0.95
-  // efficiency), counting how evenly a split's blocks fall on the kNW warps.
+  const int64_t pairs = static_cast<int64_t>(num_ctx) * P.n_chunks * cfg.n_kv_heads;
+  // Splits: one CTA per item, one CTA per SM. Estimated time = waves x (blocks
+  // per split + a per-item overhead of about 12 blocks' worth of streaming).
+  constexpr double kItemOverheadBlocks = 12.0;
   int best_s = 1;
-  double best_eff = -1.0;
-  const int smax = std::min(nblk, 256);
+  double best = -1.0;
+  const int smax = std::min(nblk, 512);
   for (int s = 1; s <= smax; ++s) {
     const int sb = (nblk + s - 1) / s;
-    const int ss = (nblk + sb - 1) / sb;
-    if (ss != s) continue;
+    if ((nblk + sb - 1) / sb != s) continue;
     const int64_t items = pairs * s;
     const int64_t waves = (items + sm_count - 1) / sm_count;
-    const double rounds = static_cast<double>((sb + kNW - 1) / kNW) * kNW / sb;  // warp balance
-    const double eff = static_cast<double>(items) / static_cast<double>(waves * sm_count) / rounds;
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
+    const double cost = static_cast<double>(waves) * (sb + kItemOverheadBlocks);
+    if (best < 0.0 || cost < best - 1e-9) {
+      best = cost;
       best_s = s;
     }
-    if (eff >= 0.95) break;
   }
   P.split_blocks = (nblk + best_s - 1) / best_s;
   P.n_splits = (nblk + P.split_blocks - 1) / P.split_blocks;
   P.n_items = pairs * P.n_splits;
-  P.grid = static_cast<int>(std::min<int64_t>(P.n_items, sm_count));
+  if (P.n_items > INT32_MAX) return false;
   const int64_t nrec = static_cast<int64_t>(num_queries) * cfg.n_q_heads * P.n_splits;
   P.ws_bytes = static_cast<size_t>((((nrec * 2 + 63) / 64) * 64 + nrec * (D + R)) * 4);
   *plan = P;
@@ -947,10 +993,8 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
 lrkv_status launch_decode_bf16(const lrkv_config& cfg, const DecodeArgs& a,
                                const DecodePlan& plan, void* workspace, cudaStream_t stream) {
   const int D = cfg.head_dim, R = cfg.rank;
-#define LRKV_DEC(d, r)                                                          \
-  if (D == d && R == r)                                                         \
-    return plan.rn == 1 ? run<d, r, 1>(cfg, a, plan, workspace, stream)         \
-                        : run<d, r, 2>(cfg, a, plan, workspace, stream);
+#define LRKV_DEC(d, r) \
+  if (D == d && R == r) return run<d, r>(cfg, a, plan, workspace, stream);
   LRKV_DEC(128, 8) LRKV_DEC(128, 16) LRKV_DEC(128, 32) LRKV_DEC(128, 64)
   LRKV_DEC(64, 8) LRKV_DEC(64, 16) LRKV_DEC(64, 32) LRKV_DEC(64, 64)
 #undef LRKV_DEC

@@ -15,17 +15,14 @@ struct RopeFreqs;  // lrkv_device.cuh
 // Split plan of the bf16 decode kernel; a pure function of the sizes and the
 // device's SM count, so the workspace query and the launch agree.
 struct DecodePlan {
-  int g;             // query heads per kv head
-  int qg_size;       // queries per query group (rows = qg_size * g <= 16)
-  int rn;            // 8-row tiles of query rows (1 or 2)
-  int n_qgroups;     // query groups per context
-  int n_splits;      // splits of each context's blocks
-  int split_blocks;  // blocks per split
-  int64_t n_items;   // num_ctx * n_qgroups * n_splits * Hkv
-  int grid;          // persistent CTAs
-  int nstage;        // pipeline stages
+  int g;              // query heads per kv head
+  int rows_per_item;  // query rows (query x head of the group) per work item
+  int n_chunks;       // row chunks per (context, kv head)
+  int n_splits;       // splits of each context's blocks
+  int split_blocks;   // blocks per split
+  int64_t n_items;    // num_ctx * n_chunks * n_splits * Hkv (one CTA each)
   int smem_bytes;
-  size_t ws_bytes;   // workspace: split partials
+  size_t ws_bytes;    // workspace: split partials
 };
 
 bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int max_ctx_len,
