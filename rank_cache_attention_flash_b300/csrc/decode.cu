@@ -51,7 +51,8 @@
 namespace lrkv {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kMaxRegs = 144;
 constexpr int kBT = 128;                   // tokens per tile (tcgen05 M)
 constexpr int kTileBlocks = kBT / kBlock;  // 8 blocks per tile
 constexpr int kMaxRows = 16;               // query rows per item (tcgen05 N of S_b, O^T)
@@ -75,6 +76,7 @@ struct DecodeParams {
   const int32_t* block_tables;
   const int32_t* ctx_lens;
   const __nv_bfloat16* B_K;
+  const __nv_bfloat16* B_V;  // only prefetched here (applied by the combine kernel)
   float* part_ml;  // [Nq*Hq][S][2] (m in log2 units, l)
   float* part_o;   // [Nq*Hq][S][D + R]
   int32_t* status;
@@ -87,9 +89,9 @@ struct DecodeParams {
 };
 
 // Shared-memory layout (byte offsets from a 1024-aligned base), fixed per (d, r).
-// A stage holds one tile of one operand pair: [low-rank 128 x RP][base atoms
-// 64 dims x 128 tokens, 128-byte swizzle]. NK stages of K_base + L_K, NV of
-// V_base + L_V.
+// One ring of NS slots carries the tiles in the order K_0, V_0, K_1, V_1, ...
+// A slot holds [low-rank 128 x RP][base atoms: 64 dims x 128 tokens, 128-byte
+// swizzle]: K_base + L_K for a K item, V_base + L_V for a V item.
 template <int D, int R>
 struct DL {
   static constexpr int HALF = D / 2;
@@ -97,6 +99,7 @@ struct DL {
   static constexpr int LSPAN = RP * 2;        // bytes per low-rank row
   static constexpr uint32_t SW_LR = tc::swizzle_code(LSPAN);
   static constexpr int RPI = (256 / R) < kMaxRows ? 256 / R : kMaxRows;  // rows per item
+  static constexpr int RH = RPI / 2;          // rows per token warpgroup
   static constexpr int NW_MAX = RPI * R;      // W columns (<= 256)
   static constexpr int KATOMS = D / 64;
   static constexpr int ATOM = kBT * 128;
@@ -107,46 +110,46 @@ struct DL {
   static constexpr int QB = KATOMS * kMaxRows * 128;
   static constexpr int PB = 2 * kMaxRows * 128;  // P^T [16 rows][128 tokens] bf16
   static constexpr int BTAB = 2 * HALF * 8;
-  static constexpr int TAIL = GAMMA + QB + 2 * PB + BTAB + 512 + 512;
-  static constexpr int NK = (4 * STAGE + TAIL + 1024 <= kSmemLimit) ? 2 : 1;
-  static constexpr int NV = 2;
-  static constexpr int off_k = 0;
-  static constexpr int off_v = NK * STAGE;
-  static constexpr int off_g = off_v + NV * STAGE;
+  static constexpr int MISC = 1024;
+  static constexpr int TAIL = GAMMA + QB + 2 * PB + BTAB + MISC + 512;
+  static constexpr int NS_FIT = (kSmemLimit - 1024 - TAIL) / STAGE;
+  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+  static constexpr int off_ring = 0;
+  static constexpr int off_g = NS * STAGE;
   static constexpr int off_q = off_g + GAMMA;
   static constexpr int off_p = off_q + QB;
   static constexpr int off_btab = off_p + 2 * PB;
   static constexpr int off_misc = off_btab + BTAB;
-  static constexpr int off_bar = off_misc + 512;
+  static constexpr int off_bar = off_misc + MISC;
   static constexpr int used = off_bar + 512;
   static constexpr int total = used + 1024;  // + alignment slack
+  static_assert(NS >= 3, "the ring needs three slots");
   static_assert(total <= kSmemLimit, "decode tile does not fit in shared memory");
-  static_assert(NW_MAX <= 256 && NW_MAX % 16 == 0, "W must be a legal tcgen05 N");
+  static_assert(NW_MAX <= 256 && NW_MAX % 64 == 0 && RH >= 2, "W split over two warpgroups");
   // The M = 128 operands V^T (d = 64) and L_V^T (r < 128) read whole 128-row
   // spans; the rows past the tile land in the following buffers (never past
   // the allocation) and only feed accumulator lanes that are never read.
-  static_assert(off_v + (NV - 1) * STAGE + LR_TILE + 2 * ATOM <= used, "V^T span");
-  static_assert(off_v + (NV - 1) * STAGE + 7 * 16 * LSPAN + (128 / RP - 1) * LR_TILE +
-                        16 * LSPAN <= used, "L_V^T span");
+  static_assert((NS - 1) * STAGE + LR_TILE + 2 * ATOM <= used, "V^T span");
+  static_assert((NS - 1) * STAGE + 7 * 16 * LSPAN + (128 / RP - 1) * LR_TILE + 16 * LSPAN <= used,
+                "L_V^T span");
 };
 
 enum : int {
-  B_FK = 0,     // [2] K_base + L_K stage full (TMA bytes)
-  B_EK = 2,     // [2] K stage consumed (token warps, after S_b completed)
-  B_FV = 4,     // [2] V_base + L_V stage full (TMA bytes)
-  B_EV = 6,     // [2] V stage consumed (commit of the O^T / O_lr^T MMAs)
-  B_UF = 8,     // U of the next tile written (token warps)
-  B_WF = 9,     // W complete (commit)
-  B_SF = 10,    // S_b complete (commit)
-  B_WR = 11,    // W and S_b read out (token warps)
-  B_PF = 12,    // [2] P^T written, O rescaled (token warps)
-  B_PR = 14,    // [2] P V of that buffer complete (commit)
-  B_DRAIN = 16, // [4] per MMA warp, on abort: its MMAs have completed
+  B_FULL = 0,    // [4] ring slot full (TMA bytes)
+  B_EMPTY = 4,   // [4] ring slot consumed: 8 token warps + the MMA commit that read it
+  B_UF = 8,      // U of the next tile written (8 token warps)
+  B_WF = 9,      // W complete (commit)
+  B_SF = 10,     // S_b complete (commit)
+  B_WR = 11,     // W and S_b read out (8 token warps)
+  B_PF = 12,     // [2] P^T written, O rescaled (8 token warps)
+  B_PR = 14,     // [2] P V of that buffer complete (commit)
+  B_DRAIN = 16,  // [4] per MMA warp, on abort: its MMAs have completed
   B_COUNT = 20
 };
 
 __device__ __forceinline__ uint32_t bar_count(int i) {
-  if (i == B_EK || i == B_EK + 1 || i == B_UF || i == B_WR || i == B_PF || i == B_PF + 1) return 4;
+  if (i >= B_EMPTY && i < B_EMPTY + 4) return 9;
+  if (i == B_UF || i == B_WR || i == B_PF || i == B_PF + 1) return 8;
   return 1;
 }
 
@@ -189,8 +192,11 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
 
+// At most kMaxRegs registers per thread: 384 x 144 leaves room on the SM for
+// one combine CTA, which then waits resident (programmatic dependent launch)
+// instead of being scheduled after the decode grid drains.
 template <int D, int R>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(kMaxRegs)
     decode_kernel(const __grid_constant__ DecodeParams p,
                   const __grid_constant__ CUtensorMap tm_base,
                   const __grid_constant__ CUtensorMap tm_lr) {
@@ -198,7 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int HALF = D / 2;
   constexpr int KS = D / 16;  // k-steps over the head dims (and over u)
   constexpr int LSPAN = L::LSPAN;
-  constexpr int NK = L::NK, NV = L::NV;
+  constexpr int NS = L::NS;
+  constexpr int RH = L::RH;
+  constexpr int WCH = RH * R / 32;  // W chunks (32 columns) per token warpgroup
+  constexpr int QH = HALF / 32;     // 16-pair rotation chunks per token warpgroup
 
   // The combine kernel may be scheduled now; it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -209,10 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + L::off_bar + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc + 4);
-  int* kmask = reinterpret_cast<int*>(smem + L::off_misc + 8);          // [2] loaded blocks per K stage
-  int* row_ad = reinterpret_cast<int*>(smem + L::off_misc + 16);        // [16]
-  float* red = reinterpret_cast<float*>(smem + L::off_misc + 128);      // [4][16]
-  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab);         // [2][HALF]
+  int* kmask = reinterpret_cast<int*>(smem + L::off_misc + 16);     // [4] loaded blocks per slot
+  int* row_ad = reinterpret_cast<int*>(smem + L::off_misc + 32);    // [16]
+  float* red = reinterpret_cast<float*>(smem + L::off_misc + 128);  // [2 groups][4 warps][8]
+  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab);     // [2][HALF]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -224,7 +233,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   rest /= p.n_splits;
   const int chunk = static_cast<int>(rest % p.n_chunks);
   const int ctx = static_cast<int>(rest / p.n_chunks);
+  const int kbeg = split * p.split_blocks;
+  const int32_t* btrow = p.block_tables + static_cast<int64_t>(ctx) * p.max_blocks;
+  // block ids of the first two tiles, fetched before the context length is known
+  int id0 = INT_MIN, id1 = INT_MIN;
+  if (warp == 0) {
+    const int kb = kbeg + (lane & 7) + (lane >> 3) * kTileBlocks;
+    const int x = (lane < 2 * kTileBlocks && kb < p.max_blocks && kb < kbeg + p.split_blocks) ? __ldg(btrow + kb) : INT_MIN;
+    id0 = __shfl_sync(0xffffffffu, x, lane & 7);
+    id1 = __shfl_sync(0xffffffffu, x, (lane & 7) + 8);
+    if (lane >= kTileBlocks) id0 = id1 = INT_MIN;
+  } else if (p.n_adapters * R <= 4096) {
+    // every adapter's B_K rows of this kv head into L2 (the rows this item
+    // needs are known only after two dependent loads), and its B_V rows for
+    // the combine kernel
+    for (int i = tid - 32; i < p.n_adapters * R * (D / 64); i += kThreads - 32) {
+      const int64_t off = (static_cast<int64_t>(i / (D / 64)) * p.Hkv + head) * D + 64 * (i % (D / 64));
+      if (p.has_bk) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p.B_K + off));
+      if (p.B_V != nullptr) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p.B_V + off));
+    }
+  }
   const int qs = __ldg(p.ctx_q_start + ctx), qe = __ldg(p.ctx_q_start + ctx + 1);
+  int len = __ldg(p.ctx_lens + ctx);
   if (qs < 0 || qe > p.num_queries) {
     if (tid == 0) report(p.status, LRKV_ERR_INDEX);
     return;
@@ -232,13 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row0 = chunk * p.rpi;
   const int nrows = min(p.rpi, (qe - qs) * p.g - row0);
   if (nrows <= 0) return;
-  int len = __ldg(p.ctx_lens + ctx);
   if (len < 1 || len > p.max_ctx_len) {
     if (tid == 0) report(p.status, LRKV_ERR_INDEX);
     len = 0;
   }
   const int nblk = (len + kBlock - 1) / kBlock;
-  const int kbeg = split * p.split_blocks;
   const int kend = min(kbeg + p.split_blocks, nblk);
   const int ntiles = kend > kbeg ? (kend - kbeg + kTileBlocks - 1) / kTileBlocks : 0;
   auto rec_of = [&](int r) -> int64_t {
@@ -255,6 +283,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.part_ml[2 * rec_of(tid) + 1] = 0.f;
     }
     return;
+  }
+
+  // warps 1-3: this item's adapter ids and Q rows, requested before the setup barrier
+  constexpr int QCH = kMaxRows * (D / 8);
+  constexpr int QIT = (QCH + 95) / 96;
+  uint4 qv[QIT];
+  int a_row = -2;
+  if (warp >= 1 && warp < 4) {
+    const int pt = tid - 32;  // 0..95
+    if (pt < nrows) a_row = __ldg(p.adapter_ids + qs + (row0 + pt) / p.g);
+#pragma unroll
+    for (int u = 0; u < QIT; ++u) {
+      const int i = pt + 96 * u;
+      const int r = i / (D / 8), c = i % (D / 8);
+      qv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < QCH && r < nrows) {
+        const int gr = row0 + r;
+        const __nv_bfloat16* src =
+            p.q + (static_cast<int64_t>(qs + gr / p.g) * p.Hq + head * p.g + gr % p.g) * D + 8 * c;
+        qv[u] = __ldg(reinterpret_cast<const uint4*>(src));
+      }
+    }
   }
 
   // ---- barriers, tensor memory
@@ -275,98 +325,75 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ============================================================ producer
   if (warp == 0) {
-    const int32_t* bt = p.block_tables + static_cast<int64_t>(ctx) * p.max_blocks;
-    auto load_id = [&](int j) -> int {
-      const int kb = kbeg + j * kTileBlocks + lane;
-      return (lane < kTileBlocks && j < ntiles && kb < kend) ? __ldg(bt + kb) : INT_MIN;
-    };
-    const uint32_t kbytes = L::KATOMS * 2048 + (p.has_bk ? 16 * LSPAN : 0);
-    const uint32_t vbytes = L::KATOMS * 2048 + (p.has_bv ? 16 * LSPAN : 0);
-    int id_cur = load_id(0);
+    const uint32_t bytes_k = L::KATOMS * 2048 + (p.has_bk ? 16 * LSPAN : 0);
+    const uint32_t bytes_v = L::KATOMS * 2048 + (p.has_bv ? 16 * LSPAN : 0);
+    const int n_items = 2 * ntiles;
+    int id = (kbeg + lane < kend) ? id0 : INT_MIN;
+    int id_next = (kbeg + kTileBlocks + lane < kend) ? id1 : INT_MIN;
+    bool valid = false;
+    uint32_t vm = 0, nv = 0;
     bool ok = true;
-    int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;  // last tile issued per stage
-    for (int j = 0; j < ntiles; ++j) {
-      const int id_nxt = load_id(j + 1);
-      bool valid = id_cur != INT_MIN;
-      if (valid && (id_cur < 0 || id_cur >= p.num_blocks)) {
-        report(p.status, LRKV_ERR_INDEX);
-        valid = false;
+    int it = 0;
+    for (; it < n_items; ++it) {
+      const int j = it >> 1, kind = it & 1, s = it % NS;
+      if (kind == 0) {
+        valid = id != INT_MIN;
+        if (valid && (id < 0 || id >= p.num_blocks)) {
+          report(p.status, LRKV_ERR_INDEX);
+          valid = false;
+        }
+        vm = __ballot_sync(0xffffffffu, valid);
+        nv = __popc(vm);
       }
-      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
-      const uint32_t nv = __popc(vm);
-      const int s = j % NK, v = j % NV;
-      if (j >= NK) ok = warp_all(wait_ab(bar(B_EK + s), ((j / NK) - 1) & 1, p.status, abort_flag));
+      if (it >= NS) ok = warp_all(wait_ab(bar(B_EMPTY + s), ((it / NS) - 1) & 1, p.status, abort_flag));
       if (!ok) break;
-      const uint32_t kst = sbase + L::off_k + s * L::STAGE;
+      const uint32_t dst = sbase + L::off_ring + s * L::STAGE;
+      const uint32_t fb = bar(B_FULL + s);
       if (lane == 0) {
-        kmask[s] = static_cast<int>(vm);  // published by the arrive (release) below
-        mbar_arrive_expect_tx(bar(B_FK + s), nv * kbytes);
+        if (kind == 0) kmask[s] = static_cast<int>(vm);  // published by the arrive (release)
+        mbar_arrive_expect_tx(fb, nv * (kind == 0 ? bytes_k : bytes_v));
       }
       __syncwarp();
-      if (s == 0) last_k0 = j; else last_k1 = j;
       if (valid) {
-        const int yk = ((id_cur * 2 + 0) * p.Hkv + head) * kBlock;
+        const int y = ((id * 2 + kind) * p.Hkv + head) * kBlock;
 #pragma unroll
         for (int a = 0; a < L::KATOMS; ++a)
-          tma_load_2d(kst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, yk, bar(B_FK + s));
-        if (p.has_bk) tma_load_2d(kst + lane * 16 * LSPAN, &tm_lr, 0, (id_cur * 2 + 0) * kBlock, bar(B_FK + s));
+          tma_load_2d(dst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, y, fb);
+        if (kind == 0 ? p.has_bk : p.has_bv)
+          tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, 0, (id * 2 + kind) * kBlock, fb);
       }
-      if (j >= NV) ok = warp_all(wait_ab(bar(B_EV + v), ((j / NV) - 1) & 1, p.status, abort_flag));
-      if (!ok) break;
-      const uint32_t vst = sbase + L::off_v + v * L::STAGE;
-      if (lane == 0) mbar_arrive_expect_tx(bar(B_FV + v), nv * vbytes);
-      __syncwarp();
-      if (v == 0) last_v0 = j; else last_v1 = j;
-      if (valid) {
-        const int yv = ((id_cur * 2 + 1) * p.Hkv + head) * kBlock;
-#pragma unroll
-        for (int a = 0; a < L::KATOMS; ++a)
-          tma_load_2d(vst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, yv, bar(B_FV + v));
-        if (p.has_bv) tma_load_2d(vst + lane * 16 * LSPAN, &tm_lr, 0, (id_cur * 2 + 1) * kBlock, bar(B_FV + v));
+      if (kind == 1) {  // block ids: tile j + 1 ready, tile j + 2 requested
+        const int kb = kbeg + (j + 2) * kTileBlocks + lane;
+        id = id_next;
+        id_next = (lane < kTileBlocks && kb < kend) ? __ldg(btrow + kb) : INT_MIN;
       }
-      id_cur = id_nxt;
     }
     if (!ok && lane == 0) *abort_flag = 1;
-    // No copy may still be landing when the CTA leaves.
-    if (last_k0 >= 0) wait_ab(bar(B_FK + 0), (last_k0 / NK) & 1, p.status, nullptr);
-    if (last_k1 >= 0) wait_ab(bar(B_FK + 1), (last_k1 / NK) & 1, p.status, nullptr);
-    if (last_v0 >= 0) wait_ab(bar(B_FV + 0), (last_v0 / NV) & 1, p.status, nullptr);
-    if (last_v1 >= 0) wait_ab(bar(B_FV + 1), (last_v1 / NV) & 1, p.status, nullptr);
+    // No copy may still be landing when the CTA leaves: wait for the last
+    // item issued into each slot.
+    for (int s = 0; s < NS; ++s) {
+      const int last = it - 1 - ((it - 1 - s) % NS + NS) % NS;
+      if (last >= 0 && last < it) wait_ab(bar(B_FULL + s), (last / NS) & 1, p.status, nullptr);
+    }
   } else {
-    // ================================================ prologue (warps 1-7)
+    // ================================================ prologue (warps 1-11)
     // Row adapters and Q (bf16, K-major, 128-byte swizzle; zero past nrows)
-    // by warps 1-3; the token warps meanwhile fill their rotation tables.
-    const int tt = tid - 128;  // token warps: token row of the tile = TMEM lane
+    // by warps 1-3; the token warpgroups meanwhile fill their rotation tables.
+    const int gq = (warp - 4) >> 2;  // token warpgroup (warps 4-7: 0, 8-11: 1)
+    const int tt = (warp & 3) * 32 + lane;  // token row of the tile = TMEM lane
     const uint32_t tl = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const int jb = gq * (HALF / 2);  // this warpgroup's rotation pairs [jb, jb + HALF/2)
     float th_hi = 0.f, th_lo = 0.f;
-    if (warp >= 4 && tt < HALF) {
-      th_hi = p.freqs.hi[tt];
-      th_lo = p.freqs.lo[tt];
+    if (warp >= 4 && tt < HALF / 2) {
+      th_hi = p.freqs.hi[jb + tt];
+      th_lo = p.freqs.lo[jb + tt];
     }
     if (warp < 4) {
       const int pt = tid - 32;  // 0..95
       if (pt < kMaxRows) {
-        int a = -2;
-        if (pt < nrows) {
-          a = __ldg(p.adapter_ids + qs + (row0 + pt) / p.g);
-          if (a < -1 || a >= p.n_adapters || !p.has_bk) a = -1;  // bad ids: reported by the combine
-        }
+        int a = a_row;
+        if (pt < nrows && (a < -1 || a >= p.n_adapters || !p.has_bk)) a = -1;  // bad ids: reported by the combine
         row_ad[pt] = a;
-      }
-      constexpr int QCH = kMaxRows * (D / 8);
-      constexpr int QIT = (QCH + 95) / 96;
-      uint4 qv[QIT];
-#pragma unroll
-      for (int u = 0; u < QIT; ++u) {
-        const int i = pt + 96 * u;
-        const int r = i / (D / 8), c = i % (D / 8);
-        qv[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < QCH && r < nrows) {
-          const int gr = row0 + r;
-          const __nv_bfloat16* src =
-              p.q + (static_cast<int64_t>(qs + gr / p.g) * p.Hq + head * p.g + gr % p.g) * D + 8 * c;
-          qv[u] = __ldg(reinterpret_cast<const uint4*>(src));
-        }
       }
 #pragma unroll
       for (int u = 0; u < QIT; ++u) {
@@ -377,34 +404,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (((c & 7) ^ (r & 7)) << 4)) = qv[u];
       }
     } else {
-      // e^{i delta theta_j} for this lane's token offset delta = tt, in TMEM
+      // e^{i delta theta_j} of this lane's token offset delta = tt, for this
+      // warpgroup's pairs, in TMEM (column 2j: cos, 2j + 1: sin)
 #pragma unroll
-      for (int q4 = 0; q4 < HALF / 16; ++q4) {
+      for (int q4 = 0; q4 < QH; ++q4) {
+        const int j0 = jb + 16 * q4;
         uint32_t dv[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 cs = rope_cos_sin_fast(tt, p.freqs.hi[16 * q4 + i], p.freqs.lo[16 * q4 + i]);
+          const float2 cs = rope_cos_sin_fast(tt, p.freqs.hi[j0 + i], p.freqs.lo[j0 + i]);
           dv[2 * i] = __float_as_uint(cs.x);
           dv[2 * i + 1] = __float_as_uint(cs.y);
         }
-        tc::st_x32(tl + DT_COL + 32 * q4, dv);
+        tc::st_x32(tl + DT_COL + 2 * j0, dv);
       }
       tc::wait_st();
-      // base angles e^{i t0 theta_j} of tiles 0 and 1
+      // base angles e^{i t0 theta_j} of tiles 0 and 1 (this warpgroup's pairs)
       const int t00 = kbeg * kBlock;
-      if (tt < HALF) btab[tt] = rope_cos_sin_fast(t00, th_hi, th_lo);
-      else if (tt < 2 * HALF && ntiles > 1)
-        btab[tt] = rope_cos_sin_fast(t00 + kBT, p.freqs.hi[tt - HALF], p.freqs.lo[tt - HALF]);
+      if (tt < HALF / 2) {
+        btab[jb + tt] = rope_cos_sin_fast(t00, th_hi, th_lo);
+        if (ntiles > 1) btab[HALF + jb + tt] = rope_cos_sin_fast(t00 + kBT, th_hi, th_lo);
+      }
     }
-    named_bar_sync(1, 224);
+    named_bar_sync(1, kThreads - 32);
     bool use_w = false;
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) use_w |= row_ad[r] >= 0;
     const int nw = ((nrows * R + 15) / 16) * 16;
 
-    // G (fp16, K-major over u, 128-byte swizzle) for rows n = row * R + k < nw
+    // G (fp16, K-major over u, 128-byte swizzle) for rows n = row * R + k < nw;
+    // one row per thread, its B_K row loaded in one burst
     if (use_w) {
-      for (int n = tid - 32; n < nw; n += 224) {
+      const int n = tid - 32;
+      if (n < nw) {
         const int r = n / R, k = n % R;
         const int a = row_ad[r];
         uint8_t* grow = smem + L::off_g + n * 128;
@@ -448,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // Q, G -> MMA operands
-    named_bar_sync(1, 224);
+    named_bar_sync(1, kThreads - 32);
 
     if (warp == 1) {
       // ======================================================= W issuer
@@ -488,18 +520,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
-        const int s = j % NK;
-        ok = warp_all(wait_ab(bar(B_FK + s), (j / NK) & 1, p.status, abort_flag));
+        const int s = (2 * j) % NS;
+        ok = warp_all(wait_ab(bar(B_FULL + s), ((2 * j) / NS) & 1, p.status, abort_flag));
         if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
         if (!ok) break;
         tc::fence_after();
         if (tc::elect_one()) {
-          const uint64_t kdesc = tc::sdesc(sbase + L::off_k + s * L::STAGE + L::LR_TILE, 16, 1024, 2);
+          const uint64_t kdesc = tc::sdesc(sbase + L::off_ring + s * L::STAGE + L::LR_TILE, 16, 1024, 2);
 #pragma unroll
           for (int k = 0; k < KS; ++k)
             tc::mma_ss(tbase + S_COL, kdesc + (((k >> 2) * L::ATOM + (k & 3) * 32) >> 4),
                        qdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ids, k > 0 ? 1u : 0u);
           tc::commit(bar(B_SF));
+          tc::commit(bar(B_EMPTY + s));
         }
         __syncwarp();
         ++issued;
@@ -518,13 +551,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
-        const int v = j % NV, b = j & 1;
-        ok = warp_all(wait_ab(bar(B_FV + v), (j / NV) & 1, p.status, abort_flag));
+        const int v = (2 * j + 1) % NS, b = j & 1;
+        ok = warp_all(wait_ab(bar(B_FULL + v), ((2 * j + 1) / NS) & 1, p.status, abort_flag));
         if (ok) ok = warp_all(wait_ab(bar(B_PF + b), (j >> 1) & 1, p.status, abort_flag));
         if (!ok) break;
         tc::fence_after();
         if (tc::elect_one()) {
-          const uint32_t vst = sbase + L::off_v + v * L::STAGE;
+          const uint32_t vst = sbase + L::off_ring + v * L::STAGE;
           // V^T: M = head dims (MN-major; 64-dim atoms ATOM bytes apart), K = tokens
           const uint64_t vdesc = tc::sdesc(vst + L::LR_TILE, L::ATOM, 1024, 2);
           // L_V^T: M = rank (MN-major, swizzled by the row span), K = tokens
@@ -538,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.has_bv) tc::mma_ss(tbase + OL_COL, lvdesc + ((k * 16 * LSPAN) >> 4), pk, ido, acc);
           }
           tc::commit(bar(B_PR + b));
-          tc::commit(bar(B_EV + v));
+          tc::commit(bar(B_EMPTY + v));
         }
         __syncwarp();
         ++issued;
@@ -552,27 +585,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // ================================================== token warps
+      // ============================================ token warpgroups
+      // Two warpgroups share the tile's 128 tokens (thread = token = TMEM
+      // lane): warpgroup gq owns query rows [gq*RH, gq*RH + RH), their W
+      // columns, their P^T rows and O columns, and rotation pairs [jb, jb + HALF/2).
+      const int bar_g = 2 + gq;  // this warpgroup's named barrier
+      const int rb = gq * RH;    // first row owned
       // U(t) = e^{i t0 theta} e^{i delta theta}, packed fp16 pairs:
       // columns [0, HALF/2) hold cos, [HALF/2, HALF) hold sin.
       auto build_u = [&](int bb) {
         const float2* bt = btab + bb * HALF;
 #pragma unroll
-        for (int q4 = 0; q4 < HALF / 16; ++q4) {
+        for (int q4 = 0; q4 < QH; ++q4) {
+          const int j0 = jb + 16 * q4;
           uint32_t dv[32];
-          tc::ld_x32(tl + DT_COL + 32 * q4, dv);
+          tc::ld_x32(tl + DT_COL + 2 * j0, dv);
           tc::wait_ld();
           uint32_t uc[8], us[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float4 b2 = *reinterpret_cast<const float4*>(bt + 16 * q4 + 2 * i);
+            const float4 b2 = *reinterpret_cast<const float4*>(bt + j0 + 2 * i);
             const float cd0 = __uint_as_float(dv[4 * i]), sd0 = __uint_as_float(dv[4 * i + 1]);
             const float cd1 = __uint_as_float(dv[4 * i + 2]), sd1 = __uint_as_float(dv[4 * i + 3]);
             uc[i] = pack_f16(fmaf(b2.x, cd0, -(b2.y * sd0)), fmaf(b2.z, cd1, -(b2.w * sd1)));
             us[i] = pack_f16(fmaf(b2.y, cd0, b2.x * sd0), fmaf(b2.w, cd1, b2.z * sd1));
           }
-          tc::st_x8(tl + U_COL + 8 * q4, uc);
-          tc::st_x8(tl + U_COL + HALF / 2 + 8 * q4, us);
+          tc::st_x8(tl + U_COL + j0 / 2, uc);
+          tc::st_x8(tl + U_COL + HALF / 2 + j0 / 2, us);
         }
         tc::wait_st();
       };
@@ -583,32 +622,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_UF));
       }
 
-      float m_run[kMaxRows], l_run[kMaxRows];
+      float m_run[RH], l_run[RH];
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
+      for (int r = 0; r < RH; ++r) {
         m_run[r] = -CUDART_INF_F;
         l_run[r] = 0.f;
       }
+      // this warpgroup's W columns that exist: [gq*RH*R, min(nw, (gq+1)*RH*R))
+      const int wch = use_w ? max(0, min(WCH, (nw - gq * RH * R + 31) / 32)) : 0;
       bool failed = false;
       for (int j = 0; j < ntiles; ++j) {
-        const int s = j % NK, v = j % NV, b = j & 1;
+        const int s = (2 * j) % NS, v = (2 * j + 1) % NS, b = j & 1;
         const int t0 = (kbeg + j * kTileBlocks) * kBlock;
-        // ---- scores of this lane's token
+        // ---- scores of this lane's token, own rows
         if (!failed && use_w) failed = !wait_ab(bar(B_WF), j & 1, p.status, abort_flag);
         if (!failed) failed = !wait_ab(bar(B_SF), j & 1, p.status, abort_flag);
-        if (!failed) failed = !wait_ab(bar(B_FK + s), (j / NK) & 1, p.status, abort_flag);
+        if (!failed) failed = !wait_ab(bar(B_FULL + s), ((2 * j) / NS) & 1, p.status, abort_flag);
         tc::fence_after();
         const int vmask = kmask[s];  // blocks of this tile that were loaded (valid ids inside the split)
-        float sc[kMaxRows];
+        float sc[RH];
         {
           uint32_t sv[16];
           tc::ld_x16(tl + S_COL, sv);
-          float slr[kMaxRows];
+          float slr[RH];
 #pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) slr[r] = 0.f;
-          if (use_w) {
+          for (int r = 0; r < RH; ++r) slr[r] = 0.f;
+          if (wch > 0) {
             float lk[R];
-            const uint8_t* lrow = smem + L::off_k + s * L::STAGE;
+            const uint8_t* lrow = smem + L::off_ring + s * L::STAGE;
 #pragma unroll
             for (int c = 0; c < (R + 7) / 8; ++c) {
               const uint4 x = *reinterpret_cast<const uint4*>(lrow + swz<LSPAN>(tt, 16 * c));
@@ -619,93 +660,109 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (8 * c + 2 * e + 1 < R) lk[8 * c + 2 * e + 1] = bf16_hi(xs[e]);
               }
             }
+            // two chunks in flight per TMEM wait; two partial sums per row
+            float acc2[RH];
 #pragma unroll
-            for (int c = 0; c < L::NW_MAX / 32; ++c) {
-              if (32 * c < nw) {
-                uint32_t w[32];
-                tc::ld_x32(tl + W_COL + 32 * c, w);
+            for (int r = 0; r < RH; ++r) acc2[r] = 0.f;
+#pragma unroll
+            for (int c = 0; c < WCH; c += 2) {
+              if (c < wch) {
+                uint32_t w0[32], w1[32];
+                const uint32_t col = W_COL + gq * RH * R + 32 * c;
+                tc::ld_x32(tl + col, w0);
+                if (c + 1 < WCH) tc::ld_x32(tl + col + 32, w1);
                 tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                   const int n = 32 * c + i;
-                  slr[n / R] = fmaf(lk[n % R], __uint_as_float(w[i]), slr[n / R]);
+                  slr[n / R] = fmaf(lk[n % R], __uint_as_float(w0[i]), slr[n / R]);
+                }
+                if (c + 1 < WCH && c + 1 < wch) {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    const int n = 32 * (c + 1) + i;
+                    acc2[n / R] = fmaf(lk[n % R], __uint_as_float(w1[i]), acc2[n / R]);
+                  }
                 }
               }
             }
+#pragma unroll
+            for (int r = 0; r < RH; ++r) slr[r] += acc2[r];
           }
           tc::wait_ld();
 #pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) sc[r] = __uint_as_float(sv[r]) + slr[r];
+          for (int r = 0; r < RH; ++r) sc[r] = __uint_as_float(gq ? sv[RH + r] : sv[r]) + slr[r];
         }
         tc::fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(bar(B_WR));
-          mbar_arrive(bar(B_EK + s));
+          mbar_arrive(bar(B_EMPTY + s));
         }
-        // ---- U of the next tile, base angles of the one after
+        // ---- U of the next tile, base angles of the one after (own pairs)
         if (use_w && j + 1 < ntiles) {
           build_u((j + 1) & 1);
           tc::fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_UF));
         }
-        if (tt < HALF && j + 2 < ntiles) btab[b * HALF + tt] = rope_cos_sin_fast(t0 + 2 * kBT, th_hi, th_lo);
+        if (tt < HALF / 2 && j + 2 < ntiles) btab[b * HALF + jb + tt] = rope_cos_sin_fast(t0 + 2 * kBT, th_hi, th_lo);
 
-        // ---- online softmax over the tile's tokens (log2 units)
+        // ---- online softmax over the tile's tokens (log2 units), own rows
         const bool tok_ok = ((vmask >> (tt >> 4)) & 1) != 0 && t0 + tt < len;
         bool need = false;
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
+        for (int r = 0; r < RH; ++r) {
           sc[r] = tok_ok ? sc[r] * p.scale_log2 : -CUDART_INF_F;
           need |= sc[r] > m_run[r] + kRescaleLog2;
         }
         if (*abort_flag != 0) failed = true;
-        if (named_bar_or(2, 128, need || failed)) {  // also publishes btab
-          if (named_bar_or(2, 128, failed)) {
+        if (named_bar_or(bar_g, 128, need || failed)) {  // also publishes btab
+          if (named_bar_or(bar_g, 128, failed)) {
             failed = true;
             break;
           }
+          float* rg = red + gq * 32;
 #pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) {
+          for (int r = 0; r < RH; ++r) {
             float x = sc[r];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-            if (lane == 0) red[(warp & 3) * kMaxRows + r] = x;
+            if (lane == 0) rg[(warp & 3) * 8 + r] = x;
           }
-          named_bar_sync(2, 128);
-          float alpha[kMaxRows];
+          named_bar_sync(bar_g, 128);
+          float alpha[RH];
 #pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) {
-            const float mx = fmaxf(fmaxf(red[r], red[kMaxRows + r]),
-                                   fmaxf(red[2 * kMaxRows + r], red[3 * kMaxRows + r]));
+          for (int r = 0; r < RH; ++r) {
+            const float mx = fmaxf(fmaxf(rg[r], rg[8 + r]), fmaxf(rg[16 + r], rg[24 + r]));
             const float mn = fmaxf(m_run[r], mx);
             alpha[r] = mn == -CUDART_INF_F ? 1.f : ex2(m_run[r] - mn);
             m_run[r] = mn;
             l_run[r] *= alpha[r];
           }
+          named_bar_sync(bar_g, 128);  // rg is rewritten by the next vote's winners
           if (j > 0) {
             // the P V of the previous tile must have landed before O is rescaled
             if (!failed) failed = !wait_ab(bar(B_PR + ((j - 1) & 1)), ((j - 1) >> 1) & 1, p.status, abort_flag);
             tc::fence_after();
-            uint32_t o[16];
-            tc::ld_x16(tl + OT_COL, o);
+            uint32_t o[RH];
+            tc::ld_cols<RH>(tl + OT_COL + rb, o);
             tc::wait_ld();
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
-            tc::st_x16(tl + OT_COL, o);
+            for (int r = 0; r < RH; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+            tc::st_cols<RH>(tl + OT_COL + rb, o);
             if (p.has_bv) {
-              tc::ld_x16(tl + OL_COL, o);
+              tc::ld_cols<RH>(tl + OL_COL + rb, o);
               tc::wait_ld();
 #pragma unroll
-              for (int r = 0; r < kMaxRows; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
-              tc::st_x16(tl + OL_COL, o);
+              for (int r = 0; r < RH; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+              tc::st_cols<RH>(tl + OL_COL + rb, o);
             }
             tc::wait_st();
           }
         }
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
+        for (int r = 0; r < RH; ++r) {
           const float pr = ex2(sc[r] - (m_run[r] == -CUDART_INF_F ? 0.f : m_run[r]));
           l_run[r] += pr;
           sc[r] = pr;
@@ -716,65 +773,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* pb = smem + L::off_p + b * L::PB + (tt >> 6) * (kMaxRows * 128) + ((tt & 7) << 1);
           const int ch = (tt & 63) >> 3;
 #pragma unroll
-          for (int r = 0; r < kMaxRows; ++r)
-            *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((ch ^ (r & 7)) << 4)) = __float2bfloat16_rn(sc[r]);
+          for (int r = 0; r < RH; ++r)
+            *reinterpret_cast<__nv_bfloat16*>(pb + (rb + r) * 128 + ((ch ^ ((rb + r) & 7)) << 4)) =
+                __float2bfloat16_rn(sc[r]);
         }
         // rows of tokens outside the context or the split, or of blocks with a
         // bad id, hold stale memory: zero their V and L_V rows so that P = 0
-        // there cannot meet a NaN
+        // there cannot meet a NaN (warpgroup 0: V atom 0, warpgroup 1: the rest)
         if (vmask != (1 << kTileBlocks) - 1 || t0 + kBT > len) {
-          if (!failed) failed = !wait_ab(bar(B_FV + v), (j / NV) & 1, p.status, abort_flag);
+          if (!failed) failed = !wait_ab(bar(B_FULL + v), ((2 * j + 1) / NS) & 1, p.status, abort_flag);
           if (!tok_ok) {
-            uint8_t* vst = smem + L::off_v + v * L::STAGE;
-#pragma unroll
-            for (int a = 0; a < L::KATOMS; ++a)
+            uint8_t* vst = smem + L::off_ring + v * L::STAGE;
+            if (gq == 0) {
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(vst + L::LR_TILE + a * L::ATOM + tt * 128 + 16 * c) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(vst + L::LR_TILE + tt * 128 + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
 #pragma unroll
-            for (int c = 0; c < LSPAN / 16; ++c)
-              *reinterpret_cast<uint4*>(vst + tt * LSPAN + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+              for (int a = 1; a < L::KATOMS; ++a)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  *reinterpret_cast<uint4*>(vst + L::LR_TILE + a * L::ATOM + tt * 128 + 16 * c) =
+                      make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+              for (int c = 0; c < LSPAN / 16; ++c)
+                *reinterpret_cast<uint4*>(vst + tt * LSPAN + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+            }
           }
         }
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PF + b));
+        if (lane == 0) {
+          mbar_arrive(bar(B_PF + b));
+          mbar_arrive(bar(B_EMPTY + v));
+        }
       }
 
-      // ---- split partial: m, l, O, O_lr of each row
-      bool aborted = named_bar_or(3, 128, failed);
+      // ---- split partial: m, l, O, O_lr of each own row
+      bool aborted = named_bar_or(bar_g, 128, failed);
       if (!aborted) {
         const bool okp = wait_ab(bar(B_PR + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, p.status, abort_flag);
-        aborted = named_bar_or(3, 128, !okp);
+        aborted = named_bar_or(bar_g, 128, !okp);
       }
       if (aborted) {
         if (tt == 0) *abort_flag = 1;
       } else {
         tc::fence_after();
-        uint32_t o[16], ol[16];
-        tc::ld_x16(tl + OT_COL, o);
-        tc::ld_x16(tl + OL_COL, ol);
+        uint32_t o[RH], ol[RH];
+        tc::ld_cols<RH>(tl + OT_COL + rb, o);
+        tc::ld_cols<RH>(tl + OL_COL + rb, ol);
         tc::wait_ld();
+        float* rg = red + gq * 32;
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
+        for (int r = 0; r < RH; ++r) {
           float x = l_run[r];
 #pragma unroll
           for (int o2 = 16; o2 > 0; o2 >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o2);
-          if (lane == 0) red[(warp & 3) * kMaxRows + r] = x;
+          if (lane == 0) rg[(warp & 3) * 8 + r] = x;
         }
-        named_bar_sync(3, 128);
+        named_bar_sync(bar_g, 128);
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-          if (r < nrows) {
-            const int64_t rec = rec_of(r);
+        for (int r = 0; r < RH; ++r) {
+          if (rb + r < nrows) {
+            const int64_t rec = rec_of(rb + r);
             float* po = p.part_o + rec * (D + R);
             if (tt < D) po[tt] = __uint_as_float(o[r]);
             if (tt < R) po[D + tt] = p.has_bv ? __uint_as_float(ol[r]) : 0.f;
             if (tt == r) {
               p.part_ml[2 * rec] = m_run[r];
-              p.part_ml[2 * rec + 1] = red[r] + red[kMaxRows + r] + red[2 * kMaxRows + r] + red[3 * kMaxRows + r];
+              p.part_ml[2 * rec + 1] = rg[r] + rg[8 + r] + rg[16 + r] + rg[24 + r];
             }
           }
         }
@@ -875,6 +943,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   p.block_tables = a.block_tables;
   p.ctx_lens = a.ctx_lens;
   p.B_K = static_cast<const __nv_bfloat16*>(a.B_K);
+  p.B_V = static_cast<const __nv_bfloat16*>(a.B_V);
   const int64_t nrec = static_cast<int64_t>(a.num_queries) * cfg.n_q_heads * plan.n_splits;
   p.part_ml = static_cast<float*>(workspace);
   p.part_o = p.part_ml + ((nrec * 2 + 63) / 64) * 64;
@@ -968,7 +1037,7 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   constexpr double kItemOverheadBlocks = 12.0;
   int best_s = 1;
   double best = -1.0;
-  const int smax = std::min(nblk, 512);
+  const int smax = std::min(nblk, 256);  // the combine kernel holds up to 256 split weights
   for (int s = 1; s <= smax; ++s) {
     const int sb = (nblk + s - 1) / s;
     if ((nblk + sb - 1) / sb != s) continue;

@@ -109,6 +109,16 @@ __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.
 
 // 32 lanes x N consecutive 32-bit columns: thread t gets lane t, columns
 // taddr.col .. +N-1 in v[0..N-1].
+__device__ __forceinline__ void ld_x2(uint32_t taddr, uint32_t (&v)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];\n"
+               : "=r"(v[0]), "=r"(v[1])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void ld_x4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr));
+}
 __device__ __forceinline__ void ld_x8(uint32_t taddr, uint32_t (&v)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                : LRKV_R8(v, 0)
@@ -126,6 +136,15 @@ __device__ __forceinline__ void ld_x32(uint32_t taddr, uint32_t (&v)[32]) {
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
       : LRKV_R8(v, 0), LRKV_R8(v, 8), LRKV_R8(v, 16), LRKV_R8(v, 24)
       : "r"(taddr));
+}
+__device__ __forceinline__ void st_x2(uint32_t taddr, const uint32_t (&v)[2]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};\n" ::"r"(taddr), "r"(v[0]), "r"(v[1])
+               : "memory");
+}
+__device__ __forceinline__ void st_x4(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
 }
 __device__ __forceinline__ void st_x8(uint32_t taddr, const uint32_t (&v)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
@@ -147,6 +166,24 @@ __device__ __forceinline__ void st_x32(uint32_t taddr, const uint32_t (&v)[32]) 
 }
 #undef LRKV_R8
 #undef LRKV_W8
+
+// N consecutive columns, N in {2, 4, 8, 16, 32}.
+template <int N>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, uint32_t (&v)[N]) {
+  if constexpr (N == 2) ld_x2(taddr, v);
+  else if constexpr (N == 4) ld_x4(taddr, v);
+  else if constexpr (N == 8) ld_x8(taddr, v);
+  else if constexpr (N == 16) ld_x16(taddr, v);
+  else ld_x32(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+  if constexpr (N == 2) st_x2(taddr, v);
+  else if constexpr (N == 4) st_x4(taddr, v);
+  else if constexpr (N == 8) st_x8(taddr, v);
+  else if constexpr (N == 16) st_x16(taddr, v);
+  else st_x32(taddr, v);
+}
 
 }  // namespace tc
 }  // namespace lrkv
