@@ -192,6 +192,11 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu, x); }
 
+// Ring positions of tile j's K and V items in the issue order
+// K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.
+__device__ __forceinline__ int kidx(int j, int n) { (void)n; return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int vidx(int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * j + 1; }
+
 // At most kMaxRegs registers per thread: 384 x 144 leaves room on the SM for
 // one combine CTA, which then waits resident (programmatic dependent launch)
 // instead of being scheduled after the decode grid drains.
@@ -324,34 +329,36 @@ __global__ void __maxnreg__(kMaxRegs)
   const uint32_t tbase = *tmem_slot;
 
   // ============================================================ producer
+  // Items in the order K_0, K_1, V_0, K_2, V_1, ...: each K tile is requested
+  // a tile ahead of the V tile before it, so V tiles (consumed last) do not
+  // hold a slot while the next K tile could be landing.
   if (warp == 0) {
     const uint32_t bytes_k = L::KATOMS * 2048 + (p.has_bk ? 16 * LSPAN : 0);
     const uint32_t bytes_v = L::KATOMS * 2048 + (p.has_bv ? 16 * LSPAN : 0);
-    const int n_items = 2 * ntiles;
-    int id = (kbeg + lane < kend) ? id0 : INT_MIN;
-    int id_next = (kbeg + kTileBlocks + lane < kend) ? id1 : INT_MIN;
-    bool valid = false;
-    uint32_t vm = 0, nv = 0;
+    auto tile_ids = [&](int j) -> int {  // this lane's block id of tile j
+      const int kb = kbeg + j * kTileBlocks + lane;
+      return (lane < kTileBlocks && kb < kend) ? __ldg(btrow + kb) : INT_MIN;
+    };
+    int id_a = (kbeg + lane < kend) ? id0 : INT_MIN;                // tile of the next V item
+    int id_b = (kbeg + kTileBlocks + lane < kend) ? id1 : INT_MIN;  // tile of the next K item
+    int id_c = ntiles > 2 ? tile_ids(2) : INT_MIN;
     bool ok = true;
-    int it = 0;
-    for (; it < n_items; ++it) {
-      const int j = it >> 1, kind = it & 1, s = it % NS;
-      if (kind == 0) {
-        valid = id != INT_MIN;
-        if (valid && (id < 0 || id >= p.num_blocks)) {
-          report(p.status, LRKV_ERR_INDEX);
-          valid = false;
-        }
-        vm = __ballot_sync(0xffffffffu, valid);
-        nv = __popc(vm);
+    int issued = 0;
+    auto issue = [&](int idx, int kind, int id) -> bool {
+      bool valid = id != INT_MIN;
+      if (valid && (id < 0 || id >= p.num_blocks)) {
+        report(p.status, LRKV_ERR_INDEX);
+        valid = false;
       }
-      if (it >= NS) ok = warp_all(wait_ab(bar(B_EMPTY + s), ((it / NS) - 1) & 1, p.status, abort_flag));
-      if (!ok) break;
+      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+      const int s = idx % NS;
+      if (idx >= NS && !warp_all(wait_ab(bar(B_EMPTY + s), ((idx / NS) - 1) & 1, p.status, abort_flag)))
+        return false;
       const uint32_t dst = sbase + L::off_ring + s * L::STAGE;
       const uint32_t fb = bar(B_FULL + s);
       if (lane == 0) {
         if (kind == 0) kmask[s] = static_cast<int>(vm);  // published by the arrive (release)
-        mbar_arrive_expect_tx(fb, nv * (kind == 0 ? bytes_k : bytes_v));
+        mbar_arrive_expect_tx(fb, __popc(vm) * (kind == 0 ? bytes_k : bytes_v));
       }
       __syncwarp();
       if (valid) {
@@ -362,18 +369,29 @@ __global__ void __maxnreg__(kMaxRegs)
         if (kind == 0 ? p.has_bk : p.has_bv)
           tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, 0, (id * 2 + kind) * kBlock, fb);
       }
-      if (kind == 1) {  // block ids: tile j + 1 ready, tile j + 2 requested
-        const int kb = kbeg + (j + 2) * kTileBlocks + lane;
-        id = id_next;
-        id_next = (lane < kTileBlocks && kb < kend) ? __ldg(btrow + kb) : INT_MIN;
+      return true;
+    };
+    ok = issue(kidx(0, ntiles), 0, id_a);
+    issued = ok ? 1 : 0;
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if (j + 1 < ntiles) {
+        ok = issue(kidx(j + 1, ntiles), 0, id_b);
+        if (!ok) break;
+        ++issued;
       }
+      ok = issue(vidx(j, ntiles), 1, id_a);
+      if (!ok) break;
+      ++issued;
+      id_a = id_b;
+      id_b = id_c;
+      id_c = j + 3 < ntiles ? tile_ids(j + 3) : INT_MIN;
     }
     if (!ok && lane == 0) *abort_flag = 1;
     // No copy may still be landing when the CTA leaves: wait for the last
-    // item issued into each slot.
+    // item issued into each slot (items are issued in index order).
     for (int s = 0; s < NS; ++s) {
-      const int last = it - 1 - ((it - 1 - s) % NS + NS) % NS;
-      if (last >= 0 && last < it) wait_ab(bar(B_FULL + s), (last / NS) & 1, p.status, nullptr);
+      const int last = issued - 1 - ((issued - 1 - s) % NS + NS) % NS;
+      if (last >= 0 && last < issued) wait_ab(bar(B_FULL + s), (last / NS) & 1, p.status, nullptr);
     }
   } else {
     // ================================================ prologue (warps 1-11)
@@ -520,8 +538,8 @@ __global__ void __maxnreg__(kMaxRegs)
       bool ok = true;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
-        const int s = (2 * j) % NS;
-        ok = warp_all(wait_ab(bar(B_FULL + s), ((2 * j) / NS) & 1, p.status, abort_flag));
+        const int ki = kidx(j, ntiles), s = ki % NS;
+        ok = warp_all(wait_ab(bar(B_FULL + s), (ki / NS) & 1, p.status, abort_flag));
         if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
         if (!ok) break;
         tc::fence_after();
@@ -551,8 +569,8 @@ __global__ void __maxnreg__(kMaxRegs)
       bool ok = true;
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
-        const int v = (2 * j + 1) % NS, b = j & 1;
-        ok = warp_all(wait_ab(bar(B_FULL + v), ((2 * j + 1) / NS) & 1, p.status, abort_flag));
+        const int vi = vidx(j, ntiles), v = vi % NS, b = j & 1;
+        ok = warp_all(wait_ab(bar(B_FULL + v), (vi / NS) & 1, p.status, abort_flag));
         if (ok) ok = warp_all(wait_ab(bar(B_PF + b), (j >> 1) & 1, p.status, abort_flag));
         if (!ok) break;
         tc::fence_after();
@@ -632,12 +650,13 @@ __global__ void __maxnreg__(kMaxRegs)
       const int wch = use_w ? max(0, min(WCH, (nw - gq * RH * R + 31) / 32)) : 0;
       bool failed = false;
       for (int j = 0; j < ntiles; ++j) {
-        const int s = (2 * j) % NS, v = (2 * j + 1) % NS, b = j & 1;
+        const int ki = kidx(j, ntiles), vi = vidx(j, ntiles);
+        const int s = ki % NS, v = vi % NS, b = j & 1;
         const int t0 = (kbeg + j * kTileBlocks) * kBlock;
         // ---- scores of this lane's token, own rows
         if (!failed && use_w) failed = !wait_ab(bar(B_WF), j & 1, p.status, abort_flag);
         if (!failed) failed = !wait_ab(bar(B_SF), j & 1, p.status, abort_flag);
-        if (!failed) failed = !wait_ab(bar(B_FULL + s), ((2 * j) / NS) & 1, p.status, abort_flag);
+        if (!failed) failed = !wait_ab(bar(B_FULL + s), (ki / NS) & 1, p.status, abort_flag);
         tc::fence_after();
         const int vmask = kmask[s];  // blocks of this tile that were loaded (valid ids inside the split)
         float sc[RH];
@@ -781,7 +800,7 @@ __global__ void __maxnreg__(kMaxRegs)
         // bad id, hold stale memory: zero their V and L_V rows so that P = 0
         // there cannot meet a NaN (warpgroup 0: V atom 0, warpgroup 1: the rest)
         if (vmask != (1 << kTileBlocks) - 1 || t0 + kBT > len) {
-          if (!failed) failed = !wait_ab(bar(B_FULL + v), ((2 * j + 1) / NS) & 1, p.status, abort_flag);
+          if (!failed) failed = !wait_ab(bar(B_FULL + v), (vi / NS) & 1, p.status, abort_flag);
           if (!tok_ok) {
             uint8_t* vst = smem + L::off_ring + v * L::STAGE;
             if (gq == 0) {
