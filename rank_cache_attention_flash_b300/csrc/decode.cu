@@ -136,20 +136,21 @@ struct DL {
 
 enum : int {
   B_FULL = 0,    // [4] ring slot full (TMA bytes)
-  B_EMPTY = 4,   // [4] ring slot consumed: 8 token warps + the MMA commit that read it
+  B_EMPTY = 4,   // [4] ring slot consumed: 8 token warps + two MMA commits (S_b twice; O^T and O_lr^T)
   B_UF = 8,      // U of the next tile written (8 token warps)
   B_WF = 9,      // W complete (commit)
   B_SF = 10,     // S_b complete (commit)
   B_WR = 11,     // W and S_b read out (8 token warps)
   B_PF = 12,     // [2] P^T written, O rescaled (8 token warps)
-  B_PR = 14,     // [2] P V of that buffer complete (commit)
+  B_PR = 14,     // [2] O^T and O_lr^T MMAs of that P buffer complete (two commits)
   B_DRAIN = 16,  // [4] per MMA warp, on abort: its MMAs have completed
   B_COUNT = 20
 };
 
 __device__ __forceinline__ uint32_t bar_count(int i) {
-  if (i >= B_EMPTY && i < B_EMPTY + 4) return 9;
+  if (i >= B_EMPTY && i < B_EMPTY + 4) return 10;
   if (i == B_UF || i == B_WR || i == B_PF || i == B_PF + 1) return 8;
+  if (i == B_PR || i == B_PR + 1) return 2;
   return 1;
 }
 
@@ -501,13 +502,16 @@ __global__ void __maxnreg__(kMaxRegs)
     named_bar_sync(1, kThreads - 32);
 
     if (warp == 1) {
-      // ======================================================= W issuer
+      // ================================== W issuer, O_lr^T issuer
+      // Iteration j issues W_j = U_j G^T, then O_lr^T += L_V^T P^T of tile j - 1
+      // (two issuing warps share the P V work of a tile).
+      const uint32_t idw = tc::idesc_f16(128, nw, false, false, false);
+      const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
+      const uint64_t gdesc = tc::sdesc(sbase + L::off_g, 16, 1024, 2);
       bool ok = true;
       int issued = 0;
-      if (use_w) {
-        const uint32_t idw = tc::idesc_f16(128, nw, false, false, false);
-        const uint64_t gdesc = tc::sdesc(sbase + L::off_g, 16, 1024, 2);
-        for (int j = 0; j < ntiles; ++j) {
+      for (int j = 0; j <= ntiles; ++j) {
+        if (use_w && j < ntiles) {
           ok = warp_all(wait_ab(bar(B_UF), j & 1, p.status, abort_flag));
           if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
           if (!ok) break;
@@ -518,6 +522,28 @@ __global__ void __maxnreg__(kMaxRegs)
               tc::mma_ts(tbase + W_COL, tbase + U_COL + 8 * k,
                          gdesc + (((k >> 2) * L::GAMMA_ATOM + (k & 3) * 32) >> 4), idw, k > 0 ? 1u : 0u);
             tc::commit(bar(B_WF));
+          }
+          __syncwarp();
+          ++issued;
+        }
+        if (p.has_bv && j > 0) {
+          const int jj = j - 1, vi = vidx(jj, ntiles), v = vi % NS, b = jj & 1;
+          ok = warp_all(wait_ab(bar(B_FULL + v), (vi / NS) & 1, p.status, abort_flag));
+          if (ok) ok = warp_all(wait_ab(bar(B_PF + b), (jj >> 1) & 1, p.status, abort_flag));
+          if (!ok) break;
+          tc::fence_after();
+          if (tc::elect_one()) {
+            const uint32_t vst = sbase + L::off_ring + v * L::STAGE;
+            // L_V^T: M = rank (MN-major, swizzled by the row span), K = tokens
+            const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
+            const uint64_t pdesc = tc::sdesc(sbase + L::off_p + b * L::PB, 16, 1024, 2);
+#pragma unroll
+            for (int k = 0; k < kBT / 16; ++k)
+              tc::mma_ss(tbase + OL_COL, lvdesc + ((k * 16 * LSPAN) >> 4),
+                         pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
+                         (jj > 0 || k > 0) ? 1u : 0u);
+            tc::commit(bar(B_PR + b));
+            tc::commit(bar(B_EMPTY + v));
           }
           __syncwarp();
           ++issued;
@@ -551,6 +577,7 @@ __global__ void __maxnreg__(kMaxRegs)
                        qdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ids, k > 0 ? 1u : 0u);
           tc::commit(bar(B_SF));
           tc::commit(bar(B_EMPTY + s));
+          tc::commit(bar(B_EMPTY + s));  // the slot's second MMA arrival (K items have one reader)
         }
         __syncwarp();
         ++issued;
@@ -564,7 +591,7 @@ __global__ void __maxnreg__(kMaxRegs)
         }
       }
     } else if (warp == 3) {
-      // ======================================= O^T / O_lr^T issuer
+      // ================================================ O^T issuer
       const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
       bool ok = true;
       int issued = 0;
@@ -578,18 +605,18 @@ __global__ void __maxnreg__(kMaxRegs)
           const uint32_t vst = sbase + L::off_ring + v * L::STAGE;
           // V^T: M = head dims (MN-major; 64-dim atoms ATOM bytes apart), K = tokens
           const uint64_t vdesc = tc::sdesc(vst + L::LR_TILE, L::ATOM, 1024, 2);
-          // L_V^T: M = rank (MN-major, swizzled by the row span), K = tokens
-          const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
           const uint64_t pdesc = tc::sdesc(sbase + L::off_p + b * L::PB, 16, 1024, 2);
 #pragma unroll
-          for (int k = 0; k < kBT / 16; ++k) {
-            const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-            const uint64_t pk = pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4);
-            tc::mma_ss(tbase + OT_COL, vdesc + ((k * 16 * 128) >> 4), pk, ido, acc);
-            if (p.has_bv) tc::mma_ss(tbase + OL_COL, lvdesc + ((k * 16 * LSPAN) >> 4), pk, ido, acc);
-          }
+          for (int k = 0; k < kBT / 16; ++k)
+            tc::mma_ss(tbase + OT_COL, vdesc + ((k * 16 * 128) >> 4),
+                       pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
+                       (j > 0 || k > 0) ? 1u : 0u);
           tc::commit(bar(B_PR + b));
           tc::commit(bar(B_EMPTY + v));
+          if (!p.has_bv) {  // no O_lr^T issuer: both arrivals from here
+            tc::commit(bar(B_PR + b));
+            tc::commit(bar(B_EMPTY + v));
+          }
         }
         __syncwarp();
         ++issued;
