@@ -37,7 +37,7 @@
 //   warps 4-7   one thread per token of the tile: U for the next tile, scores,
 //               online softmax (rescale decided by a block-wide vote), P^T,
 //               and at the end the split partial (m, l, O, O_lr)
-// combine_kernel (programmatic dependent launch) merges the splits and
+// combine_kernel (launched after it on the same stream) merges the splits and
 // applies B_V.
 #include <math_constants.h>
 
@@ -52,7 +52,6 @@ namespace lrkv {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kMaxRegs = 144;
 constexpr int kBT = 128;                   // tokens per tile (tcgen05 M)
 constexpr int kTileBlocks = kBT / kBlock;  // 8 blocks per tile
 constexpr int kMaxRows = 16;               // query rows per item (tcgen05 N of S_b, O^T)
@@ -198,11 +197,8 @@ __device__ __forceinline__ bool warp_all(bool x) { return __all_sync(0xffffffffu
 __device__ __forceinline__ int kidx(int j, int n) { (void)n; return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int vidx(int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * j + 1; }
 
-// At most kMaxRegs registers per thread: 384 x 144 leaves room on the SM for
-// one combine CTA, which then waits resident (programmatic dependent launch)
-// instead of being scheduled after the decode grid drains.
 template <int D, int R>
-__global__ void __maxnreg__(kMaxRegs)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p,
                   const __grid_constant__ CUtensorMap tm_base,
                   const __grid_constant__ CUtensorMap tm_lr) {
@@ -214,9 +210,6 @@ __global__ void __maxnreg__(kMaxRegs)
   constexpr int RH = L::RH;
   constexpr int WCH = RH * R / 32;  // W chunks (32 columns) per token warpgroup
   constexpr int QH = HALF / 32;     // 16-pair rotation chunks per token warpgroup
-
-  // The combine kernel may be scheduled now; it waits for this grid to finish.
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -907,6 +900,8 @@ __global__ void __maxnreg__(kMaxRegs)
 // Merges the splits of each (query, head) with log-sum-exp weights, applies
 // the reordered V term O_lr B_V,a once, divides by l and stores bf16.
 // One CTA per (query, head); thread t owns column t of the partial rows.
+// The (m, l) pairs, column t of up to kCombineBatch splits and the B_V rows
+// are requested together, so a merge of that many splits is one round trip.
 struct CombineParams {
   const float* part_ml;
   const float* part_o;
@@ -917,39 +912,60 @@ struct CombineParams {
   int num_queries, Hq, Hkv, g, n_splits, n_adapters, has_bv;
 };
 
+constexpr int kCombineBatch = 32;  // splits requested per round
+
 template <int D, int R>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
-  constexpr int NCOL = D + R;
-  __shared__ float w_s[256];
-  __shared__ float red[8];
+struct CombineShape {
+  static constexpr int NCOL = D + R;
+  static constexpr int NT = (NCOL + 31) / 32 * 32;  // threads: one per column
+  static constexpr int NW = NT / 32;
+};
+
+template <int D, int R>
+__global__ void __launch_bounds__(CombineShape<D, R>::NT) combine_kernel(const __grid_constant__ CombineParams p) {
+  using C = CombineShape<D, R>;
+  constexpr int NCOL = C::NCOL, NT = C::NT, NW = C::NW;
+  __shared__ float w_s[256];  // the plan keeps n_splits <= 256
+  __shared__ float red[NW];
   __shared__ float olr[R];
-  // wait until the decode grid has finished and its partials are visible
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t pair = blockIdx.x;
   const int n = static_cast<int>(pair / p.Hq), m = static_cast<int>(pair % p.Hq);
   const int S = p.n_splits;
   const int a = __ldg(p.adapter_ids + n);
   const bool bad = a < -1 || a >= p.n_adapters;
+  const bool use_lr = p.has_bv && a >= 0 && !bad;
   if (bad && tid == 0 && m == 0) report(p.status, LRKV_ERR_INDEX);
   const float* ml = p.part_ml + pair * S * 2;
+  const float* po = p.part_o + pair * S * NCOL + tid;
+  // one round: (m, l) of split tid, column tid of the first splits, B_V rows
+  float2 mlv = make_float2(-CUDART_INF_F, 0.f);
+  if (tid < S) mlv = *reinterpret_cast<const float2*>(ml + 2 * tid);
+  float pv[kCombineBatch];
+#pragma unroll
+  for (int s = 0; s < kCombineBatch; ++s) pv[s] = (tid < NCOL && s < S) ? po[static_cast<int64_t>(s) * NCOL] : 0.f;
+  const __nv_bfloat16* bvp = p.B_V + (static_cast<int64_t>(use_lr ? a : 0) * R * p.Hkv + m / p.g) * D + tid;
+  float bv[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) bv[k] = (use_lr && tid < D) ? __bfloat162float(bvp[static_cast<int64_t>(k) * p.Hkv * D]) : 0.f;
   // max over splits
-  float M = -CUDART_INF_F;
-  for (int s = tid; s < S; s += 256) M = fmaxf(M, __ldg(ml + 2 * s));
+  float M = mlv.x;
+  for (int s = tid + NT; s < S; s += NT) M = fmaxf(M, ml[2 * s]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   if (lane == 0) red[wid] = M;
   __syncthreads();
   M = red[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
+  for (int w = 1; w < NW; ++w) M = fmaxf(M, red[w]);
   __syncthreads();
+  // weights and the softmax denominator
   float Ls = 0.f;
-  for (int s = tid; s < S; s += 256) {
-    const float ms = __ldg(ml + 2 * s);
-    const float w = (M == -CUDART_INF_F || ms == -CUDART_INF_F) ? 0.f : exp2f(ms - M);
+  for (int s = tid; s < S; s += NT) {
+    const float2 x = s == tid ? mlv : *reinterpret_cast<const float2*>(ml + 2 * s);
+    const float w = (M == -CUDART_INF_F || x.x == -CUDART_INF_F) ? 0.f : exp2f(x.x - M);
     w_s[s] = w;
-    Ls += w * __ldg(ml + 2 * s + 1);
+    Ls = fmaf(w, x.y, Ls);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
@@ -957,21 +973,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   __syncthreads();
   Ls = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) Ls += red[w];
-  const bool use_lr = p.has_bv && a >= 0 && !bad;
+  for (int w = 0; w < NW; ++w) Ls += red[w];
   float v = 0.f;
   if (tid < NCOL) {
-    const float* po = p.part_o + pair * S * NCOL + tid;
-#pragma unroll 8
-    for (int s = 0; s < S; ++s) v += w_s[s] * __ldg(po + static_cast<int64_t>(s) * NCOL);
+#pragma unroll
+    for (int s = 0; s < kCombineBatch; ++s)
+      if (s < S) v = fmaf(w_s[s], pv[s], v);
+    // further splits: a batch of loads in flight, then its products
+    for (int s0 = kCombineBatch; s0 < S; s0 += kCombineBatch) {
+#pragma unroll
+      for (int s = 0; s < kCombineBatch; ++s) pv[s] = s0 + s < S ? po[static_cast<int64_t>(s0 + s) * NCOL] : 0.f;
+#pragma unroll
+      for (int s = 0; s < kCombineBatch; ++s)
+        if (s0 + s < S) v = fmaf(w_s[s0 + s], pv[s], v);
+    }
     if (tid >= D) olr[tid - D] = use_lr ? v : 0.f;
   }
   __syncthreads();
   if (tid < D) {
     if (use_lr) {
-      const __nv_bfloat16* bv = p.B_V + static_cast<int64_t>(a) * R * p.Hkv * D + (m / p.g) * D + tid;
-#pragma unroll 8
-      for (int k = 0; k < R; ++k) v = fmaf(olr[k], __bfloat162float(bv[static_cast<int64_t>(k) * p.Hkv * D]), v);
+#pragma unroll
+      for (int k = 0; k < R; ++k) v = fmaf(olr[k], bv[k], v);
     }
     const float inv = (Ls > 0.f && !bad) ? 1.f / Ls : 0.f;
     p.out[pair * D + tid] = __float2bfloat16_rn(v * inv);
@@ -1043,17 +1065,10 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   c.has_bv = a.B_V != nullptr;
   const int64_t pairs = static_cast<int64_t>(a.num_queries) * cfg.n_q_heads;
   if (pairs > 0) {
-    cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(static_cast<unsigned>(pairs));
-    lc.blockDim = dim3(256);
-    lc.dynamicSmemBytes = 0;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, combine_kernel<D, R>, c) != cudaSuccess) return LRKV_ERR_CUDA;
+    // A plain stream-ordered launch: on this part, waiting resident on the
+    // decode grid (programmatic dependent launch) released later than this.
+    combine_kernel<D, R><<<static_cast<unsigned>(pairs), CombineShape<D, R>::NT, 0, stream>>>(c);
+    if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
   }
   return LRKV_OK;
 }
