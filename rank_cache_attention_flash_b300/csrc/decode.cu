@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NS = L::NS;
   constexpr int RH = L::RH;
   constexpr int WCH = RH * R / 32;  // W chunks (32 columns) per token warpgroup
-  constexpr int QH = HALF / 32;     // 16-pair rotation chunks per token warpgroup
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -282,6 +281,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.part_ml[2 * rec_of(tid) + 1] = 0.f;
     }
     return;
+  }
+
+  // token warpgroups: e^{i delta theta_j} of this lane's token offset delta,
+  // for the warpgroup's rotation pairs, computed while the setup loads and the
+  // tensor-memory allocation are in flight (stored to TMEM after the barrier)
+  constexpr int QH = HALF / 32;  // 16-pair chunks per token warpgroup
+  uint32_t dvr[QH][32];
+  if (warp >= 4) {
+    const int jb0 = ((warp - 4) >> 2) * (HALF / 2);
+    const int dl = (warp & 3) * 32 + lane;
+#pragma unroll
+    for (int q4 = 0; q4 < QH; ++q4)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 cs = rope_cos_sin_fast(dl, p.freqs.hi[jb0 + 16 * q4 + i], p.freqs.lo[jb0 + 16 * q4 + i]);
+        dvr[q4][2 * i] = __float_as_uint(cs.x);
+        dvr[q4][2 * i + 1] = __float_as_uint(cs.y);
+      }
   }
 
   // warps 1-3: this item's adapter ids and Q rows, requested before the setup barrier
@@ -416,20 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (((c & 7) ^ (r & 7)) << 4)) = qv[u];
       }
     } else {
-      // e^{i delta theta_j} of this lane's token offset delta = tt, for this
-      // warpgroup's pairs, in TMEM (column 2j: cos, 2j + 1: sin)
+      // the rotation table into TMEM (column 2j: cos, 2j + 1: sin)
 #pragma unroll
-      for (int q4 = 0; q4 < QH; ++q4) {
-        const int j0 = jb + 16 * q4;
-        uint32_t dv[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 cs = rope_cos_sin_fast(tt, p.freqs.hi[j0 + i], p.freqs.lo[j0 + i]);
-          dv[2 * i] = __float_as_uint(cs.x);
-          dv[2 * i + 1] = __float_as_uint(cs.y);
-        }
-        tc::st_x32(tl + DT_COL + 2 * j0, dv);
-      }
+      for (int q4 = 0; q4 < QH; ++q4) tc::st_x32(tl + DT_COL + 2 * (jb + 16 * q4), dvr[q4]);
       tc::wait_st();
       // base angles e^{i t0 theta_j} of tiles 0 and 1 (this warpgroup's pairs)
       const int t00 = kbeg * kBlock;
@@ -455,17 +461,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a >= 0) {
           const uint4* brow = reinterpret_cast<const uint4*>(
               p.B_K + ((static_cast<int64_t>(a) * R + k) * p.Hkv + head) * D);
-          uint4 bv[D / 8];
+          const int gr = row0 + r;
+          const uint4* qrow = reinterpret_cast<const uint4*>(
+              p.q + (static_cast<int64_t>(qs + gr / p.g) * p.Hq + head * p.g + gr % p.g) * D);
+          uint4 bv[D / 8], qv2[D / 8];
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) bv[c] = __ldg(brow + c);
+          for (int c = 0; c < D / 8; ++c) {
+            bv[c] = __ldg(brow + c);
+            qv2[c] = __ldg(qrow + c);
+          }
 #pragma unroll
           for (int jc = 0; jc < HALF / 8; ++jc) {
             const int c2 = HALF / 8 + jc;
-            const uint4 q1 = *reinterpret_cast<const uint4*>(
-                smem + L::off_q + (jc >> 3) * (kMaxRows * 128) + r * 128 + (((jc & 7) ^ (r & 7)) << 4));
-            const uint4 q2 = *reinterpret_cast<const uint4*>(
-                smem + L::off_q + (c2 >> 3) * (kMaxRows * 128) + r * 128 + (((c2 & 7) ^ (r & 7)) << 4));
-            const uint32_t qa[4] = {q1.x, q1.y, q1.z, q1.w}, qb[4] = {q2.x, q2.y, q2.z, q2.w};
+            const uint32_t qa[4] = {qv2[jc].x, qv2[jc].y, qv2[jc].z, qv2[jc].w};
+            const uint32_t qb[4] = {qv2[c2].x, qv2[c2].y, qv2[c2].z, qv2[c2].w};
             const uint32_t ba[4] = {bv[jc].x, bv[jc].y, bv[jc].z, bv[jc].w};
             const uint32_t bb[4] = {bv[c2].x, bv[c2].y, bv[c2].z, bv[c2].w};
             uint32_t gc[4], gs[4];
