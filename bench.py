@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 DEFAULT_CONFIG = "shared_decode_llama8b"
 METRIC = "LoRA-KV attention decode tok/s & GB/s (% of HBM), prefill TFLOP/s (% peak)"
 FLUSH_BYTES = 512 << 20
-KERNEL_SOURCES = {"decode": ["decode.cu", "lrkv_device.cuh"],
+KERNEL_SOURCES = {"decode": ["decode.cu", "lrkv_device.cuh", "tcgen05.cuh"],
                   "prefill": ["prefill.cu", "lrkv_device.cuh", "tcgen05.cuh"],
                   "append": ["append.cu", "lrkv_device.cuh"]}
 
