@@ -99,6 +99,19 @@ def test_decode_many_agents_one_context(cuda_lib):
     assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case, cache="bf16"), BF16_TOL)
 
 
+def test_decode_many_splits(cuda_lib):
+    """One long context on two kv heads: the split plan takes more than 32
+    splits of the context (a ragged last tile included), so the combine merges
+    in several rounds; base-only and adapter rows together."""
+    sh = I.Shape(1024, 8, 2, 64, 16, 2, 10000.0, "bf16", 1.0, 1 / math.sqrt(1024), 1 / math.sqrt(1024),
+                 1 / math.sqrt(16), 1.0)
+    seqs = [I.Seq(0, 0, 0, 12000, 0, -1, "context")]
+    case = I._build("many_splits", sh, 0, seqs, [(0, 0), (0, 1), (0, -1)], [], False)
+    g, res = _run(case)
+    assert g.device_status() == 0
+    assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case, cache="bf16"), BF16_TOL)
+
+
 def test_decode_without_adapter_factors(cuda_lib):
     """B_K = NULL (adapter on V only), then B_V = NULL (adapter on K only)."""
     case = I.shared_decode(n=260)
