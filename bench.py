@@ -1,20 +1,31 @@
 #!/usr/bin/env python
 """Benchmark of the LoRA-KV attention hot path on B300.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl lrkv|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config all|NAME]
+                  [--impl lrkv|reference] [--no-bk]
 
-One step = one pass of the hot path over one batch of the named workload,
-inputs already resident in HBM: for the decode workloads the decode call
-(split-KV attention + combine); for the prefill workload the append of the new
-chunk tokens plus the causal prefill; for the mixed batch append + decode +
-prefill. L2 is flushed (a 512 MiB write) before every step, outside the timed
+One step = one pass of the hot path over one batch of a workload, inputs
+already resident in HBM: for the decode workloads the decode call; for the
+prefill workload the append of the new chunk tokens plus the causal prefill;
+for the mixed batch append + decode + prefill. With ``--config all`` (the
+default) every bf16 workload is timed in turn in one process and reported under
+``workloads.<name>``; the line's headline fields (value, roofline, e2e,
+cpu_baseline) are those of the long paged decode (16 x 32768 tokens, rank 64),
+and ``prefill`` carries the prefill kernel's TFLOP/s against the burst and the
+sustained bf16 peak.
+
+Timing: L2 is flushed (a 512 MiB write) before every step, outside the timed
 events; each part of the step is captured once into a CUDA graph (the same
 library calls, the same kernels) and replayed, each replay bracketed by CUDA
 events on the launching stream; the K steps are bracketed by a barrier and a
-device synchronize. The e2e figure instead calls the public API directly,
-host buffers and copies included. Rank 0 prints one
-JSON line. ``--impl reference`` times the fp64 CPU oracle instead (on the host
-cores, rank 0 only).
+device synchronize, and the step time is the max over ranks. The e2e figure
+calls the public API directly: per step one host-to-device copy of the step's
+packed inputs from pinned memory, the library calls, one device-to-host copy
+of the packed outputs. Under torchrun each rank holds its own disjoint share
+of the contexts (weak scaling; no collective on the data path). Rank 0 prints
+one JSON line. ``--impl reference`` times the fp64 CPU oracle instead (on the
+host cores, rank 0 only). ``--no-bk`` runs attention with B_K = NULL (no K
+adapter term, no rebuild): a diagnostic of the rebuild's cost, marked as such.
 """
 from __future__ import annotations
 
@@ -31,7 +42,11 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_CONFIG = "shared_decode_llama8b"
+DEFAULT_CONFIG = "all"
+ALL_WORKLOADS = ["shared_decode_llama8b", "prefill_chunk_llama8b", "long_decode_ministral8b",
+                 "mixed_batch_qwen3_1p7b"]
+HEADLINE = "long_decode_ministral8b"
+PREFILL_HEADLINE = "prefill_chunk_llama8b"
 METRIC = "LoRA-KV attention decode tok/s & GB/s (% of HBM), prefill TFLOP/s (% peak)"
 FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = {"decode": ["decode.cu", "lrkv_device.cuh", "tcgen05.cuh"],
@@ -318,7 +333,8 @@ def run_reference(args):
         return
     from rank_cache_attention_flash_b300 import inputs as I
 
-    case = I.FULL[args.config]()
+    config = HEADLINE if args.config == "all" else args.config
+    case = I.FULL[config]()
     model = workload_model(case)
     budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
     # per-step sample: one query (or chunk rows) over a leading fraction of its
@@ -370,7 +386,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.config},
+            "data": "synthetic", "config": {"workload": config},
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
                              "sample": f"per step: one query over the leading {nt} of its {L_full} keys "
                                        f"(counted as {nt}/{L_full} of a query)"},
@@ -379,65 +395,49 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------- main
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--config", default=DEFAULT_CONFIG)
-    ap.add_argument("--impl", default="lrkv", choices=["lrkv", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=200)
-    args = ap.parse_args()
-    assert args.warmup >= 3, "at least 3 warm-up steps"
-    if args.impl == "reference":
-        return run_reference(args)
+# Kernels of this library that one call of each part launches (bf16 path).
+LAUNCHES_PER_CALL = {"append": 1, "decode": 2, "prefill": 1}
 
+
+def cache_bytes(case):
+    """LRKV cache bytes vs per-agent full caches over the decode contexts."""
+    sh = case.shape
+    es = 4 if sh.dtype == "fp32" else 2
+    lr = full = 0
+    if case.dec_q.shape[0]:
+        qs = case.dec_q_start.tolist()
+        for c, s in enumerate(case.dec_ctx):
+            L = case.seqs[s].total_len
+            readers = qs[c + 1] - qs[c]
+            full += readers * L * sh.n_kv_heads * sh.head_dim * 2 * es
+            lr += L * (sh.n_kv_heads * sh.head_dim * 2 + 2 * sh.rank) * es
+    return {"lrkv": lr, "per_agent_full": full, "saving": full / lr} if full else None
+
+
+def time_workload(name, args, world, rank, dev, pk):
+    """Times one workload on this rank. Returns its report entry."""
     import torch
-    import torch.distributed as dist
 
     from rank_cache_attention_flash_b300 import inputs as I
-    from rank_cache_attention_flash_b300 import lrkv
     from rank_cache_attention_flash_b300.harness import GpuCase
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    lrkv.load()
-
-    case = I.FULL[args.config]()
+    case = I.build_shard(name, world, rank)
     model = workload_model(case)
-    g = GpuCase(case, device=dev)
+    g = GpuCase(case, device=dev, no_bk=args.no_bk)
     g.setup()
     if "prefill" in model and "append" in model and "decode" not in model:
         kinds = ["append", "prefill"]
     else:
         kinds = [k for k in ("append", "decode", "prefill") if k in model]
     dominant = "decode" if "decode" in model else "prefill"
-    launches_per_call = {"append": 1, "decode": 1 if case.shape.dtype == "fp32" else 2, "prefill": 1}
-
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     calls = {"append": g.step_append, "decode": g.decode, "prefill": g.prefill}
 
-    def one_step(evs=None, replay=False):
-        for k in kinds:
-            if evs is not None:
-                evs[k][0].record(stream)
-            if replay:
-                graphs[k].replay()
-            else:
-                calls[k]()
-            if evs is not None:
-                evs[k][1].record(stream)
-
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
-        one_step()
+        for k in kinds:
+            calls[k]()
     torch.cuda.synchronize()
     # Each part of the step is captured once into a CUDA graph and replayed in
     # the timed loop: the replay keeps host launch latency out of the device
@@ -458,155 +458,192 @@ def main():
            for _ in range(K)]
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
+        import torch.distributed as dist
+
         dist.barrier()
     torch.cuda.synchronize()
     host_t0 = time.perf_counter()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev.index) as clk:
         for i in range(K):
             flush.fill_(i & 0xFF)
             step_ev[i][0].record(stream)
-            one_step(evs[i], replay=True)
+            for k in kinds:
+                evs[i][k][0].record(stream)
+                graphs[k].replay()
+                evs[i][k][1].record(stream)
             step_ev[i][1].record(stream)
         torch.cuda.synchronize()
     host_dt = time.perf_counter() - host_t0
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    part_ms = {k: [e[k][0].elapsed_time(e[k][1]) for e in evs] for k in kinds}
+    part_ms = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in evs) / K for k in kinds}
     ms_per_step = reduce_step_time(sum(step_ms), K, world, dev)
     status = g.device_status()
+    del graphs
 
-    # ---- end to end through the public API with host buffers
-    e2e = None
-    if "decode" in model and "prefill" not in model:
-        q_host = case.dec_q.pin_memory()
-        small = [t.pin_memory() for t in (case.dec_q_start, case.dec_adapter, case.dec_lens())]
-        dsts = [g.dec_q_start, g.dec_adapter, g.dec_lens]
-        out_host = torch.empty(g.dec_out.shape, dtype=g.dec_out.dtype).pin_memory()
-        h2d = q_host.numel() * q_host.element_size() + sum(t.numel() * t.element_size() for t in small)
-        d2h = out_host.numel() * out_host.element_size()
-        e_ms = []
-        for i in range(args.e2e_steps + 5):
-            flush.fill_(i & 0xFF)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.dec_q.copy_(q_host, non_blocking=True)
-            for s_, d_ in zip(small, dsts):
-                d_.copy_(s_, non_blocking=True)
-            g.decode()
-            out_host.copy_(g.dec_out, non_blocking=True)
-            b.record(stream)
-            b.synchronize()
-            if i >= 5:
-                e_ms.append(a.elapsed_time(b))
-        e2e_ms = sum(e_ms) / len(e_ms)
-        e2e = {"value": world * model["decode"]["units"] / (e2e_ms / 1e3), "unit": "tok/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
-    else:
-        # host buffers for the step's new hidden states and queries, outputs back
-        srcs, dsts = [], []
-        if g.n_step_tokens:
-            srcs += [g.step_X.cpu().pin_memory(), g.step_pos.cpu().pin_memory(), g.step_rows.cpu().pin_memory()]
-            dsts += [g.step_X, g.step_pos, g.step_rows]
-        if g.n_dec:
-            srcs.append(case.dec_q.pin_memory())
-            dsts.append(g.dec_q)
-        if g.n_pre:
-            srcs.append(case.pre_q.pin_memory())
-            dsts.append(g.pre_q)
-        outs = [(t, torch.empty(t.shape, dtype=t.dtype).pin_memory())
-                for t in ([g.dec_out] if g.n_dec else []) + ([g.pre_out] if g.n_pre else [])]
-        h2d = sum(t.numel() * t.element_size() for t in srcs)
-        d2h = sum(h.numel() * h.element_size() for _, h in outs)
-        e_ms = []
-        for i in range(min(args.e2e_steps, 50) + 3):
-            flush.fill_(i & 0xFF)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for s_, d_ in zip(srcs, dsts):
-                d_.copy_(s_, non_blocking=True)
-            one_step()
-            for d_, h_ in outs:
-                h_.copy_(d_, non_blocking=True)
-            b.record(stream)
-            b.synchronize()
-            if i >= 3:
-                e_ms.append(a.elapsed_time(b))
-        e2e_ms = sum(e_ms) / len(e_ms)
-
-    pk = peaks()
-    dom_ms = sum(part_ms[dominant]) / K
-    dm = model[dominant]
-    if dominant == "decode":
-        achieved = dm["bytes"] / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
-                "kernel": "lrkv_attn_decode (decode_kernel + combine_kernel)",
-                "algorithmic_bytes_per_launch": dm["bytes"], "launch_ms": dom_ms,
-                "traffic": committed_traffic(args.config, "decode")}
-    else:
-        achieved = dm["flops"] / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"], "peak_source": pk["source"] + " (burst)",
-                "kernel": "lrkv_attn_prefill (prefill_kernel)",
-                "algorithmic_flops_per_launch": dm["flops"], "launch_ms": dom_ms,
-                "traffic": committed_traffic(args.config, "prefill")}
+    # ---- end to end through the public API: one packed copy in, one out
+    e_ms = []
+    n_e2e = min(args.e2e_steps, 50 if dominant == "prefill" or len(kinds) > 1 else args.e2e_steps)
+    for i in range(n_e2e + 3):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.upload_inputs()
+        for k in kinds:
+            calls[k]()
+        g.download_outputs()
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e_ms.append(a.elapsed_time(b))
+    e2e_ms = reduce_step_time(sum(e_ms), len(e_ms), world, dev)
 
     if dominant == "decode" and "prefill" not in model:
-        unit, value = "tok/s", job_throughput(dm["units"], world, ms_per_step)
+        unit = "tok/s"
+        work = model["decode"]["units"]
     elif "decode" not in model:
         unit = "TFLOP/s"
-        value = world * (model["prefill"]["flops"] + model.get("append", {"flops": 0})["flops"]) / (ms_per_step / 1e3) / 1e12
+        work = (model["prefill"]["flops"] + model.get("append", {"flops": 0})["flops"]) / 1e12
     else:
         unit = "tok/s"
-        value = job_throughput(model["decode"]["units"] + model["prefill"]["units"], world, ms_per_step)
-    if e2e is None:
-        if unit == "TFLOP/s":
-            ev = world * (model["prefill"]["flops"] + model.get("append", {"flops": 0})["flops"]) / (e2e_ms / 1e3) / 1e12
-        else:
-            ev = value * ms_per_step / e2e_ms
-        e2e = {"value": ev, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms}
+        work = model["decode"]["units"] + model["prefill"]["units"]
+    value = job_throughput(work, world, ms_per_step)
+    e2e = {"value": job_throughput(work, world, e2e_ms), "unit": unit, "h2d_bytes_per_step": g.h2d_bytes,
+           "d2h_bytes_per_step": g.d2h_bytes, "ms_per_step": e2e_ms,
+           "copies_per_step": {"h2d": 1, "d2h": 1}}
 
-    sh = case.shape
     parts = {}
     for k in kinds:
-        ms = sum(part_ms[k]) / K
+        ms = part_ms[k]
         m = model[k]
         parts[k] = {"ms": ms, "GB/s": m["bytes"] / (ms / 1e3) / 1e9, "TFLOP/s": m["flops"] / (ms / 1e3) / 1e12,
                     m["unit_name"]: m["units"]}
         parts[k]["frac_hbm"] = parts[k]["GB/s"] / pk["hbm_gbs"]
         parts[k]["frac_tensor"] = parts[k]["TFLOP/s"] / pk["bf16_tflops"]
-    bytes_lrkv = bytes_full = 0
-    es = 4 if sh.dtype == "fp32" else 2
-    if "decode" in model:
-        qs = case.dec_q_start.tolist()
-        for c, s in enumerate(case.dec_ctx):
-            L = case.seqs[s].total_len
-            readers = qs[c + 1] - qs[c]
-            bytes_full += readers * L * sh.n_kv_heads * sh.head_dim * 2 * es
-            bytes_lrkv += L * (sh.n_kv_heads * sh.head_dim * 2 + 2 * sh.rank) * es
-    line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if sh.dtype == "bf16" else "fp32", "data": "synthetic",
-        "config": {"workload": args.config, "hidden": sh.hidden, "n_q_heads": sh.n_q_heads,
+        if pk.get("bf16_tflops_sustained"):
+            parts[k]["frac_tensor_sustained"] = parts[k]["TFLOP/s"] / pk["bf16_tflops_sustained"]
+        parts[k]["roofline"] = part_roofline(k, name, m, ms, pk)
+    roof = parts[dominant]["roofline"]
+    sh = case.shape
+    entry = {
+        "workload": name, "value": value, "unit": unit, "ms_per_step": ms_per_step, "steps": K,
+        "dtype": "bf16" if sh.dtype == "bf16" else "fp32",
+        "config": {"workload": name, "hidden": sh.hidden, "n_q_heads": sh.n_q_heads,
                    "n_kv_heads": sh.n_kv_heads, "head_dim": sh.head_dim, "rank": sh.rank,
                    "n_adapters": sh.n_adapters, "contexts": len(case.seqs),
                    "max_len": max(q.total_len for q in case.seqs),
                    "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write)",
-                   "parallelism": f"replica x{world} (independent contexts per GPU)"},
+                   "parallelism": f"weak x{world}: rank {rank} holds its own share of the contexts"},
         "roofline": roof, "parts": parts, "e2e": e2e,
-        "gpu_launches": K * sum(launches_per_call[k] for k in kinds),
+        "gpu_launches": K * sum(LAUNCHES_PER_CALL[k] for k in kinds),
         "clocks": clk.summary(), "device_status": status, "host_s": host_dt,
     }
-    if bytes_full:
-        line["cache_bytes"] = {"lrkv": bytes_lrkv, "per_agent_full": bytes_full,
-                               "saving": bytes_full / bytes_lrkv}
+    if args.no_bk:
+        entry["variant"] = "no_bk: attention without B_K (diagnostic, not the method's result)"
+    cb = cache_bytes(case)
+    if cb:
+        entry["cache_bytes"] = cb
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, u, dt, desc = oracle_sample(case, 15.0, model)
-        line["cpu_baseline"] = {"value": v, "unit": u, "cores": oracle_threads(), "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+        v, u, dt, desc = oracle_sample(case, args.cpu_budget, model)
+        entry["cpu_baseline"] = {"value": v, "unit": u, "cores": oracle_threads(), "kind": "oracle",
+                                 "sample": desc, "seconds": dt}
+    del g, flush
+    torch.cuda.empty_cache()
+    return entry
+
+
+def part_roofline(kind, workload, m, ms, pk):
+    """Roofline of one part's kernel: bytes against HBM for decode, flops against
+    the bf16 tensor peak for prefill and append (burst peak: each part is timed
+    on its own, a fraction of a millisecond to a few milliseconds long)."""
+    if kind == "decode":
+        achieved = m["bytes"] / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"],
+                "kernel": "lrkv_attn_decode (decode_kernel + combine_kernel)",
+                "algorithmic_bytes_per_launch": m["bytes"], "launch_ms": ms,
+                "traffic": committed_traffic(workload, "decode")}
+    achieved = m["flops"] / (ms / 1e3) / 1e12
+    r = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+         "frac": achieved / pk["bf16_tflops"], "peak_source": pk["source"] + " (burst)",
+         "kernel": "lrkv_attn_prefill (prefill_kernel)" if kind == "prefill" else "lrkv_append (append kernel)",
+         "algorithmic_flops_per_launch": m["flops"], "launch_ms": ms,
+         "traffic": committed_traffic(workload, kind)}
+    if pk.get("bf16_tflops_sustained"):
+        r["frac_sustained"] = achieved / pk["bf16_tflops_sustained"]
+    return r
+
+
+def merge_clocks(entries):
+    sums = [e["clocks"] for e in entries]
+    med = [c["sm_mhz"] for c in sums if c.get("sm_mhz")]
+    out = {"sm_mhz": statistics.median(med) if med else None,
+           "sm_max_mhz": next((c["sm_max_mhz"] for c in sums if c.get("sm_max_mhz")), None),
+           "reasons": sorted(set(r for c in sums for r in c.get("reasons", []))),
+           "samples": sum(c.get("samples", 0) for c in sums)}
+    errs = [c["error"] for c in sums if c.get("error")]
+    if errs:
+        out["error"] = errs[0]
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=["all"] + ALL_WORKLOADS + ["tiny_fp32_decode"])
+    ap.add_argument("--impl", default="lrkv", choices=["lrkv", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work per workload")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-bk", action="store_true", help="attention without B_K (diagnostic)")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from rank_cache_attention_flash_b300 import lrkv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lrkv.load()
+    pk = peaks()
+
+    names = ALL_WORKLOADS if args.config == "all" else [args.config]
+    entries = {n: time_workload(n, args, world, rank, dev, pk) for n in names}
+    head = entries[HEADLINE] if HEADLINE in entries else entries[names[0]]
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
+        "config": head["config"], "roofline": head["roofline"], "e2e": head["e2e"],
+        "gpu_launches": sum(e["gpu_launches"] for e in entries.values()),
+        "clocks": merge_clocks(list(entries.values())),
+        "device_status": max(e["device_status"] for e in entries.values()),
+    }
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if "cache_bytes" in head:
+        line["cache_bytes"] = head["cache_bytes"]
+    if PREFILL_HEADLINE in entries:
+        pr = entries[PREFILL_HEADLINE]["parts"]["prefill"]
+        line["prefill"] = {"workload": PREFILL_HEADLINE, "TFLOP/s": pr["TFLOP/s"], "launch_ms": pr["ms"],
+                           "frac_burst": pr["frac_tensor"], "frac_sustained": pr.get("frac_tensor_sustained"),
+                           "peak_burst": pk["bf16_tflops"], "peak_sustained": pk.get("bf16_tflops_sustained")}
+    if args.no_bk:
+        line["variant"] = head.get("variant")
+    if len(entries) > 1:
+        line["workloads"] = entries
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

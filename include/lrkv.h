@@ -228,7 +228,10 @@ size_t lrkv_prefill_workspace_bytes(const lrkv_config* cfg, int32_t num_seqs, in
  *   LRKV_NOALLOC_SCRATCH_BYTES return LRKV_ERR_WORKSPACE before any launch.
  * - First call on a device: resolves the array's device address for that
  *   device (with that device current) and caches it; make that first call
- *   before any stream capture on the device.
+ *   before any stream capture on the device. The cached address belongs to
+ *   the device's current context: after cudaDeviceReset (or anything else
+ *   that destroys the primary context) this entry point must not be called
+ *   again in the same process, since the array may then live elsewhere.
  * - Sharing: every call on a device uses the same array. Nothing in it needs
  *   to start at zero (it holds split partials that are written before they
  *   are read), but calls whose kernels overlap on the GPU (on different

@@ -18,7 +18,7 @@ per-agent key and value materialised in full, then textbook softmax attention:
   base cache comes from the pretrained weights and the low-rank cache is
   produced once, when a context segment is first processed (the "append").
 
-Readings where the pages are silent (each listed in the design doc as well):
+Readings where the pages are silent:
 row-vector convention X·W; rotate-half RoPE pairing (j, j + d/2) with
 theta_j = base^(-2j/d) and no frequency scaling; LoRA scale folded into B;
 softmax scale 1/sqrt(d); q head m reads kv head floor(m / (Hq/Hkv)); query k of

@@ -233,13 +233,7 @@ lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X, int T,
   p.num_seqs = num_seqs;
   p.max_blocks = max_blocks;
   rope_freqs(cfg, &p.freqs);
-  static bool attr_set = false;  // idempotent per-process kernel attribute
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(append_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_TOTAL) != cudaSuccess)
-      return LRKV_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(append_gemm_kernel), SMEM_TOTAL)) return LRKV_ERR_CUDA;
   dim3 grid((p.N + BN - 1) / BN, (T + BM - 1) / BM);
   append_gemm_kernel<<<grid, NTHR, SMEM_TOTAL, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;

@@ -1048,13 +1048,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
 
   if (plan.n_items > 0) {
     auto kern = decode_kernel<D, R>;
-    static bool attr_set = false;  // idempotent per-process kernel attribute
-    if (!attr_set) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes) !=
-          cudaSuccess)
-        return LRKV_ERR_CUDA;
-      attr_set = true;
-    }
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), plan.smem_bytes)) return LRKV_ERR_CUDA;
     kern<<<static_cast<unsigned>(plan.n_items), kThreads, plan.smem_bytes, stream>>>(p, tb, tl);
     if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
   }

@@ -13,7 +13,9 @@
 // library holds LRKV_NOALLOC_SCRATCH_BYTES of it until the process exits. Host
 // code cannot use the variable's name as a device address, so on the first
 // call on each device (with that device current) the address is resolved
-// once with cudaGetSymbolAddress and cached per device.
+// once with cudaGetSymbolAddress and cached per device. The cache is never
+// invalidated: a process that resets a device (cudaDeviceReset) must not call
+// this entry point on that device afterwards.
 #include <mutex>
 
 #include "lrkv.h"

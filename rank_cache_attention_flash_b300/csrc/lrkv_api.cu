@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "lrkv.h"
 #include "lrkv_device.cuh"
@@ -27,6 +28,28 @@ int device_sm_count() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return n;
+}
+
+bool ensure_smem_attr(const void* func, int bytes) {
+  // (kernel, device, bytes) triples already applied; a handful of kernels
+  // times the devices in the process, so a linear scan is enough.
+  struct Entry {
+    const void* func;
+    int dev;
+    int bytes;
+  };
+  static std::mutex mu;
+  static Entry done[256];
+  static int n_done = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].func == func && done[i].dev == dev && done[i].bytes >= bytes) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  if (n_done < 256) done[n_done++] = Entry{func, dev, bytes};
+  return true;
 }
 
 namespace {

@@ -112,4 +112,9 @@ lrkv_status launch_prefill_fp32(const lrkv_config& cfg, const PrefillArgs& a,
 
 int device_sm_count();
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device. The attribute is per device, so it is set once per (kernel, device)
+// pair, under a lock (concurrent first calls from several threads are safe).
+bool ensure_smem_attr(const void* func, int bytes);
+
 }  // namespace lrkv

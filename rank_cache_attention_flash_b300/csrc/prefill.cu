@@ -902,12 +902,7 @@ lrkv_status run(const lrkv_config& cfg, const PrefillArgs& a, cudaStream_t strea
     return LRKV_ERR_CUDA;
   auto kern = prefill_kernel<D, R>;
   constexpr int smem = PL<D, R>::total;
-  static bool attr_set = false;  // idempotent per-process kernel attribute
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return LRKV_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return LRKV_ERR_CUDA;
   const int tiles = (a.max_q_len * p.g + BM - 1) / BM;
   dim3 grid(tiles, cfg.n_kv_heads, a.num_seqs);
   kern<<<grid, kThreads, smem, stream>>>(p, tb, tlk, tbr, tlr);

@@ -16,9 +16,50 @@ from . import inputs as I
 from . import lrkv
 
 
+def _align(n: int, a: int = 256) -> int:
+    return (n + a - 1) // a * a
+
+
+class _Arena:
+    """One contiguous byte buffer holding several tensors as views, so that a
+    step's inputs (or outputs) move between host and device in one copy."""
+
+    def __init__(self):
+        self.parts = []  # (name, offset, dtype, shape)
+        self.nbytes = 0
+
+    def add(self, name: str, t: torch.Tensor) -> None:
+        self.parts.append((name, self.nbytes, t.dtype, tuple(t.shape), t))
+        self.nbytes = _align(self.nbytes + t.numel() * t.element_size())
+
+    def materialise(self, device, fill_from_parts: bool):
+        """(device buffer, pinned host buffer or None, {name: device view})."""
+        dev_buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+        host_buf = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8).pin_memory() \
+            if torch.cuda.is_available() else None
+        views = {}
+        for name, off, dt, shape, src in self.parts:
+            n = src.numel() * src.element_size()
+            views[name] = dev_buf[off:off + n].view(dt).view(shape)
+            if fill_from_parts and host_buf is not None:
+                host_buf[off:off + n].view(dt).view(shape).copy_(src)
+        if fill_from_parts and host_buf is not None:
+            dev_buf.copy_(host_buf)
+        return dev_buf, host_buf, views
+
+
 class GpuCase:
+    """A workload on one GPU. The step's per-call inputs (queries, context
+    lengths, adapter ids, the new tokens' hidden states and positions) live in
+    one input arena and its outputs in one output arena, each with a pinned
+    host mirror: ``upload_inputs`` / ``download_outputs`` are then one copy
+    each. Pools, weights and block tables stay resident.
+
+    no_bk: pass B_K = NULL to attention (the K adapter term and its rebuild
+    are skipped), a diagnostic that isolates the rebuild's cost."""
+
     def __init__(self, case: I.Case, device="cuda", pool_fill: Optional[float] = None,
-                 setup_chunk_tokens: int = 1 << 16):
+                 setup_chunk_tokens: int = 1 << 16, no_bk: bool = False):
         self.case = case
         self.device = torch.device(device)
         sh = case.shape
@@ -29,25 +70,27 @@ class GpuCase:
         self.W_cat = lrkv.pack_w_cat(w["W_K"], w["W_V"], w["A_K"], w["A_V"]).to(dev)
         self.B_K = w["B_K"].contiguous().to(dev)
         self.B_V = w["B_V"].contiguous().to(dev)
+        self.attn_B_K = None if no_bk else self.B_K
         self.block_tables = case.block_tables.to(dev)
         self.base_pool, self.lr_pool = lrkv.new_pools(self.cfg, case.num_blocks, dev, pool_fill)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.scale = 1.0 / math.sqrt(sh.head_dim)
         self.setup_chunk_tokens = setup_chunk_tokens
-        # decode arguments
+        ins, outs = _Arena(), _Arena()
         bt = case.block_tables
+        # decode arguments
         self.n_dec = int(case.dec_q.shape[0])
         if self.n_dec:
-            self.dec_q = case.dec_q.to(dev)
-            self.dec_q_start = case.dec_q_start.to(dev)
-            self.dec_adapter = case.dec_adapter.to(dev)
-            self.dec_bt = bt[torch.tensor(case.dec_ctx, dtype=torch.long)].contiguous().to(dev)
+            ins.add("dec_q", case.dec_q)
+            ins.add("dec_q_start", case.dec_q_start)
+            ins.add("dec_adapter", case.dec_adapter)
             lens = case.dec_lens()
-            self.dec_lens = lens.to(dev)
+            ins.add("dec_lens", lens)
+            outs.add("dec_out", case.dec_q)
+            self.dec_bt = bt[torch.tensor(case.dec_ctx, dtype=torch.long)].contiguous().to(dev)
             self.dec_max_len = int(lens.max())
             qs = case.dec_q_start
             self.dec_max_q = int((qs[1:] - qs[:-1]).max())
-            self.dec_out = torch.empty_like(self.dec_q)
             self.dec_ws = torch.empty(
                 max(1, lrkv.decode_workspace_bytes(self.cfg, self.n_dec, len(case.dec_ctx),
                                                    self.dec_max_len, self.dec_max_q)),
@@ -55,16 +98,16 @@ class GpuCase:
         # prefill arguments
         self.n_pre = len(case.pre_seq)
         if self.n_pre:
-            self.pre_q = case.pre_q.to(dev)
-            self.pre_q_start = case.pre_q_start.to(dev)
-            self.pre_adapter = case.pre_adapter.to(dev)
-            self.pre_bt = bt[torch.tensor(case.pre_seq, dtype=torch.long)].contiguous().to(dev)
+            ins.add("pre_q", case.pre_q)
+            ins.add("pre_q_start", case.pre_q_start)
+            ins.add("pre_adapter", case.pre_adapter)
             lens = case.pre_lens()
-            self.pre_lens = lens.to(dev)
+            ins.add("pre_lens", lens)
+            outs.add("pre_out", case.pre_q)
+            self.pre_bt = bt[torch.tensor(case.pre_seq, dtype=torch.long)].contiguous().to(dev)
             self.pre_max_len = int(lens.max())
             qs = case.pre_q_start
             self.pre_max_q = int((qs[1:] - qs[:-1]).max())
-            self.pre_out = torch.empty_like(self.pre_q)
         # step append arguments (all new tokens in one call)
         xs, pos, rows = [], [], []
         for s, a, b in case.step_appends():
@@ -73,11 +116,27 @@ class GpuCase:
             rows.append(torch.full((b - a,), s, dtype=torch.int32))
         self.n_step_tokens = sum(x.shape[0] for x in xs)
         if xs:
-            self.step_X = torch.cat(xs).to(dev)
-            self.step_pos = torch.cat(pos).to(dev)
-            self.step_rows = torch.cat(rows).to(dev)
+            ins.add("step_X", torch.cat(xs))
+            ins.add("step_pos", torch.cat(pos))
+            ins.add("step_rows", torch.cat(rows))
+        self.in_dev, self.in_host, views = ins.materialise(dev, True)
+        self.out_dev, self.out_host, oviews = outs.materialise(dev, False)
+        self.h2d_bytes = ins.nbytes
+        self.d2h_bytes = outs.nbytes
+        for k, v in {**views, **oviews}.items():
+            setattr(self, k, v)
 
     # ------------------------------------------------------------------
+    def upload_inputs(self, stream=None) -> None:
+        """The step's inputs from pinned host memory: one host-to-device copy."""
+        with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
+            self.in_dev.copy_(self.in_host, non_blocking=True)
+
+    def download_outputs(self, stream=None) -> None:
+        """The step's outputs to pinned host memory: one device-to-host copy."""
+        with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
+            self.out_host.copy_(self.out_dev, non_blocking=True)
+
     def setup(self) -> None:
         """Untimed: append the tokens cached before the step."""
         case, dev = self.case, self.device
@@ -115,7 +174,7 @@ class GpuCase:
             return None
         return lrkv.attn_decode(self.cfg, self.dec_q, self.dec_q_start, self.dec_adapter,
                                 self.dec_bt, self.dec_lens, self.dec_max_len, self.dec_max_q,
-                                self.base_pool, self.lr_pool, self.B_K, self.B_V, self.scale,
+                                self.base_pool, self.lr_pool, self.attn_B_K, self.B_V, self.scale,
                                 out=self.dec_out, workspace=self.dec_ws, status=self.status,
                                 stream=stream)
 
@@ -124,7 +183,7 @@ class GpuCase:
             return None
         return lrkv.attn_prefill(self.cfg, self.pre_q, self.pre_q_start, self.pre_max_q,
                                  self.pre_lens, self.pre_max_len, self.pre_adapter, self.pre_bt,
-                                 self.base_pool, self.lr_pool, self.B_K, self.B_V, self.scale,
+                                 self.base_pool, self.lr_pool, self.attn_B_K, self.B_V, self.scale,
                                  out=self.pre_out, status=self.status, stream=stream)
 
     def step(self) -> Dict[str, Optional[torch.Tensor]]:

@@ -226,13 +226,15 @@ def _tables(seqs: List[Seq], seed: int, permute: bool):
     return bt, total
 
 
-def _q(shape: Shape, seed: int, stream: int, n: int) -> torch.Tensor:
+def _q(shape: Shape, seed: int, stream: int, n: int, skip: int = 0) -> torch.Tensor:
+    """Query rows [skip, skip + n) of a query stream (the rows before ``skip``
+    belong to the contexts of other shards)."""
     g = _gen(seed, stream)
-    x = torch.randn(n, shape.n_q_heads, shape.head_dim, generator=g).mul_(shape.q_std)
+    x = torch.randn(skip + n, shape.n_q_heads, shape.head_dim, generator=g)[skip:].mul_(shape.q_std)
     return x.to(shape.torch_dtype)
 
 
-def _build(name, shape, seed, seqs, dec, pre, permute):
+def _build(name, shape, seed, seqs, dec, pre, permute, q_skip=(0, 0)):
     """dec: list of (ctx_row, adapter) sorted by ctx_row; pre: list of seq rows."""
     bt, nblocks = _tables(seqs, seed, permute)
     dec_ctx = []
@@ -254,10 +256,10 @@ def _build(name, shape, seed, seqs, dec, pre, permute):
         name=name, shape=shape, seed=seed, seqs=seqs, num_blocks=nblocks, block_tables=bt,
         dec_ctx=dec_ctx, dec_q_start=torch.tensor(starts, dtype=torch.int32),
         dec_adapter=torch.tensor(adapters, dtype=torch.int32),
-        dec_q=_q(shape, seed, _S_QDEC, len(adapters)),
+        dec_q=_q(shape, seed, _S_QDEC, len(adapters), q_skip[0]),
         pre_seq=list(pre), pre_q_start=torch.tensor(pre_start, dtype=torch.int32),
         pre_adapter=torch.tensor([seqs[s].adapter for s in pre], dtype=torch.int32),
-        pre_q=_q(shape, seed, _S_QPRE, pre_start[-1]),
+        pre_q=_q(shape, seed, _S_QPRE, pre_start[-1], q_skip[1]),
         weights=_weights(shape, seed),
     )
 
@@ -280,65 +282,108 @@ def shape_qwen3_1p7b() -> Shape:
     return Shape(2048, 16, 8, 128, 8, 8, 10000.0, "bf16", 1.0, w, w, 1 / math.sqrt(8), 1.0)
 
 
-def tiny_fp32_decode(seed: int = 0, n: int = 128) -> Case:
-    """Tiny fp32 decode: 2 agents query one shared n-token context."""
+def tiny_fp32_decode(seed: int = 0, n: int = 128, first: int = 0) -> Case:
+    """Tiny fp32 decode: 2 agents query one shared n-token context.
+    ``first``: global index of this shard's context (see ``shard_range``)."""
     shape = shape_tiny_fp32()
-    seqs = [Seq(0, 0, 0, n, 0, -1, "context")]
-    return _build("tiny_fp32_decode", shape, seed, seqs, [(0, 0), (0, 1)], [], False)
+    seqs = [Seq(first, 0, first, n, 0, -1, "context")]
+    return _build("tiny_fp32_decode", shape, seed, seqs, [(0, 0), (0, 1)], [], False, (2 * first, 0))
 
 
-def shared_decode(seed: int = 0, n: int = 8192, n_agents: int = 4, rank: int = 16) -> Case:
+def shared_decode(seed: int = 0, n: int = 8192, n_agents: int = 4, rank: int = 16,
+                  first: int = 0) -> Case:
     """Llama-3.1-8B-shaped decode: n_agents queries on one shared n-token context,
-    identity block table."""
+    identity block table. ``first``: global index of this shard's context."""
     shape = shape_llama8b(rank, n_agents)
-    seqs = [Seq(0, 0, 0, n, 0, -1, "context")]
+    seqs = [Seq(first, 0, first, n, 0, -1, "context")]
     dec = [(0, a) for a in range(n_agents)]
-    return _build("shared_decode_llama8b", shape, seed, seqs, dec, [], False)
+    return _build("shared_decode_llama8b", shape, seed, seqs, dec, [], False, (n_agents * first, 0))
 
 
 def prefill_chunk(seed: int = 0, prefix: int = 16384, chunk: int = 512, n_agents: int = 4,
-                  rank: int = 16) -> Case:
+                  rank: int = 16, first: int = 0) -> Case:
     """Each agent appends a new chunk and attends causally over the shared prefix
-    plus its own chunk. The prefix blocks are shared physically."""
+    plus its own chunk. The prefix blocks are shared physically. ``first``:
+    global index of this shard's shared context (its prefix and chunks use
+    hidden-state streams of their own)."""
     shape = shape_llama8b(rank, n_agents)
-    seqs = [Seq(0, prefix, 1 + a, prefix, chunk, a, "prefill") for a in range(n_agents)]
-    return _build("prefill_chunk_llama8b", shape, seed, seqs, [], list(range(n_agents)), False)
+    base = first * (n_agents + 1)
+    seqs = [Seq(base, prefix, base + 1 + a, prefix, chunk, a, "prefill") for a in range(n_agents)]
+    return _build("prefill_chunk_llama8b", shape, seed, seqs, [], list(range(n_agents)), False,
+                  (0, first * n_agents * chunk))
 
 
 def long_decode(seed: int = 0, n_seqs: int = 16, n: int = 32768, n_agents: int = 8,
-                rank: int = 64) -> Case:
+                rank: int = 64, first: int = 0) -> Case:
     """Ministral-8B-shaped paged decode: independent sequences, adapter ids uniform
-    over the agents, blocks placed by a seeded permutation of the pool."""
+    over the agents, blocks placed by a seeded permutation of the pool.
+    ``first``: global index of this shard's first sequence."""
     shape = shape_llama8b(rank, n_agents)
-    ad = torch.randint(0, n_agents, (n_seqs,), generator=_gen(seed, _S_ADAPT)).tolist()
-    seqs = [Seq(0, 0, 1 + s, n, 0, ad[s], "context") for s in range(n_seqs)]
+    ad = torch.randint(0, n_agents, (first + n_seqs,), generator=_gen(seed, _S_ADAPT))[first:].tolist()
+    seqs = [Seq(0, 0, 1 + first + s, n, 0, ad[s], "context") for s in range(n_seqs)]
     dec = [(s, ad[s]) for s in range(n_seqs)]
-    return _build("long_decode_ministral8b", shape, seed, seqs, dec, [], True)
+    return _build("long_decode_ministral8b", shape, seed, seqs, dec, [], True, (first, 0))
 
 
 def mixed_batch(seed: int = 0, n_seqs: int = 64, n_decode: int = 48, chunk: int = 256,
-                lo: int = 1024, hi: int = 16384, n_agents: int = 8) -> Case:
+                lo: int = 1024, hi: int = 16384, n_agents: int = 8, first: int = 0) -> Case:
     """Qwen3-1.7B-shaped mixed serving batch: ``n_decode`` sequences decode one new
     token, the rest prefill a ``chunk``-token chunk; context lengths uniform in
-    [lo, hi] (cached before the step); random block tables."""
+    [lo, hi] (cached before the step); random block tables. ``first``: global
+    index of this shard's batch (its sequences are global sequences
+    [first * n_seqs, (first + 1) * n_seqs))."""
     shape = shape_qwen3_1p7b()
-    lens = torch.randint(lo, hi + 1, (n_seqs,), generator=_gen(seed, _S_LENS)).tolist()
-    ad = torch.randint(0, n_agents, (n_seqs,), generator=_gen(seed, _S_ADAPT)).tolist()
+    g0 = first * n_seqs
+    lens = torch.randint(lo, hi + 1, (g0 + n_seqs,), generator=_gen(seed, _S_LENS))[g0:].tolist()
+    ad = torch.randint(0, n_agents, (g0 + n_seqs,), generator=_gen(seed, _S_ADAPT))[g0:].tolist()
     seqs = []
     for s in range(n_seqs):
         dec = s < n_decode
-        seqs.append(Seq(0, 0, 1 + s, lens[s], 1 if dec else chunk, ad[s], "decode" if dec else "prefill"))
+        seqs.append(Seq(0, 0, 1 + g0 + s, lens[s], 1 if dec else chunk, ad[s], "decode" if dec else "prefill"))
     dec = [(s, ad[s]) for s in range(n_decode)]
     pre = list(range(n_decode, n_seqs))
-    return _build("mixed_batch_qwen3_1p7b", shape, seed, seqs, dec, pre, True)
+    return _build("mixed_batch_qwen3_1p7b", shape, seed, seqs, dec, pre, True,
+                  (first * n_decode, first * (n_seqs - n_decode) * chunk))
+
+
+def shard_range(n_global: int, world: int, rank: int) -> range:
+    """The contiguous share [lo, hi) of ``n_global`` independent contexts that
+    rank ``rank`` of ``world`` owns (sizes differ by at most one)."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank / world")
+    q, r = divmod(n_global, world)
+    lo = rank * q + min(rank, r)
+    return range(lo, lo + q + (1 if rank < r else 0))
+
+
+# Units of independent work per workload (contexts that share nothing but the
+# weights): the weak-scaling job on N GPUs holds N times these, and rank k
+# builds the share shard_range(N * units, N, k) through the builders' ``first``.
+SHARD_UNITS = {
+    "tiny_fp32_decode": 1,
+    "shared_decode_llama8b": 1,
+    "prefill_chunk_llama8b": 1,
+    "long_decode_ministral8b": 16,
+    "mixed_batch_qwen3_1p7b": 1,
+}
+
+
+def build_shard(name: str, world: int = 1, rank: int = 0, seed: int = 0) -> Case:
+    """Rank ``rank``'s share of the weak-scaling job of ``world`` GPUs."""
+    units = SHARD_UNITS[name]
+    share = shard_range(world * units, world, rank)
+    if len(share) != units:
+        raise AssertionError("weak scaling: every rank holds the same number of contexts")
+    first = share.start if name == "long_decode_ministral8b" else share.start // units
+    return FULL[name](seed, first)
 
 
 FULL = {
-    "tiny_fp32_decode": lambda seed=0: tiny_fp32_decode(seed),
-    "shared_decode_llama8b": lambda seed=0: shared_decode(seed),
-    "prefill_chunk_llama8b": lambda seed=0: prefill_chunk(seed),
-    "long_decode_ministral8b": lambda seed=0: long_decode(seed),
-    "mixed_batch_qwen3_1p7b": lambda seed=0: mixed_batch(seed),
+    "tiny_fp32_decode": lambda seed=0, first=0: tiny_fp32_decode(seed, first=first),
+    "shared_decode_llama8b": lambda seed=0, first=0: shared_decode(seed, first=first),
+    "prefill_chunk_llama8b": lambda seed=0, first=0: prefill_chunk(seed, first=first),
+    "long_decode_ministral8b": lambda seed=0, first=0: long_decode(seed, first=first),
+    "mixed_batch_qwen3_1p7b": lambda seed=0, first=0: mixed_batch(seed, first=first),
 }
 
 # Small variants: same layer shapes, lengths the oracle finishes in seconds,
