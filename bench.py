@@ -626,7 +626,7 @@ def main():
         "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
-        "config": head["config"], "roofline": head["roofline"], "e2e": head["e2e"],
+        "config": head["config"], "roofline": head["roofline"], "parts": head["parts"], "e2e": head["e2e"],
         "gpu_launches": sum(e["gpu_launches"] for e in entries.values()),
         "clocks": merge_clocks(list(entries.values())),
         "device_status": max(e["device_status"] for e in entries.values()),

@@ -126,6 +126,32 @@ lrkv_status lrkv_append(const lrkv_config* cfg, const void* X, int32_t T,
                         int32_t* dev_status, lrkv_stream_t stream);
 
 /*
+ * lrkv_append_rebase -- lrkv_append with the base and the low-rank part of
+ * the cache written from different hidden states, or only one of the parts.
+ *
+ * Defines: PReCache (thelatestinai.com/papers/2609.34054), Abstract and
+ * Figure 1 (ReBaseShared): the shared base cache is reconstructed from
+ * adapter-free hidden states, which lowers the error that the previous
+ * agent's adapted representation leaves in it; the reconstruction runs either
+ * alongside the adapted pass (both paths batched together, "DB") or as a
+ * separate prefill after the agent's turn ("LP").
+ *
+ * For token n (slot as in lrkv_append):
+ *   X_base != NULL: base_pool rows = RoPE(X_base W_K), X_base W_V   (re-based)
+ *   X_lr   != NULL: lr_pool rows   = X_lr A_K, X_lr A_V
+ * A NULL source leaves that part of the pools untouched (X_lr = NULL is the
+ * base-only re-base after a turn; X_base = X_lr is exactly lrkv_append). Both
+ * NULL with T > 0 is LRKV_ERR_INVALID_ARG. One launch either way; X_base and
+ * X_lr are [T][h], same dtype and alignment rules as X. Other arguments,
+ * errors and dev_status: as lrkv_append.
+ */
+lrkv_status lrkv_append_rebase(const lrkv_config* cfg, const void* X_base, const void* X_lr, int32_t T,
+                               const int32_t* positions, const int32_t* seq_rows,
+                               const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
+                               const void* W_cat, void* base_pool, void* lr_pool, int64_t num_blocks,
+                               int32_t* dev_status, lrkv_stream_t stream);
+
+/*
  * lrkv_attn_decode -- one query token per query row, many agents per context.
  *
  * Defines: LRAgent (arXiv 2602.01053), Abstract -- Flash-LoRA-Attention

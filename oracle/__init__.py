@@ -3,6 +3,7 @@ from .lrkv_oracle import (  # noqa: F401
     BLOCK,
     agent_kv,
     agent_kv_from_cache,
+    agent_kv_rebased,
     append_pools,
     apply_rope,
     attend,
@@ -10,6 +11,7 @@ from .lrkv_oracle import (  # noqa: F401
     decode,
     gqa_attention,
     prefill,
+    rebase_pools,
     rope_inv_freq,
     round_bf16,
 )

@@ -139,6 +139,38 @@ def agent_kv_from_cache(X, positions, W_K, W_V, A_K, A_V, B_K_i, B_V_i, n_kv_hea
     return k, v
 
 
+def agent_kv_rebased(X_base, X_lr, positions, W_K, W_V, A_K, A_V, B_K_i, B_V_i, n_kv_heads: int,
+                     head_dim: int, base: float, cache_dtype=None):
+    """One agent's keys and values over a re-based cache (PReCache, Abstract and
+    Figure 1, ReBaseShared): the shared base part is rebuilt from the
+    adapter-free hidden states X_base, while the low-rank part stays the one
+    computed from X_lr, so
+        K_i = RoPE(X_base·W_K + (X_lr·A_K)·B_K,i),  V_i = X_base·W_V + (X_lr·A_V)·B_V,i.
+    cache_dtype="bf16": the four stored components are rounded to bf16 first
+    (as agent_kv_from_cache does for a single source)."""
+    X_base = _f64(X_base)
+    X_lr = _f64(X_lr)
+    T = X_base.shape[0]
+    if cache_dtype is None:
+        k_pre = X_base @ _f64(W_K)
+        v = X_base @ _f64(W_V)
+        if B_K_i is not None:
+            k_pre = k_pre + (X_lr @ _f64(A_K)) @ _f64(B_K_i)
+        if B_V_i is not None:
+            v = v + (X_lr @ _f64(A_V)) @ _f64(B_V_i)
+        k = apply_rope(k_pre.reshape(T, n_kv_heads, head_dim), positions, base)
+        return k, v.reshape(T, n_kv_heads, head_dim)
+    assert cache_dtype == "bf16"
+    kb, vb, _, _ = base_and_lowrank(X_base, positions, W_K, W_V, A_K, A_V, n_kv_heads, head_dim, base)
+    _, _, lk, lv = base_and_lowrank(X_lr, positions, W_K, W_V, A_K, A_V, n_kv_heads, head_dim, base)
+    k, v = round_bf16(kb), round_bf16(vb)
+    if B_K_i is not None:
+        k = k + apply_rope((round_bf16(lk) @ _f64(B_K_i)).reshape(T, n_kv_heads, head_dim), positions, base)
+    if B_V_i is not None:
+        v = v + (round_bf16(lv) @ _f64(B_V_i)).reshape(T, n_kv_heads, head_dim)
+    return k, v
+
+
 # ---------------------------------------------------------------------------
 # Attention.
 
@@ -179,12 +211,19 @@ def _adapter_B(weights, adapter: int):
 
 
 def attend(X_seq, adapter: int, q, q_positions, weights, n_kv_heads: int, head_dim: int,
-           base: float, scale: float, cache_dtype=None) -> np.ndarray:
+           base: float, scale: float, cache_dtype=None, X_lr=None) -> np.ndarray:
     """Queries q [N, Hq, d] of one agent over a sequence whose hidden states at
     positions 0..L-1 are X_seq [L, h]: materialise the agent's K, V, then attend.
-    cache_dtype="bf16" uses the bf16-stored cache components (agent_kv_from_cache)."""
+    cache_dtype="bf16" uses the bf16-stored cache components (agent_kv_from_cache).
+    X_lr (ReBaseShared): the low-rank part of the cache came from these hidden
+    states instead, the base part from X_seq (agent_kv_rebased)."""
     L = np.asarray(X_seq).shape[0]
     B_K, B_V = _adapter_B(weights, adapter)
+    if X_lr is not None:
+        K, V = agent_kv_rebased(X_seq, X_lr, np.arange(L), weights["W_K"], weights["W_V"],
+                                weights["A_K"], weights["A_V"], B_K, B_V, n_kv_heads, head_dim,
+                                base, cache_dtype)
+        return gqa_attention(q, q_positions, K, V, scale)
     make = agent_kv if cache_dtype is None else agent_kv_from_cache
     K, V = make(X_seq, np.arange(L), weights["W_K"], weights["W_V"], weights["A_K"],
                 weights["A_V"], B_K, B_V, n_kv_heads, head_dim, base)
@@ -192,25 +231,25 @@ def attend(X_seq, adapter: int, q, q_positions, weights, n_kv_heads: int, head_d
 
 
 def decode(X_ctx, q, adapters, weights, n_kv_heads: int, head_dim: int, base: float,
-           scale: float, cache_dtype=None) -> np.ndarray:
+           scale: float, cache_dtype=None, X_lr=None) -> np.ndarray:
     """Decode queries of several agents on one context X_ctx [L, h]: each query
     (one per row of q [N, Hq, d], adapter ids [N]) sits at position L - 1."""
     L = np.asarray(X_ctx).shape[0]
     out = np.empty(np.asarray(q).shape, dtype=np.float64)
     for n, a in enumerate(np.asarray(adapters).tolist()):
         out[n: n + 1] = attend(X_ctx, int(a), np.asarray(q)[n: n + 1], [L - 1], weights,
-                               n_kv_heads, head_dim, base, scale, cache_dtype)
+                               n_kv_heads, head_dim, base, scale, cache_dtype, X_lr)
     return out
 
 
 def prefill(X_seq, q_chunk, adapter: int, weights, n_kv_heads: int, head_dim: int,
-            base: float, scale: float, cache_dtype=None) -> np.ndarray:
+            base: float, scale: float, cache_dtype=None, X_lr=None) -> np.ndarray:
     """A chunk of q_len queries at the end of a sequence of L tokens (the chunk's
     own tokens included): query k sits at position L - q_len + k."""
     L = np.asarray(X_seq).shape[0]
     n = np.asarray(q_chunk).shape[0]
     return attend(X_seq, adapter, q_chunk, np.arange(L - n, L), weights, n_kv_heads,
-                  head_dim, base, scale, cache_dtype)
+                  head_dim, base, scale, cache_dtype, X_lr)
 
 
 def append_pools(base_pool, lr_pool, X, positions, seq_rows, block_tables, W_K, W_V, A_K,
@@ -231,4 +270,30 @@ def append_pools(base_pool, lr_pool, X, positions, seq_rows, block_tables, W_K, 
         base_pool[blk, 1, :, row, :] = vb[n]
         lr_pool[blk, 0, row, :] = lk[n]
         lr_pool[blk, 1, row, :] = lv[n]
+    return base_pool, lr_pool
+
+
+def rebase_pools(base_pool, lr_pool, X_base, X_lr, positions, seq_rows, block_tables, W_K, W_V,
+                 A_K, A_V, n_kv_heads: int, head_dim: int, base: float):
+    """Expected pool contents after a re-based append (PReCache, Abstract and
+    Figure 1, ReBaseShared), written in place: the base rows (K_base, V_base)
+    of each token from the adapter-free hidden states X_base, its low-rank rows
+    (L_K, L_V) from X_lr. A source of None leaves that part untouched (a
+    base-only re-base after an agent's turn keeps the low-rank cache)."""
+    kb = vb = lk = lv = None
+    if X_base is not None:
+        kb, vb, _, _ = base_and_lowrank(X_base, positions, W_K, W_V, A_K, A_V, n_kv_heads,
+                                        head_dim, base)
+    if X_lr is not None:
+        _, _, lk, lv = base_and_lowrank(X_lr, positions, W_K, W_V, A_K, A_V, n_kv_heads,
+                                        head_dim, base)
+    for n, (p, s) in enumerate(zip(np.asarray(positions).tolist(), np.asarray(seq_rows).tolist())):
+        blk = int(block_tables[s][p // BLOCK])
+        row = p % BLOCK
+        if kb is not None:
+            base_pool[blk, 0, :, row, :] = kb[n]
+            base_pool[blk, 1, :, row, :] = vb[n]
+        if lk is not None:
+            lr_pool[blk, 0, row, :] = lk[n]
+            lr_pool[blk, 1, row, :] = lv[n]
     return base_pool, lr_pool

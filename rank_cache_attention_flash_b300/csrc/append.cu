@@ -1,34 +1,56 @@
-// Cache append: one GEMM Y = X W_cat^T over the hidden size, then a fused
-// epilogue that rotates the K columns (RoPE at each token's position), casts
-// to bf16 and scatters every token row into its paged slot:
+// Cache append: one GEMM Y = X W_cat^T over the hidden size on the
+// 5th-generation tensor cores, then an epilogue read straight from tensor
+// memory that rotates the K columns (RoPE at each token's position), casts to
+// bf16 and scatters every token row into its paged slot:
 //   base_pool[blk][0][kv][row][:] = RoPE(Y_K),  base_pool[blk][1][kv][row][:] = Y_V,
 //   lr_pool[blk][0][row][:] = Y_AK,              lr_pool[blk][1][row][:] = Y_AV.
 // LRAgent (arXiv 2602.01053), Abstract: the base component is produced by the
 // pretrained weights and the adapter component is kept low-rank; PReCache,
 // Abstract: the low-rank cache is produced once, when a segment is first seen.
 //
-// GEMM: 128x128x32 CTA tiles, 8 warps of 64x32, legacy warp MMAs
-// (m16n8k16 bf16, fp32 accumulate), 4-stage cp.async pipeline with an XOR
-// swizzle so every ldmatrix is conflict-free.
-#include <algorithm>
+// Re-based appends (PReCache, Abstract and Figure 1, ReBaseShared): the base
+// columns may come from one set of hidden states (the adapter-free pass) and
+// the low-rank columns from another (the adapted pass), in one launch ("double
+// batching", both paths together), or either part alone (a base-only re-base
+// after an agent's turn, "lazy prefill"). The column tiles are laid out so
+// that no tile mixes base and low-rank columns: base tiles of up to 256
+// columns over [0, 2 Hkv d), then one tile of the 2r low-rank columns.
+//
+// One CTA per (column tile, 128-token tile):
+//   warp 0      TMA producer: X and W_cat k-slices (64 wide, 128-byte swizzle)
+//               into a 4-stage mbarrier ring
+//   warp 1      owns the tensor memory, issues tcgen05.mma (M = 128 tokens,
+//               N = tile width, K = 16) into a fp32 accumulator in TMEM
+//   warps 4-11  epilogue, two warpgroups splitting the tile's columns; thread
+//               = token row = TMEM lane: tcgen05.ld, RoPE, bf16, 16-byte stores
+// Every wait is bounded; a wait that gives up stores LRKV_ERR_TIMEOUT, raises
+// the CTA's abort flag, and no copy or MMA is left in flight at exit.
+#include <climits>
 
 #include "lrkv_device.cuh"
 #include "lrkv_internal.h"
+#include "tcgen05.cuh"
 
 namespace lrkv {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 32, NSTAGE = 4, NTHR = 256;
-constexpr int TILE_BYTES = BM * BK * 2;  // 8 KB per operand per stage
-constexpr int EPI_PITCH = BN + 4;        // floats
-constexpr int SMEM_PIPE = NSTAGE * 2 * TILE_BYTES;
-constexpr int SMEM_EPI = BM * EPI_PITCH * 4;
-constexpr int SMEM_ROWS = BM * 16;  // per-row slot info
-constexpr int SMEM_TOTAL = (SMEM_PIPE > SMEM_EPI ? SMEM_PIPE : SMEM_EPI) + SMEM_ROWS;
+constexpr int AM = 128;   // tokens per tile (MMA M, TMEM lanes)
+constexpr int AN = 256;   // widest column tile (MMA N)
+constexpr int AK = 64;    // k-slice: 64 bf16 = one 128-byte swizzle row
+constexpr int NST = 4;    // pipeline stages
+constexpr int kThreads = 384;
+constexpr int A_BYTES = AM * AK * 2;            // 16 KB
+constexpr int B_BYTES = AN * AK * 2;            // 32 KB
+constexpr int STAGE = A_BYTES + B_BYTES;        // 48 KB
+constexpr int OFF_BAR = NST * STAGE;
+constexpr int SMEM_USED = OFF_BAR + 256;
+constexpr int SMEM_TOTAL = SMEM_USED + 1024;    // + alignment slack
+constexpr uint32_t kTmemCols = 256;
+constexpr long long kWaitCycles = 1ll << 31;    // ~1 s: a wait this long has failed
+
+enum : int { B_FULL = 0, B_EMPTY = NST, B_ACC = 2 * NST, B_DRAIN = 2 * NST + 1, B_COUNT = 2 * NST + 2 };
 
 struct AppendParams {
-  const __nv_bfloat16* X;
-  const __nv_bfloat16* W;  // [N][h]
   const int32_t* positions;
   const int32_t* seq_rows;
   const int32_t* block_tables;
@@ -36,187 +58,236 @@ struct AppendParams {
   __nv_bfloat16* lr_pool;
   int32_t* status;
   int64_t num_blocks;
-  int T, h, N, Hkv, D, R, num_seqs, max_blocks;
+  int T, h, Hkv, D, R, num_seqs, max_blocks;
+  int kvc2;          // base columns: 2 * Hkv * D
+  int n_base_tiles;  // base column tiles in the grid (0 when the base part is not written)
+  int write_lr;      // the grid has one low-rank tile after the base tiles
   RopeFreqs freqs;
 };
 
-// 64-byte rows of 4 16-byte chunks; chunk index XOR (row / 2) % 4.
-__device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
-  return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+// Waits for an mbarrier phase; gives up (LRKV_ERR_TIMEOUT, false) after
+// kWaitCycles, or early once another role has raised the abort flag.
+__device__ __forceinline__ bool wait_ab(uint32_t bar, uint32_t parity, int32_t* st,
+                                        const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag != 0) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      report(st, LRKV_ERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
-  const int n = pred ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+__device__ __forceinline__ uint4 pack8(const uint32_t* v) {
+  return make_uint4(pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                    pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                    pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                    pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7])));
 }
 
-__global__ void __launch_bounds__(NTHR) append_gemm_kernel(const __grid_constant__ AppendParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t sb = smem_u32(smem);
-  int* rowinfo = reinterpret_cast<int*>(smem + (SMEM_PIPE > SMEM_EPI ? SMEM_PIPE : SMEM_EPI));
+__global__ void __launch_bounds__(kThreads, 1)
+    append_tc_kernel(const __grid_constant__ AppendParams p,
+                     const __grid_constant__ CUtensorMap tm_xb,   // X of the base columns
+                     const __grid_constant__ CUtensorMap tm_xl,   // X of the low-rank columns
+                     const __grid_constant__ CUtensorMap tm_w) {  // W_cat [N][h]
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 8 * B_COUNT + 4);
+
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-  const int wm = warp >> 2, wn = warp & 3;  // 2 x 4 warps, 64 x 32 each
+  const bool lr_tile = static_cast<int>(blockIdx.x) >= p.n_base_tiles;
+  const int n0 = lr_tile ? p.kvc2 : static_cast<int>(blockIdx.x) * AN;  // first output column
+  const int width = lr_tile ? 2 * p.R : min(AN, p.kvc2 - n0);          // multiple of 16
+  const int m0 = static_cast<int>(blockIdx.y) * AM;
+  const int KT = p.h / AK;
 
-  auto load_stage = [&](int s, int k0) {
-    const uint32_t xa = sb + s * 2 * TILE_BYTES, wa = xa + TILE_BYTES;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int v = tid + i * NTHR;  // 512 16-byte vectors per operand
-      const int row = v >> 2, ch = v & 3;
-      const int xr = m0 + row, wr = n0 + row;
-      const bool px = xr < p.T, pw = wr < p.N;
-      const __nv_bfloat16* xs = p.X + static_cast<int64_t>(px ? xr : 0) * p.h + k0 + ch * 8;
-      const __nv_bfloat16* ws = p.W + static_cast<int64_t>(pw ? wr : 0) * p.h + k0 + ch * 8;
-      cp_async16(xa + sw_off(row, ch), xs, px);
-      cp_async16(wa + sw_off(row, ch), ws, pw);
-    }
-  };
-
-  float acc[4][4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
-
-  const int KT = p.h / BK;
-#pragma unroll
-  for (int s = 0; s < NSTAGE - 1; ++s) {
-    if (s < KT) load_stage(s, s * BK);
-    cp_commit();
+  if (tid == 0) {
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
   }
-  for (int kt = 0; kt < KT; ++kt) {
-    cp_wait<NSTAGE - 2>();
-    __syncthreads();
-    const int nk = kt + NSTAGE - 1;
-    if (nk < KT) load_stage(nk % NSTAGE, nk * BK);
-    cp_commit();
-    const int s = kt % NSTAGE;
-    const uint32_t xa = sb + s * 2 * TILE_BYTES, wa = xa + TILE_BYTES;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {  // two k16 steps per BK = 32
-      uint32_t af[4][4], bfr[2][4];
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int mi = lane >> 3;
-        const int row = wm * 64 + mt * 16 + (lane & 7) + (mi & 1) * 8;
-        const int ch = kk * 2 + (mi >> 1);
-        ldsm_x4(af[mt], xa + sw_off(row, ch));
-      }
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        // W rows are output columns (B "col" operand): non-transposed ldmatrix
-        const int mi = lane >> 3;
-        const int row = wn * 32 + np * 16 + (lane & 7) + (mi >> 1) * 8;
-        const int ch = kk * 2 + (mi & 1);
-        ldsm_x4(bfr[np], wa + sw_off(row, ch));
-      }
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-          mma16816(acc[mt][nt], af[mt], bfr[nt >> 1][(nt & 1) * 2], bfr[nt >> 1][(nt & 1) * 2 + 1]);
-    }
-  }
-  cp_wait<0>();
+  if (warp == 1) tc::alloc(smem_u32(tmem_slot), kTmemCols);
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tmem_slot;
 
-  // ---- stage the fp32 tile and the per-row slot info
-  float* ep = reinterpret_cast<float*>(smem);
-#pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int r = wm * 64 + mt * 16 + (lane >> 2);
-      const int c = wn * 32 + nt * 8 + (lane & 3) * 2;
-      ep[r * EPI_PITCH + c] = acc[mt][nt][0];
-      ep[r * EPI_PITCH + c + 1] = acc[mt][nt][1];
-      ep[(r + 8) * EPI_PITCH + c] = acc[mt][nt][2];
-      ep[(r + 8) * EPI_PITCH + c + 1] = acc[mt][nt][3];
+  if (warp == 0) {
+    // =========================================================== producer
+    const CUtensorMap* xm = lr_tile ? &tm_xl : &tm_xb;
+    if (lane == 0) {
+      prefetch_tmap(xm);
+      prefetch_tmap(&tm_w);
+      bool ok = true;
+      int issued = 0;
+      for (int kt = 0; kt < KT; ++kt) {
+        const int s = kt % NST;
+        if (kt >= NST && !wait_ab(bar(B_EMPTY + s), ((kt / NST) - 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = sbase + s * STAGE;
+        mbar_arrive_expect_tx(bar(B_FULL + s), STAGE);
+        tma_load_2d(st, xm, kt * AK, m0, bar(B_FULL + s));
+        tma_load_2d(st + A_BYTES, &tm_w, kt * AK, n0, bar(B_FULL + s));
+        ++issued;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        // no copy may still be landing when the CTA leaves
+        for (int j = issued > NST ? issued - NST : 0; j < issued; ++j)
+          wait_ab(bar(B_FULL + j % NST), (j / NST) & 1, p.status, nullptr);
+      }
     }
-  if (tid < BM) {
-    const int t = m0 + tid;
+    __syncwarp();
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    const uint32_t idesc = tc::idesc_f16(AM, width, true, false, false);
+    bool ok = true;
+    int issued = 0;
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % NST;
+      ok = __all_sync(0xffffffffu, wait_ab(bar(B_FULL + s), (kt / NST) & 1, p.status, abort_flag));
+      if (!ok) break;
+      tc::fence_after();
+      if (tc::elect_one()) {
+        const uint32_t st = sbase + s * STAGE;
+        const uint64_t ad = tc::sdesc(st, 16, 1024, 2);
+        const uint64_t bd = tc::sdesc(st + A_BYTES, 16, 1024, 2);
+#pragma unroll
+        for (int k = 0; k < AK / 16; ++k)  // 32 bytes along K per step, inside the swizzle row
+          tc::mma_ss(tbase, ad + 2 * k, bd + 2 * k, idesc, (kt > 0 || k > 0) ? 1u : 0u);
+        tc::commit(bar(B_EMPTY + s));
+        if (kt == KT - 1) tc::commit(bar(B_ACC));
+      }
+      __syncwarp();
+      ++issued;
+    }
+    if (!ok) {
+      if (lane == 0) *abort_flag = 1;
+      if (issued > 0) {
+        if (tc::elect_one()) tc::commit(bar(B_DRAIN));
+        __syncwarp();
+        wait_ab(bar(B_DRAIN), 0, p.status, nullptr);
+      }
+    }
+  } else if (warp >= 4) {
+    // ============================================================== epilogue
+    const int ew = warp - 4;
+    const int grp = ew >> 2;  // column half [128 grp, 128 grp + 128) of the tile
+    const int row = (ew & 3) * 32 + lane;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(32 * (ew & 3)) << 16);
+    // this thread's token: block and row of its slot (skipped when out of range)
+    const int t = m0 + row;
     int blk = -1, pos = 0;
     if (t < p.T) {
       const int s = __ldg(p.seq_rows + t);
       pos = __ldg(p.positions + t);
       if (s < 0 || s >= p.num_seqs || pos < 0 || pos >= p.max_blocks * kBlock) {
-        if (blockIdx.x == 0) report(p.status, LRKV_ERR_INDEX);
+        if (blockIdx.x == 0 && grp == 0) report(p.status, LRKV_ERR_INDEX);
       } else {
         const int b = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks + pos / kBlock);
         if (b < 0 || b >= p.num_blocks) {
-          if (blockIdx.x == 0) report(p.status, LRKV_ERR_INDEX);
+          if (blockIdx.x == 0 && grp == 0) report(p.status, LRKV_ERR_INDEX);
         } else {
           blk = b;
         }
       }
     }
-    rowinfo[tid * 2] = blk;
-    rowinfo[tid * 2 + 1] = pos;
-  }
-  __syncthreads();
-
-  // ---- rotate / cast / scatter, 8 columns per task
-  const int kvc = p.Hkv * p.D;
-  const int half = p.D / 2;
-  for (int task = tid; task < BM * (BN / 8); task += NTHR) {
-    const int r = task / (BN / 8), c8 = (task % (BN / 8)) * 8;
-    const int n = n0 + c8;
-    const int blk = rowinfo[r * 2];
-    if (n >= p.N || blk < 0) continue;
-    const int pos = rowinfo[r * 2 + 1];
-    const float* src = ep + r * EPI_PITCH + c8;
-    float v[8];
-    __nv_bfloat16* dst;
-    if (n < kvc) {  // K: rotate with the partner half of the same head
-      const int kv = n / p.D, j0 = n % p.D;
-      const bool lo = j0 < half;
-      const float* partner = src + (lo ? half : -half);
+    const int slot_row = pos % kBlock;
+    const int c_beg = grp * 128, c_end = min(width, c_beg + 128);
+    const bool ok = __all_sync(0xffffffffu, wait_ab(bar(B_ACC), 0, p.status, abort_flag));
+    if (ok && c_beg < c_end) {
+      tc::fence_after();
+      const int half = p.D / 2;
+      const int kvc = p.kvc2 / 2;
+      for (int c = c_beg; c < c_end; c += 16) {
+        const int n = n0 + c;  // global output column of this 16-column group
+        if (lr_tile) {
+          uint32_t v[16];
+          tc::ld_x16(tl + c, v);
+          tc::wait_ld();
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int jj = (j0 + e) % half;
-        const float2 cs = rope_cos_sin(pos, p.freqs.hi[jj], p.freqs.lo[jj]);
-        v[e] = lo ? (src[e] * cs.x - partner[e] * cs.y) : (src[e] * cs.x + partner[e] * cs.y);
+          for (int e = 0; e < 2; ++e) {
+            const int nn = n - p.kvc2 + 8 * e;  // low-rank column in [0, 2r)
+            if (blk >= 0 && nn < 2 * p.R) {
+              const int plane = nn / p.R, k0 = nn % p.R;
+              *reinterpret_cast<uint4*>(p.lr_pool + ((static_cast<int64_t>(blk) * 2 + plane) * kBlock +
+                                                     slot_row) * p.R + k0) = pack8(v + 8 * e);
+            }
+          }
+        } else if (n < kvc) {
+          // K: rotate the pair (j, j + d/2) of the head; the partner group sits
+          // d/2 columns further in the same tile half (heads are d-aligned)
+          const int j0 = n % p.D;
+          if (j0 >= half) continue;  // handled with its low half
+          uint32_t lo[16], hi[16];
+          tc::ld_x16(tl + c, lo);
+          tc::ld_x16(tl + c + half, hi);
+          tc::wait_ld();
+          uint32_t rl[16], rh[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 cs = rope_cos_sin_fast(pos, p.freqs.hi[j0 + e], p.freqs.lo[j0 + e]);
+            const float a = __uint_as_float(lo[e]), b = __uint_as_float(hi[e]);
+            rl[e] = __float_as_uint(fmaf(a, cs.x, -(b * cs.y)));
+            rh[e] = __float_as_uint(fmaf(b, cs.x, a * cs.y));
+          }
+          if (blk >= 0) {
+            __nv_bfloat16* dst = p.base_pool + (((static_cast<int64_t>(blk) * 2 + 0) * p.Hkv + n / p.D) * kBlock +
+                                                slot_row) * p.D + j0;
+            *reinterpret_cast<uint4*>(dst) = pack8(rl);
+            *reinterpret_cast<uint4*>(dst + 8) = pack8(rl + 8);
+            *reinterpret_cast<uint4*>(dst + half) = pack8(rh);
+            *reinterpret_cast<uint4*>(dst + half + 8) = pack8(rh + 8);
+          }
+        } else {
+          // V: stored as computed
+          uint32_t v[16];
+          tc::ld_x16(tl + c, v);
+          tc::wait_ld();
+          if (blk >= 0) {
+            const int nn = n - kvc;
+            __nv_bfloat16* dst = p.base_pool + (((static_cast<int64_t>(blk) * 2 + 1) * p.Hkv + nn / p.D) * kBlock +
+                                                slot_row) * p.D + nn % p.D;
+            *reinterpret_cast<uint4*>(dst) = pack8(v);
+            *reinterpret_cast<uint4*>(dst + 8) = pack8(v + 8);
+          }
+        }
       }
-      dst = p.base_pool + (((static_cast<int64_t>(blk) * 2 + 0) * p.Hkv + kv) * kBlock + pos % kBlock) * p.D + j0;
-    } else if (n < 2 * kvc) {
-      const int nn = n - kvc, kv = nn / p.D, j0 = nn % p.D;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = src[e];
-      dst = p.base_pool + (((static_cast<int64_t>(blk) * 2 + 1) * p.Hkv + kv) * kBlock + pos % kBlock) * p.D + j0;
-    } else {
-      const int nn = n - 2 * kvc;  // [0, 2R)
-      const int plane = nn / p.R, k0 = nn % p.R;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = src[e];
-      dst = p.lr_pool + ((static_cast<int64_t>(blk) * 2 + plane) * kBlock + pos % kBlock) * p.R + k0;
     }
-    uint4 pk;
-    pk.x = pack_bf16(v[0], v[1]);
-    pk.y = pack_bf16(v[2], v[3]);
-    pk.z = pack_bf16(v[4], v[5]);
-    pk.w = pack_bf16(v[6], v[7]);
-    *reinterpret_cast<uint4*>(dst) = pk;
   }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tbase, kTmemCols);
+  }
+}
+
+// Tensor map over a row-major bf16 matrix [rows][h], box {64, box_rows},
+// 128-byte swizzle (one box row = one swizzle row).
+bool make_kmajor_map(const void* base, int64_t rows, int h, int box_rows, CUtensorMap* map) {
+  return make_bf16_2d_map(base, h, rows, static_cast<int64_t>(h) * 2, AK, box_rows, 128, map);
 }
 
 }  // namespace
 
-lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X, int T,
+lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X_base, const void* X_lr, int T,
                                const int32_t* positions, const int32_t* seq_rows,
                                const int32_t* block_tables, int num_seqs, int max_blocks,
                                const void* W_cat, void* base_pool, void* lr_pool,
                                int64_t num_blocks, int32_t* status, cudaStream_t stream) {
-  if (T == 0) return LRKV_OK;
+  if (T == 0 || (X_base == nullptr && X_lr == nullptr)) return LRKV_OK;
   AppendParams p{};
-  p.X = static_cast<const __nv_bfloat16*>(X);
-  p.W = static_cast<const __nv_bfloat16*>(W_cat);
   p.positions = positions;
   p.seq_rows = seq_rows;
   p.block_tables = block_tables;
@@ -229,13 +300,22 @@ lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X, int T,
   p.Hkv = cfg.n_kv_heads;
   p.D = cfg.head_dim;
   p.R = cfg.rank;
-  p.N = 2 * cfg.n_kv_heads * cfg.head_dim + 2 * cfg.rank;
   p.num_seqs = num_seqs;
   p.max_blocks = max_blocks;
+  p.kvc2 = 2 * cfg.n_kv_heads * cfg.head_dim;
+  p.n_base_tiles = X_base != nullptr ? (p.kvc2 + AN - 1) / AN : 0;
+  p.write_lr = X_lr != nullptr ? 1 : 0;
   rope_freqs(cfg, &p.freqs);
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(append_gemm_kernel), SMEM_TOTAL)) return LRKV_ERR_CUDA;
-  dim3 grid((p.N + BN - 1) / BN, (T + BM - 1) / BM);
-  append_gemm_kernel<<<grid, NTHR, SMEM_TOTAL, stream>>>(p);
+  const int64_t N = p.kvc2 + 2 * cfg.rank;
+  CUtensorMap xb, xl, wm;
+  const void* xb_src = X_base != nullptr ? X_base : X_lr;
+  const void* xl_src = X_lr != nullptr ? X_lr : X_base;
+  if (!make_kmajor_map(xb_src, T, cfg.hidden, AM, &xb) || !make_kmajor_map(xl_src, T, cfg.hidden, AM, &xl) ||
+      !make_kmajor_map(W_cat, N, cfg.hidden, AN, &wm))
+    return LRKV_ERR_CUDA;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(append_tc_kernel), SMEM_TOTAL)) return LRKV_ERR_CUDA;
+  dim3 grid(p.n_base_tiles + p.write_lr, (T + AM - 1) / AM);
+  append_tc_kernel<<<grid, kThreads, SMEM_TOTAL, stream>>>(p, xb, xl, wm);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }
 

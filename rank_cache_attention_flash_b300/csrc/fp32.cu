@@ -20,8 +20,9 @@ namespace {
 constexpr int kChunk = 128;
 
 struct Fp32AppendParams {
-  const float* X;
-  const float* W;  // [N][h]
+  const float* X_base;  // hidden states of the base columns (NULL: base part not written)
+  const float* X_lr;    // hidden states of the low-rank columns (NULL: low-rank part not written)
+  const float* W;       // [N][h]
   const int32_t* positions;
   const int32_t* seq_rows;
   const int32_t* block_tables;
@@ -46,7 +47,11 @@ __global__ void append_fp32_kernel(const __grid_constant__ Fp32AppendParams p) {
     if (threadIdx.x == 0) report(p.status, LRKV_ERR_INDEX);
     return;
   }
-  for (int k = threadIdx.x; k < p.h; k += blockDim.x) xs[k] = p.X[static_cast<int64_t>(t) * p.h + k];
+  // xs[0, h): the base columns' hidden state; xs[h, 2h): the low-rank columns'
+  for (int k = threadIdx.x; k < p.h; k += blockDim.x) {
+    if (p.X_base != nullptr) xs[k] = p.X_base[static_cast<int64_t>(t) * p.h + k];
+    if (p.X_lr != nullptr) xs[p.h + k] = p.X_lr[static_cast<int64_t>(t) * p.h + k];
+  }
   __syncthreads();
   const int row = pos % kBlock, half = p.D / 2;
   const int kvc = p.Hkv * p.D;
@@ -54,11 +59,13 @@ __global__ void append_fp32_kernel(const __grid_constant__ Fp32AppendParams p) {
   const int units = n_pairs + kvc + 2 * p.R;
   auto dot = [&](int n) {
     const float* w = p.W + static_cast<int64_t>(n) * p.h;
+    const float* x = n < 2 * kvc ? xs : xs + p.h;
     float acc = 0.f;
-    for (int k = 0; k < p.h; ++k) acc = fmaf(w[k], xs[k], acc);
+    for (int k = 0; k < p.h; ++k) acc = fmaf(w[k], x[k], acc);
     return acc;
   };
   for (int u = threadIdx.x; u < units; u += blockDim.x) {
+    if ((u < n_pairs + kvc) ? p.X_base == nullptr : p.X_lr == nullptr) continue;
     if (u < n_pairs) {
       const int kv = u / half, j = u % half;
       const float x = dot(kv * p.D + j), y = dot(kv * p.D + j + half);
@@ -255,14 +262,15 @@ lrkv_status attn_fp32(const lrkv_config& cfg, const float* q, const int32_t* row
 
 }  // namespace
 
-lrkv_status launch_append_fp32(const lrkv_config& cfg, const void* X, int T,
+lrkv_status launch_append_fp32(const lrkv_config& cfg, const void* X_base, const void* X_lr, int T,
                                const int32_t* positions, const int32_t* seq_rows,
                                const int32_t* block_tables, int num_seqs, int max_blocks,
                                const void* W_cat, void* base_pool, void* lr_pool,
                                int64_t num_blocks, int32_t* status, cudaStream_t stream) {
-  if (T == 0) return LRKV_OK;
+  if (T == 0 || (X_base == nullptr && X_lr == nullptr)) return LRKV_OK;
   Fp32AppendParams p{};
-  p.X = static_cast<const float*>(X);
+  p.X_base = static_cast<const float*>(X_base);
+  p.X_lr = static_cast<const float*>(X_lr);
   p.W = static_cast<const float*>(W_cat);
   p.positions = positions;
   p.seq_rows = seq_rows;
@@ -278,7 +286,7 @@ lrkv_status launch_append_fp32(const lrkv_config& cfg, const void* X, int T,
   p.num_seqs = num_seqs;
   p.max_blocks = max_blocks;
   rope_freqs(cfg, &p.freqs);
-  const size_t smem = static_cast<size_t>(cfg.hidden) * 4;
+  const size_t smem = static_cast<size_t>(cfg.hidden) * 2 * 4;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(append_fp32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)

@@ -143,6 +143,27 @@ bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* l
   return true;
 }
 
+// 2-D map over a bf16 matrix whose rows hold `inner` elements `row_stride`
+// bytes apart; box {box_inner, box_rows} with the swizzle matching a box row
+// of `swizzle_span` bytes (128, 64, 32; anything else: none). Coordinates past
+// the matrix read as zero.
+bool make_bf16_2d_map(const void* base, int64_t inner, int64_t rows, int64_t row_stride, int box_inner,
+                      int box_rows, int swizzle_span, CUtensorMap* map) {
+  EncodeTiled enc = get_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle_span == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (swizzle_span == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (swizzle_span == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Low-rank pool map whose box is `box_cols` wide (>= rank): the columns past
 // the rank read as zero (out-of-bounds fill), so a rank-8 tile lands in smem
 // as a 16-column tile; rows of box_cols * 2 bytes with the matching swizzle.
@@ -224,28 +245,49 @@ const char* lrkv_status_string(lrkv_status s) {
 
 int32_t lrkv_version(void) { return 100; }
 
+namespace {
+
+lrkv_status append_common(const lrkv_config* cfg, const void* X_base, const void* X_lr, int32_t T,
+                          const int32_t* positions, const int32_t* seq_rows, const int32_t* block_tables,
+                          int32_t num_seqs, int32_t max_blocks, const void* W_cat, void* base_pool,
+                          void* lr_pool, int64_t num_blocks, int32_t* dev_status, lrkv_stream_t stream) {
+  lrkv_status st = check_config(cfg);
+  if (st != LRKV_OK) return st;
+  if (T < 0 || num_seqs < 0) return LRKV_ERR_INVALID_ARG;
+  if (T == 0) return LRKV_OK;
+  if ((X_base == nullptr && X_lr == nullptr) || positions == nullptr || seq_rows == nullptr ||
+      block_tables == nullptr || W_cat == nullptr || num_seqs == 0)
+    return LRKV_ERR_INVALID_ARG;
+  if ((X_base != nullptr && !aligned16(X_base)) || (X_lr != nullptr && !aligned16(X_lr)) || !aligned16(W_cat) ||
+      !aligned4(positions) || !aligned4(seq_rows) || !aligned4(block_tables))
+    return LRKV_ERR_INVALID_ARG;
+  if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->dtype == LRKV_FP32)
+    return launch_append_fp32(*cfg, X_base, X_lr, T, positions, seq_rows, block_tables, num_seqs, max_blocks,
+                              W_cat, base_pool, lr_pool, num_blocks, dev_status, s);
+  return launch_append_bf16(*cfg, X_base, X_lr, T, positions, seq_rows, block_tables, num_seqs, max_blocks,
+                            W_cat, base_pool, lr_pool, num_blocks, dev_status, s);
+}
+
+}  // namespace
+
 lrkv_status lrkv_append(const lrkv_config* cfg, const void* X, int32_t T,
                         const int32_t* positions, const int32_t* seq_rows,
                         const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
                         const void* W_cat, void* base_pool, void* lr_pool, int64_t num_blocks,
                         int32_t* dev_status, lrkv_stream_t stream) {
-  lrkv_status st = check_config(cfg);
-  if (st != LRKV_OK) return st;
-  if (T < 0 || num_seqs < 0) return LRKV_ERR_INVALID_ARG;
-  if (T == 0) return LRKV_OK;
-  if (X == nullptr || positions == nullptr || seq_rows == nullptr || block_tables == nullptr ||
-      W_cat == nullptr || num_seqs == 0)
-    return LRKV_ERR_INVALID_ARG;
-  if (!aligned16(X) || !aligned16(W_cat) || !aligned4(positions) || !aligned4(seq_rows) ||
-      !aligned4(block_tables))
-    return LRKV_ERR_INVALID_ARG;
-  if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cfg->dtype == LRKV_FP32)
-    return launch_append_fp32(*cfg, X, T, positions, seq_rows, block_tables, num_seqs, max_blocks,
-                              W_cat, base_pool, lr_pool, num_blocks, dev_status, s);
-  return launch_append_bf16(*cfg, X, T, positions, seq_rows, block_tables, num_seqs, max_blocks,
-                            W_cat, base_pool, lr_pool, num_blocks, dev_status, s);
+  return append_common(cfg, X, X, T, positions, seq_rows, block_tables, num_seqs, max_blocks, W_cat,
+                       base_pool, lr_pool, num_blocks, dev_status, stream);
+}
+
+lrkv_status lrkv_append_rebase(const lrkv_config* cfg, const void* X_base, const void* X_lr, int32_t T,
+                               const int32_t* positions, const int32_t* seq_rows,
+                               const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
+                               const void* W_cat, void* base_pool, void* lr_pool, int64_t num_blocks,
+                               int32_t* dev_status, lrkv_stream_t stream) {
+  return append_common(cfg, X_base, X_lr, T, positions, seq_rows, block_tables, num_seqs, max_blocks, W_cat,
+                       base_pool, lr_pool, num_blocks, dev_status, stream);
 }
 
 size_t lrkv_decode_workspace_bytes(const lrkv_config* cfg, int32_t num_queries, int32_t num_ctx,

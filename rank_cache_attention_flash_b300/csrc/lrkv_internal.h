@@ -55,6 +55,10 @@ void rope_freqs(const lrkv_config& cfg, RopeFreqs* f);
 // Tensor maps over the paged pools (lr_map may be NULL: base map only).
 bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
                     int64_t num_blocks, CUtensorMap* base_map, CUtensorMap* lr_map);
+// 2-D map over a bf16 matrix [rows][inner] (rows row_stride bytes apart),
+// box {box_inner, box_rows}, swizzle for box rows of swizzle_span bytes.
+bool make_bf16_2d_map(const void* base, int64_t inner, int64_t rows, int64_t row_stride, int box_inner,
+                      int box_rows, int swizzle_span, CUtensorMap* map);
 // Low-rank pool map with a box of box_cols (>= rank) columns, zero-filled past the rank.
 bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks, int box_cols,
                  CUtensorMap* lr_map);
@@ -68,7 +72,9 @@ bool make_run_maps(const lrkv_config& cfg, const void* base_pool, const void* lr
 lrkv_status launch_decode_bf16(const lrkv_config& cfg, const DecodeArgs& a,
                                const DecodePlan& plan, void* workspace, cudaStream_t stream);
 
-lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X, int T,
+// X_base feeds the base columns (K_base, V_base), X_lr the low-rank columns
+// (L_K, L_V); a NULL source leaves that part of the pools untouched.
+lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X_base, const void* X_lr, int T,
                                const int32_t* positions, const int32_t* seq_rows,
                                const int32_t* block_tables, int num_seqs, int max_blocks,
                                const void* W_cat, void* base_pool, void* lr_pool,
@@ -100,7 +106,7 @@ lrkv_status launch_prefill_bf16(const lrkv_config& cfg, const PrefillArgs& a,
                                 cudaStream_t stream);
 
 // fp32 path (plain FMA, no tensor cores).
-lrkv_status launch_append_fp32(const lrkv_config& cfg, const void* X, int T,
+lrkv_status launch_append_fp32(const lrkv_config& cfg, const void* X_base, const void* X_lr, int T,
                                const int32_t* positions, const int32_t* seq_rows,
                                const int32_t* block_tables, int num_seqs, int max_blocks,
                                const void* W_cat, void* base_pool, void* lr_pool,

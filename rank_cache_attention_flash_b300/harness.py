@@ -127,15 +127,15 @@ class GpuCase:
             setattr(self, k, v)
 
     # ------------------------------------------------------------------
-    def upload_inputs(self, stream=None) -> None:
-        """The step's inputs from pinned host memory: one host-to-device copy."""
-        with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
-            self.in_dev.copy_(self.in_host, non_blocking=True)
+    def upload_inputs(self) -> None:
+        """The step's inputs from pinned host memory: one host-to-device copy on
+        the current stream."""
+        self.in_dev.copy_(self.in_host, non_blocking=True)
 
-    def download_outputs(self, stream=None) -> None:
-        """The step's outputs to pinned host memory: one device-to-host copy."""
-        with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
-            self.out_host.copy_(self.out_dev, non_blocking=True)
+    def download_outputs(self) -> None:
+        """The step's outputs to pinned host memory: one device-to-host copy on
+        the current stream."""
+        self.out_host.copy_(self.out_dev, non_blocking=True)
 
     def setup(self) -> None:
         """Untimed: append the tokens cached before the step."""

@@ -38,6 +38,7 @@ BLOCK = 16  # tokens per paged block
 _S_WK, _S_WV, _S_AK, _S_AV, _S_BK, _S_BV = 3, 4, 5, 6, 7, 8
 _S_QDEC, _S_QPRE, _S_PERM, _S_LENS, _S_ADAPT = 9, 10, 11, 12, 13
 _S_XSTREAM = 1000  # + stream index
+_S_NEUTRAL = 500_000  # added to a hidden-state stream index: its adapter-free twin
 
 
 def _gen(seed: int, stream: int) -> torch.Generator:
@@ -137,6 +138,20 @@ class Case:
         if not parts:
             return torch.empty(0, self.shape.hidden, dtype=self.shape.torch_dtype)
         return torch.cat(parts, 0) if len(parts) > 1 else parts[0]
+
+    def seq_hidden_neutral(self, s: int, start: int = 0, stop: Optional[int] = None) -> torch.Tensor:
+        """Adapter-free hidden states of sequence ``s`` at positions [start, stop):
+        the same layout as ``seq_hidden`` drawn from streams of their own (a
+        re-based cache takes its base part from these)."""
+        q = self.seqs[s]
+        shifted = dataclasses.replace(q, prefix_stream=q.prefix_stream + _S_NEUTRAL,
+                                      own_stream=q.own_stream + _S_NEUTRAL)
+        saved = self.seqs[s]
+        self.seqs[s] = shifted
+        try:
+            return self.seq_hidden(s, start, stop)
+        finally:
+            self.seqs[s] = saved
 
     # ----- append plans --------------------------------------------------
     def setup_appends(self):

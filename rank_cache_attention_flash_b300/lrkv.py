@@ -4,7 +4,7 @@ streams. The library must be built (``python -m rank_cache_attention_flash_b300.
 nothing here falls back to another implementation.
 
 Entry points mirror the C ABI in ``include/lrkv.h``:
-  append, attn_decode, attn_prefill, decode_workspace_bytes,
+  append, append_rebase, attn_decode, attn_prefill, decode_workspace_bytes,
   prefill_workspace_bytes, status_string, version, attn_decode_noalloc.
 """
 from __future__ import annotations
@@ -25,7 +25,7 @@ STATUS = {0: "LRKV_OK", 1: "LRKV_ERR_INVALID_ARG", 2: "LRKV_ERR_UNSUPPORTED", 3:
           4: "LRKV_ERR_INDEX", 5: "LRKV_ERR_TIMEOUT", 6: "LRKV_ERR_WORKSPACE"}
 BF16, FP32 = 0, 1
 
-EXPORTS = ("lrkv_append", "lrkv_attn_decode", "lrkv_decode_workspace_bytes", "lrkv_attn_prefill",
+EXPORTS = ("lrkv_append", "lrkv_append_rebase", "lrkv_attn_decode", "lrkv_decode_workspace_bytes", "lrkv_attn_prefill",
            "lrkv_prefill_workspace_bytes", "lrkv_status_string", "lrkv_version",
            "lrkv_attn_decode_noalloc")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # LRKV_NOALLOC_SCRATCH_BYTES in lrkv.h
@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
     cfgp = ctypes.POINTER(Config)
     lib.lrkv_append.argtypes = [cfgp, _P, _I32, _P, _P, _P, _I32, _I32, _P, _P, _P, _I64, _P, _P]
     lib.lrkv_append.restype = ctypes.c_int
+    lib.lrkv_append_rebase.argtypes = [cfgp, _P, _P, _I32, _P, _P, _P, _I32, _I32, _P, _P, _P, _I64, _P, _P]
+    lib.lrkv_append_rebase.restype = ctypes.c_int
     lib.lrkv_attn_decode.argtypes = [cfgp, _P, _I32, _P, _I32, _P, _P, _I32, _P, _I32, _I32, _P, _P,
                                      _I64, _P, _P, _I32, _F, _P, _P, _SZ, _P, _P]
     lib.lrkv_attn_decode.restype = ctypes.c_int
@@ -169,6 +171,33 @@ def append(cfg: Config, X: torch.Tensor, positions: torch.Tensor, seq_rows: torc
                            _ptr(W_cat), _ptr(base_pool), _ptr(lr_pool), base_pool.shape[0],
                            _ptr(status), _stream(stream))
     _raise(code, "lrkv_append")
+
+
+def append_rebase(cfg: Config, X_base: Optional[torch.Tensor], X_lr: Optional[torch.Tensor],
+                  positions: torch.Tensor, seq_rows: torch.Tensor, block_tables: torch.Tensor,
+                  W_cat: torch.Tensor, base_pool: torch.Tensor, lr_pool: torch.Tensor,
+                  status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """lrkv_append_rebase: base rows from X_base, low-rank rows from X_lr (either
+    may be None: that part of the pools is left as it is)."""
+    lib = load()
+    dev = base_pool.device
+    _check(X_base, "X_base", cfg.torch_dtype, dev)
+    _check(X_lr, "X_lr", cfg.torch_dtype, dev)
+    _check(W_cat, "W_cat", cfg.torch_dtype, dev)
+    for t, n in ((positions, "positions"), (seq_rows, "seq_rows"), (block_tables, "block_tables")):
+        _check(t, n, torch.int32, dev)
+    _check(status, "status", torch.int32, dev)
+    T = positions.numel()
+    for X in (X_base, X_lr):
+        if X is not None and X.shape != (T, cfg.hidden):
+            raise ValueError("append_rebase: X must be [T, h]")
+    if seq_rows.numel() != T or W_cat.shape != (cfg.n_cols, cfg.hidden):
+        raise ValueError("append_rebase: shape mismatch")
+    code = lib.lrkv_append_rebase(ctypes.byref(cfg), _ptr(X_base), _ptr(X_lr), T, _ptr(positions),
+                                  _ptr(seq_rows), _ptr(block_tables), block_tables.shape[0],
+                                  block_tables.shape[1], _ptr(W_cat), _ptr(base_pool), _ptr(lr_pool),
+                                  base_pool.shape[0], _ptr(status), _stream(stream))
+    _raise(code, "lrkv_append_rebase")
 
 
 def decode_workspace_bytes(cfg: Config, num_queries: int, num_ctx: int, max_ctx_len: int,

@@ -336,6 +336,89 @@ def pin_bf16_cache_variant_is_exact_on_representable_data(O):
     assert 1e-5 < rel < 2 ** -7, rel
 
 
+# ------------------------------------------------------ re-based cache pins
+def pin_rebase_integer_bruteforce(O):
+    """ReBaseShared append: base rows from one integer source, low-rank rows from
+    another, recomputed with Python ints; a source of None leaves its part of
+    the pools untouched (NaN sentinels)."""
+    r = _rng(14)
+    h, Hkv, d, rank = 10, 2, 4, 2
+    Xb = r.integers(-3, 4, size=(4, h)).astype(np.float64)
+    Xl = r.integers(-3, 4, size=(4, h)).astype(np.float64)
+    W = {k: r.integers(0, 2, size=(h, n)).astype(np.float64)
+         for k, n in (("W_K", Hkv * d), ("W_V", Hkv * d), ("A_K", rank), ("A_V", rank))}
+    pos = np.array([0, 0, 16, 0])
+    seqs = np.array([0, 1, 1, 2])
+    bt = np.array([[3, 1], [0, 6], [5, 2]])
+    slot = {0: (3, 0), 1: (0, 0), 2: (6, 0), 3: (5, 0)}
+
+    def isum(X, n, M, col):
+        return sum(int(X[n, k]) * int(M[k, col]) for k in range(h))
+
+    for xb, xl in ((Xb, Xl), (Xb, None), (None, Xl)):
+        bp = np.full((8, 2, Hkv, 16, d), np.nan)
+        lp = np.full((8, 2, 16, rank), np.nan)
+        O.rebase_pools(bp, lp, xb, xl, pos, seqs, bt, W["W_K"], W["W_V"], W["A_K"], W["A_V"], Hkv, d, 10000.0)
+        for n in range(4):
+            blk, row = slot[n]
+            for hh in range(Hkv):
+                for j in range(d):
+                    if xb is None:
+                        assert np.isnan(bp[blk, :, hh, row, j]).all()
+                        continue
+                    assert bp[blk, 1, hh, row, j] == isum(Xb, n, W["W_V"], hh * d + j)
+                    if pos[n] == 0:
+                        assert bp[blk, 0, hh, row, j] == isum(Xb, n, W["W_K"], hh * d + j)
+            for k in range(rank):
+                if xl is None:
+                    assert np.isnan(lp[blk, :, row, k]).all()
+                    continue
+                assert lp[blk, 0, row, k] == isum(Xl, n, W["A_K"], k)
+                assert lp[blk, 1, row, k] == isum(Xl, n, W["A_V"], k)
+
+
+def pin_rebased_kv_stacked_weights(O):
+    """A re-based agent's keys and values are one projection of the two sources
+    side by side, [X_base | X_lr] times the stacked weights [W; A·B_i], before
+    the rotation; with X_base = X_lr they are the ordinary agent_kv."""
+    r = _rng(15)
+    h, Hkv, d, rank = 12, 2, 8, 3
+    w = _small_weights(r, h, Hkv, d, rank)
+    T = 11
+    Xb = r.standard_normal((T, h))
+    Xl = r.standard_normal((T, h))
+    pos = np.arange(T) + 3
+    for i in range(3):
+        k, v = O.agent_kv_rebased(Xb, Xl, pos, w["W_K"], w["W_V"], w["A_K"], w["A_V"], w["B_K"][i],
+                                  w["B_V"][i], Hkv, d, 10000.0)
+        XX = np.hstack([Xb, Xl])
+        k_pre = XX @ np.vstack([w["W_K"], w["A_K"] @ w["B_K"][i]])
+        v_want = XX @ np.vstack([w["W_V"], w["A_V"] @ w["B_V"][i]])
+        assert np.allclose(k, O.apply_rope(k_pre.reshape(T, Hkv, d), pos, 10000.0), rtol=1e-12, atol=1e-12)
+        assert np.allclose(v, v_want.reshape(T, Hkv, d), rtol=1e-12, atol=1e-12)
+        k1, v1 = O.agent_kv(Xb, pos, w["W_K"], w["W_V"], w["A_K"], w["A_V"], w["B_K"][i], w["B_V"][i],
+                            Hkv, d, 10000.0)
+        k2, v2 = O.agent_kv_rebased(Xb, Xb, pos, w["W_K"], w["W_V"], w["A_K"], w["A_V"], w["B_K"][i],
+                                    w["B_V"][i], Hkv, d, 10000.0)
+        assert np.allclose(k1, k2, rtol=1e-13, atol=1e-13) and np.allclose(v1, v2, rtol=1e-13, atol=1e-13)
+    # attention over the re-based cache: a query over K_i, V_i as defined above
+    q = r.standard_normal((1, 4, d))
+    got = O.attend(Xb, 1, q, [T - 1], w, Hkv, d, 10000.0, 0.4, X_lr=Xl)
+    k, v = O.agent_kv_rebased(Xb, Xl, np.arange(T), w["W_K"], w["W_V"], w["A_K"], w["A_V"], w["B_K"][1],
+                              w["B_V"][1], Hkv, d, 10000.0)
+    assert np.allclose(got, _sdpa(q * 0.4 * math.sqrt(d), k, v, causal=False), rtol=1e-12, atol=1e-13)
+    # the bf16-stored variant is exact when every component is bf16-representable
+    Xi = r.integers(-2, 3, size=(T, h)).astype(np.float64)
+    Xj = r.integers(-2, 3, size=(T, h)).astype(np.float64)
+    Wi = {k_: r.integers(0, 2, size=x.shape).astype(np.float64) for k_, x in w.items() if k_[0] in "WA"}
+    z = np.zeros(T, dtype=int)
+    e1 = O.agent_kv_rebased(Xi, Xj, z, Wi["W_K"], Wi["W_V"], Wi["A_K"], Wi["A_V"], w["B_K"][0], w["B_V"][0],
+                            Hkv, d, 10000.0)
+    e2 = O.agent_kv_rebased(Xi, Xj, z, Wi["W_K"], Wi["W_V"], Wi["A_K"], Wi["A_V"], w["B_K"][0], w["B_V"][0],
+                            Hkv, d, 10000.0, "bf16")
+    assert np.allclose(e1[0], e2[0], rtol=1e-13, atol=1e-13) and np.allclose(e1[1], e2[1], rtol=1e-13, atol=1e-13)
+
+
 ALL_PINS = [
     pin_rope_closed_form, pin_rope_frequencies, pin_rope_invariants,
     pin_attention_sdpa_decode, pin_attention_sdpa_prefill, pin_attention_brute_force,
@@ -343,4 +426,5 @@ ALL_PINS = [
     pin_reordered_equals_materialised, pin_base_equals_ordinary_attention,
     pin_append_integer_bruteforce, pin_prefill_last_row_equals_decode, pin_multi_agent_batch,
     pin_round_bf16_matches_library, pin_bf16_cache_variant_is_exact_on_representable_data,
+    pin_rebase_integer_bruteforce, pin_rebased_kv_stacked_weights,
 ]

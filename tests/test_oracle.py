@@ -60,6 +60,13 @@ MUTATIONS = {
     "bf16_ties_away": ("u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000", "u = (u + 0x8000) & 0xFFFF0000"),
     "cache_variant_drops_rope": ("k = k + apply_rope((lk @ _f64(B_K_i)).reshape(T, n_kv_heads, head_dim), positions, base)",
                                  "k = k + (lk @ _f64(B_K_i)).reshape(T, n_kv_heads, head_dim)"),
+    "rebase_base_from_lowrank_source": ("kb, vb, _, _ = base_and_lowrank(X_base, positions,",
+                                        "kb, vb, _, _ = base_and_lowrank(X_lr if X_lr is not None else X_base, positions,"),
+    "rebase_lowrank_from_base_source": ("_, _, lk, lv = base_and_lowrank(X_lr, positions,",
+                                        "_, _, lk, lv = base_and_lowrank(X_base if X_base is not None else X_lr, positions,"),
+    "rebased_kv_lowrank_from_base": ("k_pre = k_pre + (X_lr @ _f64(A_K)) @ _f64(B_K_i)",
+                                     "k_pre = k_pre + (X_base @ _f64(A_K)) @ _f64(B_K_i)"),
+    "rebased_v_from_lowrank_source": ("        v = X_base @ _f64(W_V)\n", "        v = X_lr @ _f64(W_V)\n"),
     "swapped_B": ('return weights["B_K"][adapter], weights["B_V"][adapter]',
                   'return weights["B_V"][adapter], weights["B_K"][adapter]'),
 }
