@@ -51,7 +51,7 @@ METRIC = "LoRA-KV attention decode tok/s & GB/s (% of HBM), prefill TFLOP/s (% p
 FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = {"decode": ["decode.cu", "lrkv_device.cuh", "tcgen05.cuh"],
                   "prefill": ["prefill.cu", "lrkv_device.cuh", "tcgen05.cuh"],
-                  "append": ["append.cu", "lrkv_device.cuh"]}
+                  "append": ["append.cu", "lrkv_device.cuh", "tcgen05.cuh"]}
 
 
 # ----------------------------------------------------------------- helpers
@@ -72,12 +72,12 @@ def kernel_sha(kind: str) -> str:
 
 
 def committed_traffic(workload: str, kind: str):
-    """Per-launch DRAM bytes from a committed ncu capture, if the kernel source is
-    unchanged since; else None."""
+    """Per-launch DRAM bytes (read + write) of this part's kernel from a committed
+    ncu capture, if the kernel's sources are unchanged since; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    d = json.load(open(path)).get(workload)
+    d = json.load(open(path)).get(workload, {}).get(kind)
     if not d or d.get("source_sha") != kernel_sha(kind):
         return None
     return d.get("dram_bytes_per_launch")

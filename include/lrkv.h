@@ -180,9 +180,15 @@ lrkv_status lrkv_append_rebase(const lrkv_config* cfg, const void* X_base, const
  *   workspace    >= lrkv_decode_workspace_bytes(...) bytes (fp32 split partials
  *                and bookkeeping); contents need no initialisation and are
  *                garbage afterwards
+ * Two kernel launches: the split-KV sweep, then a merge of the splits that
+ * applies B_V.
  * A context with zero queries is skipped; ctx_lens[c] outside
  * [1, max_ctx_len] or a bad block / adapter id gives LRKV_ERR_INDEX in
- * dev_status and zero output for the affected queries.
+ * dev_status and zero output for the affected queries. A context with more
+ * queries than max_q_per_ctx gives LRKV_ERR_INDEX and zero output for the
+ * query heads past the planned rows; a query that no valid ctx_q_start range
+ * holds (ranges that decrease, or do not cover [0, num_queries)) gives
+ * LRKV_ERR_INDEX and zero output.
  */
 lrkv_status lrkv_attn_decode(const lrkv_config* cfg, const void* q, int32_t num_queries,
                              const int32_t* ctx_q_start, int32_t num_ctx,

@@ -253,10 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int qs = __ldg(p.ctx_q_start + ctx), qe = __ldg(p.ctx_q_start + ctx + 1);
   int len = __ldg(p.ctx_lens + ctx);
-  if (qs < 0 || qe > p.num_queries) {
+  if (qs < 0 || qe > p.num_queries || qs > qe) {  // this context's query range is broken: skipped
     if (tid == 0) report(p.status, LRKV_ERR_INDEX);
     return;
   }
+  // more queries on this context than max_q_per_ctx promised: the rows past
+  // the last chunk get no partial (the combine zeroes their output)
+  if (tid == 0 && chunk == 0 && split == 0 && (qe - qs) * p.g > p.n_chunks * p.rpi)
+    report(p.status, LRKV_ERR_INDEX);
   const int row0 = chunk * p.rpi;
   const int nrows = min(p.rpi, (qe - qs) * p.g - row0);
   if (nrows <= 0) return;
@@ -914,11 +918,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 struct CombineParams {
   const float* part_ml;
   const float* part_o;
+  const int32_t* ctx_q_start;
   const int32_t* adapter_ids;
   const __nv_bfloat16* B_V;
   __nv_bfloat16* out;
   int32_t* status;
-  int num_queries, Hq, Hkv, g, n_splits, n_adapters, has_bv;
+  int num_queries, num_ctx, Hq, Hkv, g, n_splits, n_adapters, has_bv;
+  int covered_rows;  // rows per context the decode grid covers (n_chunks * rows per item)
 };
 
 constexpr int kCombineBatch = 32;  // splits requested per round
@@ -941,6 +947,27 @@ __global__ void __launch_bounds__(CombineShape<D, R>::NT) combine_kernel(const _
   const int64_t pair = blockIdx.x;
   const int n = static_cast<int>(pair / p.Hq), m = static_cast<int>(pair % p.Hq);
   const int S = p.n_splits;
+  // the context holding query n (ctx_q_start is non-decreasing): its row of
+  // head m must lie inside the rows the decode grid covered, else no split
+  // wrote a partial for it and the output is zero
+  __shared__ int covered;
+  if (tid == 0) {
+    int lo = 0, hi = p.num_ctx;  // find the last c with ctx_q_start[c] <= n
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.ctx_q_start + mid) <= n) lo = mid;
+      else hi = mid;
+    }
+    const int q0 = __ldg(p.ctx_q_start + lo), q1 = __ldg(p.ctx_q_start + lo + 1);
+    const bool inside = q0 <= n && n < q1 && q0 >= 0 && q1 <= p.num_queries;
+    covered = inside && (n - q0) * p.g + m % p.g < p.covered_rows;
+    if (!covered) report(p.status, LRKV_ERR_INDEX);
+  }
+  __syncthreads();
+  if (!covered) {
+    if (tid < D) p.out[pair * D + tid] = __float2bfloat16_rn(0.f);
+    return;
+  }
   const int a = __ldg(p.adapter_ids + n);
   const bool bad = a < -1 || a >= p.n_adapters;
   const bool use_lr = p.has_bv && a >= 0 && !bad;
@@ -1055,6 +1082,9 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   CombineParams c{};
   c.part_ml = p.part_ml;
   c.part_o = p.part_o;
+  c.ctx_q_start = a.ctx_q_start;
+  c.num_ctx = a.num_ctx;
+  c.covered_rows = plan.n_chunks * plan.rows_per_item;
   c.adapter_ids = a.adapter_ids;
   c.B_V = static_cast<const __nv_bfloat16*>(a.B_V);
   c.out = static_cast<__nv_bfloat16*>(a.out);

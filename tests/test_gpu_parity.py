@@ -240,6 +240,72 @@ def test_bad_adapter_id_gives_zero_and_status(cuda_lib):
     assert_close(out[0:2].double().cpu().numpy(), oracle_decode_rows(case, rows=[0, 1], cache="bf16"), BF16_TOL)
 
 
+def test_zero_length_context_gives_zero_and_status(cuda_lib):
+    """ctx_lens = 0 is outside [1, max_ctx_len]: LRKV_ERR_INDEX, zero output for
+    that context's queries, the other context unaffected."""
+    case = I.long_decode(n_seqs=2, n=100)
+    g = GpuCase(case, pool_fill=0.0)
+    g.setup()
+    lens = g.dec_lens.clone()
+    lens[1] = 0
+    out = cuda_lib.attn_decode(g.cfg, g.dec_q, g.dec_q_start, g.dec_adapter, g.dec_bt, lens, g.dec_max_len,
+                               g.dec_max_q, g.base_pool, g.lr_pool, g.B_K, g.B_V, g.scale, status=g.status)
+    torch.cuda.synchronize()
+    assert g.device_status() == 4
+    assert float(out[1].float().abs().max()) == 0.0
+    assert_close(out[0:1].double().cpu().numpy(), oracle_decode_rows(case, rows=[0], cache="bf16"), BF16_TOL)
+
+
+def test_more_queries_than_max_q_per_ctx(cuda_lib):
+    """max_q_per_ctx smaller than a context's query count: LRKV_ERR_INDEX, the
+    query heads past the planned rows get zero output, the planned ones stay
+    exact."""
+    case = I.shared_decode(n=300, n_agents=8)
+    g = GpuCase(case, pool_fill=0.0)
+    g.setup()
+    # rank 16: 16 rows per chunk, g = 4 -> max_q_per_ctx = 4 plans one chunk of 4 queries
+    out = cuda_lib.attn_decode(g.cfg, g.dec_q, g.dec_q_start, g.dec_adapter, g.dec_bt, g.dec_lens,
+                               g.dec_max_len, 4, g.base_pool, g.lr_pool, g.B_K, g.B_V, g.scale,
+                               status=g.status)
+    torch.cuda.synchronize()
+    assert g.device_status() == 4
+    assert float(out[4:].float().abs().max()) == 0.0
+    assert_close(out[:4].double().cpu().numpy(), oracle_decode_rows(case, rows=[0, 1, 2, 3], cache="bf16"),
+                 BF16_TOL)
+
+
+def test_query_outside_every_context_range(cuda_lib):
+    """ctx_q_start that stops short of num_queries: the uncovered query gets
+    LRKV_ERR_INDEX and zero output, the covered ones stay exact."""
+    case = I.shared_decode(n=200)
+    g = GpuCase(case, pool_fill=0.0)
+    g.setup()
+    qstart = torch.tensor([0, 3], dtype=torch.int32, device=g.device)  # query 3 is in no range
+    out = cuda_lib.attn_decode(g.cfg, g.dec_q, qstart, g.dec_adapter, g.dec_bt, g.dec_lens, g.dec_max_len,
+                               g.dec_max_q, g.base_pool, g.lr_pool, g.B_K, g.B_V, g.scale, status=g.status)
+    torch.cuda.synchronize()
+    assert g.device_status() == 4
+    assert float(out[3].float().abs().max()) == 0.0
+    assert_close(out[:3].double().cpu().numpy(), oracle_decode_rows(case, rows=[0, 1, 2], cache="bf16"), BF16_TOL)
+
+
+def test_rope_base_500000(cuda_lib):
+    """A Llama-3-style RoPE base (500000): decode and prefill against the oracle."""
+    import dataclasses
+
+    sh = dataclasses.replace(I.shape_llama8b(16, 2), rope_base=500000.0)
+    seqs = [I.Seq(0, 272, 1 + a, 272, 77, a, "prefill") for a in range(2)]
+    case = I._build("rope_base_500k", sh, 0, seqs, [(0, 0), (0, 1), (0, -1)], [0, 1], False)
+    g, res = _run(case)
+    assert g.device_status() == 0
+    assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case, cache="bf16"), BF16_TOL,
+                 "decode")
+    w64 = weights64(case)
+    for p in range(g.n_pre):
+        rows, want = oracle_prefill_seq(case, p, w64=w64, cache="bf16")
+        assert_close(res["prefill"][rows].double().cpu().numpy(), want, BF16_TOL, f"prefill seq {p}")
+
+
 def test_workspace_too_small_is_rejected(cuda_lib):
     case = I.shared_decode(n=64)
     g = GpuCase(case, pool_fill=0.0)

@@ -18,12 +18,20 @@ pytestmark = pytest.mark.gpu
 NAN = float("nan")
 
 
-def _bits_close(got: torch.Tensor, want: torch.Tensor, ulps: int):
+def _bits_close(got: torch.Tensor, want: torch.Tensor, ulps: int, abs_slack: float = 0.0):
+    """Within `ulps` bf16 ulps of the larger magnitude, plus an absolute slack."""
     a, b = got.float(), want.float()
     big = torch.maximum(a.abs(), b.abs())
     ulp = torch.where(big > 0, torch.exp2(torch.floor(torch.log2(big.clamp(min=1e-30))) - 7),
                       torch.zeros_like(big))
-    return bool(((a - b).abs() <= ulps * ulp).all())
+    return bool(((a - b).abs() <= ulps * ulp + abs_slack).all())
+
+
+# K_base is the fp32 rotation of integer projections |y| <= 256 (h = 256): the
+# rotation's fp32 cos/sin carry an absolute error near 2^-21, so a K value
+# whose exact rotation nearly cancels to 0 lands within 256 * 2^-21 ~ 1.2e-4 of
+# it rather than within one bf16 ulp of a tiny number.
+K_ABS_SLACK = 3e-4
 
 
 @pytest.mark.parametrize("mode", ["both", "base_only", "lowrank_only"])
@@ -72,7 +80,7 @@ def test_append_rebase_integer_sources(cuda_lib, mode):
             vm = written[:, 1]
             assert torch.equal(got[:, 1][vm].view(torch.int16), want[:, 1][vm].view(torch.int16)), "V_base"
             km = written[:, 0]
-            assert _bits_close(got[:, 0][km], want[:, 0][km], 1), "K_base beyond 1 ulp"
+            assert _bits_close(got[:, 0][km], want[:, 0][km], 1, K_ABS_SLACK), "K_base beyond 1 ulp"
         else:
             assert torch.equal(got[written].view(torch.int16), want[written].view(torch.int16)), "L_K / L_V"
 
