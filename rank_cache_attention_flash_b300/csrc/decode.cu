@@ -909,6 +909,699 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ================================================================ rebuild mode
+// Items whose rows all belong to one query, hence to one adapter (rank 64,
+// four rows per item: a query's four heads of a kv head). The item keeps B_K^T
+// of that adapter in shared memory (16 KB) instead of G (64 KB), and the
+// adapter K term is rebuilt per tile on chip, as the pages describe it:
+//   Y   = L_K B_K^T                      warp 1, tcgen05 (M = 128 tokens, N = d)
+//   K_a = K_base + RoPE(Y)               token threads, fp16, in place of K_base
+//   S   = K_a Q^T                        warp 2, tcgen05 (fp16)
+//   O^T += V_base^T P^T, O_lr^T += L_V^T P^T   warps 3 and 1
+// The two token warpgroups are two independent pipelines: warpgroup b takes
+// the tiles j = b, b + 2, ... with its own Y, S, P, O and O_lr buffers and its
+// own online softmax, and stores its own split partial (the combine merges
+// 2 x n_splits partials per query head). While one warpgroup waits on a tensor
+// or memory operation of its tile, the other works on the next tile.
+namespace rb {
+constexpr int kRows = 4;          // query rows per item (one query)
+constexpr uint32_t RY_COL = 0;     // [2][d]  Y of the pipeline's tile, fp32
+constexpr uint32_t RDT_COL = 256;  // [d]     e^{i delta theta_j} of this lane's token offset (cos, sin)
+constexpr uint32_t RS_COL = 384;   // [2][16] S
+constexpr uint32_t ROT_COL = 416;  // [2][16] O^T (lane = head dim)
+constexpr uint32_t ROL_COL = 448;  // [2][16] O_lr^T (lane = rank index)
+
+enum : int {
+  FULL = 0,    // [4] ring slot full (TMA bytes)
+  EMPTY = 4,   // [4] ring slot consumed: 4 token warps + two MMA commits
+  YF = 8,      // [2] Y complete (commit)
+  YR = 10,     // [2] Y read out (4 warps)
+  KA = 12,     // [2] K_a written (4 warps)
+  SF = 14,     // [2] S complete (commit)
+  SR = 16,     // [2] S read out (4 warps)
+  PF = 18,     // [2] P^T written, O rescaled (4 warps)
+  PR = 20,     // [2] O^T and O_lr^T MMAs of that pipeline's tile complete (two commits)
+  DRAIN = 22,  // [4] per MMA warp, on abort
+  COUNT = 26
+};
+
+__device__ __forceinline__ uint32_t rb_bar_count(int i) {
+  if (i >= EMPTY && i < EMPTY + 4) return 6;
+  if ((i >= YR && i < YR + 2) || (i >= KA && i < KA + 2) || (i >= SR && i < SR + 2) || (i >= PF && i < PF + 2))
+    return 4;
+  if (i >= PR && i < PR + 2) return 2;
+  return 1;
+}
+
+// Shared-memory layout (byte offsets from a 1024-aligned base).
+template <int D, int R>
+struct Layout {
+  static constexpr int HALF = D / 2;
+  static constexpr int RP = R < 16 ? 16 : R;
+  static constexpr int LSPAN = RP * 2;
+  static constexpr uint32_t SW_LR = tc::swizzle_code(LSPAN);
+  static constexpr int KATOMS = D / 64;
+  static constexpr int ATOM = kBT * 128;
+  static constexpr int LR_TILE = kBT * LSPAN;
+  static constexpr int STAGE = LR_TILE + KATOMS * ATOM;
+  static constexpr int BKT = D * LSPAN;  // B_K^T [d][r'] bf16, K-major, rows swizzled by LSPAN
+  static constexpr int QB = KATOMS * kMaxRows * 128;
+  static constexpr int PB = 2 * kMaxRows * 128;  // P^T [16 rows][128 tokens] bf16, per pipeline
+  static constexpr int BTAB = 4 * HALF * 8;      // per pipeline, two buffers: base angles of its tiles
+  static constexpr int MISC = 1024;
+  static constexpr int TAIL = BKT + QB + 2 * PB + BTAB + MISC + 512;
+  static constexpr int NS_FIT = (kSmemLimit - 1024 - TAIL) / STAGE;
+  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+  static constexpr int off_ring = 0;
+  static constexpr int off_bk = NS * STAGE;
+  static constexpr int off_q = off_bk + BKT;
+  static constexpr int off_p = off_q + QB;
+  static constexpr int off_btab = off_p + 2 * PB;
+  static constexpr int off_misc = off_btab + BTAB;
+  static constexpr int off_bar = off_misc + MISC;
+  static constexpr int used = off_bar + 512;
+  static constexpr int total = used + 1024;
+  static_assert(NS >= 3, "the ring needs three slots");
+  static_assert(total <= kSmemLimit, "decode tile does not fit in shared memory");
+  static_assert(2 * D <= 256, "two Y buffers below the rotation table");
+  static_assert((NS - 1) * STAGE + LR_TILE + 2 * ATOM <= used, "V^T span");
+  static_assert((NS - 1) * STAGE + 7 * 16 * LSPAN + (128 / RP - 1) * LR_TILE + 16 * LSPAN <= used,
+                "L_V^T span");
+};
+}  // namespace rb
+
+template <int D, int R>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_rb_kernel(const __grid_constant__ DecodeParams p,
+                     const __grid_constant__ CUtensorMap tm_base,
+                     const __grid_constant__ CUtensorMap tm_lr) {
+  using L = rb::Layout<D, R>;
+  using namespace rb;
+  constexpr int HALF = D / 2;
+  constexpr int KS = D / 16;
+  constexpr int LSPAN = L::LSPAN;
+  constexpr int NS = L::NS;
+  constexpr int QH = HALF / 16;  // 16-pair chunks of a token's rotation
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + L::off_bar + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::off_misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::off_misc + 4);
+  int* kmask = reinterpret_cast<int*>(smem + L::off_misc + 16);     // [4] loaded blocks per slot
+  float* red = reinterpret_cast<float*>(smem + L::off_misc + 128);  // [2 pipelines][4 warps][kRows]
+  float2* btab = reinterpret_cast<float2*>(smem + L::off_btab);     // [2 pipelines][2][HALF]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- the work item (as in decode_kernel)
+  int64_t rest = blockIdx.x;
+  const int head = static_cast<int>(rest % p.Hkv);
+  rest /= p.Hkv;
+  const int split = static_cast<int>(rest % p.n_splits);
+  rest /= p.n_splits;
+  const int chunk = static_cast<int>(rest % p.n_chunks);
+  const int ctx = static_cast<int>(rest / p.n_chunks);
+  const int kbeg = split * p.split_blocks;
+  const int32_t* btrow = p.block_tables + static_cast<int64_t>(ctx) * p.max_blocks;
+  int id0 = INT_MIN, id1 = INT_MIN;
+  if (warp == 0) {
+    const int kb = kbeg + (lane & 7) + (lane >> 3) * kTileBlocks;
+    const int x = (lane < 2 * kTileBlocks && kb < p.max_blocks && kb < kbeg + p.split_blocks) ? __ldg(btrow + kb) : INT_MIN;
+    id0 = __shfl_sync(0xffffffffu, x, lane & 7);
+    id1 = __shfl_sync(0xffffffffu, x, (lane & 7) + 8);
+    if (lane >= kTileBlocks) id0 = id1 = INT_MIN;
+  } else if (p.n_adapters * R <= 4096) {
+    for (int i = tid - 32; i < p.n_adapters * R * (D / 64); i += kThreads - 32) {
+      const int64_t off = (static_cast<int64_t>(i / (D / 64)) * p.Hkv + head) * D + 64 * (i % (D / 64));
+      if (p.has_bk) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p.B_K + off));
+      if (p.B_V != nullptr) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p.B_V + off));
+    }
+  }
+  const int qs = __ldg(p.ctx_q_start + ctx), qe = __ldg(p.ctx_q_start + ctx + 1);
+  int len = __ldg(p.ctx_lens + ctx);
+  if (qs < 0 || qe > p.num_queries || qs > qe) {
+    if (tid == 0) report(p.status, LRKV_ERR_INDEX);
+    return;
+  }
+  if (tid == 0 && chunk == 0 && split == 0 && (qe - qs) * p.g > p.n_chunks * p.rpi)
+    report(p.status, LRKV_ERR_INDEX);
+  const int row0 = chunk * p.rpi;
+  const int nrows = min(p.rpi, (qe - qs) * p.g - row0);
+  if (nrows <= 0) return;
+  if (len < 1 || len > p.max_ctx_len) {
+    if (tid == 0) report(p.status, LRKV_ERR_INDEX);
+    len = 0;
+  }
+  // the item's one adapter (a bad id scores as base only; the combine reports it)
+  const int item_ad = __ldg(p.adapter_ids + qs + row0 / p.g);
+  const bool rebuild = p.has_bk && item_ad >= 0 && item_ad < p.n_adapters;
+  const int nblk = (len + kBlock - 1) / kBlock;
+  const int kend = min(kbeg + p.split_blocks, nblk);
+  const int ntiles = kend > kbeg ? (kend - kbeg + kTileBlocks - 1) / kTileBlocks : 0;
+  auto rec_of = [&](int r, int part) -> int64_t {
+    const int gr = row0 + r;
+    const int n = qs + gr / p.g, m = head * p.g + gr % p.g;
+    return ((static_cast<int64_t>(n) * p.Hq + m) * p.n_splits + split) * 2 + part;
+  };
+  if (ntiles == 0) {
+    for (int i = tid; i < 2 * nrows * (D + R); i += kThreads) {
+      const int part = i / (nrows * (D + R)), k = i % (nrows * (D + R));
+      p.part_o[rec_of(k / (D + R), part) * (D + R) + k % (D + R)] = 0.f;
+    }
+    if (tid < 2 * nrows) {
+      p.part_ml[2 * rec_of(tid % nrows, tid / nrows)] = -CUDART_INF_F;
+      p.part_ml[2 * rec_of(tid % nrows, tid / nrows) + 1] = 0.f;
+    }
+    return;
+  }
+
+  // token warps: e^{i delta theta_j} of this lane's token offset, for half of
+  // the pairs (warpgroup b: pairs [b d/4, (b + 1) d/4)), stored after the barrier
+  constexpr int QD = HALF / 32;
+  uint32_t dvr[QD][32];
+  if (warp >= 4) {
+    const int jb0 = ((warp - 4) >> 2) * (HALF / 2);
+    const int dl = (warp & 3) * 32 + lane;
+#pragma unroll
+    for (int q4 = 0; q4 < QD; ++q4)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 cs = rope_cos_sin_fast(dl, p.freqs.hi[jb0 + 16 * q4 + i], p.freqs.lo[jb0 + 16 * q4 + i]);
+        dvr[q4][2 * i] = __float_as_uint(cs.x);
+        dvr[q4][2 * i + 1] = __float_as_uint(cs.y);
+      }
+  }
+  // warps 1-3: Q rows of the item (fp16 when scored against fp16 K_a)
+  constexpr int QCH = kMaxRows * (D / 8);
+  constexpr int QIT = (QCH + 95) / 96;
+  uint4 qv[QIT];
+  if (warp >= 1 && warp < 4) {
+    const int pt = tid - 32;
+#pragma unroll
+    for (int u = 0; u < QIT; ++u) {
+      const int i = pt + 96 * u;
+      const int r = i / (D / 8), c = i % (D / 8);
+      qv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < QCH && r < nrows) {
+        const int gr = row0 + r;
+        qv[u] = __ldg(reinterpret_cast<const uint4*>(
+            p.q + (static_cast<int64_t>(qs + gr / p.g) * p.Hq + head * p.g + gr % p.g) * D + 8 * c));
+      }
+    }
+  }
+
+  // ---- barriers, tensor memory
+  if (tid == 0) {
+    for (int i = 0; i < COUNT; ++i) mbar_init(bar(i), rb_bar_count(i));
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tc::alloc(smem_u32(tmem_slot), kTmemCols);
+  if (tid == 0) {
+    prefetch_tmap(&tm_base);
+    prefetch_tmap(&tm_lr);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ============================================================ producer
+    const uint32_t bytes_k = L::KATOMS * 2048 + (rebuild ? 16 * LSPAN : 0);
+    const uint32_t bytes_v = L::KATOMS * 2048 + (p.has_bv ? 16 * LSPAN : 0);
+    auto tile_ids = [&](int j) -> int {
+      const int kb = kbeg + j * kTileBlocks + lane;
+      return (lane < kTileBlocks && kb < kend) ? __ldg(btrow + kb) : INT_MIN;
+    };
+    int id_a = (kbeg + lane < kend) ? id0 : INT_MIN;
+    int id_b = (kbeg + kTileBlocks + lane < kend) ? id1 : INT_MIN;
+    int id_c = ntiles > 2 ? tile_ids(2) : INT_MIN;
+    bool ok = true;
+    int issued = 0;
+    auto issue = [&](int idx, int kind, int id) -> bool {
+      bool valid = id != INT_MIN;
+      if (valid && (id < 0 || id >= p.num_blocks)) {
+        report(p.status, LRKV_ERR_INDEX);
+        valid = false;
+      }
+      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+      const int s = idx % NS;
+      if (idx >= NS && !warp_all(wait_ab(bar(EMPTY + s), ((idx / NS) - 1) & 1, p.status, abort_flag)))
+        return false;
+      const uint32_t dst = sbase + L::off_ring + s * L::STAGE;
+      const uint32_t fb = bar(FULL + s);
+      if (lane == 0) {
+        if (kind == 0) kmask[s] = static_cast<int>(vm);
+        mbar_arrive_expect_tx(fb, __popc(vm) * (kind == 0 ? bytes_k : bytes_v));
+      }
+      __syncwarp();
+      if (valid) {
+        const int y = ((id * 2 + kind) * p.Hkv + head) * kBlock;
+#pragma unroll
+        for (int a = 0; a < L::KATOMS; ++a)
+          tma_load_2d(dst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, y, fb);
+        if (kind == 0 ? rebuild : p.has_bv)
+          tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, 0, (id * 2 + kind) * kBlock, fb);
+      }
+      return true;
+    };
+    ok = issue(kidx(0, ntiles), 0, id_a);
+    issued = ok ? 1 : 0;
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if (j + 1 < ntiles) {
+        ok = issue(kidx(j + 1, ntiles), 0, id_b);
+        if (!ok) break;
+        ++issued;
+      }
+      ok = issue(vidx(j, ntiles), 1, id_a);
+      if (!ok) break;
+      ++issued;
+      id_a = id_b;
+      id_b = id_c;
+      id_c = j + 3 < ntiles ? tile_ids(j + 3) : INT_MIN;
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
+    for (int s = 0; s < NS; ++s) {
+      const int last = issued - 1 - ((issued - 1 - s) % NS + NS) % NS;
+      if (last >= 0 && last < issued) wait_ab(bar(FULL + s), (last / NS) & 1, p.status, nullptr);
+    }
+  } else {
+    // ================================================ prologue (warps 1-11)
+    const int pb = (warp - 4) >> 2;  // token warps: pipeline (tiles pb, pb + 2, ...)
+    const int tt = (warp & 3) * 32 + lane;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    if (warp < 4) {
+      const int pt = tid - 32;
+#pragma unroll
+      for (int u = 0; u < QIT; ++u) {
+        const int i = pt + 96 * u;
+        const int r = i / (D / 8), c = i % (D / 8);
+        uint4 v = qv[u];
+        if (rebuild) {
+          v.x = bf16x2_to_f16x2(v.x);
+          v.y = bf16x2_to_f16x2(v.y);
+          v.z = bf16x2_to_f16x2(v.z);
+          v.w = bf16x2_to_f16x2(v.w);
+        }
+        if (i < QCH)
+          *reinterpret_cast<uint4*>(smem + L::off_q + (c >> 3) * (kMaxRows * 128) + r * 128 +
+                                    (((c & 7) ^ (r & 7)) << 4)) = v;
+      }
+      // B_K^T of the item's adapter: row n = head dim n, column k = rank index
+      if (rebuild) {
+        const __nv_bfloat16* src = p.B_K + static_cast<int64_t>(item_ad) * R * p.Hkv * D + head * D;
+        for (int e = pt; e < D * (L::RP / 2); e += 96) {
+          const int n = e % D, k0 = 2 * (e / D);
+          const uint32_t lo = k0 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0) * p.Hkv * D + n]) : 0u;
+          const uint32_t hi =
+              k0 + 1 < R ? __bfloat16_as_ushort(src[static_cast<int64_t>(k0 + 1) * p.Hkv * D + n]) : 0u;
+          *reinterpret_cast<uint32_t*>(smem + L::off_bk + swz<LSPAN>(n, 2 * k0)) = lo | (hi << 16);
+        }
+      }
+    } else {
+      const int jb = pb * (HALF / 2);
+#pragma unroll
+      for (int q4 = 0; q4 < QD; ++q4) tc::st_x32(tl + RDT_COL + 2 * (jb + 16 * q4), dvr[q4]);
+      tc::wait_st();
+      // base angles of the pipeline's first tile (tile pb)
+      if (tt < HALF && pb < ntiles)
+        btab[2 * pb * HALF + tt] = rope_cos_sin_fast((kbeg + pb * kTileBlocks) * kBlock, p.freqs.hi[tt], p.freqs.lo[tt]);
+    }
+    tc::fence_before();
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // Q, B_K^T -> MMA operands
+    named_bar_sync(1, kThreads - 32);
+    tc::fence_after();
+
+    if (warp == 1) {
+      // ======================================== Y issuer, O_lr^T issuer
+      const uint32_t idy = tc::idesc_f16(128, D, true, false, false);
+      const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
+      const uint64_t bdesc = tc::sdesc(sbase + L::off_bk, 16, 8 * LSPAN, L::SW_LR);
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j <= ntiles; ++j) {
+        if (rebuild && j < ntiles) {
+          const int b = j & 1, i = j >> 1, ki = kidx(j, ntiles), s = ki % NS;
+          ok = warp_all(wait_ab(bar(FULL + s), (ki / NS) & 1, p.status, abort_flag));
+          if (ok && i > 0) ok = warp_all(wait_ab(bar(YR + b), (i - 1) & 1, p.status, abort_flag));
+          if (!ok) break;
+          tc::fence_after();
+          if (tc::elect_one()) {
+            const uint64_t ldesc = tc::sdesc(sbase + L::off_ring + s * L::STAGE, 16, 8 * LSPAN, L::SW_LR);
+#pragma unroll
+            for (int k = 0; k < L::RP / 16; ++k)
+              tc::mma_ss(tbase + RY_COL + b * D, ldesc + 2 * k, bdesc + 2 * k, idy, k > 0 ? 1u : 0u);
+            tc::commit(bar(YF + b));
+          }
+          __syncwarp();
+          ++issued;
+        }
+        if (p.has_bv && j > 0) {
+          const int jj = j - 1, b = jj & 1, i = jj >> 1, vi = vidx(jj, ntiles), v = vi % NS;
+          ok = warp_all(wait_ab(bar(FULL + v), (vi / NS) & 1, p.status, abort_flag));
+          if (ok) ok = warp_all(wait_ab(bar(PF + b), i & 1, p.status, abort_flag));
+          if (!ok) break;
+          tc::fence_after();
+          if (tc::elect_one()) {
+            const uint32_t vst = sbase + L::off_ring + v * L::STAGE;
+            const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
+            const uint64_t pdesc = tc::sdesc(sbase + L::off_p + b * L::PB, 16, 1024, 2);
+#pragma unroll
+            for (int k = 0; k < kBT / 16; ++k)
+              tc::mma_ss(tbase + ROL_COL + 16 * b, lvdesc + ((k * 16 * LSPAN) >> 4),
+                         pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
+                         (i > 0 || k > 0) ? 1u : 0u);
+            tc::commit(bar(PR + b));
+            tc::commit(bar(EMPTY + v));
+          }
+          __syncwarp();
+          ++issued;
+        }
+      }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        if (issued > 0) {
+          if (tc::elect_one()) tc::commit(bar(DRAIN + 1));
+          __syncwarp();
+          wait_ab(bar(DRAIN + 1), 0, p.status, nullptr);
+        }
+      }
+    } else if (warp == 2) {
+      // ======================================================== S issuer
+      const uint32_t ids = tc::idesc_f16(128, kMaxRows, !rebuild, false, false);
+      const uint64_t qdesc = tc::sdesc(sbase + L::off_q, 16, 1024, 2);
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int b = j & 1, i = j >> 1, ki = kidx(j, ntiles), s = ki % NS;
+        ok = warp_all(wait_ab(bar(FULL + s), (ki / NS) & 1, p.status, abort_flag));
+        if (ok) ok = warp_all(wait_ab(bar(KA + b), i & 1, p.status, abort_flag));
+        if (ok && i > 0) ok = warp_all(wait_ab(bar(SR + b), (i - 1) & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after();
+        if (tc::elect_one()) {
+          const uint64_t kdesc = tc::sdesc(sbase + L::off_ring + s * L::STAGE + L::LR_TILE, 16, 1024, 2);
+#pragma unroll
+          for (int k = 0; k < KS; ++k)
+            tc::mma_ss(tbase + RS_COL + 16 * b, kdesc + (((k >> 2) * L::ATOM + (k & 3) * 32) >> 4),
+                       qdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ids, k > 0 ? 1u : 0u);
+          tc::commit(bar(SF + b));
+          tc::commit(bar(EMPTY + s));
+          tc::commit(bar(EMPTY + s));  // K items have one MMA reader after the rebuild: both arrivals here
+        }
+        __syncwarp();
+        ++issued;
+      }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        if (issued > 0) {
+          if (tc::elect_one()) tc::commit(bar(DRAIN + 2));
+          __syncwarp();
+          wait_ab(bar(DRAIN + 2), 0, p.status, nullptr);
+        }
+      }
+    } else if (warp == 3) {
+      // ================================================ O^T issuer
+      const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int b = j & 1, i = j >> 1, vi = vidx(j, ntiles), v = vi % NS;
+        ok = warp_all(wait_ab(bar(FULL + v), (vi / NS) & 1, p.status, abort_flag));
+        if (ok) ok = warp_all(wait_ab(bar(PF + b), i & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after();
+        if (tc::elect_one()) {
+          const uint32_t vst = sbase + L::off_ring + v * L::STAGE;
+          const uint64_t vdesc = tc::sdesc(vst + L::LR_TILE, L::ATOM, 1024, 2);
+          const uint64_t pdesc = tc::sdesc(sbase + L::off_p + b * L::PB, 16, 1024, 2);
+#pragma unroll
+          for (int k = 0; k < kBT / 16; ++k)
+            tc::mma_ss(tbase + ROT_COL + 16 * b, vdesc + ((k * 16 * 128) >> 4),
+                       pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
+                       (i > 0 || k > 0) ? 1u : 0u);
+          tc::commit(bar(PR + b));
+          tc::commit(bar(EMPTY + v));
+          if (!p.has_bv) {
+            tc::commit(bar(PR + b));
+            tc::commit(bar(EMPTY + v));
+          }
+        }
+        __syncwarp();
+        ++issued;
+      }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        if (issued > 0) {
+          if (tc::elect_one()) tc::commit(bar(DRAIN + 3));
+          __syncwarp();
+          wait_ab(bar(DRAIN + 3), 0, p.status, nullptr);
+        }
+      }
+    } else {
+      // ================================== token pipelines (warps 4-7, 8-11)
+      const int bar_g = 2 + pb;
+      // base angles: the i-th tile of this pipeline reads buffer i & 1; the
+      // (i+1)-th tile's are written into the other buffer, which every thread
+      // of the pipeline finished reading before the previous tile's vote
+      float2* btp = btab + 2 * pb * HALF;
+      float m_run[kRows], l_run[kRows];
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        m_run[r] = -CUDART_INF_F;
+        l_run[r] = 0.f;
+      }
+      const float th_hi = tt < HALF ? p.freqs.hi[tt] : 0.f, th_lo = tt < HALF ? p.freqs.lo[tt] : 0.f;
+      bool failed = false;
+      int i = 0;
+      for (int j = pb; j < ntiles; j += 2, ++i) {
+        const int ki = kidx(j, ntiles), vi = vidx(j, ntiles);
+        const int s = ki % NS, v = vi % NS;
+        const uint32_t ph = i & 1;
+        const int t0 = (kbeg + j * kTileBlocks) * kBlock;
+        // ---- K_a = K_base + RoPE(Y) for this lane's token, every pair, fp16 in place
+        if (rebuild) {
+          if (!failed) failed = !wait_ab(bar(YF + pb), ph, p.status, abort_flag);
+          if (!failed) failed = !wait_ab(bar(FULL + s), (ki / NS) & 1, p.status, abort_flag);
+          tc::fence_after();
+          uint8_t* kt = smem + L::off_ring + s * L::STAGE + L::LR_TILE;
+          const uint32_t ycol = RY_COL + pb * D;
+          const float2* bt = btp + (i & 1) * HALF;
+#pragma unroll 1
+          for (int q4 = 0; q4 < QH; ++q4) {
+            const int j0 = 16 * q4;
+            uint32_t dv[32], ylo[16], yhi[16];
+            tc::ld_x32(tl + RDT_COL + 2 * j0, dv);
+            tc::ld_x16(tl + ycol + j0, ylo);
+            tc::ld_x16(tl + ycol + HALF + j0, yhi);
+            tc::wait_ld();
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {  // 8 pairs per 16-byte chunk
+              const int dlo = j0 + 8 * hc, dhi = dlo + HALF;
+              uint4* plo = reinterpret_cast<uint4*>(kt + (dlo >> 6) * L::ATOM + swz<128>(tt, (dlo & 63) * 2));
+              uint4* phi = reinterpret_cast<uint4*>(kt + (dhi >> 6) * L::ATOM + swz<128>(tt, (dhi & 63) * 2));
+              const uint4 klo = *plo, khi = *phi;
+              const uint32_t kl[4] = {klo.x, klo.y, klo.z, klo.w};
+              const uint32_t kh[4] = {khi.x, khi.y, khi.z, khi.w};
+              uint32_t olo[4], ohi[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                float rl[2], rh[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int k = 8 * hc + 2 * w + e;  // pair j0 + k
+                  const float2 b2 = bt[j0 + k];
+                  const float cd = __uint_as_float(dv[2 * k]), sd = __uint_as_float(dv[2 * k + 1]);
+                  const float c = fmaf(b2.x, cd, -(b2.y * sd)), sn = fmaf(b2.y, cd, b2.x * sd);
+                  const float yl = __uint_as_float(ylo[k]), yh = __uint_as_float(yhi[k]);
+                  const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
+                  const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
+                  rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
+                  rh[e] = fmaf(yh, c, fmaf(yl, sn, bh));
+                }
+                olo[w] = pack_f16(rl[0], rl[1]);
+                ohi[w] = pack_f16(rh[0], rh[1]);
+              }
+              *plo = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+              *phi = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+            }
+          }
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(YR + pb));
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // K_a -> S operand
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KA + pb));
+
+        // ---- scores of this lane's token, every row
+        if (!failed) failed = !wait_ab(bar(SF + pb), ph, p.status, abort_flag);
+        if (!failed) failed = !wait_ab(bar(FULL + s), (ki / NS) & 1, p.status, abort_flag);
+        tc::fence_after();
+        const int vmask = kmask[s];
+        float sc[kRows];
+        {
+          uint32_t sv[kRows];
+          tc::ld_cols<kRows>(tl + RS_COL + 16 * pb, sv);
+          tc::wait_ld();
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) sc[r] = __uint_as_float(sv[r]);
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(SR + pb));
+          mbar_arrive(bar(EMPTY + s));
+        }
+        // base angles of this pipeline's next tile (j + 2), published by the vote below
+        if (tt < HALF && j + 2 < ntiles) btp[((i + 1) & 1) * HALF + tt] = rope_cos_sin_fast(t0 + 2 * kBT, th_hi, th_lo);
+
+        // ---- online softmax over the tile's tokens (log2 units)
+        const bool tok_ok = ((vmask >> (tt >> 4)) & 1) != 0 && t0 + tt < len;
+        bool need = false;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          sc[r] = tok_ok ? sc[r] * p.scale_log2 : -CUDART_INF_F;
+          need |= sc[r] > m_run[r] + kRescaleLog2;
+        }
+        if (*abort_flag != 0) failed = true;
+        if (named_bar_or(bar_g, 128, need || failed)) {  // also publishes bt
+          if (named_bar_or(bar_g, 128, failed)) {
+            failed = true;
+            break;
+          }
+          float* rg = red + pb * 4 * kRows;
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {
+            float x = sc[r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+            if (lane == 0) rg[(warp & 3) * kRows + r] = x;
+          }
+          named_bar_sync(bar_g, 128);
+          float alpha[kRows];
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {
+            const float mx = fmaxf(fmaxf(rg[r], rg[kRows + r]), fmaxf(rg[2 * kRows + r], rg[3 * kRows + r]));
+            const float mn = fmaxf(m_run[r], mx);
+            alpha[r] = mn == -CUDART_INF_F ? 1.f : ex2(m_run[r] - mn);
+            m_run[r] = mn;
+            l_run[r] *= alpha[r];
+          }
+          named_bar_sync(bar_g, 128);
+          if (i > 0) {
+            // the P V of this pipeline's previous tile must have landed before O is rescaled
+            if (!failed) failed = !wait_ab(bar(PR + pb), (i - 1) & 1, p.status, abort_flag);
+            tc::fence_after();
+            uint32_t o[kRows];
+            tc::ld_cols<kRows>(tl + ROT_COL + 16 * pb, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+            tc::st_cols<kRows>(tl + ROT_COL + 16 * pb, o);
+            if (p.has_bv) {
+              tc::ld_cols<kRows>(tl + ROL_COL + 16 * pb, o);
+              tc::wait_ld();
+#pragma unroll
+              for (int r = 0; r < kRows; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+              tc::st_cols<kRows>(tl + ROL_COL + 16 * pb, o);
+            }
+            tc::wait_st();
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          const float pr = ex2(sc[r] - (m_run[r] == -CUDART_INF_F ? 0.f : m_run[r]));
+          l_run[r] += pr;
+          sc[r] = pr;
+        }
+        // ---- P^T (bf16, K-major over tokens) once this pipeline's previous P V has read it
+        if (i > 0 && !failed) failed = !wait_ab(bar(PR + pb), (i - 1) & 1, p.status, abort_flag);
+        {
+          uint8_t* pbuf = smem + L::off_p + pb * L::PB + (tt >> 6) * (kMaxRows * 128) + ((tt & 7) << 1);
+          const int ch = (tt & 63) >> 3;
+#pragma unroll
+          for (int r = 0; r < kRows; ++r)
+            *reinterpret_cast<__nv_bfloat16*>(pbuf + r * 128 + ((ch ^ (r & 7)) << 4)) = __float2bfloat16_rn(sc[r]);
+        }
+        // V and L_V rows of tokens outside the context, the split or a loaded
+        // block hold stale memory: zero them so that P = 0 cannot meet a NaN
+        if (vmask != (1 << kTileBlocks) - 1 || t0 + kBT > len) {
+          if (!failed) failed = !wait_ab(bar(FULL + v), (vi / NS) & 1, p.status, abort_flag);
+          if (!tok_ok) {
+            uint8_t* vst = smem + L::off_ring + v * L::STAGE;
+#pragma unroll
+            for (int a = 0; a < L::KATOMS; ++a)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(vst + L::LR_TILE + a * L::ATOM + tt * 128 + 16 * c) =
+                    make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < LSPAN / 16; ++c)
+              *reinterpret_cast<uint4*>(vst + tt * LSPAN + 16 * c) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(PF + pb));
+          mbar_arrive(bar(EMPTY + v));
+        }
+      }
+
+      // ---- this pipeline's split partial: m, l, O, O_lr of every row
+      bool aborted = named_bar_or(bar_g, 128, failed);
+      if (!aborted && i > 0) {
+        const bool okp = wait_ab(bar(PR + pb), (i - 1) & 1, p.status, abort_flag);
+        aborted = named_bar_or(bar_g, 128, !okp);
+      }
+      if (aborted) {
+        if (tt == 0) *abort_flag = 1;
+      } else {
+        uint32_t o[kRows], ol[kRows];
+        if (i > 0) {
+          tc::fence_after();
+          tc::ld_cols<kRows>(tl + ROT_COL + 16 * pb, o);
+          tc::ld_cols<kRows>(tl + ROL_COL + 16 * pb, ol);
+          tc::wait_ld();
+        }
+        float* rg = red + pb * 4 * kRows;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          float x = l_run[r];
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o2);
+          if (lane == 0) rg[(warp & 3) * kRows + r] = x;
+        }
+        named_bar_sync(bar_g, 128);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+          if (r < nrows) {
+            const int64_t rec = rec_of(r, pb);
+            float* po = p.part_o + rec * (D + R);
+            if (tt < D) po[tt] = i > 0 ? __uint_as_float(o[r]) : 0.f;
+            if (tt < R) po[D + tt] = (i > 0 && p.has_bv) ? __uint_as_float(ol[r]) : 0.f;
+            if (tt == r) {
+              p.part_ml[2 * rec] = m_run[r];
+              p.part_ml[2 * rec + 1] = rg[r] + rg[kRows + r] + rg[2 * kRows + r] + rg[3 * kRows + r];
+            }
+          }
+        }
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tbase, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- combine
 // Merges the splits of each (query, head) with log-sum-exp weights, applies
 // the reordered V term O_lr B_V,a once, divides by l and stores bf16.
@@ -1048,7 +1741,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   p.ctx_lens = a.ctx_lens;
   p.B_K = static_cast<const __nv_bfloat16*>(a.B_K);
   p.B_V = static_cast<const __nv_bfloat16*>(a.B_V);
-  const int64_t nrec = static_cast<int64_t>(a.num_queries) * cfg.n_q_heads * plan.n_splits;
+  const int64_t nrec = static_cast<int64_t>(a.num_queries) * cfg.n_q_heads * plan.n_splits * (plan.rebuild ? 2 : 1);
   p.part_ml = static_cast<float*>(workspace);
   p.part_o = p.part_ml + ((nrec * 2 + 63) / 64) * 64;
   p.status = a.status;
@@ -1075,6 +1768,9 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
 
   if (plan.n_items > 0) {
     auto kern = decode_kernel<D, R>;
+    if constexpr (R == 64) {
+      if (plan.rebuild) kern = decode_rb_kernel<D, R>;
+    }
     if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), plan.smem_bytes)) return LRKV_ERR_CUDA;
     kern<<<static_cast<unsigned>(plan.n_items), kThreads, plan.smem_bytes, stream>>>(p, tb, tl);
     if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
@@ -1093,7 +1789,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   c.Hq = cfg.n_q_heads;
   c.Hkv = cfg.n_kv_heads;
   c.g = plan.g;
-  c.n_splits = plan.n_splits;
+  c.n_splits = plan.n_splits * (plan.rebuild ? 2 : 1);  // rebuild mode: one partial per pipeline
   c.n_adapters = a.n_adapters;
   c.has_bv = a.B_V != nullptr;
   const int64_t pairs = static_cast<int64_t>(a.num_queries) * cfg.n_q_heads;
@@ -1114,6 +1810,10 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   DecodePlan P{};
   P.g = cfg.n_q_heads / cfg.n_kv_heads;
   if (P.g < 1 || P.g > kMaxRows) return false;
+  // Rebuild mode (decode_rb_kernel) at rank 64, four rows per item: when every
+  // item's rows belong to one query -- a multiple of 4 query heads per kv head,
+  // or one query per context.
+  P.rebuild = (R == 64 && (P.g % 4 == 0 || max_q_per_ctx == 1)) ? 1 : 0;
   int rpi = 0, total = 0;
 #define LRKV_L(d, r) \
   if (D == d && R == r) { rpi = DL<d, r>::RPI; total = DL<d, r>::total; }
@@ -1121,6 +1821,7 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   LRKV_L(64, 8) LRKV_L(64, 16) LRKV_L(64, 32) LRKV_L(64, 64)
 #undef LRKV_L
   if (rpi == 0) return false;
+  if (P.rebuild) total = D == 128 ? rb::Layout<128, 64>::total : rb::Layout<64, 64>::total;
   P.rows_per_item = rpi;
   P.smem_bytes = std::max(total, kMinSmem);
   P.n_chunks = std::max(1, (max_q_per_ctx * P.g + rpi - 1) / rpi);
@@ -1131,7 +1832,8 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   constexpr double kItemOverheadBlocks = 12.0;
   int best_s = 1;
   double best = -1.0;
-  const int smax = std::min(nblk, 256);  // the combine kernel holds up to 256 split weights
+  // the combine kernel holds up to 256 split weights (rebuild mode: two partials per split)
+  const int smax = std::min(nblk, P.rebuild ? 128 : 256);
   for (int s = 1; s <= smax; ++s) {
     const int sb = (nblk + s - 1) / s;
     if ((nblk + sb - 1) / sb != s) continue;
@@ -1147,7 +1849,7 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   P.n_splits = (nblk + P.split_blocks - 1) / P.split_blocks;
   P.n_items = pairs * P.n_splits;
   if (P.n_items > INT32_MAX) return false;
-  const int64_t nrec = static_cast<int64_t>(num_queries) * cfg.n_q_heads * P.n_splits;
+  const int64_t nrec = static_cast<int64_t>(num_queries) * cfg.n_q_heads * P.n_splits * (P.rebuild ? 2 : 1);
   P.ws_bytes = static_cast<size_t>((((nrec * 2 + 63) / 64) * 64 + nrec * (D + R)) * 4);
   *plan = P;
   return true;

@@ -21,6 +21,7 @@ struct DecodePlan {
   int n_splits;       // splits of each context's blocks
   int split_blocks;   // blocks per split
   int64_t n_items;    // num_ctx * n_chunks * n_splits * Hkv (one CTA each)
+  int rebuild;        // 1: rebuild-mode kernel (one query per item, K_a rebuilt per tile)
   int smem_bytes;
   size_t ws_bytes;    // workspace: split partials
 };

@@ -99,6 +99,19 @@ def test_decode_many_agents_one_context(cuda_lib):
     assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case, cache="bf16"), BF16_TOL)
 
 
+def test_rebuild_mode_with_base_only_queries(cuda_lib):
+    """Rank 64, one query per context (the rebuild mode): contexts whose query
+    has no adapter (-1) score against K_base alone, in bf16, next to adapted
+    ones."""
+    case = I.long_decode(n_seqs=4, n=333)
+    case.dec_adapter = torch.tensor([-1, 3, -1, 6], dtype=torch.int32)
+    for k in range(4):
+        case.seqs[k].adapter = int(case.dec_adapter[k])
+    g, res = _run(case)
+    assert g.device_status() == 0
+    assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case, cache="bf16"), BF16_TOL)
+
+
 def test_decode_many_splits(cuda_lib):
     """One long context on two kv heads: the split plan takes more than 32
     splits of the context (a ragged last tile included), so the combine merges
@@ -112,9 +125,11 @@ def test_decode_many_splits(cuda_lib):
     assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case, cache="bf16"), BF16_TOL)
 
 
-def test_decode_without_adapter_factors(cuda_lib):
-    """B_K = NULL (adapter on V only), then B_V = NULL (adapter on K only)."""
-    case = I.shared_decode(n=260)
+@pytest.mark.parametrize("rank", [16, 64])
+def test_decode_without_adapter_factors(cuda_lib, rank):
+    """B_K = NULL (adapter on V only), then B_V = NULL (adapter on K only); rank
+    64 runs the rebuild mode (one query per item), rank 16 the G mode."""
+    case = I.shared_decode(n=260, rank=rank)
     g = GpuCase(case, pool_fill=NAN)
     g.setup()
     w64 = weights64(case)
