@@ -29,7 +29,14 @@
  *   (every tensor fp32; plain fp32 FMA arithmetic, no tensor cores).
  * - Paged pools (PagedAttention-style blocks of 16 tokens):
  *     base_pool [num_blocks][2][Hkv][16][d]  plane 0 = K_base (rotated), 1 = V_base
- *     lr_pool   [num_blocks][2][16][r]       plane 0 = L_K, 1 = L_V
+ *     lr_pool   [num_blocks][2][16][G*r]     plane 0 = L_K, 1 = L_V; group g's r
+ *                                            columns at [g*r, (g+1)*r)
+ * - Low-rank groups (lr_groups = G): G = 1 is the shared-A cache of LRAgent
+ *   (arXiv 2602.01053, Abstract): L = X A with one A for every agent. G > 1 is
+ *   PReCache's PreLRShared (thelatestinai.com/papers/2609.34054, Abstract and
+ *   Figure 1): each agent has its own A; one append computes every agent's
+ *   low-rank cache, L = [X A_0 | ... | X A_{G-1}], and agent a reads group a
+ *   (adapter ids must then be < G, n_adapters <= G).
  *   Token at position p of a sequence whose block-table row is bt lives in
  *   block bt[p / 16], row p % 16. Each (block, plane, kv head) is one
  *   contiguous 16*d element chunk (4 KB for bf16, d = 128).
@@ -88,6 +95,8 @@ typedef struct {
   int32_t block_size; /* must be 16 */
   float rope_base;    /* theta_j = rope_base^(-2j/d) */
   int32_t dtype;      /* lrkv_dtype of every tensor argument */
+  int32_t lr_groups;  /* G >= 1 low-rank groups: 1 = one A shared by every agent;
+                         G > 1 = agent a has its own A_K,a, A_V,a and reads group a */
 } lrkv_config;
 
 /*
@@ -103,6 +112,7 @@ typedef struct {
  *   base_pool[blk][0][k][row][:] = RoPE(Y[n, K cols of kv head k], position)
  *   base_pool[blk][1][k][row][:] = Y[n, V cols of kv head k]
  *   lr_pool[blk][0][row][:] = Y[n, A_K cols],  lr_pool[blk][1][row][:] = Y[n, A_V cols]
+ *   (all G groups' columns)
  * with blk = block_tables[seq_rows[n]][positions[n] / 16], row = positions[n] % 16.
  *
  *   X            [T][h]                 hidden states of the new tokens
@@ -110,10 +120,10 @@ typedef struct {
  *   positions    int32 [T]              position of each token in its sequence
  *   seq_rows     int32 [T]              block-table row of each token (< num_seqs)
  *   block_tables int32 [num_seqs][max_blocks]
- *   W_cat        [N][h], N = 2*Hkv*d + 2*r: the packed projection weights in
+ *   W_cat        [N][h], N = 2*Hkv*d + 2*G*r: the packed projection weights in
  *                nn.Linear layout (row n = weights of output column n):
  *                rows [0, Hkv*d) = W_K^T, [Hkv*d, 2*Hkv*d) = W_V^T,
- *                next r rows = A_K^T, last r rows = A_V^T
+ *                next G*r rows = A_K,0^T .. A_K,G-1^T, last G*r rows = A_V,g^T
  *   base_pool, lr_pool  written (only the rows of the T tokens)
  *   num_blocks   number of blocks in both pools (block ids must be < num_blocks)
  * Tokens whose row, position or block id is out of range are skipped

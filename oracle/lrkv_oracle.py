@@ -71,6 +71,15 @@ def apply_rope(x: np.ndarray, positions: np.ndarray, base: float) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # Cache construction.
 
+def _lowrank(X, A):
+    """X·A for a shared A [h, r]; for agent-specific A [G, h, r] the G products
+    side by side, group g in columns [g r, (g + 1) r)."""
+    A = _f64(A)
+    if A.ndim == 2:
+        return X @ A
+    return np.concatenate([X @ A[g] for g in range(A.shape[0])], axis=1)
+
+
 def base_and_lowrank(X, positions, W_K, W_V, A_K, A_V, n_kv_heads: int, head_dim: int,
                      base: float):
     """What one append writes for tokens X [T, h] at the given positions.
@@ -79,12 +88,16 @@ def base_and_lowrank(X, positions, W_K, W_V, A_K, A_V, n_kv_heads: int, head_dim
     component kept in its low-rank form, shared when A is shared):
         K_base = RoPE(X·W_K)  [T, Hkv, d]     V_base = X·W_V  [T, Hkv, d]
         L_K    = X·A_K        [T, r]          L_V    = X·A_V  [T, r]
+    PReCache, Abstract and Figure 1 (PreLRShared): with agent-specific
+    A_K,g, A_V,g (arrays [G, h, r]) every agent's low-rank cache is produced
+    when the segment is first processed: L_K = [X·A_K,0 | ... | X·A_K,G-1]
+    [T, G r], likewise L_V.
     """
     X = _f64(X)
     T = X.shape[0]
     k_pre = (X @ _f64(W_K)).reshape(T, n_kv_heads, head_dim)
     v = (X @ _f64(W_V)).reshape(T, n_kv_heads, head_dim)
-    return (apply_rope(k_pre, positions, base), v, X @ _f64(A_K), X @ _f64(A_V))
+    return (apply_rope(k_pre, positions, base), v, _lowrank(X, A_K), _lowrank(X, A_V))
 
 
 def agent_kv(X, positions, W_K, W_V, A_K, A_V, B_K_i, B_V_i, n_kv_heads: int,
@@ -210,6 +223,17 @@ def _adapter_B(weights, adapter: int):
     return weights["B_K"][adapter], weights["B_V"][adapter]
 
 
+def _agent_A(weights, adapter: int):
+    """The A factors agent `adapter` uses: the shared A [h, r], or its own
+    A_g [G, h, r] -> A[adapter] (PReCache, PreLRShared); base-only rows
+    (adapter -1) use no A."""
+    A_K, A_V = weights["A_K"], weights["A_V"]
+    if np.ndim(A_K) == 3:
+        g = max(adapter, 0)
+        return A_K[g], A_V[g]
+    return A_K, A_V
+
+
 def attend(X_seq, adapter: int, q, q_positions, weights, n_kv_heads: int, head_dim: int,
            base: float, scale: float, cache_dtype=None, X_lr=None) -> np.ndarray:
     """Queries q [N, Hq, d] of one agent over a sequence whose hidden states at
@@ -219,14 +243,14 @@ def attend(X_seq, adapter: int, q, q_positions, weights, n_kv_heads: int, head_d
     states instead, the base part from X_seq (agent_kv_rebased)."""
     L = np.asarray(X_seq).shape[0]
     B_K, B_V = _adapter_B(weights, adapter)
+    A_K, A_V = _agent_A(weights, adapter)
     if X_lr is not None:
         K, V = agent_kv_rebased(X_seq, X_lr, np.arange(L), weights["W_K"], weights["W_V"],
-                                weights["A_K"], weights["A_V"], B_K, B_V, n_kv_heads, head_dim,
-                                base, cache_dtype)
+                                A_K, A_V, B_K, B_V, n_kv_heads, head_dim, base, cache_dtype)
         return gqa_attention(q, q_positions, K, V, scale)
     make = agent_kv if cache_dtype is None else agent_kv_from_cache
-    K, V = make(X_seq, np.arange(L), weights["W_K"], weights["W_V"], weights["A_K"],
-                weights["A_V"], B_K, B_V, n_kv_heads, head_dim, base)
+    K, V = make(X_seq, np.arange(L), weights["W_K"], weights["W_V"], A_K, A_V, B_K, B_V,
+                n_kv_heads, head_dim, base)
     return gqa_attention(q, q_positions, K, V, scale)
 
 
@@ -257,7 +281,8 @@ def append_pools(base_pool, lr_pool, X, positions, seq_rows, block_tables, W_K, 
     """Expected pool contents after an append, written in place.
 
     base_pool [num_blocks, 2, Hkv, 16, d]: plane 0 = K_base, plane 1 = V_base.
-    lr_pool   [num_blocks, 2, 16, r]:      plane 0 = L_K, plane 1 = L_V.
+    lr_pool   [num_blocks, 2, 16, G r]:    plane 0 = L_K, plane 1 = L_V (G = 1 for a
+                                           shared A; group g in columns [g r, (g+1) r)).
     Token n goes to block block_tables[seq_rows[n], positions[n] // 16], row
     positions[n] % 16 (PagedAttention-style block table).
     """

@@ -14,7 +14,9 @@
 // batching", both paths together), or either part alone (a base-only re-base
 // after an agent's turn, "lazy prefill"). The column tiles are laid out so
 // that no tile mixes base and low-rank columns: base tiles of up to 256
-// columns over [0, 2 Hkv d), then one tile of the 2r low-rank columns.
+// columns over [0, 2 Hkv d), then tiles of up to 256 over the 2 G r low-rank
+// columns (G = lr_groups; PReCache, PreLRShared: every agent's own A in one
+// GEMM when the segment is first processed).
 //
 // One CTA per (column tile, 128-token tile):
 //   warp 0      TMA producer: X and W_cat k-slices (64 wide, 128-byte swizzle)
@@ -60,8 +62,8 @@ struct AppendParams {
   int64_t num_blocks;
   int T, h, Hkv, D, R, num_seqs, max_blocks;
   int kvc2;          // base columns: 2 * Hkv * D
+  int lrw;           // low-rank row width: G * R (plane 0 = L_K, plane 1 = L_V)
   int n_base_tiles;  // base column tiles in the grid (0 when the base part is not written)
-  int write_lr;      // the grid has one low-rank tile after the base tiles
   RopeFreqs freqs;
 };
 
@@ -104,8 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool lr_tile = static_cast<int>(blockIdx.x) >= p.n_base_tiles;
-  const int n0 = lr_tile ? p.kvc2 : static_cast<int>(blockIdx.x) * AN;  // first output column
-  const int width = lr_tile ? 2 * p.R : min(AN, p.kvc2 - n0);          // multiple of 16
+  const int lt = static_cast<int>(blockIdx.x) - p.n_base_tiles;  // low-rank tile index
+  const int n0 = lr_tile ? p.kvc2 + lt * AN : static_cast<int>(blockIdx.x) * AN;  // first output column
+  const int width = lr_tile ? min(AN, 2 * p.lrw - lt * AN) : min(AN, p.kvc2 - n0);  // multiple of 16
   const int m0 = static_cast<int>(blockIdx.y) * AM;
   const int KT = p.h / AK;
 
@@ -217,11 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::wait_ld();
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int nn = n - p.kvc2 + 8 * e;  // low-rank column in [0, 2r)
-            if (blk >= 0 && nn < 2 * p.R) {
-              const int plane = nn / p.R, k0 = nn % p.R;
+            const int nn = n - p.kvc2 + 8 * e;  // low-rank column in [0, 2 G r)
+            if (blk >= 0 && nn < 2 * p.lrw) {
+              const int plane = nn / p.lrw, k0 = nn % p.lrw;
               *reinterpret_cast<uint4*>(p.lr_pool + ((static_cast<int64_t>(blk) * 2 + plane) * kBlock +
-                                                     slot_row) * p.R + k0) = pack8(v + 8 * e);
+                                                     slot_row) * p.lrw + k0) = pack8(v + 8 * e);
             }
           }
         } else if (n < kvc) {
@@ -303,10 +306,11 @@ lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X_base, const
   p.num_seqs = num_seqs;
   p.max_blocks = max_blocks;
   p.kvc2 = 2 * cfg.n_kv_heads * cfg.head_dim;
+  p.lrw = lr_width(cfg);
   p.n_base_tiles = X_base != nullptr ? (p.kvc2 + AN - 1) / AN : 0;
-  p.write_lr = X_lr != nullptr ? 1 : 0;
+  const int n_lr_tiles = X_lr != nullptr ? (2 * p.lrw + AN - 1) / AN : 0;
   rope_freqs(cfg, &p.freqs);
-  const int64_t N = p.kvc2 + 2 * cfg.rank;
+  const int64_t N = p.kvc2 + 2 * p.lrw;
   CUtensorMap xb, xl, wm;
   const void* xb_src = X_base != nullptr ? X_base : X_lr;
   const void* xl_src = X_lr != nullptr ? X_lr : X_base;
@@ -314,7 +318,7 @@ lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X_base, const
       !make_kmajor_map(W_cat, N, cfg.hidden, AN, &wm))
     return LRKV_ERR_CUDA;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(append_tc_kernel), SMEM_TOTAL)) return LRKV_ERR_CUDA;
-  dim3 grid(p.n_base_tiles + p.write_lr, (T + AM - 1) / AM);
+  dim3 grid(p.n_base_tiles + n_lr_tiles, (T + AM - 1) / AM);
   append_tc_kernel<<<grid, kThreads, SMEM_TOTAL, stream>>>(p, xb, xl, wm);
   return cudaGetLastError() == cudaSuccess ? LRKV_OK : LRKV_ERR_CUDA;
 }

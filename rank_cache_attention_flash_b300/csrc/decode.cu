@@ -81,6 +81,7 @@ struct DecodeParams {
   int32_t* status;
   int64_t num_blocks;
   int max_blocks, max_ctx_len, n_adapters, num_queries, Hq, Hkv, g;
+  int lr_groups;  // > 1: agent-specific A, adapter a's low-rank group at columns [a r, (a+1) r)
   int rpi, n_chunks, n_splits, split_blocks;
   int has_bk, has_bv;
   float scale_log2;
@@ -264,6 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row0 = chunk * p.rpi;
   const int nrows = min(p.rpi, (qe - qs) * p.g - row0);
   if (nrows <= 0) return;
+  // agent-specific A: the item's rows all belong to one query (the plan makes
+  // them so); its low-rank tiles are that adapter's group of columns
+  int lr_x = 0;
+  if (p.lr_groups > 1) {
+    const int a0 = __ldg(p.adapter_ids + qs + row0 / p.g);
+    if (a0 >= 0 && a0 < p.lr_groups) lr_x = a0 * R;
+  }
   if (len < 1 || len > p.max_ctx_len) {
     if (tid == 0) report(p.status, LRKV_ERR_INDEX);
     len = 0;
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < L::KATOMS; ++a)
           tma_load_2d(dst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, y, fb);
         if (kind == 0 ? p.has_bk : p.has_bv)
-          tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, 0, (id * 2 + kind) * kBlock, fb);
+          tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, lr_x, (id * 2 + kind) * kBlock, fb);
       }
       return true;
     };
@@ -1050,6 +1058,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row0 = chunk * p.rpi;
   const int nrows = min(p.rpi, (qe - qs) * p.g - row0);
   if (nrows <= 0) return;
+  // agent-specific A: the item's rows all belong to one query (the plan makes
+  // them so); its low-rank tiles are that adapter's group of columns
+  int lr_x = 0;
+  if (p.lr_groups > 1) {
+    const int a0 = __ldg(p.adapter_ids + qs + row0 / p.g);
+    if (a0 >= 0 && a0 < p.lr_groups) lr_x = a0 * R;
+  }
   if (len < 1 || len > p.max_ctx_len) {
     if (tid == 0) report(p.status, LRKV_ERR_INDEX);
     len = 0;
@@ -1164,7 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < L::KATOMS; ++a)
           tma_load_2d(dst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, y, fb);
         if (kind == 0 ? rebuild : p.has_bv)
-          tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, 0, (id * 2 + kind) * kBlock, fb);
+          tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, lr_x, (id * 2 + kind) * kBlock, fb);
       }
       return true;
     };
@@ -1760,6 +1775,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   p.has_bk = a.B_K != nullptr;
   p.has_bv = a.B_V != nullptr;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.lr_groups = cfg.lr_groups;
   rope_freqs(cfg, &p.freqs);
 
   CUtensorMap tb, tl;
@@ -1821,6 +1837,12 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   LRKV_L(64, 8) LRKV_L(64, 16) LRKV_L(64, 32) LRKV_L(64, 64)
 #undef LRKV_L
   if (rpi == 0) return false;
+  if (cfg.lr_groups > 1 && !P.rebuild) {
+    // agent-specific A: an item's rows must belong to one query (one adapter,
+    // one low-rank group): a query's heads of the kv head, or a part of them
+    if (P.g <= rpi) rpi = P.g;
+    else if (P.g % rpi != 0) return false;
+  }
   if (P.rebuild) total = D == 128 ? rb::Layout<128, 64>::total : rb::Layout<64, 64>::total;
   P.rows_per_item = rpi;
   P.smem_bytes = std::max(total, kMinSmem);

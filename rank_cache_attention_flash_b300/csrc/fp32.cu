@@ -30,7 +30,7 @@ struct Fp32AppendParams {
   float* lr_pool;
   int32_t* status;
   int64_t num_blocks;
-  int h, Hkv, D, R, num_seqs, max_blocks;
+  int h, Hkv, D, R, lrw, num_seqs, max_blocks;  // lrw: low-rank row width G * R
   RopeFreqs freqs;
 };
 
@@ -56,7 +56,7 @@ __global__ void append_fp32_kernel(const __grid_constant__ Fp32AppendParams p) {
   const int row = pos % kBlock, half = p.D / 2;
   const int kvc = p.Hkv * p.D;
   const int n_pairs = p.Hkv * half;
-  const int units = n_pairs + kvc + 2 * p.R;
+  const int units = n_pairs + kvc + 2 * p.lrw;
   auto dot = [&](int n) {
     const float* w = p.W + static_cast<int64_t>(n) * p.h;
     const float* x = n < 2 * kvc ? xs : xs + p.h;
@@ -78,9 +78,9 @@ __global__ void append_fp32_kernel(const __grid_constant__ Fp32AppendParams p) {
       const int kv = n / p.D, j = n % p.D;
       p.base_pool[(((static_cast<int64_t>(blk) * 2 + 1) * p.Hkv + kv) * kBlock + row) * p.D + j] = dot(kvc + n);
     } else {
-      const int n = u - n_pairs - kvc;  // [0, 2R)
-      const int plane = n / p.R, k = n % p.R;
-      p.lr_pool[((static_cast<int64_t>(blk) * 2 + plane) * kBlock + row) * p.R + k] = dot(2 * kvc + n);
+      const int n = u - n_pairs - kvc;  // [0, 2 G R)
+      const int plane = n / p.lrw, k = n % p.lrw;
+      p.lr_pool[((static_cast<int64_t>(blk) * 2 + plane) * kBlock + row) * p.lrw + k] = dot(2 * kvc + n);
     }
   }
 }
@@ -99,6 +99,7 @@ struct Fp32AttnParams {
   int32_t* status;
   int64_t num_blocks;
   int max_blocks, max_len, Hq, Hkv, D, R, n_adapters;
+  int lrw, lr_groups;  // low-rank row width G * R; G > 1: adapter a reads group a
   int decode;  // 1: adapter per query row; 0: adapter per sequence
   float scale;
   RopeFreqs freqs;
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(kChunk) attn_fp32_kernel(const __grid_constant
   const int pos = p.decode ? (len - 1) : (len - nq + qi);
   const int kv = m / (p.Hq / p.Hkv), half = D / 2;
   const bool bk = p.B_K != nullptr && a >= 0, bv = p.B_V != nullptr && a >= 0;
+  const int loff = (p.lr_groups > 1 && a >= 0) ? a * R : 0;  // this adapter's low-rank group
   for (int j = tid; j < D; j += kChunk) qv[j] = p.q[(static_cast<int64_t>(n) * p.Hq + m) * D + j];
   for (int j = tid; j < D + R; j += kChunk) acc[j] = 0.f;
   __syncthreads();
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kChunk) attn_fp32_kernel(const __grid_constant
       if (blk >= 0 && blk < p.num_blocks) {
         const int row = t % kBlock;
         const float* kb = p.base_pool + (((static_cast<int64_t>(blk) * 2 + 0) * p.Hkv + kv) * kBlock + row) * D;
-        const float* lk = p.lr_pool + ((static_cast<int64_t>(blk) * 2 + 0) * kBlock + row) * R;
+        const float* lk = p.lr_pool + ((static_cast<int64_t>(blk) * 2 + 0) * kBlock + row) * p.lrw + loff;
         float dotv = 0.f;
         for (int j = 0; j < half; ++j) {
           float x = 0.f, y = 0.f;
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(kChunk) attn_fp32_kernel(const __grid_constant
           const int tt = c0 + i;
           const int blk = __ldg(p.block_tables + static_cast<int64_t>(c) * p.max_blocks + tt / kBlock);
           if (blk < 0 || blk >= p.num_blocks || sc[i] == 0.f) continue;
-          v = fmaf(sc[i], p.lr_pool[((static_cast<int64_t>(blk) * 2 + 1) * kBlock + tt % kBlock) * R + (j - D)], v);
+          v = fmaf(sc[i], p.lr_pool[((static_cast<int64_t>(blk) * 2 + 1) * kBlock + tt % kBlock) * p.lrw + loff + (j - D)], v);
         }
       }
       acc[j] = v;
@@ -250,6 +252,8 @@ lrkv_status attn_fp32(const lrkv_config& cfg, const float* q, const int32_t* row
   p.Hkv = cfg.n_kv_heads;
   p.D = cfg.head_dim;
   p.R = cfg.rank;
+  p.lrw = lr_width(cfg);
+  p.lr_groups = cfg.lr_groups;
   p.n_adapters = n_adapters;
   p.decode = decode;
   p.scale = scale;
@@ -283,6 +287,7 @@ lrkv_status launch_append_fp32(const lrkv_config& cfg, const void* X_base, const
   p.Hkv = cfg.n_kv_heads;
   p.D = cfg.head_dim;
   p.R = cfg.rank;
+  p.lrw = lr_width(cfg);
   p.num_seqs = num_seqs;
   p.max_blocks = max_blocks;
   rope_freqs(cfg, &p.freqs);

@@ -90,6 +90,8 @@ lrkv_status check_config(const lrkv_config* cfg) {
     return LRKV_ERR_UNSUPPORTED;
   if (cfg->n_q_heads / cfg->n_kv_heads > 16) return LRKV_ERR_UNSUPPORTED;
   if (cfg->hidden % 64 != 0) return LRKV_ERR_UNSUPPORTED;
+  if (cfg->lr_groups < 1) return LRKV_ERR_INVALID_ARG;
+  if (cfg->lr_groups > 64) return LRKV_ERR_UNSUPPORTED;
   return LRKV_OK;
 }
 
@@ -126,9 +128,9 @@ bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* l
   }
   if (lr_map == nullptr) return true;
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cfg.rank),
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lr_width(cfg)),
                                 static_cast<cuuint64_t>(num_blocks) * 2 * kBlock};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cfg.rank) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lr_width(cfg)) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(cfg.rank), kBlock};
     const cuuint32_t es[2] = {1, 1};
     CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -171,9 +173,9 @@ bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks
                  CUtensorMap* lr_map) {
   EncodeTiled enc = get_encoder();
   if (enc == nullptr || box_cols < cfg.rank) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cfg.rank),
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lr_width(cfg)),
                               static_cast<cuuint64_t>(num_blocks) * 2 * kBlock};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cfg.rank) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lr_width(cfg)) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), kBlock};
   const cuuint32_t es[2] = {1, 1};
   CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_32B;
@@ -208,7 +210,7 @@ bool make_run_maps(const lrkv_config& cfg, const void* base_pool, const void* lr
       return false;
   }
   {
-    const cuuint64_t r = static_cast<cuuint64_t>(cfg.rank);
+    const cuuint64_t r = static_cast<cuuint64_t>(lr_width(cfg));
     const cuuint64_t dims[4] = {r, kBlock, 2, static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t strides[3] = {r * 2, r * 2 * kBlock, r * 2 * kBlock * 2};
     const cuuint32_t box[4] = {static_cast<cuuint32_t>(lr_cols), kBlock, 1, static_cast<cuuint32_t>(nb)};
@@ -243,7 +245,7 @@ const char* lrkv_status_string(lrkv_status s) {
   return "LRKV_UNKNOWN_STATUS";
 }
 
-int32_t lrkv_version(void) { return 100; }
+int32_t lrkv_version(void) { return 20000; }
 
 namespace {
 
@@ -326,6 +328,7 @@ lrkv_status lrkv_attn_decode(const lrkv_config* cfg, const void* q, int32_t num_
   if ((B_K != nullptr && !aligned16(B_K)) || (B_V != nullptr && !aligned16(B_V)))
     return LRKV_ERR_INVALID_ARG;
   if ((B_K != nullptr || B_V != nullptr) && n_adapters == 0) return LRKV_ERR_INVALID_ARG;
+  if (cfg->lr_groups > 1 && n_adapters > cfg->lr_groups) return LRKV_ERR_INVALID_ARG;
   if (max_ctx_len < 1 || max_q_per_ctx < 1 || !(scale == scale)) return LRKV_ERR_INVALID_ARG;
   if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
   if (static_cast<int64_t>(max_ctx_len) > static_cast<int64_t>(max_blocks) * kBlock)
@@ -379,6 +382,7 @@ lrkv_status lrkv_attn_prefill(const lrkv_config* cfg, const void* q, const int32
   if ((B_K != nullptr && !aligned16(B_K)) || (B_V != nullptr && !aligned16(B_V)))
     return LRKV_ERR_INVALID_ARG;
   if ((B_K != nullptr || B_V != nullptr) && n_adapters == 0) return LRKV_ERR_INVALID_ARG;
+  if (cfg->lr_groups > 1 && n_adapters > cfg->lr_groups) return LRKV_ERR_INVALID_ARG;
   if (max_q_len < 1 || max_seq_len < max_q_len || !(scale == scale)) return LRKV_ERR_INVALID_ARG;
   if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
   if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * kBlock)

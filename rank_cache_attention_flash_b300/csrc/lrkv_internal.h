@@ -12,6 +12,9 @@ namespace lrkv {
 
 struct RopeFreqs;  // lrkv_device.cuh
 
+// Columns of one low-rank pool row: every group's r columns side by side.
+inline int lr_width(const lrkv_config& cfg) { return cfg.lr_groups * cfg.rank; }
+
 // Split plan of the bf16 decode kernel; a pure function of the sizes and the
 // device's SM count, so the workspace query and the launch agree.
 struct DecodePlan {

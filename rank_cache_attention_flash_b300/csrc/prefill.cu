@@ -69,6 +69,7 @@ struct PrefillParams {
   int32_t* status;
   int64_t num_blocks;
   int num_seqs, max_blocks, max_seq_len, n_adapters, Hq, Hkv, g;
+  int lr_groups;  // > 1: agent-specific A, adapter a's low-rank group at columns [a r, (a+1) r)
   int has_bk, has_bv;
   float scale_log2;
   RopeFreqs freqs;
@@ -242,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const bool rebuild = p.has_bk && adapter >= 0;
   const bool use_lr = p.has_bv && adapter >= 0;
+  // agent-specific A: this sequence's adapter reads its own low-rank group
+  const int lr_x = (p.lr_groups > 1 && adapter >= 0) ? adapter * R : 0;
   const int k_first = row0 / g;
   const int k_last = min(q_len, (row0 + BM + g - 1) / g) - 1;
   const int pos_min = Ls - q_len + k_first;
@@ -384,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(st + L::off_k + h * (BN * 128), &tm_base_run, 64 * h, 0, head, blk0, fb);
             tma_load_4d(st + L::off_v + h * (BN * 128), &tm_base_run, 64 * h, 0, p.Hkv + head, blk0, fb);
           }
-          if (use_lr) tma_load_4d(st + L::off_lv, &tm_lr_run, 0, 0, 1, blk0, fb);
-          if (rebuild) tma_load_4d(st + L::off_lk, &tm_lr_run, 0, 0, 0, blk0, fb);
+          if (use_lr) tma_load_4d(st + L::off_lv, &tm_lr_run, lr_x, 0, 1, blk0, fb);
+          if (rebuild) tma_load_4d(st + L::off_lk, &tm_lr_run, lr_x, 0, 0, blk0, fb);
         }
       } else if (blk >= 0) {
         const int yk = ((blk * 2 + 0) * p.Hkv + head) * kBlock;
@@ -395,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(st + L::off_k + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yk, fb);
           tma_load_2d(st + L::off_v + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yv, fb);
         }
-        if (use_lr) tma_load_2d(st + L::off_lv + lane * kBlock * LSPAN, &tm_lk, 0, (blk * 2 + 1) * kBlock, fb);
-        if (rebuild) tma_load_2d(st + L::off_lk + lane * kBlock * LSPAN, &tm_lk, 0, (blk * 2 + 0) * kBlock, fb);
+        if (use_lr) tma_load_2d(st + L::off_lv + lane * kBlock * LSPAN, &tm_lk, lr_x, (blk * 2 + 1) * kBlock, fb);
+        if (rebuild) tma_load_2d(st + L::off_lk + lane * kBlock * LSPAN, &tm_lk, lr_x, (blk * 2 + 0) * kBlock, fb);
       }
       ++issued;
     }
@@ -893,6 +896,7 @@ lrkv_status run(const lrkv_config& cfg, const PrefillArgs& a, cudaStream_t strea
   p.g = cfg.n_q_heads / cfg.n_kv_heads;
   p.has_bk = a.B_K != nullptr;
   p.has_bv = a.B_V != nullptr;
+  p.lr_groups = cfg.lr_groups;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   rope_freqs(cfg, &p.freqs);
   CUtensorMap tb, tlk, tbr, tlr;

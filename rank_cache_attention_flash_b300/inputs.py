@@ -60,6 +60,7 @@ class Shape:
     a_std: float
     b_std: float
     q_std: float
+    lr_groups: int = 1  # 1: one A shared by every agent; n: agent a has its own A (PreLRShared)
 
     @property
     def kv_cols(self) -> int:
@@ -67,7 +68,7 @@ class Shape:
 
     @property
     def n_cols(self) -> int:  # packed projection width: K | V | A_K | A_V
-        return 2 * self.kv_cols + 2 * self.rank
+        return 2 * self.kv_cols + 2 * self.lr_groups * self.rank
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -107,7 +108,7 @@ class Case:
     pre_q_start: torch.Tensor           # int32 [P + 1]
     pre_adapter: torch.Tensor           # int32 [P]
     pre_q: torch.Tensor                 # [Np, Hq, d]
-    weights: Dict[str, torch.Tensor]    # W_K, W_V [h, Hkv*d]; A_K, A_V [h, r]; B_K, B_V [n_adapters, r, Hkv*d]
+    weights: Dict[str, torch.Tensor]    # W_K, W_V [h, Hkv*d]; A_K, A_V [h, r] or [G, h, r]; B_K, B_V [n_adapters, r, Hkv*d]
     _xcache: Dict[int, torch.Tensor] = dataclasses.field(default_factory=dict)
 
     # ----- hidden states -------------------------------------------------
@@ -195,11 +196,17 @@ def _weights(shape: Shape, seed: int) -> Dict[str, torch.Tensor]:
     def draw(stream, size, std):
         return torch.randn(*size, generator=_gen(seed, stream)).mul_(std).to(dt)
 
+    def draw_a(stream):
+        # shared A: [h, r]; agent-specific A: [G, h, r], group g from its own stream
+        if shape.lr_groups == 1:
+            return draw(stream, (h, r), shape.a_std)
+        return torch.stack([draw(stream + 100 * g, (h, r), shape.a_std) for g in range(shape.lr_groups)])
+
     return {
         "W_K": draw(_S_WK, (h, kc), shape.w_std),
         "W_V": draw(_S_WV, (h, kc), shape.w_std),
-        "A_K": draw(_S_AK, (h, r), shape.a_std),
-        "A_V": draw(_S_AV, (h, r), shape.a_std),
+        "A_K": draw_a(_S_AK),
+        "A_V": draw_a(_S_AV),
         "B_K": draw(_S_BK, (na, r, kc), shape.b_std),
         "B_V": draw(_S_BV, (na, r, kc), shape.b_std),
     }
@@ -297,31 +304,33 @@ def shape_qwen3_1p7b() -> Shape:
     return Shape(2048, 16, 8, 128, 8, 8, 10000.0, "bf16", 1.0, w, w, 1 / math.sqrt(8), 1.0)
 
 
-def tiny_fp32_decode(seed: int = 0, n: int = 128, first: int = 0) -> Case:
+def tiny_fp32_decode(seed: int = 0, n: int = 128, first: int = 0, lr_groups: int = 1) -> Case:
     """Tiny fp32 decode: 2 agents query one shared n-token context.
-    ``first``: global index of this shard's context (see ``shard_range``)."""
-    shape = shape_tiny_fp32()
+    ``first``: global index of this shard's context (see ``shard_range``);
+    ``lr_groups``: 1 = shared A, n = each agent its own A (PreLRShared)."""
+    shape = dataclasses.replace(shape_tiny_fp32(), lr_groups=lr_groups)
     seqs = [Seq(first, 0, first, n, 0, -1, "context")]
     return _build("tiny_fp32_decode", shape, seed, seqs, [(0, 0), (0, 1)], [], False, (2 * first, 0))
 
 
 def shared_decode(seed: int = 0, n: int = 8192, n_agents: int = 4, rank: int = 16,
-                  first: int = 0) -> Case:
+                  first: int = 0, lr_groups: int = 1) -> Case:
     """Llama-3.1-8B-shaped decode: n_agents queries on one shared n-token context,
-    identity block table. ``first``: global index of this shard's context."""
-    shape = shape_llama8b(rank, n_agents)
+    identity block table. ``first``: global index of this shard's context;
+    ``lr_groups``: 1 = shared A, n = each agent its own A (PreLRShared)."""
+    shape = dataclasses.replace(shape_llama8b(rank, n_agents), lr_groups=lr_groups)
     seqs = [Seq(first, 0, first, n, 0, -1, "context")]
     dec = [(0, a) for a in range(n_agents)]
     return _build("shared_decode_llama8b", shape, seed, seqs, dec, [], False, (n_agents * first, 0))
 
 
 def prefill_chunk(seed: int = 0, prefix: int = 16384, chunk: int = 512, n_agents: int = 4,
-                  rank: int = 16, first: int = 0) -> Case:
+                  rank: int = 16, first: int = 0, lr_groups: int = 1) -> Case:
     """Each agent appends a new chunk and attends causally over the shared prefix
     plus its own chunk. The prefix blocks are shared physically. ``first``:
     global index of this shard's shared context (its prefix and chunks use
     hidden-state streams of their own)."""
-    shape = shape_llama8b(rank, n_agents)
+    shape = dataclasses.replace(shape_llama8b(rank, n_agents), lr_groups=lr_groups)
     base = first * (n_agents + 1)
     seqs = [Seq(base, prefix, base + 1 + a, prefix, chunk, a, "prefill") for a in range(n_agents)]
     return _build("prefill_chunk_llama8b", shape, seed, seqs, [], list(range(n_agents)), False,
@@ -329,11 +338,11 @@ def prefill_chunk(seed: int = 0, prefix: int = 16384, chunk: int = 512, n_agents
 
 
 def long_decode(seed: int = 0, n_seqs: int = 16, n: int = 32768, n_agents: int = 8,
-                rank: int = 64, first: int = 0) -> Case:
+                rank: int = 64, first: int = 0, lr_groups: int = 1) -> Case:
     """Ministral-8B-shaped paged decode: independent sequences, adapter ids uniform
     over the agents, blocks placed by a seeded permutation of the pool.
     ``first``: global index of this shard's first sequence."""
-    shape = shape_llama8b(rank, n_agents)
+    shape = dataclasses.replace(shape_llama8b(rank, n_agents), lr_groups=lr_groups)
     ad = torch.randint(0, n_agents, (first + n_seqs,), generator=_gen(seed, _S_ADAPT))[first:].tolist()
     seqs = [Seq(0, 0, 1 + first + s, n, 0, ad[s], "context") for s in range(n_seqs)]
     dec = [(s, ad[s]) for s in range(n_seqs)]

@@ -41,21 +41,30 @@ class Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("rank", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("rope_base", ctypes.c_float), ("dtype", ctypes.c_int32)]
+                ("rope_base", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("lr_groups", ctypes.c_int32)]
 
     @property
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == BF16 else torch.float32
 
     @property
+    def lr_width(self) -> int:
+        """Columns of a low-rank pool row: every group's r columns side by side."""
+        return max(1, self.lr_groups) * self.rank
+
+    @property
     def n_cols(self) -> int:
-        return 2 * self.n_kv_heads * self.head_dim + 2 * self.rank
+        return 2 * self.n_kv_heads * self.head_dim + 2 * self.lr_width
 
 
 def make_config(hidden: int, n_q_heads: int, n_kv_heads: int, head_dim: int, rank: int,
-                rope_base: float = 10000.0, dtype: torch.dtype = torch.bfloat16) -> Config:
+                rope_base: float = 10000.0, dtype: torch.dtype = torch.bfloat16,
+                lr_groups: int = 1) -> Config:
+    """lr_groups = 1: one A shared by every agent; lr_groups = n: agent a has its
+    own A_a and reads low-rank group a (PreLRShared)."""
     return Config(hidden, n_q_heads, n_kv_heads, head_dim, rank, BLOCK, rope_base,
-                  BF16 if dtype == torch.bfloat16 else FP32)
+                  BF16 if dtype == torch.bfloat16 else FP32, lr_groups)
 
 
 _lib = None
@@ -134,8 +143,12 @@ def version() -> int:
 # ------------------------------------------------------------------ helpers
 def pack_w_cat(W_K: torch.Tensor, W_V: torch.Tensor, A_K: torch.Tensor, A_V: torch.Tensor) -> torch.Tensor:
     """One-time weight layout for append: [N, h] rows = output columns
-    (nn.Linear layout), in the order K | V | A_K | A_V."""
-    return torch.cat([W_K.t(), W_V.t(), A_K.t(), A_V.t()], 0).contiguous()
+    (nn.Linear layout), in the order K | V | A_K | A_V. Agent-specific factors
+    A_K, A_V of shape [G, h, r] contribute their groups in order (group g's r
+    rows after group g-1's)."""
+    def rows(A):
+        return A.t() if A.dim() == 2 else A.permute(0, 2, 1).reshape(-1, A.shape[1])
+    return torch.cat([W_K.t(), W_V.t(), rows(A_K), rows(A_V)], 0).contiguous()
 
 
 def new_pools(cfg: Config, num_blocks: int, device, fill: Optional[float] = None
@@ -143,7 +156,7 @@ def new_pools(cfg: Config, num_blocks: int, device, fill: Optional[float] = None
     """Allocates (base_pool, lr_pool) for ``num_blocks`` blocks."""
     dt = cfg.torch_dtype
     base = torch.empty(num_blocks, 2, cfg.n_kv_heads, BLOCK, cfg.head_dim, dtype=dt, device=device)
-    lr = torch.empty(num_blocks, 2, BLOCK, cfg.rank, dtype=dt, device=device)
+    lr = torch.empty(num_blocks, 2, BLOCK, cfg.lr_width, dtype=dt, device=device)
     if fill is not None:
         base.fill_(fill)
         lr.fill_(fill)

@@ -419,6 +419,69 @@ def pin_rebased_kv_stacked_weights(O):
     assert np.allclose(e1[0], e2[0], rtol=1e-13, atol=1e-13) and np.allclose(e1[1], e2[1], rtol=1e-13, atol=1e-13)
 
 
+# ------------------------------------------------ agent-specific A (PreLRShared)
+def pin_prelr_merged_weights(O):
+    """With agent-specific A_i (weights A_K, A_V of shape [G, h, r]), agent i's
+    attention is ordinary attention over its own non-shared cache, one GEMM with
+    the merged weights W + A_i B_i per projection (checked against SDPA); the
+    agents' results differ; G = 1 equals the shared-A form."""
+    r = _rng(16)
+    h, Hq, Hkv, d, rank, G = 20, 4, 2, 8, 3, 3
+    w = _small_weights(r, h, Hkv, d, rank, G)
+    w["A_K"] = r.standard_normal((G, h, rank))
+    w["A_V"] = r.standard_normal((G, h, rank))
+    L = 17
+    X = r.standard_normal((L, h))
+    q = r.standard_normal((1, Hq, d))
+    scale = 1 / math.sqrt(d)
+    outs = []
+    for i in range(G):
+        got = O.attend(X, i, q, [L - 1], w, Hkv, d, 10000.0, scale)
+        K = O.apply_rope((X @ (w["W_K"] + w["A_K"][i] @ w["B_K"][i])).reshape(L, Hkv, d), np.arange(L), 10000.0)
+        V = (X @ (w["W_V"] + w["A_V"][i] @ w["B_V"][i])).reshape(L, Hkv, d)
+        assert np.allclose(got, _sdpa(q * scale * math.sqrt(d), K, V, causal=False), rtol=1e-12, atol=1e-13)
+        outs.append(got)
+    assert not np.allclose(outs[0], outs[1])
+    # base-only rows ignore A
+    got0 = O.attend(X, -1, q, [L - 1], w, Hkv, d, 10000.0, scale)
+    K = O.apply_rope((X @ w["W_K"]).reshape(L, Hkv, d), np.arange(L), 10000.0)
+    assert np.allclose(got0, _sdpa(q, K, (X @ w["W_V"]).reshape(L, Hkv, d), causal=False), rtol=1e-12, atol=1e-13)
+    # one group is the shared-A form
+    w1 = dict(w)
+    w1["A_K"], w1["A_V"] = w["A_K"][1:2], w["A_V"][1:2]
+    w2 = dict(w)
+    w2["A_K"], w2["A_V"] = w["A_K"][1], w["A_V"][1]
+    assert np.allclose(O.attend(X, 0, q, [L - 1], w1, Hkv, d, 10000.0, scale),
+                       O.attend(X, 0, q, [L - 1], w2, Hkv, d, 10000.0, scale), rtol=1e-14, atol=1e-15)
+
+
+def pin_prelr_pool_bruteforce(O):
+    """PreLRShared append on integer data: every agent's low-rank rows, side by
+    side (group g in columns [g r, (g + 1) r)), recomputed with Python ints."""
+    r = _rng(17)
+    h, Hkv, d, rank, G = 9, 1, 4, 2, 3
+    X = r.integers(-3, 4, size=(3, h)).astype(np.float64)
+    WK = r.integers(0, 2, size=(h, Hkv * d)).astype(np.float64)
+    WV = r.integers(0, 2, size=(h, Hkv * d)).astype(np.float64)
+    AK = r.integers(-1, 2, size=(G, h, rank)).astype(np.float64)
+    AV = r.integers(-1, 2, size=(G, h, rank)).astype(np.float64)
+    pos = np.array([5, 0, 31])
+    seqs = np.array([0, 1, 0])
+    bt = np.array([[2, 0], [1, 3]])
+    bp = np.full((4, 2, Hkv, 16, d), np.nan)
+    lp = np.full((4, 2, 16, G * rank), np.nan)
+    O.append_pools(bp, lp, X, pos, seqs, bt, WK, WV, AK, AV, Hkv, d, 10000.0)
+    slot = {0: (2, 5), 1: (1, 0), 2: (0, 15)}
+    for n in range(3):
+        blk, row = slot[n]
+        for g in range(G):
+            for k in range(rank):
+                want_k = sum(int(X[n, j]) * int(AK[g, j, k]) for j in range(h))
+                want_v = sum(int(X[n, j]) * int(AV[g, j, k]) for j in range(h))
+                assert lp[blk, 0, row, g * rank + k] == want_k
+                assert lp[blk, 1, row, g * rank + k] == want_v
+
+
 ALL_PINS = [
     pin_rope_closed_form, pin_rope_frequencies, pin_rope_invariants,
     pin_attention_sdpa_decode, pin_attention_sdpa_prefill, pin_attention_brute_force,
@@ -427,4 +490,5 @@ ALL_PINS = [
     pin_append_integer_bruteforce, pin_prefill_last_row_equals_decode, pin_multi_agent_batch,
     pin_round_bf16_matches_library, pin_bf16_cache_variant_is_exact_on_representable_data,
     pin_rebase_integer_bruteforce, pin_rebased_kv_stacked_weights,
+    pin_prelr_merged_weights, pin_prelr_pool_bruteforce,
 ]

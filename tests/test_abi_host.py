@@ -46,7 +46,7 @@ def test_status_strings_and_version(lib):
 
 def _cfg(**kw):
     base = dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, rank=8, block_size=16,
-                rope_base=10000.0, dtype=0)
+                rope_base=10000.0, dtype=0, lr_groups=1)
     base.update(kw)
     return lrkv.Config(**base)
 
@@ -54,7 +54,7 @@ def _cfg(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=96), 2), (dict(rank=12), 2), (dict(block_size=32), 2), (dict(dtype=5), 2),
     (dict(n_q_heads=5), 1), (dict(hidden=0), 1), (dict(rope_base=0.0), 1), (dict(hidden=100), 2),
-    (dict(n_q_heads=64, n_kv_heads=2), 2),
+    (dict(n_q_heads=64, n_kv_heads=2), 2), (dict(lr_groups=0), 1), (dict(lr_groups=65), 2),
 ])
 def test_bad_config_rejected_before_launch(lib, kw, code):
     cfg = _cfg(**kw)

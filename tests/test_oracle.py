@@ -43,7 +43,11 @@ MUTATIONS = {
     "drop_v_adapter": ("v = v + (X @ _f64(A_V)) @ _f64(B_V_i)", "v = v"),
     "swap_A_in_agent_kv": ("k_pre = k_pre + (X @ _f64(A_K)) @ _f64(B_K_i)",
                            "k_pre = k_pre + (X @ _f64(A_V)) @ _f64(B_K_i)"),
-    "swap_lowrank_outputs": ("X @ _f64(A_K), X @ _f64(A_V))", "X @ _f64(A_V), X @ _f64(A_K))"),
+    "swap_lowrank_outputs": ("_lowrank(X, A_K), _lowrank(X, A_V))", "_lowrank(X, A_V), _lowrank(X, A_K))"),
+    "prelr_groups_reversed": ("np.concatenate([X @ A[g] for g in range(A.shape[0])], axis=1)",
+                              "np.concatenate([X @ A[g] for g in reversed(range(A.shape[0]))], axis=1)"),
+    "prelr_agent_uses_group_0": ("        g = max(adapter, 0)\n", "        g = 0\n"),
+    "prelr_agent_off_by_one": ("        g = max(adapter, 0)\n", "        g = (adapter + 1) % A_K.shape[0]\n"),
     "kv_head_modulo": ("kv = m // g", "kv = m % Hkv"),
     "causal_strict": ("np.arange(L)[None, :] <= qp[:, None]", "np.arange(L)[None, :] < qp[:, None]"),
     "causal_peek_ahead": ("np.arange(L)[None, :] <= qp[:, None]", "np.arange(L)[None, :] <= qp[:, None] + 1"),
