@@ -44,7 +44,7 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "all"
 ALL_WORKLOADS = ["shared_decode_llama8b", "prefill_chunk_llama8b", "long_decode_ministral8b",
-                 "mixed_batch_qwen3_1p7b"]
+                 "mixed_batch_qwen3_1p7b", "prelr_decode_llama8b", "rebase_prefill_llama8b"]
 HEADLINE = "long_decode_ministral8b"
 PREFILL_HEADLINE = "prefill_chunk_llama8b"
 METRIC = "LoRA-KV attention decode tok/s & GB/s (% of HBM), prefill TFLOP/s (% peak)"
@@ -121,8 +121,9 @@ def workload_model(case):
                           "unit_name": "prefill tokens", "pairs": pairs}
     T = sum(b - a for _, a, b in case.step_appends())
     if T:
-        N = 2 * Hkv * D + 2 * R
-        out["append"] = {"bytes": (T * sh.hidden + N * sh.hidden + T * N) * es,
+        N = 2 * Hkv * D + 2 * sh.lr_groups * R
+        n_src = 2 if case.rebase else 1  # a re-based append reads two sets of hidden states
+        out["append"] = {"bytes": (n_src * T * sh.hidden + N * sh.hidden + T * N) * es,
                          "flops": 2 * T * sh.hidden * N, "units": T, "unit_name": "appended tokens"}
     return out
 
@@ -273,7 +274,7 @@ def oracle_sample(case, budget_s: float, model):
     import numpy as np
 
     import oracle
-    from tests.parity import weights64
+    from tests.parity import _hidden, weights64
 
     sh = case.shape
     w64 = weights64(case)
@@ -286,9 +287,9 @@ def oracle_sample(case, budget_s: float, model):
         for r in range(case.dec_q.shape[0]):
             c = next(i for i in range(len(case.dec_ctx)) if qs[i] <= r < qs[i + 1])
             L_full = case.seqs[case.dec_ctx[c]].total_len
-            X = case.seq_hidden(case.dec_ctx[c]).double().numpy()
+            X, X_lr = _hidden(case, case.dec_ctx[c])
             oracle.decode(X, case.dec_q[r:r + 1].double().numpy(), case.dec_adapter[r:r + 1].numpy(),
-                          w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+                          w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale, X_lr=X_lr)
             done += 1.0
             n_full += 1
             if time.perf_counter() - t0 > budget_s:
@@ -301,11 +302,12 @@ def oracle_sample(case, budget_s: float, model):
         a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
         n = b - a
         rows = list(range(0, n, max(1, n // 16)))
-        X = case.seq_hidden(s).double().numpy()
+        X, X_lr = _hidden(case, s)
         L = X.shape[0]
         t0 = time.perf_counter()
         oracle.attend(X, int(case.pre_adapter[p]), case.pre_q[a:b][rows].double().numpy(),
-                      np.array([L - n + k for k in rows]), w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+                      np.array([L - n + k for k in rows]), w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale,
+                      X_lr=X_lr)
         dt = time.perf_counter() - t0
         vis = sum(L - n + k + 1 for k in rows)
         fl = sh.n_q_heads * vis * (4 * sh.head_dim + 2 * sh.rank)
@@ -313,15 +315,15 @@ def oracle_sample(case, budget_s: float, model):
     # mixed: one decode query and one prefill sequence's sampled rows, in tokens/s
     t0 = time.perf_counter()
     c = 0
-    X = case.seq_hidden(case.dec_ctx[c]).double().numpy()
+    X, X_lr = _hidden(case, case.dec_ctx[c])
     oracle.decode(X, case.dec_q[0:1].double().numpy(), case.dec_adapter[0:1].numpy(), w64, sh.n_kv_heads,
-                  sh.head_dim, sh.rope_base, scale)
+                  sh.head_dim, sh.rope_base, scale, X_lr=X_lr)
     p = 0
     s = case.pre_seq[p]
     a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
-    X = case.seq_hidden(s).double().numpy()
+    X, X_lr = _hidden(case, s)
     oracle.prefill(X, case.pre_q[a:b].double().numpy(), int(case.pre_adapter[p]), w64, sh.n_kv_heads,
-                   sh.head_dim, sh.rope_base, scale)
+                   sh.head_dim, sh.rope_base, scale, X_lr=X_lr)
     dt = time.perf_counter() - t0
     return (1 + (b - a)) / dt, "tok/s", dt, f"1 decode query + 1 prefill chunk of {b - a} tokens"
 
@@ -342,7 +344,7 @@ def run_reference(args):
     import numpy as np
 
     import oracle
-    from tests.parity import weights64
+    from tests.parity import _hidden, weights64
 
     sh = case.shape
     w64 = weights64(case)
@@ -351,23 +353,24 @@ def run_reference(args):
     if decode_like:
         s = case.dec_ctx[0]
         L_full = case.seqs[s].total_len
-        X_full = case.seq_hidden(s).double().numpy()
+        X_full, X_lr = _hidden(case, s)
         q = case.dec_q[0:1].double().numpy()
         ad = case.dec_adapter[0:1].numpy()
 
         def one(nt):
-            oracle.decode(X_full[:nt], q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+            oracle.decode(X_full[:nt], q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale,
+                          X_lr=None if X_lr is None else X_lr[:nt])
     else:
         p = 0
         s = case.pre_seq[p]
         a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
-        X_full = case.seq_hidden(s).double().numpy()
+        X_full, X_lr = _hidden(case, s)
         L_full = X_full.shape[0]
         qrow = case.pre_q[b - 1:b].double().numpy()
 
         def one(nt):
             oracle.attend(X_full[:nt], int(case.pre_adapter[p]), qrow, [nt - 1], w64, sh.n_kv_heads,
-                          sh.head_dim, sh.rope_base, scale)
+                          sh.head_dim, sh.rope_base, scale, X_lr=None if X_lr is None else X_lr[:nt])
     # calibrate tokens per step
     nt = min(L_full, 256)
     t0 = time.perf_counter()
@@ -483,8 +486,14 @@ def time_workload(name, args, world, rank, dev, pk):
     del graphs
 
     # ---- end to end through the public API: one packed copy in, one out
+    # (the host enqueues each step while the GPU runs it: Python's garbage
+    # collector stays off in this loop so a collection pause is not timed)
+    import gc
+
     e_ms = []
     n_e2e = min(args.e2e_steps, 50 if dominant == "prefill" or len(kinds) > 1 else args.e2e_steps)
+    gc.collect()
+    gc.disable()
     for i in range(n_e2e + 3):
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -497,6 +506,7 @@ def time_workload(name, args, world, rank, dev, pk):
         b.synchronize()
         if i >= 3:
             e_ms.append(a.elapsed_time(b))
+    gc.enable()
     e2e_ms = reduce_step_time(sum(e_ms), len(e_ms), world, dev)
 
     if dominant == "decode" and "prefill" not in model:
@@ -510,7 +520,7 @@ def time_workload(name, args, world, rank, dev, pk):
         work = model["decode"]["units"] + model["prefill"]["units"]
     value = job_throughput(work, world, ms_per_step)
     e2e = {"value": job_throughput(work, world, e2e_ms), "unit": unit, "h2d_bytes_per_step": g.h2d_bytes,
-           "d2h_bytes_per_step": g.d2h_bytes, "ms_per_step": e2e_ms,
+           "d2h_bytes_per_step": g.d2h_bytes, "ms_per_step": e2e_ms, "ms_median": statistics.median(e_ms),
            "copies_per_step": {"h2d": 1, "d2h": 1}}
 
     parts = {}

@@ -119,6 +119,8 @@ class GpuCase:
             ins.add("step_X", torch.cat(xs))
             ins.add("step_pos", torch.cat(pos))
             ins.add("step_rows", torch.cat(rows))
+            if case.rebase:  # the new tokens' adapter-free hidden states (base part)
+                ins.add("step_Xb", torch.cat([case.seq_hidden_neutral(s, a, b) for s, a, b in case.step_appends()]))
         self.in_dev, self.in_host, views = ins.materialise(dev, True)
         self.out_dev, self.out_host, oviews = outs.materialise(dev, False)
         self.h2d_bytes = ins.nbytes
@@ -142,21 +144,29 @@ class GpuCase:
         case, dev = self.case, self.device
         pend_x, pend_p, pend_r, n = [], [], [], 0
 
+        pend_xb = []
+
         def flush():
-            nonlocal pend_x, pend_p, pend_r, n
+            nonlocal pend_x, pend_xb, pend_p, pend_r, n
             if not pend_x:
                 return
             X = torch.cat(pend_x).to(dev)
             P = torch.cat(pend_p).to(dev)
             Rw = torch.cat(pend_r).to(dev)
-            lrkv.append(self.cfg, X, P, Rw, self.block_tables, self.W_cat, self.base_pool,
-                        self.lr_pool, self.status)
-            pend_x, pend_p, pend_r, n = [], [], [], 0
+            if case.rebase:
+                lrkv.append_rebase(self.cfg, torch.cat(pend_xb).to(dev), X, P, Rw, self.block_tables,
+                                   self.W_cat, self.base_pool, self.lr_pool, self.status)
+            else:
+                lrkv.append(self.cfg, X, P, Rw, self.block_tables, self.W_cat, self.base_pool,
+                            self.lr_pool, self.status)
+            pend_x, pend_xb, pend_p, pend_r, n = [], [], [], [], 0
 
         for s, a, b in case.setup_appends():
             for lo in range(a, b, self.setup_chunk_tokens):
                 hi = min(b, lo + self.setup_chunk_tokens)
                 pend_x.append(case.seq_hidden(s, lo, hi))
+                if case.rebase:
+                    pend_xb.append(case.seq_hidden_neutral(s, lo, hi))
                 pend_p.append(torch.arange(lo, hi, dtype=torch.int32))
                 pend_r.append(torch.full((hi - lo,), s, dtype=torch.int32))
                 n += hi - lo
@@ -165,7 +175,12 @@ class GpuCase:
         flush()
 
     def step_append(self) -> None:
-        if self.n_step_tokens:
+        if not self.n_step_tokens:
+            return
+        if self.case.rebase:  # one launch, base part from the adapter-free states
+            lrkv.append_rebase(self.cfg, self.step_Xb, self.step_X, self.step_pos, self.step_rows,
+                               self.block_tables, self.W_cat, self.base_pool, self.lr_pool, self.status)
+        else:
             lrkv.append(self.cfg, self.step_X, self.step_pos, self.step_rows, self.block_tables,
                         self.W_cat, self.base_pool, self.lr_pool, self.status)
 

@@ -109,6 +109,7 @@ class Case:
     pre_adapter: torch.Tensor           # int32 [P]
     pre_q: torch.Tensor                 # [Np, Hq, d]
     weights: Dict[str, torch.Tensor]    # W_K, W_V [h, Hkv*d]; A_K, A_V [h, r] or [G, h, r]; B_K, B_V [n_adapters, r, Hkv*d]
+    rebase: bool = False                # every append re-based: base part from the adapter-free states
     _xcache: Dict[int, torch.Tensor] = dataclasses.field(default_factory=dict)
 
     # ----- hidden states -------------------------------------------------
@@ -370,6 +371,25 @@ def mixed_batch(seed: int = 0, n_seqs: int = 64, n_decode: int = 48, chunk: int 
                   (first * n_decode, first * (n_seqs - n_decode) * chunk))
 
 
+def prelr_decode(seed: int = 0, n: int = 8192, n_agents: int = 4, rank: int = 16, first: int = 0) -> Case:
+    """The shared-context decode with agent-specific A (PReCache, PreLRShared):
+    each of the 4 agents reads its own low-rank group of the cache."""
+    case = shared_decode(seed, n, n_agents, rank, first, lr_groups=n_agents)
+    case.name = "prelr_decode_llama8b"
+    return case
+
+
+def rebase_prefill(seed: int = 0, prefix: int = 16384, chunk: int = 512, n_agents: int = 4,
+                   rank: int = 16, first: int = 0) -> Case:
+    """The prefill-chunk workload with a re-based cache (PReCache, ReBaseShared):
+    every append writes the base part from the adapter-free hidden states and
+    the low-rank part from the adapted ones, in one launch."""
+    case = prefill_chunk(seed, prefix, chunk, n_agents, rank, first)
+    case.name = "rebase_prefill_llama8b"
+    case.rebase = True
+    return case
+
+
 def shard_range(n_global: int, world: int, rank: int) -> range:
     """The contiguous share [lo, hi) of ``n_global`` independent contexts that
     rank ``rank`` of ``world`` owns (sizes differ by at most one)."""
@@ -389,6 +409,8 @@ SHARD_UNITS = {
     "prefill_chunk_llama8b": 1,
     "long_decode_ministral8b": 16,
     "mixed_batch_qwen3_1p7b": 1,
+    "prelr_decode_llama8b": 1,
+    "rebase_prefill_llama8b": 1,
 }
 
 
@@ -408,6 +430,8 @@ FULL = {
     "prefill_chunk_llama8b": lambda seed=0, first=0: prefill_chunk(seed, first=first),
     "long_decode_ministral8b": lambda seed=0, first=0: long_decode(seed, first=first),
     "mixed_batch_qwen3_1p7b": lambda seed=0, first=0: mixed_batch(seed, first=first),
+    "prelr_decode_llama8b": lambda seed=0, first=0: prelr_decode(seed, first=first),
+    "rebase_prefill_llama8b": lambda seed=0, first=0: rebase_prefill(seed, first=first),
 }
 
 # Small variants: same layer shapes, lengths the oracle finishes in seconds,

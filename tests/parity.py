@@ -58,6 +58,14 @@ def assert_close(got, want, tol, what=""):
     return mx, rf
 
 
+def _hidden(case, s):
+    """Hidden states of sequence s as the oracle takes them: (X, None), or for a
+    re-based cache (X_base = the adapter-free states, X_lr = the adapted ones)."""
+    if case.rebase:
+        return case.seq_hidden_neutral(s).double().numpy(), case.seq_hidden(s).double().numpy()
+    return case.seq_hidden(s).double().numpy(), None
+
+
 def oracle_decode_rows(case, rows: Optional[Iterable[int]] = None, w64=None, cache=None):
     """Oracle outputs [n, Hq, d] of the decode queries ``rows`` (default: all).
     cache="bf16": the oracle's cache components rounded to bf16 first."""
@@ -72,10 +80,10 @@ def oracle_decode_rows(case, rows: Optional[Iterable[int]] = None, w64=None, cac
         c = next(i for i in range(len(case.dec_ctx)) if qs[i] <= r < qs[i + 1])
         by_ctx.setdefault(c, []).append(r)
     for c, rs in by_ctx.items():
-        X = case.seq_hidden(case.dec_ctx[c]).double().numpy()
+        X, X_lr = _hidden(case, case.dec_ctx[c])
         q = case.dec_q[rs].double().numpy()
         ad = case.dec_adapter[rs].numpy()
-        o = oracle.decode(X, q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale, cache)
+        o = oracle.decode(X, q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale, cache, X_lr)
         for i, r in enumerate(rs):
             out[r] = o[i]
     return np.stack([out[r] for r in rows])
@@ -88,7 +96,7 @@ def oracle_prefill_seq(case, p: int, q_rows: Optional[Iterable[int]] = None, w64
     w64 = w64 or weights64(case)
     scale = 1.0 / math.sqrt(sh.head_dim)
     s = case.pre_seq[p]
-    X = case.seq_hidden(s).double().numpy()
+    X, X_lr = _hidden(case, s)
     a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
     n = b - a
     q_rows = list(range(n)) if q_rows is None else list(q_rows)
@@ -96,5 +104,5 @@ def oracle_prefill_seq(case, p: int, q_rows: Optional[Iterable[int]] = None, w64
     q = case.pre_q[a:b][q_rows].double().numpy()
     pos = np.array([L - n + k for k in q_rows])
     out = oracle.attend(X, int(case.pre_adapter[p]), q, pos, w64, sh.n_kv_heads, sh.head_dim,
-                        sh.rope_base, scale, cache)
+                        sh.rope_base, scale, cache, X_lr)
     return [a + k for k in q_rows], out

@@ -121,3 +121,21 @@ def test_full_mixed(cuda_lib):
                       lambda n=n: oracle_decode_rows(case, rows=[n], w64=w64, cache="bf16")[0])
     got, want = _prefill_all(case, g, res, w64)
     _whole([dec_got] + got, [dec_want] + want, case, "mixed batch")
+
+
+def test_full_prelr_decode(cuda_lib):
+    """The shared-context decode with agent-specific A (each agent its own
+    low-rank group), all 4 queries against the literal oracle."""
+    case, g, res = _run("prelr_decode_llama8b")
+    assert case.shape.lr_groups == 4
+    assert_close(res["decode"].double().cpu().numpy(), oracle_decode_rows(case), tol_for(case))
+
+
+def test_full_rebase_prefill(cuda_lib):
+    """The prefill workload over a re-based cache (base part from the
+    adapter-free states), all rows against the literal oracle's
+    K_i = RoPE(X_base W_K + X_lr A_K B_K,i)."""
+    case, g, res = _run("rebase_prefill_llama8b")
+    assert case.rebase
+    got, want = _prefill_all(case, g, res, weights64(case))
+    _whole(got, want, case, "re-based prefill")
