@@ -151,18 +151,6 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
   return r != 0;
 }
 
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool test_parity(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 constexpr long long kWaitCycles = 1ll << 31;  // ~1 s: a wait this long has failed
 
 // Waits for an mbarrier phase with try_wait (which suspends until the phase
@@ -205,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NB = L::NB;
   constexpr uint32_t SW_LK = tc::swizzle_code(LSPAN);
   constexpr int NQ = HALF / 16;  // Y quarters of 16 RoPE pairs per tile
+  static_assert(NQ % 2 == 0, "the rebuild takes the quarters in pairs");
   constexpr uint32_t kIdY = tc::idesc_f16(128, 32, true, false, false);
   constexpr uint32_t kIdS16 = tc::idesc_f16(128, BN, false, false, false);  // fp16 Q, K_a
   constexpr uint32_t kIdSbf = tc::idesc_f16(128, BN, true, false, false);   // bf16 Q, K_base
@@ -750,58 +739,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* kbuf = smem + s * L::STAGE + L::off_k;  // this tile's K buffer
       if (rebuild) {
         const float2* bt = btab + bb * HALF;
-#pragma unroll 1
-        for (int q = 0; q < NQ; ++q) {
-          const int g = j * NQ + q;
+        // Rotates quarter q (pairs 16 q .. 16 q + 15: y[0..15] low dims, y[16..31]
+        // their partners), adds K_base and writes fp16 K_a in place.
+        auto rotate_quarter = [&](int q, const uint32_t (&y)[32]) {
+          if (!key_ok) return;
+#pragma unroll
+          for (int hc = 0; hc < 2; ++hc) {  // 8 pairs per 16-byte chunk
+            const int dlo = 16 * q + 8 * hc, dhi = dlo + HALF;
+            // this thread's own K row: plain shared accesses the compiler may schedule
+            uint4* plo = reinterpret_cast<uint4*>(kbuf + (dlo / 64) * (BN * 128) + swz<128>(i, (dlo % 64) * 2));
+            uint4* phi = reinterpret_cast<uint4*>(kbuf + (dhi / 64) * (BN * 128) + swz<128>(i, (dhi % 64) * 2));
+            const uint4 klo = *plo, khi = *phi;
+            const uint32_t kl[4] = {klo.x, klo.y, klo.z, klo.w};
+            const uint32_t kh[4] = {khi.x, khi.y, khi.z, khi.w};
+            uint32_t olo[4], ohi[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              float rl[2], rh[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int pp = 8 * hc + 2 * w + e;  // pair index within the quarter
+                const int jj = 16 * q + pp;
+                const float2 b2 = bt[jj];
+                const float cd = drow[2 * jj], sd = drow[2 * jj + 1];
+                const float c = b2.x * cd - b2.y * sd;
+                const float sn = b2.y * cd + b2.x * sd;
+                const float yl = __uint_as_float(y[pp]), yh = __uint_as_float(y[16 + pp]);
+                const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
+                const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
+                rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
+                rh[e] = fmaf(yh, c, fmaf(yl, sn, bh));
+              }
+              olo[w] = pack_f16(rl[0], rl[1]);
+              ohi[w] = pack_f16(rh[0], rh[1]);
+            }
+            *plo = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+            *phi = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+          }
+        };
+        // Waits for quarter g and starts reading it from TMEM into y (the read
+        // completes at the next tcgen05.wait::ld); false once a wait has failed.
+        auto fetch_quarter = [&](int g, uint32_t (&y)[32]) -> bool {
           bool oky = !failed && wait_phase(bar(B_YFULL + (g & 1)), (g >> 1) & 1, p.status);
           oky = __all_sync(0xffffffffu, oky);
           if (!oky && !failed) {
             failed = true;
             *abort_flag = 1;
           }
-          if (failed) continue;
-          uint32_t ylo[16], yhi[16];  // pairs 16 q + e: low dim, its partner
+          if (failed) return false;
           tc::fence_after();
-          tc::ld_x16(tbase + lane_off + Y_COL + 32 * (g & 1), ylo);
-          tc::ld_x16(tbase + lane_off + Y_COL + 32 * (g & 1) + 16, yhi);
+          tc::ld_x32(tbase + lane_off + Y_COL + 32 * (g & 1), y);  // 16 low dims, then their partners
+          return true;
+        };
+        // Quarters in pairs: while quarter q is rotated, quarter q + 1 is
+        // already on its way out of TMEM (its own buffer, Y ping-pong).
+        uint32_t ya[32], yb[32];
+        const int g0 = j * NQ;
+        bool have = fetch_quarter(g0, ya);
+#pragma unroll 1
+        for (int q = 0; q < NQ; q += 2) {
+          const int g = g0 + q;
+          if (!have) break;
           tc::wait_ld();
           tc::fence_before();
           mbar_arrive(bar(B_YFREE + (g & 1)));  // the buffer may take quarter g + 2
-          if (key_ok) {
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {  // 8 pairs per 16-byte chunk
-              const int dlo = 16 * q + 8 * hc, dhi = dlo + HALF;
-              // this thread's own K row: plain shared accesses the compiler may schedule
-              uint4* plo = reinterpret_cast<uint4*>(kbuf + (dlo / 64) * (BN * 128) + swz<128>(i, (dlo % 64) * 2));
-              uint4* phi = reinterpret_cast<uint4*>(kbuf + (dhi / 64) * (BN * 128) + swz<128>(i, (dhi % 64) * 2));
-              const uint4 klo = *plo, khi = *phi;
-              const uint32_t kl[4] = {klo.x, klo.y, klo.z, klo.w};
-              const uint32_t kh[4] = {khi.x, khi.y, khi.z, khi.w};
-              uint32_t olo[4], ohi[4];
-#pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                float rl[2], rh[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const int pp = 8 * hc + 2 * w + e;  // pair index within the quarter
-                  const int jj = 16 * q + pp;
-                  const float2 b2 = bt[jj];
-                  const float cd = drow[2 * jj], sd = drow[2 * jj + 1];
-                  const float c = b2.x * cd - b2.y * sd;
-                  const float sn = b2.y * cd + b2.x * sd;
-                  const float yl = __uint_as_float(ylo[pp]), yh = __uint_as_float(yhi[pp]);
-                  const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
-                  const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
-                  rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
-                  rh[e] = fmaf(yh, c, fmaf(yl, sn, bh));
-                }
-                olo[w] = pack_f16(rl[0], rl[1]);
-                ohi[w] = pack_f16(rh[0], rh[1]);
-              }
-              *plo = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-              *phi = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-            }
-          }
+          const bool have_b = fetch_quarter(g + 1, yb);
+          rotate_quarter(q, ya);
+          if (!have_b) break;
+          tc::wait_ld();
+          tc::fence_before();
+          mbar_arrive(bar(B_YFREE + ((g + 1) & 1)));
+          have = q + 2 < NQ && fetch_quarter(g + 2, ya);
+          rotate_quarter(q + 1, yb);
         }
       }
       if (failed) continue;
