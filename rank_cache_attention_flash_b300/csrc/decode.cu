@@ -67,6 +67,7 @@ constexpr uint32_t OT_COL = 464;  // [16]   O^T  (lane = head dim)
 constexpr uint32_t OL_COL = 480;  // [16]   O_lr^T (lane = rank index)
 constexpr float kRescaleLog2 = 8.f;         // lazy rescale threshold (log2 units)
 constexpr long long kWaitCycles = 1ll << 31;  // ~1 s: a wait this long has failed
+constexpr long long kTestWaitCycles = 1ll << 20;  // the test-only stalled wait gives up after ~0.5 ms
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -82,6 +83,7 @@ struct DecodeParams {
   int64_t num_blocks;
   int max_blocks, max_ctx_len, n_adapters, num_queries, Hq, Hkv, g;
   int lr_groups;  // > 1: agent-specific A, adapter a's low-rank group at columns [a r, (a+1) r)
+  int test_stall;  // test only: the W issuer's first wait is on a barrier nobody arrives at
   int rpi, n_chunks, n_splits, split_blocks;
   int has_bk, has_bv;
   float scale_log2;
@@ -144,7 +146,8 @@ enum : int {
   B_PF = 12,     // [2] P^T written, O rescaled (8 token warps)
   B_PR = 14,     // [2] O^T and O_lr^T MMAs of that P buffer complete (two commits)
   B_DRAIN = 16,  // [4] per MMA warp, on abort: its MMAs have completed
-  B_COUNT = 20
+  B_TEST = 20,   // test only: a barrier nothing arrives at (a bounded wait that must run out)
+  B_COUNT = 21
 };
 
 __device__ __forceinline__ uint32_t bar_count(int i) {
@@ -178,6 +181,19 @@ __device__ __forceinline__ bool wait_ab(uint32_t bar, uint32_t parity, int32_t* 
       if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag != 0) return false;
     if (clock64() - t0 > kWaitCycles) {
+      report(st, LRKV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// A wait bounded by `limit` cycles (used by the test-only stall): gives up
+// with LRKV_ERR_TIMEOUT like wait_ab.
+__device__ __forceinline__ bool wait_limited(uint32_t bar, uint32_t parity, int32_t* st, long long limit) {
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) {
       report(st, LRKV_ERR_TIMEOUT);
       return false;
     }
@@ -525,6 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int issued = 0;
       for (int j = 0; j <= ntiles; ++j) {
+        if (p.test_stall && j == 0) {
+          // test only: a wait that runs out, then the abort path of every role
+          ok = warp_all(wait_limited(bar(B_TEST), 0, p.status, kTestWaitCycles));
+          if (!ok) break;
+        }
         if (use_w && j < ntiles) {
           ok = warp_all(wait_ab(bar(B_UF), j & 1, p.status, abort_flag));
           if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
@@ -1776,6 +1797,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   p.has_bv = a.B_V != nullptr;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.lr_groups = cfg.lr_groups;
+  p.test_stall = decode_test_stall();
   rope_freqs(cfg, &p.freqs);
 
   CUtensorMap tb, tl;

@@ -1,12 +1,14 @@
 // C-ABI host layer of liblrkv: argument validation, RoPE frequency table,
 // TMA descriptors over the paged pools, split planning and dispatch to the
 // bf16 (tensor-core) or fp32 kernels. Allocates nothing and keeps no state.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 
 #include "lrkv.h"
+#include "lrkv_testing.h"
 #include "lrkv_device.cuh"
 #include "lrkv_internal.h"
 
@@ -22,6 +24,12 @@ void rope_freqs(const lrkv_config& cfg, RopeFreqs* f) {
     f->lo[j] = static_cast<float>(th - static_cast<double>(hi));
   }
 }
+
+namespace {
+std::atomic<int> g_decode_test_stall{0};
+}  // namespace
+
+int decode_test_stall() { return g_decode_test_stall.load(std::memory_order_relaxed); }
 
 int device_sm_count() {
   int dev = 0, n = 0;
@@ -246,6 +254,10 @@ const char* lrkv_status_string(lrkv_status s) {
 }
 
 int32_t lrkv_version(void) { return 20000; }
+
+void lrkv_testing_set_decode_stall(int32_t enable) {
+  g_decode_test_stall.store(enable != 0 ? 1 : 0, std::memory_order_relaxed);
+}
 
 namespace {
 

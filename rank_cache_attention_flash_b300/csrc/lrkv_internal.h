@@ -122,6 +122,10 @@ lrkv_status launch_prefill_fp32(const lrkv_config& cfg, const PrefillArgs& a,
 
 int device_sm_count();
 
+// Test only (include/lrkv_testing.h): nonzero makes the next G-mode decode
+// launches stall one bounded wait until it runs out.
+int decode_test_stall();
+
 // Raises a kernel's dynamic shared-memory limit to `bytes` on the current
 // device. The attribute is per device, so it is set once per (kernel, device)
 // pair, under a lock (concurrent first calls from several threads are safe).

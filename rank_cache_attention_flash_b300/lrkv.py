@@ -27,7 +27,7 @@ BF16, FP32 = 0, 1
 
 EXPORTS = ("lrkv_append", "lrkv_append_rebase", "lrkv_attn_decode", "lrkv_decode_workspace_bytes", "lrkv_attn_prefill",
            "lrkv_prefill_workspace_bytes", "lrkv_status_string", "lrkv_version",
-           "lrkv_attn_decode_noalloc")
+           "lrkv_attn_decode_noalloc", "lrkv_testing_set_decode_stall")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # LRKV_NOALLOC_SCRATCH_BYTES in lrkv.h
 
 
@@ -102,6 +102,8 @@ def load() -> ctypes.CDLL:
     lib.lrkv_status_string.restype = ctypes.c_char_p
     lib.lrkv_version.argtypes = []
     lib.lrkv_version.restype = ctypes.c_int32
+    lib.lrkv_testing_set_decode_stall.argtypes = [_I32]
+    lib.lrkv_testing_set_decode_stall.restype = None
     _lib = lib
     return lib
 
@@ -138,6 +140,13 @@ def status_string(code: int) -> str:
 
 def version() -> int:
     return load().lrkv_version()
+
+
+def testing_set_decode_stall(enable: bool) -> None:
+    """Test only (include/lrkv_testing.h): while enabled, every G-mode decode
+    launch makes one bounded wait run out, reports LRKV_ERR_TIMEOUT in its
+    status word and returns through its abort path."""
+    load().lrkv_testing_set_decode_stall(1 if enable else 0)
 
 
 # ------------------------------------------------------------------ helpers

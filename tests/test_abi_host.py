@@ -1,7 +1,8 @@
 """Host-only checks of the C ABI (no GPU needed): the library loads, exports every
-entry point that include/lrkv.h declares, and rejects bad arguments before any
-launch."""
+entry point that the headers under include/ declare, and rejects bad arguments
+before any launch."""
 import ctypes
+import glob
 import os
 import re
 
@@ -10,7 +11,8 @@ import pytest
 from rank_cache_attention_flash_b300 import build as B
 from rank_cache_attention_flash_b300 import lrkv
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lrkv.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "lrkv.h")
 
 
 @pytest.fixture(scope="module")
@@ -19,21 +21,25 @@ def lib():
     return lrkv.load()
 
 
-def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(lrkv_[a-z0-9_]+)\s*\(", src)))
+def declared_functions(headers=None):
+    names = set()
+    for h in headers or sorted(glob.glob(os.path.join(INCLUDE, "*.h"))):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(lrkv_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_the_entry_points():
-    names = declared_functions()
-    for n in ("lrkv_append", "lrkv_attn_decode", "lrkv_attn_prefill", "lrkv_decode_workspace_bytes"):
+    names = declared_functions([HEADER])
+    for n in ("lrkv_append", "lrkv_append_rebase", "lrkv_attn_decode", "lrkv_attn_prefill",
+              "lrkv_decode_workspace_bytes", "lrkv_attn_decode_noalloc"):
         assert n in names
+    assert "lrkv_testing_set_decode_stall" in declared_functions([os.path.join(INCLUDE, "lrkv_testing.h")])
 
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
-        assert hasattr(lib, name), f"{name} declared in lrkv.h but not exported"
+        assert hasattr(lib, name), f"{name} declared under include/ but not exported"
     assert set(lrkv.EXPORTS) <= set(declared_functions())
 
 
