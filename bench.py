@@ -10,9 +10,9 @@ prefill workload the append of the new chunk tokens plus the causal prefill;
 for the mixed batch append + decode + prefill. With ``--config all`` (the
 default) every bf16 workload is timed in turn in one process and reported under
 ``workloads.<name>``; the line's headline fields (value, roofline, e2e,
-cpu_baseline) are those of the long paged decode (16 x 32768 tokens, rank 64),
-and ``prefill`` carries the prefill kernel's TFLOP/s against the burst and the
-sustained bf16 peak.
+cpu_baseline) are those of the shared-context decode (Llama-3.1-8B-shaped
+layer, 4 agents on one 8192-token context, rank 16), and ``prefill`` carries the
+prefill kernel's TFLOP/s against the burst and the sustained bf16 peak.
 
 Timing: L2 is flushed (a 512 MiB write) before every step, outside the timed
 events; each part of the step is captured once into a CUDA graph (the same
@@ -45,7 +45,7 @@ sys.path.insert(0, ROOT)
 DEFAULT_CONFIG = "all"
 ALL_WORKLOADS = ["shared_decode_llama8b", "prefill_chunk_llama8b", "long_decode_ministral8b",
                  "mixed_batch_qwen3_1p7b", "prelr_decode_llama8b", "rebase_prefill_llama8b"]
-HEADLINE = "long_decode_ministral8b"
+HEADLINE = "shared_decode_llama8b"
 PREFILL_HEADLINE = "prefill_chunk_llama8b"
 METRIC = "LoRA-KV attention decode tok/s & GB/s (% of HBM), prefill TFLOP/s (% peak)"
 FLUSH_BYTES = 512 << 20
@@ -97,7 +97,9 @@ def workload_model(case):
             ads = case.dec_adapter[qs[c]:qs[c + 1]].tolist()
             rows = len(ads) * (Hq // Hkv)
             distinct = len({a for a in ads if a >= 0})
-            nbytes += L * (Hkv * D * 2 + 2 * R) * es
+            # low-rank groups read: one (shared A), or each reading agent's own (agent-specific A)
+            groups = max(1, distinct) if sh.lr_groups > 1 else 1
+            nbytes += L * (Hkv * D * 2 + 2 * R * groups) * es
             nbytes += distinct * 2 * R * Hkv * D * es
             nbytes += len(ads) * Hq * D * es * 2
             flops += L * Hkv * (distinct * 2 * R * D + rows * (4 * D + 2 * R))

@@ -25,10 +25,10 @@
 // warpgroup. Y is produced in quarters of 16 RoPE pairs (B_K^T is staged
 // with its rows in that order) into two TMEM buffers, so the next quarters
 // compute while the current one is rotated.
-// Warp roles (384 threads): warp 0 streams K, V, L_V, L_K tiles with 2-D TMA
+// Warp roles (512 threads): warp 0 streams K, V, L_V, L_K tiles with 2-D TMA
 // copies into an mbarrier ring; warp 1 owns the tensor memory and issues S;
 // warps 2 and 3 issue P V and P L_V; warps 4-7 run the softmax; warps 8-11
-// rebuild K_a. Tensor-memory columns: Q [0, d/2) (packed 16-bit),
+// rebuild K_a; warp 12 issues Y (warps 13-15 only take part in the barriers). Tensor-memory columns: Q [0, d/2) (packed 16-bit),
 // S [64, 64 + BN), P [192, 192 + BN/2) (packed bf16), O [256, 256 + d),
 // O_lr [256 + d, 256 + d + r'), Y [448, 512) (two buffers of 32 columns).
 // Every wait is bounded: a wait that gives up stores LRKV_ERR_TIMEOUT, sets a
@@ -315,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  // Register split: the launch gives every thread kLaunchRegs; warpgroup 0
-  // (producer and MMA issuers) hands registers to the softmax and rebuild
-  // warpgroups (128 * kLowRegs + 256 * kHighRegs = 384 * kLaunchRegs), each
-  // warpgroup at the top of its own branch below.
+  // Register split: the launch gives every thread kLaunchRegs; warpgroups 0
+  // and 3 (producer, MMA issuers, Y issuer) hand registers to the softmax and
+  // rebuild warpgroups (256 * kLowRegs + 256 * kHighRegs = 512 * kLaunchRegs),
+  // each warpgroup at the top of its own branch below.
   auto uni = [&](bool c) { return __shfl_sync(0xffffffffu, static_cast<int>(c), 0) != 0; };
 
   if (warp < kSmWarp0) {
