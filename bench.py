@@ -44,6 +44,7 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "all"
 ALL_WORKLOADS = ["shared_decode_llama8b", "prefill_chunk_llama8b", "long_decode_ministral8b",
+                 "long_decode_codec_ministral8b",
                  "mixed_batch_qwen3_1p7b", "prelr_decode_llama8b", "rebase_prefill_llama8b"]
 HEADLINE = "shared_decode_llama8b"
 PREFILL_HEADLINE = "prefill_chunk_llama8b"
@@ -99,7 +100,10 @@ def workload_model(case):
             distinct = len({a for a in ads if a >= 0})
             # low-rank groups read: one (shared A), or each reading agent's own (agent-specific A)
             groups = max(1, distinct) if sh.lr_groups > 1 else 1
-            nbytes += L * (Hkv * D * 2 + 2 * R * groups) * es
+            # base part per token and kv head: K and V planes, or one compressed
+            # chunk row (q8_0 keys, 3-bit values: (23 d + 64) / 16 bytes)
+            base_tok = Hkv * (23 * D + 64) // 16 if sh.kv_codec else Hkv * D * 2 * es
+            nbytes += L * (base_tok + 2 * R * groups * es)
             nbytes += distinct * 2 * R * Hkv * D * es
             nbytes += len(ads) * Hq * D * es * 2
             flops += L * Hkv * (distinct * 2 * R * D + rows * (4 * D + 2 * R))
@@ -276,6 +280,7 @@ def oracle_sample(case, budget_s: float, model):
     import numpy as np
 
     import oracle
+    from oracle import polykv
     from tests.parity import _hidden, weights64
 
     sh = case.shape
@@ -290,8 +295,12 @@ def oracle_sample(case, budget_s: float, model):
             c = next(i for i in range(len(case.dec_ctx)) if qs[i] <= r < qs[i + 1])
             L_full = case.seqs[case.dec_ctx[c]].total_len
             X, X_lr = _hidden(case, case.dec_ctx[c])
-            oracle.decode(X, case.dec_q[r:r + 1].double().numpy(), case.dec_adapter[r:r + 1].numpy(),
-                          w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale, X_lr=X_lr)
+            if sh.kv_codec:
+                polykv.decode_codec(X, case.dec_q[r:r + 1].double().numpy(), case.dec_adapter[r:r + 1].numpy(),
+                                    w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+            else:
+                oracle.decode(X, case.dec_q[r:r + 1].double().numpy(), case.dec_adapter[r:r + 1].numpy(),
+                              w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale, X_lr=X_lr)
             done += 1.0
             n_full += 1
             if time.perf_counter() - t0 > budget_s:
@@ -346,6 +355,7 @@ def run_reference(args):
     import numpy as np
 
     import oracle
+    from oracle import polykv
     from tests.parity import _hidden, weights64
 
     sh = case.shape
@@ -360,8 +370,11 @@ def run_reference(args):
         ad = case.dec_adapter[0:1].numpy()
 
         def one(nt):
-            oracle.decode(X_full[:nt], q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale,
-                          X_lr=None if X_lr is None else X_lr[:nt])
+            if sh.kv_codec:
+                polykv.decode_codec(X_full[:nt], q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale)
+            else:
+                oracle.decode(X_full[:nt], q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale,
+                              X_lr=None if X_lr is None else X_lr[:nt])
     else:
         p = 0
         s = case.pre_seq[p]
@@ -415,7 +428,8 @@ def cache_bytes(case):
             L = case.seqs[s].total_len
             readers = qs[c + 1] - qs[c]
             full += readers * L * sh.n_kv_heads * sh.head_dim * 2 * es
-            lr += L * (sh.n_kv_heads * sh.head_dim * 2 + 2 * sh.rank) * es
+            base = sh.n_kv_heads * (23 * sh.head_dim + 64) // 16 if sh.kv_codec else sh.n_kv_heads * sh.head_dim * 2 * es
+            lr += L * (base + 2 * sh.lr_groups * sh.rank * es)
     return {"lrkv": lr, "per_agent_full": full, "saving": full / lr} if full else None
 
 

@@ -40,6 +40,24 @@
  *   Token at position p of a sequence whose block-table row is bt lives in
  *   block bt[p / 16], row p % 16. Each (block, plane, kv head) is one
  *   contiguous 16*d element chunk (4 KB for bf16, d = 128).
+ * - Compressed base pool (kv_codec = LRKV_CODEC_POLYKV, bf16 only). This is
+ *   the PolyKV codec (the abstract printed at the end of the PReCache page):
+ *   keys are int8 in q8_0 blocks, and values are rotated by a Walsh-Hadamard
+ *   transform and quantised to 3 bits with Lloyd-Max centroids for N(0,1).
+ *   The low-rank pool is unchanged. base_pool is bytes
+ *   [num_blocks][Hkv][23*d + 64], and each (block, kv head) chunk holds
+ *     Kq int8    [16][d]        q8_0 codes of K_base (rotated keys)
+ *     Ks fp16    [16][d/32]     q8_0 scale of each 32-dim block, max|x| / 127
+ *     Vq uint8   [16][3][d/8]   value codes as three bit planes: plane b, byte
+ *                               j/8, bit j%8 = bit b of dim j's 3-bit code
+ *     Vn fp32    [16]           ||V_base row||
+ *   A key element decodes to q * s; q = round(x / s), ties away from zero.
+ *   A value row v decodes to v^ = (H/sqrt(d)) y^, with y^_j = c[code_j] ||v|| / sqrt(d)
+ *   (H the Sylvester-Hadamard matrix, c the 8 Lloyd-Max centroids for N(0,1)
+ *   in ascending order); code_j counts the Lloyd-Max thresholds below
+ *   u_j = y_j sqrt(d) / ||v||, y = (H/sqrt(d)) v. Attention reads
+ *   K_i = K^_base + RoPE(L_K B_K,i), V_i = V^_base + L_V B_V,i (decode only;
+ *   prefill on a compressed pool returns LRKV_ERR_UNSUPPORTED).
  * - Block tables: int32 [rows][max_blocks] row-major.
  * - RoPE: rotate-half pairing (j, j + d/2), angle p * theta_j with
  *   theta_j = rope_base^(-2j/d), no frequency scaling. Queries arrive already
@@ -86,6 +104,8 @@ typedef enum {
 
 typedef enum { LRKV_BF16 = 0, LRKV_FP32 = 1 } lrkv_dtype;
 
+typedef enum { LRKV_CODEC_NONE = 0, LRKV_CODEC_POLYKV = 1 } lrkv_codec;
+
 typedef struct {
   int32_t hidden;     /* h */
   int32_t n_q_heads;  /* Hq */
@@ -97,7 +117,15 @@ typedef struct {
   int32_t dtype;      /* lrkv_dtype of every tensor argument */
   int32_t lr_groups;  /* G >= 1 low-rank groups: 1 = one A shared by every agent;
                          G > 1 = agent a has its own A_K,a, A_V,a and reads group a */
+  int32_t kv_codec;   /* lrkv_codec of the base pool: NONE (bf16/fp32 planes) or POLYKV */
 } lrkv_config;
+
+/*
+ * lrkv_base_pool_block_bytes -- bytes of one block of base_pool for cfg (all
+ * kv heads): 2*Hkv*16*d*elem for LRKV_CODEC_NONE, Hkv*(23*d + 64) for
+ * LRKV_CODEC_POLYKV; 0 for an invalid configuration. Host only.
+ */
+size_t lrkv_base_pool_block_bytes(const lrkv_config* cfg);
 
 /*
  * lrkv_append -- write the cache entries of T new tokens.

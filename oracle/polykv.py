@@ -135,20 +135,32 @@ def tq3_encode(v):
     return codes, n32
 
 
-def tq3_decode(codes, norms) -> np.ndarray:
+def tq3_decode(codes, norms, operand: bool = False) -> np.ndarray:
+    """operand=True: the rotated values are rounded to bf16 before rotating back
+    (the bf16-cache reading below)."""
     c, _ = centroids_thresholds()
     codes = np.asarray(codes)
     d = codes.shape[-1]
     yhat = c[codes.astype(np.int64)] * (np.asarray(norms, dtype=np.float32).astype(np.float64) / np.sqrt(d))[..., None]
+    if operand:
+        yhat = O.round_bf16(yhat)
     return rotate(yhat)
 
 
-def base_roundtrip(kb, vb):
+def base_roundtrip(kb, vb, operand: bool = False):
     """The base part as the compressed pool returns it: K_base through q8_0,
-    V_base through the rotated 3-bit code."""
+    V_base through the rotated 3-bit code.
+
+    operand=True is the bf16-cache reading of the oracle (the components a
+    kernel holds in 16 bits are rounded as it holds them): for the compressed
+    pool those are the expanded keys q * s in fp16 and the expanded rotated
+    values c[code] ||v|| / sqrt(d) in bf16, before the rotation back."""
     kq, ks = q8_0_encode(kb)
     vq, vn = tq3_encode(vb)
-    return q8_0_decode(kq, ks), tq3_decode(vq, vn)
+    k = q8_0_decode(kq, ks)
+    if operand:
+        k = k.astype(np.float16).astype(np.float64)
+    return k, tq3_decode(vq, vn, operand)
 
 
 # ---------------------------------------------------------------------------
@@ -159,9 +171,10 @@ def agent_kv_codec(X, positions, W_K, W_V, A_K, A_V, B_K_i, B_V_i, n_kv_heads: i
     """One agent's keys and values read from a compressed base pool:
         K_i = dec(enc(K_base)) + RoPE(L_K B_K,i),   V_i = dec(enc(V_base)) + L_V B_V,i,
     K_base = RoPE(X W_K), V_base = X W_V, L_K = X A_K, L_V = X A_V (exact).
-    lr_dtype="bf16": L_K, L_V rounded to bf16, as the low-rank pool stores them."""
+    lr_dtype="bf16": L_K, L_V rounded to bf16, as the low-rank pool stores them,
+    and the expanded base operands rounded as a kernel holds them (base_roundtrip)."""
     kb, vb, lk, lv = O.base_and_lowrank(X, positions, W_K, W_V, A_K, A_V, n_kv_heads, head_dim, base)
-    k, v = base_roundtrip(kb, vb)
+    k, v = base_roundtrip(kb, vb, operand=lr_dtype == "bf16")
     if lr_dtype == "bf16":
         lk, lv = O.round_bf16(lk), O.round_bf16(lv)
     T = k.shape[0]

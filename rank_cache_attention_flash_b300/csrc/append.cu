@@ -64,8 +64,60 @@ struct AppendParams {
   int kvc2;          // base columns: 2 * Hkv * D
   int lrw;           // low-rank row width: G * R (plane 0 = L_K, plane 1 = L_V)
   int n_base_tiles;  // base column tiles in the grid (0 when the base part is not written)
+  int codec;         // 1: the base pool is compressed (q8_0 keys, rotated 3-bit values)
+  float vthr[7];     // value-code thresholds (Lloyd-Max for N(0,1)), ascending
   RopeFreqs freqs;
 };
+
+// ------------------------------------------------------ compressed base pool
+// One (block, kv head) chunk: Kq int8 [16][d] | Ks fp16 [16][d/32] |
+// Vq u8 [16][3][d/8] | Vn fp32 [16] (PolyKV codec: the abstract printed at
+// the end of the PReCache page).
+
+// q8_0 of 32 values: scale s = max|x| / 127 (stored fp16), codes
+// round(x / s) with ties away from zero; 32 bytes of codes.
+__device__ __forceinline__ void q8_0_store(const float* x, int8_t* codes, __half* scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  const float s = amax / 127.0f;
+  const float inv = s > 0.f ? 1.0f / s : 0.f;
+  uint32_t w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float q = fminf(fmaxf(roundf(x[4 * k + e] * inv), -127.f), 127.f);
+      v |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xffu) << (8 * e);
+    }
+    w[k] = v;
+  }
+  *reinterpret_cast<uint4*>(codes) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(codes + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+  *scale = __float2half_rn(s);
+}
+
+// In-register Walsh-Hadamard transform of 32 values (Sylvester order, unnormalised).
+__device__ __forceinline__ void fwht32(float* z) {
+#pragma unroll
+  for (int len = 1; len < 32; len <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((i & len) == 0) {
+        const float a = z[i], b = z[i + len];
+        z[i] = a + b;
+        z[i + len] = a - b;
+      }
+}
+
+// 3-bit code of u: the number of (ascending) thresholds below u, in three compares.
+__device__ __forceinline__ uint32_t code3(float u, const float* t) {
+  const bool b2 = t[3] < u;
+  const bool b1 = (b2 ? t[5] : t[1]) < u;
+  const float tl = b2 ? (b1 ? t[6] : t[4]) : (b1 ? t[2] : t[0]);
+  return (b2 ? 4u : 0u) + (b1 ? 2u : 0u) + (tl < u ? 1u : 0u);
+}
 
 // Waits for an mbarrier phase; gives up (LRKV_ERR_TIMEOUT, false) after
 // kWaitCycles, or early once another role has raised the abort flag.
@@ -212,6 +264,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after();
       const int half = p.D / 2;
       const int kvc = p.kvc2 / 2;
+      if (p.codec && !lr_tile) {
+        // compressed base pool: one kv head's K or V columns per pass
+        const int D = p.D, nb = p.D / 32;
+        for (int c = c_beg; c < c_end; c += D) {
+          const int n = n0 + c;
+          const bool is_k = n < kvc;
+          const int head = (is_k ? n : n - kvc) / D;
+          uint8_t* chunk = blk >= 0 ? reinterpret_cast<uint8_t*>(p.base_pool) +
+                                          (static_cast<int64_t>(blk) * p.Hkv + head) * (23 * D + 64)
+                                    : nullptr;
+          if (is_k) {
+            // RoPE of the pairs (j, j + d/2), then q8_0 of each 32-dim block
+            for (int j0 = 0; j0 < half; j0 += 32) {
+              uint32_t lo[32], hi[32];
+              tc::ld_x32(tl + c + j0, lo);
+              tc::ld_x32(tl + c + j0 + half, hi);
+              tc::wait_ld();
+              float rl[32], rh[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float2 cs = rope_cos_sin_fast(pos, p.freqs.hi[j0 + e], p.freqs.lo[j0 + e]);
+                const float a = __uint_as_float(lo[e]), b = __uint_as_float(hi[e]);
+                rl[e] = fmaf(a, cs.x, -(b * cs.y));
+                rh[e] = fmaf(b, cs.x, a * cs.y);
+              }
+              if (chunk != nullptr) {
+                int8_t* kq = reinterpret_cast<int8_t*>(chunk) + slot_row * D;
+                __half* ks = reinterpret_cast<__half*>(chunk + 16 * D) + slot_row * nb;
+                q8_0_store(rl, kq + j0, ks + j0 / 32);
+                q8_0_store(rh, kq + j0 + half, ks + (j0 + half) / 32);
+              }
+            }
+          } else {
+            // ||v||, then (H v)_j / ||v|| per 32-wide group: H_d = H_{d/32} (x) H_32
+            // (Sylvester), so group g is FWHT32 of sum_k (-1)^popc(g & k) v[32k ..]
+            float ss = 0.f;
+            for (int k = 0; k < nb; ++k) {
+              uint32_t x[32];
+              tc::ld_x32(tl + c + 32 * k, x);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ss = fmaf(__uint_as_float(x[e]), __uint_as_float(x[e]), ss);
+            }
+            const float nrm = sqrtf(ss);
+            const float inv = nrm > 0.f ? 1.0f / nrm : 0.f;
+            uint32_t plane[3][4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              plane[0][g] = plane[1][g] = plane[2][g] = 0u;
+              if (g < nb) {
+                float z[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) z[e] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  if (k < nb) {
+                    uint32_t x[32];
+                    tc::ld_x32(tl + c + 32 * k, x);
+                    tc::wait_ld();
+                    const bool neg = (__popc(g & k) & 1) != 0;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) z[e] += neg ? -__uint_as_float(x[e]) : __uint_as_float(x[e]);
+                  }
+                }
+                fwht32(z);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  const uint32_t q = code3(z[e] * inv, p.vthr);
+                  plane[0][g] |= (q & 1u) << e;
+                  plane[1][g] |= ((q >> 1) & 1u) << e;
+                  plane[2][g] |= (q >> 2) << e;
+                }
+              }
+            }
+            if (chunk != nullptr) {
+              uint32_t* vq = reinterpret_cast<uint32_t*>(chunk + 17 * D + slot_row * (3 * D / 8));
+#pragma unroll
+              for (int b = 0; b < 3; ++b)
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                  if (g < nb) vq[b * nb + g] = plane[b][g];
+              reinterpret_cast<float*>(chunk + 23 * D)[slot_row] = nrm;
+            }
+          }
+        }
+      } else
       for (int c = c_beg; c < c_end; c += 16) {
         const int n = n0 + c;  // global output column of this 16-column group
         if (lr_tile) {
@@ -308,6 +446,8 @@ lrkv_status launch_append_bf16(const lrkv_config& cfg, const void* X_base, const
   p.kvc2 = 2 * cfg.n_kv_heads * cfg.head_dim;
   p.lrw = lr_width(cfg);
   p.n_base_tiles = X_base != nullptr ? (p.kvc2 + AN - 1) / AN : 0;
+  p.codec = cfg.kv_codec == LRKV_CODEC_POLYKV ? 1 : 0;
+  for (int k = 0; k < 7; ++k) p.vthr[k] = polykv_codec().threshold[k];
   const int n_lr_tiles = X_lr != nullptr ? (2 * p.lrw + AN - 1) / AN : 0;
   rope_freqs(cfg, &p.freqs);
   const int64_t N = p.kvc2 + 2 * p.lrw;

@@ -84,6 +84,9 @@ struct DecodeParams {
   int max_blocks, max_ctx_len, n_adapters, num_queries, Hq, Hkv, g;
   int lr_groups;  // > 1: agent-specific A, adapter a's low-rank group at columns [a r, (a+1) r)
   int test_stall;  // test only: the W issuer's first wait is on a barrier nobody arrives at
+  int codec;       // compressed base pool (rebuild-mode kernel only): chunks of codec_chunk_bytes(D)
+  const uint8_t* cbase;  // the compressed base pool
+  float vcent[8];  // value-code centroids (Lloyd-Max for N(0,1)), ascending
   int rpi, n_chunks, n_splits, split_blocks;
   int has_bk, has_bv;
   float scale_log2;
@@ -952,6 +955,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // own online softmax, and stores its own split partial (the combine merges
 // 2 x n_splits partials per query head). While one warpgroup waits on a tensor
 // or memory operation of its tile, the other works on the next tile.
+// sqrt(d) of the value rotation's scale, d = 64 or 128
+template <int D>
+constexpr float kSqrtD = D == 128 ? 11.313708498984760f : 8.0f;
+
+// Bits 0-3 of x moved to bits 0, 8, 16, 24 (x < 16).
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
 namespace rb {
 constexpr int kRows = 4;          // query rows per item (one query)
 constexpr uint32_t RY_COL = 0;     // [2][d]  Y of the pipeline's tile, fp32
@@ -971,12 +981,14 @@ enum : int {
   PF = 18,     // [2] P^T written, O rescaled (4 warps)
   PR = 20,     // [2] O^T and O_lr^T MMAs of that pipeline's tile complete (two commits)
   DRAIN = 22,  // [4] per MMA warp, on abort
-  COUNT = 26
+  VX = 26,     // [2] compressed pool: V^ of that pipeline's tile expanded (4 warps)
+  COUNT = 28
 };
 
 __device__ __forceinline__ uint32_t rb_bar_count(int i) {
   if (i >= EMPTY && i < EMPTY + 4) return 6;
-  if ((i >= YR && i < YR + 2) || (i >= KA && i < KA + 2) || (i >= SR && i < SR + 2) || (i >= PF && i < PF + 2))
+  if ((i >= YR && i < YR + 2) || (i >= KA && i < KA + 2) || (i >= SR && i < SR + 2) || (i >= PF && i < PF + 2) ||
+      (i >= VX && i < VX + 2))
     return 4;
   if (i >= PR && i < PR + 2) return 2;
   return 1;
@@ -1008,7 +1020,10 @@ struct Layout {
   static constexpr int off_btab = off_p + 2 * PB;
   static constexpr int off_misc = off_btab + BTAB;
   static constexpr int off_bar = off_misc + MISC;
-  static constexpr int used = off_bar + 512;
+  // the V^T operand of the last slot spans 128 head dims: at d = 64 the rows
+  // past d (whose products are never read) may reach beyond the layout
+  static constexpr int VSPAN = (NS - 1) * STAGE + LR_TILE + 2 * ATOM;
+  static constexpr int used = off_bar + 512 > VSPAN ? off_bar + 512 : VSPAN;
   static constexpr int total = used + 1024;
   static_assert(NS >= 3, "the ring needs three slots");
   static_assert(total <= kSmemLimit, "decode tile does not fit in shared memory");
@@ -1019,7 +1034,7 @@ struct Layout {
 };
 }  // namespace rb
 
-template <int D, int R>
+template <int D, int R, bool CODEC>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_rb_kernel(const __grid_constant__ DecodeParams p,
                      const __grid_constant__ CUtensorMap tm_base,
@@ -1093,6 +1108,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the item's one adapter (a bad id scores as base only; the combine reports it)
   const int item_ad = __ldg(p.adapter_ids + qs + row0 / p.g);
   const bool rebuild = p.has_bk && item_ad >= 0 && item_ad < p.n_adapters;
+  // compressed base pool: K tiles arrive as q8_0 codes and are expanded to
+  // fp16 on chip (then scored in fp16 like a rebuilt K_a); V tiles arrive as
+  // rotated 3-bit codes and are expanded to bf16 before the P V product
+  constexpr bool codec = CODEC;  // a separate instantiation: the plain path carries none of it
+  const bool kconv = rebuild || codec;
   const int nblk = (len + kBlock - 1) / kBlock;
   const int kend = min(kbeg + p.split_blocks, nblk);
   const int ntiles = kend > kbeg ? (kend - kbeg + kTileBlocks - 1) / kTileBlocks : 0;
@@ -1129,7 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dvr[q4][2 * i + 1] = __float_as_uint(cs.y);
       }
   }
-  // warps 1-3: Q rows of the item (fp16 when scored against fp16 K_a)
+  // warps 1-3: Q rows of the item (fp16 when scored against fp16 K_a or K^)
   constexpr int QCH = kMaxRows * (D / 8);
   constexpr int QIT = (QCH + 95) / 96;
   uint4 qv[QIT];
@@ -1156,7 +1176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tc::alloc(smem_u32(tmem_slot), kTmemCols);
   if (tid == 0) {
-    prefetch_tmap(&tm_base);
+    if (!codec) prefetch_tmap(&tm_base);
     prefetch_tmap(&tm_lr);
   }
   tc::fence_before();
@@ -1166,8 +1186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ============================================================ producer
-    const uint32_t bytes_k = L::KATOMS * 2048 + (rebuild ? 16 * LSPAN : 0);
-    const uint32_t bytes_v = L::KATOMS * 2048 + (p.has_bv ? 16 * LSPAN : 0);
+    // per block: K_base (or its codes Kq | Ks) and L_K; V_base (or Vq | Vn) and L_V
+    const uint32_t kbase_bytes = codec ? codec_k_bytes(D) : L::KATOMS * 2048;
+    const uint32_t vbase_bytes = codec ? codec_v_bytes(D) : L::KATOMS * 2048;
+    const uint32_t bytes_k = kbase_bytes + (rebuild ? 16 * LSPAN : 0);
+    const uint32_t bytes_v = vbase_bytes + (p.has_bv ? 16 * LSPAN : 0);
     auto tile_ids = [&](int j) -> int {
       const int kb = kbeg + j * kTileBlocks + lane;
       return (lane < kTileBlocks && kb < kend) ? __ldg(btrow + kb) : INT_MIN;
@@ -1195,10 +1218,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (valid) {
-        const int y = ((id * 2 + kind) * p.Hkv + head) * kBlock;
+        if (codec) {
+          // the block's codes, staged at the front of the tile's K or V area
+          const uint8_t* chunk = p.cbase + (static_cast<int64_t>(id) * p.Hkv + head) * codec_chunk_bytes(D);
+          bulk_load(dst + L::LR_TILE + lane * (kind == 0 ? kbase_bytes : vbase_bytes),
+                    chunk + (kind == 0 ? 0 : codec_k_bytes(D)), kind == 0 ? kbase_bytes : vbase_bytes, fb);
+        } else {
+          const int y = ((id * 2 + kind) * p.Hkv + head) * kBlock;
 #pragma unroll
-        for (int a = 0; a < L::KATOMS; ++a)
-          tma_load_2d(dst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, y, fb);
+          for (int a = 0; a < L::KATOMS; ++a)
+            tma_load_2d(dst + L::LR_TILE + a * L::ATOM + lane * 2048, &tm_base, 64 * a, y, fb);
+        }
         if (kind == 0 ? rebuild : p.has_bv)
           tma_load_2d(dst + lane * 16 * LSPAN, &tm_lr, lr_x, (id * 2 + kind) * kBlock, fb);
       }
@@ -1236,7 +1266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = pt + 96 * u;
         const int r = i / (D / 8), c = i % (D / 8);
         uint4 v = qv[u];
-        if (rebuild) {
+        if (kconv) {
           v.x = bf16x2_to_f16x2(v.x);
           v.y = bf16x2_to_f16x2(v.y);
           v.z = bf16x2_to_f16x2(v.z);
@@ -1327,7 +1357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 2) {
       // ======================================================== S issuer
-      const uint32_t ids = tc::idesc_f16(128, kMaxRows, !rebuild, false, false);
+      const uint32_t ids = tc::idesc_f16(128, kMaxRows, !kconv, false, false);
       const uint64_t qdesc = tc::sdesc(sbase + L::off_q, 16, 1024, 2);
       bool ok = true;
       int issued = 0;
@@ -1368,6 +1398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = j & 1, i = j >> 1, vi = vidx(j, ntiles), v = vi % NS;
         ok = warp_all(wait_ab(bar(FULL + v), (vi / NS) & 1, p.status, abort_flag));
         if (ok) ok = warp_all(wait_ab(bar(PF + b), i & 1, p.status, abort_flag));
+        if (ok && codec) ok = warp_all(wait_ab(bar(VX + b), i & 1, p.status, abort_flag));
         if (!ok) break;
         tc::fence_after();
         if (tc::elect_one()) {
@@ -1412,18 +1443,124 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float th_hi = tt < HALF ? p.freqs.hi[tt] : 0.f, th_lo = tt < HALF ? p.freqs.lo[tt] : 0.f;
       bool failed = false;
+      // Compressed pool: V^ of this pipeline's previous tile, in the rotated
+      // domain, c[code_j] ||v|| / sqrt(d), bf16, expanded over the staged codes
+      // once this pipeline reaches its next tile (the codes landed long ago):
+      // every thread first takes its row's codes, then all write. Rows outside
+      // the context, the split or a loaded block get 0. The combine rotates the
+      // merged sum back.
+      int prev_v = 0;
+      uint32_t prev_vpar = 0;
+      bool prev_tok = false, pending_v = false;
+      auto expand_v = [&](int vs_slot, uint32_t vpar, bool ok_tok) {
+        if (!failed) failed = !wait_ab(bar(FULL + vs_slot), vpar, p.status, abort_flag);
+        uint8_t* vst = smem + L::off_ring + vs_slot * L::STAGE;
+        uint8_t* vt = vst + L::LR_TILE;
+        const uint8_t* vrow = vt + (tt >> 4) * codec_v_bytes(D);
+        // each bit plane of the row in one load (rows 3 d / 8 bytes apart: no bank conflicts)
+        uint32_t pw[3][D / 32];
+#pragma unroll
+        for (int b = 0; b < 3; ++b) {
+          const uint8_t* pp = vrow + (tt & 15) * (3 * D / 8) + b * (D / 8);
+          if constexpr (D == 128) {
+            const uint4 x = *reinterpret_cast<const uint4*>(pp);
+            pw[b][0] = x.x;
+            pw[b][1] = x.y;
+            pw[b][2] = x.z;
+            pw[b][3] = x.w;
+          } else {
+            const uint2 x = *reinterpret_cast<const uint2*>(pp);
+            pw[b][0] = x.x;
+            pw[b][1] = x.y;
+          }
+        }
+        const float nv = *reinterpret_cast<const float*>(vrow + 6 * D + 4 * (tt & 15));
+        named_bar_sync(bar_g, 128);
+        const float vs = ok_tok ? nv * (1.0f / kSqrtD<D>) : 0.f;
+        // the 8 scaled centroids as bf16: codes 0-3 in {t1:t0}, 4-7 in {t3:t2}
+        const uint32_t t0 = pack_bf16(p.vcent[0] * vs, p.vcent[1] * vs), t1 = pack_bf16(p.vcent[2] * vs, p.vcent[3] * vs);
+        const uint32_t t2 = pack_bf16(p.vcent[4] * vs, p.vcent[5] * vs), t3 = pack_bf16(p.vcent[6] * vs, p.vcent[7] * vs);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {  // dims 8c .. 8c + 7
+          uint32_t o[4];
+#pragma unroll
+          for (int h4 = 0; h4 < 2; ++h4) {  // 4 dims: their code bits spread to one byte each
+            const int j = 8 * c + 4 * h4, g = j >> 5, sh = j & 31;
+            const uint32_t lo2 = spread4((pw[0][g] >> sh) & 15u) | (spread4((pw[1][g] >> sh) & 15u) << 1);
+            const uint32_t hi8 = spread4((pw[2][g] >> sh) & 15u) * 0xffu;  // 0xff where code >= 4
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {  // a pair of dims: byte selectors 2l, 2l + 1 per element
+              const uint32_t sel = 0x1010u + 0x22u * ((lo2 >> (16 * e)) & 0xffffu);
+              const uint32_t m = __byte_perm(hi8, 0u, e ? 0x3322u : 0x1100u);
+              o[2 * h4 + e] = (__byte_perm(t0, t1, sel) & ~m) | (__byte_perm(t2, t3, sel) & m);
+            }
+          }
+          *reinterpret_cast<uint4*>(vt + ((8 * c) >> 6) * L::ATOM + swz<128>(tt, ((8 * c) & 63) * 2)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // V^ -> P V operand
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(VX + pb));
+          mbar_arrive(bar(EMPTY + vs_slot));
+        }
+        pending_v = false;
+      };
       int i = 0;
       for (int j = pb; j < ntiles; j += 2, ++i) {
         const int ki = kidx(j, ntiles), vi = vidx(j, ntiles);
         const int s = ki % NS, v = vi % NS;
         const uint32_t ph = i & 1;
         const int t0 = (kbeg + j * kTileBlocks) * kBlock;
+        if (pending_v) expand_v(prev_v, prev_vpar, prev_tok);
         // ---- K_a = K_base + RoPE(Y) for this lane's token, every pair, fp16 in place
-        if (rebuild) {
-          if (!failed) failed = !wait_ab(bar(YF + pb), ph, p.status, abort_flag);
+        if (kconv) {
+          if (!failed && rebuild) failed = !wait_ab(bar(YF + pb), ph, p.status, abort_flag);
           if (!failed) failed = !wait_ab(bar(FULL + s), (ki / NS) & 1, p.status, abort_flag);
           tc::fence_after();
           uint8_t* kt = smem + L::off_ring + s * L::STAGE + L::LR_TILE;
+          if (codec) {
+            // K^ = q s (q8_0), fp16, over the staged codes. Each quarter-warp
+            // takes one row's D code bytes as 16-byte pieces (contiguous: no
+            // bank conflicts), warp w the rows 32 (w % 4) ..; all the pipeline's
+            // codes are read before any expanded row is written over them.
+            constexpr int PR = D / 16;             // 16-byte pieces per row
+            constexpr int RPI = 32 / PR;           // rows per warp pass
+            constexpr int NP = 32 / RPI;           // passes over the warp's 32 rows
+            const int pc = lane % PR;              // this thread's piece: dims 16 pc ..
+            uint4 kc[NP];
+            float ksc[NP];
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+              const int row = 32 * (warp & 3) + RPI * i + lane / PR;
+              const uint8_t* kb = kt + (row >> 4) * codec_k_bytes(D);
+              kc[i] = *reinterpret_cast<const uint4*>(kb + (row & 15) * D + 16 * pc);
+              ksc[i] = __half2float(reinterpret_cast<const __half*>(kb + 16 * D)[(row & 15) * (D / 32) + pc / 2]);
+            }
+            named_bar_sync(bar_g, 128);
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+              const int row = 32 * (warp & 3) + RPI * i + lane / PR;
+              const uint32_t w[4] = {kc[i].x, kc[i].y, kc[i].z, kc[i].w};
+              uint32_t o[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const uint32_t x = w[e >> 1] >> (16 * (e & 1));
+                o[e] = pack_f16(static_cast<float>(static_cast<int8_t>(x & 0xffu)) * ksc[i],
+                                static_cast<float>(static_cast<int8_t>((x >> 8) & 0xffu)) * ksc[i]);
+              }
+              // the pieces of atom 1 store their halves in the other order, so
+              // that the 8 stores of one row's quarter-warp hit 8 bank groups
+#pragma unroll
+              for (int hp = 0; hp < 2; ++hp) {
+                const int hf = hp ^ ((pc >> 2) & 1);
+                const int dim = 16 * pc + 8 * hf;
+                *reinterpret_cast<uint4*>(kt + (dim >> 6) * L::ATOM + swz<128>(row, (dim & 63) * 2)) =
+                    hf ? make_uint4(o[4], o[5], o[6], o[7]) : make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            }
+          }
+          if (rebuild) {
           const uint32_t ycol = RY_COL + pb * D;
           const float2* bt = btp + (i & 1) * HALF;
 #pragma unroll 1
@@ -1453,8 +1590,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float cd = __uint_as_float(dv[2 * k]), sd = __uint_as_float(dv[2 * k + 1]);
                   const float c = fmaf(b2.x, cd, -(b2.y * sd)), sn = fmaf(b2.y, cd, b2.x * sd);
                   const float yl = __uint_as_float(ylo[k]), yh = __uint_as_float(yhi[k]);
-                  const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
-                  const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
+                  // K_base as loaded (bf16), or K^ expanded above (fp16)
+                  const float bl = codec ? (e ? f16_hi(kl[w]) : f16_lo(kl[w])) : (e ? bf16_hi(kl[w]) : bf16_lo(kl[w]));
+                  const float bh = codec ? (e ? f16_hi(kh[w]) : f16_lo(kh[w])) : (e ? bf16_hi(kh[w]) : bf16_lo(kh[w]));
                   rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
                   rh[e] = fmaf(yh, c, fmaf(yl, sn, bh));
                 }
@@ -1468,7 +1606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(YR + pb));
-          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // K_a -> S operand
+          }
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // K_a or K^ -> S operand
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(KA + pb));
@@ -1563,14 +1702,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < kRows; ++r)
             *reinterpret_cast<__nv_bfloat16*>(pbuf + r * 128 + ((ch ^ (r & 7)) << 4)) = __float2bfloat16_rn(sc[r]);
         }
-        // V and L_V rows of tokens outside the context, the split or a loaded
-        // block hold stale memory: zero them so that P = 0 cannot meet a NaN
         if (vmask != (1 << kTileBlocks) - 1 || t0 + kBT > len) {
+          // V and L_V rows of tokens outside the context, the split or a loaded
+          // block hold stale memory: zero them so that P = 0 cannot meet a NaN
+          // (a compressed V tile still holds every row's codes: its expansion
+          // zeroes those rows instead)
           if (!failed) failed = !wait_ab(bar(FULL + v), (vi / NS) & 1, p.status, abort_flag);
           if (!tok_ok) {
             uint8_t* vst = smem + L::off_ring + v * L::STAGE;
 #pragma unroll
-            for (int a = 0; a < L::KATOMS; ++a)
+            for (int a = 0; a < (codec ? 0 : L::KATOMS); ++a)
 #pragma unroll
               for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<uint4*>(vst + L::LR_TILE + a * L::ATOM + tt * 128 + 16 * c) =
@@ -1585,9 +1726,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(bar(PF + pb));
-          mbar_arrive(bar(EMPTY + v));
+          if (!codec) mbar_arrive(bar(EMPTY + v));
         }
+        prev_v = v;
+        prev_vpar = (vi / NS) & 1;
+        prev_tok = tok_ok;
+        pending_v = codec;
       }
+      if (pending_v) expand_v(prev_v, prev_vpar, prev_tok);
 
       // ---- this pipeline's split partial: m, l, O, O_lr of every row
       bool aborted = named_bar_or(bar_g, 128, failed);
@@ -1654,6 +1800,7 @@ struct CombineParams {
   int32_t* status;
   int num_queries, num_ctx, Hq, Hkv, g, n_splits, n_adapters, has_bv;
   int covered_rows;  // rows per context the decode grid covers (n_chunks * rows per item)
+  int codec;         // the base part was accumulated over rotated values: rotate the merged sum back
 };
 
 constexpr int kCombineBatch = 32;  // splits requested per round
@@ -1672,6 +1819,7 @@ __global__ void __launch_bounds__(CombineShape<D, R>::NT) combine_kernel(const _
   __shared__ float w_s[256];  // the plan keeps n_splits <= 256
   __shared__ float red[NW];
   __shared__ float olr[R];
+  __shared__ float orot[D];  // compressed pool: the merged base part before the rotation back
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t pair = blockIdx.x;
   const int n = static_cast<int>(pair / p.Hq), m = static_cast<int>(pair % p.Hq);
@@ -1753,8 +1901,17 @@ __global__ void __launch_bounds__(CombineShape<D, R>::NT) combine_kernel(const _
         if (s0 + s < S) v = fmaf(w_s[s0 + s], pv[s], v);
     }
     if (tid >= D) olr[tid - D] = use_lr ? v : 0.f;
+    if (p.codec && tid < D) orot[tid] = v;
   }
   __syncthreads();
+  if (p.codec && tid < D) {
+    // O_base = (H / sqrt(d)) O_rot, H the Sylvester-Hadamard matrix: entry
+    // (tid, i) is (-1)^popcount(tid & i)
+    float acc = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) acc += (__popc(tid & i) & 1) ? -orot[i] : orot[i];
+    v = acc * (1.0f / kSqrtD<D>);
+  }
   if (tid < D) {
     if (use_lr) {
 #pragma unroll
@@ -1798,17 +1955,18 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.lr_groups = cfg.lr_groups;
   p.test_stall = decode_test_stall();
+  p.codec = cfg.kv_codec == LRKV_CODEC_POLYKV ? 1 : 0;
+  p.cbase = static_cast<const uint8_t*>(a.base_pool);
+  for (int k = 0; k < 8; ++k) p.vcent[k] = polykv_codec().centroid[k];
   rope_freqs(cfg, &p.freqs);
 
-  CUtensorMap tb, tl;
-  if (!make_pool_maps(cfg, a.base_pool, nullptr, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
+  CUtensorMap tb{}, tl;
+  // a compressed base pool is read with plain bulk copies (no tensor map)
+  if (!p.codec && !make_pool_maps(cfg, a.base_pool, nullptr, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
   if (!make_lr_map(cfg, a.lr_pool, a.num_blocks, L::RP, &tl)) return LRKV_ERR_CUDA;
 
   if (plan.n_items > 0) {
-    auto kern = decode_kernel<D, R>;
-    if constexpr (R == 64) {
-      if (plan.rebuild) kern = decode_rb_kernel<D, R>;
-    }
+    auto kern = !plan.rebuild ? decode_kernel<D, R> : p.codec ? decode_rb_kernel<D, R, true> : decode_rb_kernel<D, R, false>;
     if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), plan.smem_bytes)) return LRKV_ERR_CUDA;
     kern<<<static_cast<unsigned>(plan.n_items), kThreads, plan.smem_bytes, stream>>>(p, tb, tl);
     if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
@@ -1830,6 +1988,7 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   c.n_splits = plan.n_splits * (plan.rebuild ? 2 : 1);  // rebuild mode: one partial per pipeline
   c.n_adapters = a.n_adapters;
   c.has_bv = a.B_V != nullptr;
+  c.codec = p.codec;
   const int64_t pairs = static_cast<int64_t>(a.num_queries) * cfg.n_q_heads;
   if (pairs > 0) {
     // A plain stream-ordered launch: on this part, waiting resident on the
@@ -1852,6 +2011,15 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
   // item's rows belong to one query -- a multiple of 4 query heads per kv head,
   // or one query per context.
   P.rebuild = (R == 64 && (P.g % 4 == 0 || max_q_per_ctx == 1)) ? 1 : 0;
+  // A compressed base pool is read by the rebuild-mode kernel only (it expands
+  // the codes where it rebuilds K_a), at every rank; its items hold rows of one
+  // query: up to 4 of them, a divisor of g unless each context has one query.
+  int rb_rows = 4;
+  if (cfg.kv_codec == LRKV_CODEC_POLYKV) {
+    P.rebuild = 1;
+    if (max_q_per_ctx > 1)
+      while (P.g % rb_rows != 0) --rb_rows;
+  }
   int rpi = 0, total = 0;
 #define LRKV_L(d, r) \
   if (D == d && R == r) { rpi = DL<d, r>::RPI; total = DL<d, r>::total; }
@@ -1865,7 +2033,14 @@ bool plan_decode_bf16(const lrkv_config& cfg, int num_queries, int num_ctx, int 
     if (P.g <= rpi) rpi = P.g;
     else if (P.g % rpi != 0) return false;
   }
-  if (P.rebuild) total = D == 128 ? rb::Layout<128, 64>::total : rb::Layout<64, 64>::total;
+  if (P.rebuild) {
+    rpi = rb_rows;
+#define LRKV_RB(d, r) \
+  if (D == d && R == r) total = rb::Layout<d, r>::total;
+    LRKV_RB(128, 8) LRKV_RB(128, 16) LRKV_RB(128, 32) LRKV_RB(128, 64)
+    LRKV_RB(64, 8) LRKV_RB(64, 16) LRKV_RB(64, 32) LRKV_RB(64, 64)
+#undef LRKV_RB
+  }
   P.rows_per_item = rpi;
   P.smem_bytes = std::max(total, kMinSmem);
   P.n_chunks = std::max(1, (max_q_per_ctx * P.g + rpi - 1) / rpi);

@@ -100,6 +100,8 @@ lrkv_status check_config(const lrkv_config* cfg) {
   if (cfg->hidden % 64 != 0) return LRKV_ERR_UNSUPPORTED;
   if (cfg->lr_groups < 1) return LRKV_ERR_INVALID_ARG;
   if (cfg->lr_groups > 64) return LRKV_ERR_UNSUPPORTED;
+  if (cfg->kv_codec != LRKV_CODEC_NONE && cfg->kv_codec != LRKV_CODEC_POLYKV) return LRKV_ERR_INVALID_ARG;
+  if (cfg->kv_codec == LRKV_CODEC_POLYKV && cfg->dtype != LRKV_BF16) return LRKV_ERR_UNSUPPORTED;
   return LRKV_OK;
 }
 
@@ -118,6 +120,39 @@ lrkv_status check_pool(const lrkv_config& cfg, const void* base_pool, const void
 }
 
 }  // namespace
+
+// The 8-level Lloyd-Max quantiser for N(0, 1): Lloyd's iteration (thresholds
+// at the midpoints of neighbouring centroids, centroids at the conditional
+// means of their cells) in double precision, made exactly symmetric, rounded
+// to float once. Computed on first use.
+Codec make_polykv_codec() {
+  constexpr int kL = 8;
+  const double kInvSqrt2Pi = 0.39894228040143267794;
+  auto pdf = [&](double x) { return std::isinf(x) ? 0.0 : kInvSqrt2Pi * std::exp(-0.5 * x * x); };
+  auto upper = [](double x) { return 0.5 * std::erfc(x / std::sqrt(2.0)); };  // P(X > x)
+  double c[kL], t[kL + 1];
+  for (int k = 0; k < kL; ++k) c[k] = -2.0 + 4.0 * k / (kL - 1);
+  for (int it = 0; it < 20000; ++it) {
+    t[0] = -INFINITY;
+    t[kL] = INFINITY;
+    for (int k = 1; k < kL; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
+    double diff = 0.0;
+    for (int k = 0; k < kL; ++k) {
+      const double mass = upper(t[k]) - upper(t[k + 1]);
+      const double next = (pdf(t[k]) - pdf(t[k + 1])) / mass;
+      diff = std::max(diff, std::fabs(next - c[k]));
+      c[k] = next;
+    }
+    if (diff < 1e-15) break;
+  }
+  Codec q{};
+  for (int k = 0; k < kL; ++k) q.centroid[k] = static_cast<float>(0.5 * (c[k] - c[kL - 1 - k]));
+  for (int k = 0; k + 1 < kL; ++k) {
+    const double a = 0.5 * (c[k] - c[kL - 1 - k]), b = 0.5 * (c[k + 1] - c[kL - 2 - k]);
+    q.threshold[k] = static_cast<float>(0.5 * (a + b));
+  }
+  return q;
+}
 
 bool make_pool_maps(const lrkv_config& cfg, const void* base_pool, const void* lr_pool,
                     int64_t num_blocks, CUtensorMap* base_map, CUtensorMap* lr_map) {
@@ -253,7 +288,12 @@ const char* lrkv_status_string(lrkv_status s) {
   return "LRKV_UNKNOWN_STATUS";
 }
 
-int32_t lrkv_version(void) { return 20000; }
+int32_t lrkv_version(void) { return 20100; }
+
+size_t lrkv_base_pool_block_bytes(const lrkv_config* cfg) {
+  if (check_config(cfg) != LRKV_OK) return 0;
+  return base_block_bytes(*cfg);
+}
 
 void lrkv_testing_set_decode_stall(int32_t enable) {
   g_decode_test_stall.store(enable != 0 ? 1 : 0, std::memory_order_relaxed);
@@ -384,6 +424,7 @@ lrkv_status lrkv_attn_prefill(const lrkv_config* cfg, const void* q, const int32
   if (st != LRKV_OK) return st;
   if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0 || n_adapters < 0)
     return LRKV_ERR_INVALID_ARG;
+  if (cfg->kv_codec != LRKV_CODEC_NONE) return LRKV_ERR_UNSUPPORTED;  // prefill reads bf16 base planes
   if (num_seqs == 0 || total_q == 0) return LRKV_OK;
   if (q == nullptr || q_start == nullptr || seq_lens == nullptr || adapter_ids == nullptr ||
       block_tables == nullptr || out == nullptr)

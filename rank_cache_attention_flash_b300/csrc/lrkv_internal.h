@@ -15,6 +15,27 @@ struct RopeFreqs;  // lrkv_device.cuh
 // Columns of one low-rank pool row: every group's r columns side by side.
 inline int lr_width(const lrkv_config& cfg) { return cfg.lr_groups * cfg.rank; }
 
+// Compressed base pool (LRKV_CODEC_POLYKV): per (block, kv head) one chunk of
+//   Kq int8 [16][d] | Ks fp16 [16][d/32] | Vq u8 [16][3][d/8] | Vn fp32 [16]
+__host__ __device__ constexpr int codec_chunk_bytes(int d) { return 23 * d + 64; }
+__host__ __device__ constexpr int codec_k_bytes(int d) { return 17 * d; }      // Kq + Ks: what a K item copies per block
+__host__ __device__ constexpr int codec_v_bytes(int d) { return 6 * d + 64; }  // Vq + Vn: what a V item copies per block
+inline size_t base_block_bytes(const lrkv_config& cfg) {
+  if (cfg.kv_codec == LRKV_CODEC_POLYKV) return static_cast<size_t>(cfg.n_kv_heads) * codec_chunk_bytes(cfg.head_dim);
+  return static_cast<size_t>(2) * cfg.n_kv_heads * 16 * cfg.head_dim * (cfg.dtype == LRKV_FP32 ? 4 : 2);
+}
+
+// The 8-level Lloyd-Max quantiser for N(0,1) of the value codes, ascending.
+struct Codec {
+  float centroid[8];
+  float threshold[7];
+};
+Codec make_polykv_codec();
+inline const Codec& polykv_codec() {
+  static const Codec c = make_polykv_codec();
+  return c;
+}
+
 // Split plan of the bf16 decode kernel; a pure function of the sizes and the
 // device's SM count, so the workspace query and the launch agree.
 struct DecodePlan {

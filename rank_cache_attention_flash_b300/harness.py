@@ -64,7 +64,7 @@ class GpuCase:
         self.device = torch.device(device)
         sh = case.shape
         self.cfg = lrkv.make_config(sh.hidden, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.rank,
-                                    sh.rope_base, sh.torch_dtype, sh.lr_groups)
+                                    sh.rope_base, sh.torch_dtype, sh.lr_groups, sh.kv_codec)
         dev = self.device
         w = case.weights
         self.W_cat = lrkv.pack_w_cat(w["W_K"], w["W_V"], w["A_K"], w["A_V"]).to(dev)

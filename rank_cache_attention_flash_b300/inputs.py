@@ -61,6 +61,7 @@ class Shape:
     b_std: float
     q_std: float
     lr_groups: int = 1  # 1: one A shared by every agent; n: agent a has its own A (PreLRShared)
+    kv_codec: int = 0   # 1: the base pool is compressed (PolyKV codec: q8_0 keys, rotated 3-bit values)
 
     @property
     def kv_cols(self) -> int:
@@ -379,6 +380,37 @@ def prelr_decode(seed: int = 0, n: int = 8192, n_agents: int = 4, rank: int = 16
     return case
 
 
+def codec_long_decode(seed: int = 0, n_seqs: int = 16, n: int = 32768, n_agents: int = 8,
+                      rank: int = 64, first: int = 0) -> Case:
+    """The paged long decode over a compressed base pool (PolyKV, the abstract
+    printed at the end of the PReCache page: int8 q8_0 keys, Walsh-Hadamard
+    rotated 3-bit values); same sequences, adapters and block placement."""
+    case = long_decode(seed, n_seqs, n, n_agents, rank, first)
+    case.shape = dataclasses.replace(case.shape, kv_codec=1)
+    case.name = "long_decode_codec_ministral8b"
+    return case
+
+
+def codec_decode(seed: int = 0, n: int = 700, n_agents: int = 4, rank: int = 16, n_ctx: int = 1,
+                 head_dim: int = 128, n_q_heads: int = 32, n_kv_heads: int = 8, q_per_ctx: int = 0) -> Case:
+    """Decode over a compressed base pool at small sizes: n_ctx contexts of n
+    tokens (the last one shorter: a ragged tail), q_per_ctx queries on each
+    (0: n_agents), adapters cycling over the agents with a base-only query when
+    there are more than one."""
+    shape = dataclasses.replace(shape_llama8b(rank, n_agents), head_dim=head_dim, n_q_heads=n_q_heads,
+                                n_kv_heads=n_kv_heads, kv_codec=1)
+    q_per_ctx = q_per_ctx or n_agents
+    seqs, dec = [], []
+    for c in range(n_ctx):
+        L = n if c + 1 < n_ctx else max(1, n - 37 * c - 5)
+        seqs.append(Seq(c, 0, c, L, 0, -1, "context"))
+        for k in range(q_per_ctx):
+            a = (c + k) % n_agents
+            dec.append((c, -1 if (q_per_ctx > 1 and k == q_per_ctx - 1) else a))
+    case = _build("codec_decode", shape, seed, seqs, dec, [], n_ctx > 1, (0, 0))
+    return case
+
+
 def rebase_prefill(seed: int = 0, prefix: int = 16384, chunk: int = 512, n_agents: int = 4,
                    rank: int = 16, first: int = 0) -> Case:
     """The prefill-chunk workload with a re-based cache (PReCache, ReBaseShared):
@@ -411,6 +443,7 @@ SHARD_UNITS = {
     "mixed_batch_qwen3_1p7b": 1,
     "prelr_decode_llama8b": 1,
     "rebase_prefill_llama8b": 1,
+    "long_decode_codec_ministral8b": 16,
 }
 
 
@@ -420,7 +453,7 @@ def build_shard(name: str, world: int = 1, rank: int = 0, seed: int = 0) -> Case
     share = shard_range(world * units, world, rank)
     if len(share) != units:
         raise AssertionError("weak scaling: every rank holds the same number of contexts")
-    first = share.start if name == "long_decode_ministral8b" else share.start // units
+    first = share.start
     return FULL[name](seed, first)
 
 
@@ -432,6 +465,7 @@ FULL = {
     "mixed_batch_qwen3_1p7b": lambda seed=0, first=0: mixed_batch(seed, first=first),
     "prelr_decode_llama8b": lambda seed=0, first=0: prelr_decode(seed, first=first),
     "rebase_prefill_llama8b": lambda seed=0, first=0: rebase_prefill(seed, first=first),
+    "long_decode_codec_ministral8b": lambda seed=0, first=0: codec_long_decode(seed, first=first),
 }
 
 # Small variants: same layer shapes, lengths the oracle finishes in seconds,

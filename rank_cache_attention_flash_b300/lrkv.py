@@ -24,10 +24,11 @@ BLOCK = 16
 STATUS = {0: "LRKV_OK", 1: "LRKV_ERR_INVALID_ARG", 2: "LRKV_ERR_UNSUPPORTED", 3: "LRKV_ERR_CUDA",
           4: "LRKV_ERR_INDEX", 5: "LRKV_ERR_TIMEOUT", 6: "LRKV_ERR_WORKSPACE"}
 BF16, FP32 = 0, 1
+CODEC_NONE, CODEC_POLYKV = 0, 1
 
 EXPORTS = ("lrkv_append", "lrkv_append_rebase", "lrkv_attn_decode", "lrkv_decode_workspace_bytes", "lrkv_attn_prefill",
            "lrkv_prefill_workspace_bytes", "lrkv_status_string", "lrkv_version",
-           "lrkv_attn_decode_noalloc", "lrkv_testing_set_decode_stall")
+           "lrkv_attn_decode_noalloc", "lrkv_testing_set_decode_stall", "lrkv_base_pool_block_bytes")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # LRKV_NOALLOC_SCRATCH_BYTES in lrkv.h
 
 
@@ -42,7 +43,7 @@ class Config(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("rank", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("rope_base", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("lr_groups", ctypes.c_int32)]
+                ("lr_groups", ctypes.c_int32), ("kv_codec", ctypes.c_int32)]
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -54,17 +55,23 @@ class Config(ctypes.Structure):
         return max(1, self.lr_groups) * self.rank
 
     @property
+    def codec_chunk_bytes(self) -> int:
+        """Bytes of one (block, kv head) chunk of a compressed base pool."""
+        return 23 * self.head_dim + 64
+
+    @property
     def n_cols(self) -> int:
         return 2 * self.n_kv_heads * self.head_dim + 2 * self.lr_width
 
 
 def make_config(hidden: int, n_q_heads: int, n_kv_heads: int, head_dim: int, rank: int,
                 rope_base: float = 10000.0, dtype: torch.dtype = torch.bfloat16,
-                lr_groups: int = 1) -> Config:
+                lr_groups: int = 1, kv_codec: int = 0) -> Config:
     """lr_groups = 1: one A shared by every agent; lr_groups = n: agent a has its
-    own A_a and reads low-rank group a (PreLRShared)."""
+    own A_a and reads low-rank group a (PreLRShared). kv_codec = CODEC_POLYKV:
+    the base pool is compressed (q8_0 keys, rotated 3-bit values)."""
     return Config(hidden, n_q_heads, n_kv_heads, head_dim, rank, BLOCK, rope_base,
-                  BF16 if dtype == torch.bfloat16 else FP32, lr_groups)
+                  BF16 if dtype == torch.bfloat16 else FP32, lr_groups, kv_codec)
 
 
 _lib = None
@@ -102,6 +109,8 @@ def load() -> ctypes.CDLL:
     lib.lrkv_status_string.restype = ctypes.c_char_p
     lib.lrkv_version.argtypes = []
     lib.lrkv_version.restype = ctypes.c_int32
+    lib.lrkv_base_pool_block_bytes.argtypes = [ctypes.POINTER(Config)]
+    lib.lrkv_base_pool_block_bytes.restype = _SZ
     lib.lrkv_testing_set_decode_stall.argtypes = [_I32]
     lib.lrkv_testing_set_decode_stall.restype = None
     _lib = lib
@@ -162,14 +171,44 @@ def pack_w_cat(W_K: torch.Tensor, W_V: torch.Tensor, A_K: torch.Tensor, A_V: tor
 
 def new_pools(cfg: Config, num_blocks: int, device, fill: Optional[float] = None
               ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Allocates (base_pool, lr_pool) for ``num_blocks`` blocks."""
+    """Allocates (base_pool, lr_pool) for ``num_blocks`` blocks. A compressed
+    base pool is bytes [num_blocks][Hkv][23 d + 64]; ``fill`` then fills only
+    the low-rank pool (the base pool's bytes are set to 0xFF)."""
     dt = cfg.torch_dtype
-    base = torch.empty(num_blocks, 2, cfg.n_kv_heads, BLOCK, cfg.head_dim, dtype=dt, device=device)
+    if cfg.kv_codec == CODEC_POLYKV:
+        base = torch.empty(num_blocks, cfg.n_kv_heads, cfg.codec_chunk_bytes, dtype=torch.uint8, device=device)
+    else:
+        base = torch.empty(num_blocks, 2, cfg.n_kv_heads, BLOCK, cfg.head_dim, dtype=dt, device=device)
     lr = torch.empty(num_blocks, 2, BLOCK, cfg.lr_width, dtype=dt, device=device)
     if fill is not None:
-        base.fill_(fill)
+        if cfg.kv_codec == CODEC_POLYKV:
+            base.fill_(255)
+        else:
+            base.fill_(fill)
         lr.fill_(fill)
     return base, lr
+
+
+def base_pool_block_bytes(cfg: Config) -> int:
+    return int(load().lrkv_base_pool_block_bytes(ctypes.byref(cfg)))
+
+
+def unpack_codec_pool(cfg: Config, base: torch.Tensor):
+    """Host-side view of a compressed base pool: dict of CPU arrays over
+    [num_blocks, Hkv, 16]: Kq int8 [.., d], Ks fp16 [.., d/32], Vq uint8 codes
+    0..7 [.., d] (from the three bit planes), Vn fp32 [..]."""
+    import numpy as np
+    d = cfg.head_dim
+    b = base.cpu().numpy()
+    nb, hkv = b.shape[0], b.shape[1]
+    o_ks, o_vq, o_vn = 16 * d, 17 * d, 23 * d
+    Kq = b[:, :, :o_ks].view(np.int8).reshape(nb, hkv, BLOCK, d)
+    Ks = np.ascontiguousarray(b[:, :, o_ks:o_vq]).view(np.float16).reshape(nb, hkv, BLOCK, d // 32)
+    planes = b[:, :, o_vq:o_vn].reshape(nb, hkv, BLOCK, 3, d // 8)
+    bits = np.unpackbits(planes, axis=-1, bitorder="little")  # [.., 3, d]
+    Vq = (bits[..., 0, :] | (bits[..., 1, :] << 1) | (bits[..., 2, :] << 2)).astype(np.uint8)
+    Vn = np.ascontiguousarray(b[:, :, o_vn:o_vn + 64]).view(np.float32).reshape(nb, hkv, BLOCK)
+    return {"Kq": Kq, "Ks": Ks, "Vq": Vq, "Vn": Vn}
 
 
 # ------------------------------------------------------------- entry points

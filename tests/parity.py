@@ -8,6 +8,7 @@ import numpy as np
 import torch
 
 import oracle
+from oracle import polykv
 
 # Tolerances (relative Frobenius and max-abs error against the fp64 oracle).
 BF16_TOL = dict(max_abs=2e-2, rel_fro=5e-3)
@@ -83,7 +84,12 @@ def oracle_decode_rows(case, rows: Optional[Iterable[int]] = None, w64=None, cac
         X, X_lr = _hidden(case, case.dec_ctx[c])
         q = case.dec_q[rs].double().numpy()
         ad = case.dec_adapter[rs].numpy()
-        o = oracle.decode(X, q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale, cache, X_lr)
+        if getattr(sh, "kv_codec", 0):
+            # compressed base pool: the oracle encodes its own exact base part
+            o = polykv.decode_codec(X, q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale,
+                                    "bf16" if cache == "bf16" else None)
+        else:
+            o = oracle.decode(X, q, ad, w64, sh.n_kv_heads, sh.head_dim, sh.rope_base, scale, cache, X_lr)
         for i, r in enumerate(rs):
             out[r] = o[i]
     return np.stack([out[r] for r in rows])

@@ -52,7 +52,7 @@ def test_status_strings_and_version(lib):
 
 def _cfg(**kw):
     base = dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, rank=8, block_size=16,
-                rope_base=10000.0, dtype=0, lr_groups=1)
+                rope_base=10000.0, dtype=0, lr_groups=1, kv_codec=0)
     base.update(kw)
     return lrkv.Config(**base)
 
@@ -61,6 +61,7 @@ def _cfg(**kw):
     (dict(head_dim=96), 2), (dict(rank=12), 2), (dict(block_size=32), 2), (dict(dtype=5), 2),
     (dict(n_q_heads=5), 1), (dict(hidden=0), 1), (dict(rope_base=0.0), 1), (dict(hidden=100), 2),
     (dict(n_q_heads=64, n_kv_heads=2), 2), (dict(lr_groups=0), 1), (dict(lr_groups=65), 2),
+    (dict(kv_codec=2), 1), (dict(kv_codec=-1), 1), (dict(kv_codec=1, dtype=1), 2),
 ])
 def test_bad_config_rejected_before_launch(lib, kw, code):
     cfg = _cfg(**kw)
@@ -115,3 +116,22 @@ def test_positions_limit_rejected(lib):
     # max_blocks * 16 above 2^20 positions
     r = lib.lrkv_append(ctypes.byref(cfg), P, 4, P, P, P, 1, (1 << 16) + 1, P, P, P, 10, None, None)
     assert r == 2
+
+
+def test_base_pool_block_bytes(lib):
+    """bf16 / fp32 planes: 2 Hkv 16 d elements; compressed: Hkv (23 d + 64) bytes
+    (Kq 16 d, Ks 16 d/32 fp16, Vq 16 x 3 x d/8, Vn 16 fp32)."""
+    assert lrkv.base_pool_block_bytes(_cfg()) == 2 * 2 * 16 * 64 * 2
+    assert lrkv.base_pool_block_bytes(_cfg(dtype=1)) == 2 * 2 * 16 * 64 * 4
+    for d in (64, 128):
+        want = 2 * (16 * d + 16 * (d // 32) * 2 + 16 * 3 * (d // 8) + 16 * 4)
+        assert lrkv.base_pool_block_bytes(_cfg(kv_codec=1, head_dim=d)) == want == 2 * (23 * d + 64)
+    assert lrkv.base_pool_block_bytes(_cfg(kv_codec=3)) == 0
+
+
+def test_prefill_on_compressed_pool_unsupported(lib):
+    cfg = _cfg(kv_codec=1)
+    P = 1 << 20
+    pargs = [ctypes.byref(cfg), P, P, 1, 8, 8, P, 64, P, P, 4, P, P, 8, P, P, 2, 0.125, P, None, 0,
+             None, None]
+    assert lib.lrkv_attn_prefill(*pargs) == 2

@@ -139,3 +139,67 @@ def test_full_rebase_prefill(cuda_lib):
     assert case.rebase
     got, want = _prefill_all(case, g, res, weights64(case))
     _whole(got, want, case, "re-based prefill")
+
+
+def test_full_codec_long_decode(cuda_lib):
+    """The long decode over a compressed base pool (PolyKV codec): all 16 queries,
+    each over its whole 32768-token context, against the codec oracle (which
+    encodes its own exact base part). Gated per configuration: whole-output
+    relative Frobenius error <= 5e-3 and the per-element bound. Per query the
+    error is reported, not gated: a code decided at a rounding boundary may
+    differ by one step between the GPU's fp32 projections and the oracle's
+    exact ones (test_full_codec_codes checks every such code), and when the
+    token holding it dominates a head, that one step moves the head by a few
+    tenths of a percent to a few percent."""
+    case, g, res = _run("long_decode_codec_ministral8b")
+    assert case.shape.kv_codec == 1 and case.dec_q.shape[0] == 16
+    w64 = weights64(case)
+    got = res["decode"].double().cpu().numpy()
+    want = oracle_decode_rows(case, w64=w64)
+    for n in range(16):
+        mx, rf = errors(got[n], want[n])
+        print(f"query {n}: max_abs {mx:.3e} rel_fro {rf:.3e}")
+    _whole([got], [want], case, "compressed long decode")
+
+
+def test_full_codec_codes(cuda_lib):
+    """Every code of one 32768-token context of the compressed long decode
+    against the codec oracle: keys and values, scales and norms. Codes are
+    bit-exact except where the oracle's exact value lies within rounding of a
+    decision boundary (q8_0: x / s within 1e-3 of a half; values: u within 1e-5
+    of a threshold), and there they differ by one step."""
+    import oracle.lrkv_oracle as OL
+    from oracle import polykv
+    from tests.parity import _hidden
+    case = I.codec_long_decode(n_seqs=4)
+    g = GpuCase(case)
+    g.setup()
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    pool = cuda_lib.unpack_codec_pool(g.cfg, g.base_pool)
+    sh = case.shape
+    w64 = weights64(case)
+    ctx = case.dec_ctx[3]
+    X, _ = _hidden(case, ctx)
+    L = X.shape[0]
+    pos = np.arange(L)
+    bt = case.block_tables.numpy()[ctx]
+    blk, row = bt[pos // 16], pos % 16
+    kb, vb, _, _ = OL.base_and_lowrank(X, pos, w64["W_K"], w64["W_V"], w64["A_K"], w64["A_V"], sh.n_kv_heads,
+                                      sh.head_dim, sh.rope_base)
+    kq, ks = polykv.q8_0_encode(kb)
+    vq, vn = polykv.tq3_encode(vb)
+    gk, gks = pool["Kq"][blk, :, row], pool["Ks"][blk, :, row]
+    gv, gvn = pool["Vq"][blk, :, row], pool["Vn"][blk, :, row]
+    np.testing.assert_allclose(gks.astype(np.float64), ks.astype(np.float64), rtol=2 ** -10)
+    np.testing.assert_allclose(gvn, vn, rtol=1e-5)
+    dk = gk.astype(int) - kq.astype(int)
+    sc = np.repeat(ks.astype(np.float64), 32, axis=-1)
+    frac = np.abs(np.abs(kb / np.where(sc > 0, sc, 1)) % 1 - 0.5)
+    assert (np.abs(dk) <= 1).all() and (frac[dk != 0] < 1e-3).all() and (dk != 0).mean() < 1e-3
+    dv = gv.astype(int) - vq.astype(int)
+    _, t = polykv.centroids_thresholds()
+    u = polykv.rotate(vb) * np.sqrt(sh.head_dim) / np.linalg.norm(vb, axis=-1, keepdims=True)
+    dist = np.min(np.abs(u[..., None] - t), axis=-1)
+    assert (np.abs(dv) <= 1).all() and (dist[dv != 0] < 1e-5).all() and (dv != 0).mean() < 1e-4
+    print(f"key codes differing at a boundary: {(dk != 0).mean():.2e}; value codes: {(dv != 0).mean():.2e}")

@@ -201,9 +201,32 @@ def pin_append_codec_routing(M):
                 assert (pool["Kq"][blk, :, row] == -128).all() and (pool["Vq"][blk, :, row] == 255).all()
 
 
+def pin_operand_rounding_bounds(M):
+    """The bf16-cache reading changes each expanded key by at most half an fp16
+    step and each rotated value by at most half a bf16 step, so the values it
+    rotates back move by at most that, in norm (the rotation is orthonormal);
+    and the rounded quantities are exactly those a kernel holds: the keys are
+    fp16 numbers, the values are bf16 numbers in the rotated domain."""
+    r = _rng(7)
+    kb = r.standard_normal((20, 2, 64)) * 3
+    vb = r.standard_normal((20, 2, 64))
+    k0, v0 = M.base_roundtrip(kb, vb)
+    k1, v1 = M.base_roundtrip(kb, vb, operand=True)
+    assert np.all(np.abs(k1 - k0) <= np.abs(k0) * 2.0 ** -11 + 1e-12) and np.any(k1 != k0)
+    vq, vn = M.tq3_encode(vb)
+    c, _ = M.lloyd_max_gaussian()
+    yhat = c[vq.astype(np.int64)] * (vn.astype(np.float64) / 8.0)[..., None]
+    bound = np.linalg.norm(yhat, axis=-1) * 2.0 ** -8  # bf16: 8 significant bits
+    assert np.all(np.linalg.norm(v1 - v0, axis=-1) <= bound + 1e-12) and np.any(v1 != v0)
+    # what is rounded is what the kernel holds: fp16 keys, and bf16 values in the rotated domain
+    assert np.array_equal(k1, k1.astype(np.float16).astype(np.float64))
+    y1 = M.rotate(v1)
+    assert np.allclose(y1, O.round_bf16(y1), rtol=1e-12, atol=1e-15)
+
+
 ALL_PINS = [pin_lloyd_max_gaussian, pin_rotation_is_sylvester_hadamard, pin_q8_0_hand_blocks,
             pin_tq3_nearest_centroid, pin_tq3_distortion, pin_codec_lossless_equals_plain,
-            pin_codec_close_to_plain, pin_append_codec_routing]
+            pin_codec_close_to_plain, pin_append_codec_routing, pin_operand_rounding_bounds]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -239,6 +262,8 @@ MUTATIONS = {
                                      "k = k + (lk @ np.asarray(B_K_i, dtype=np.float64)).reshape(T, n_kv_heads, head_dim)"),
     "codec_v_adapter_from_lk": ("v = v + (lv @ np.asarray(B_V_i", "v = v + (lk[:, :lv.shape[1]] @ np.asarray(B_V_i"),
     "append_codec_row_shift": ("        row = p % O.BLOCK\n", "        row = (p + 1) % O.BLOCK\n"),
+    "operand_rounding_after_rotation": ("        yhat = O.round_bf16(yhat)\n    return rotate(yhat)",
+                                        "        return O.round_bf16(rotate(yhat))\n    return rotate(yhat)"),
 }
 
 
