@@ -165,9 +165,9 @@ def test_full_codec_long_decode(cuda_lib):
 def test_full_codec_codes(cuda_lib):
     """Every code of one 32768-token context of the compressed long decode
     against the codec oracle: keys and values, scales and norms. Codes are
-    bit-exact except where the oracle's exact value lies within rounding of a
-    decision boundary (q8_0: x / s within 1e-3 of a half; values: u within 1e-5
-    of a threshold), and there they differ by one step."""
+    bit-exact except where the oracle's exact value lies within the GPU's rounding
+    of a decision boundary (q8_0: x / s within the fast RoPE's error of a half;
+    values: u within 1e-5 of a threshold), and there they differ by one step."""
     import oracle.lrkv_oracle as OL
     from oracle import polykv
     from tests.parity import _hidden
@@ -194,9 +194,14 @@ def test_full_codec_codes(cuda_lib):
     np.testing.assert_allclose(gks.astype(np.float64), ks.astype(np.float64), rtol=2 ** -10)
     np.testing.assert_allclose(gvn, vn, rtol=1e-5)
     dk = gk.astype(int) - kq.astype(int)
-    sc = np.repeat(ks.astype(np.float64), 32, axis=-1)
-    frac = np.abs(np.abs(kb / np.where(sc > 0, sc, 1)) % 1 - 0.5)
-    assert (np.abs(dk) <= 1).all() and (frac[dk != 0] < 1e-3).all() and (dk != 0).mean() < 1e-3
+    # the decision is x / s with s = max |x| / 127 (unrounded); the GPU's keys carry
+    # the fast RoPE's absolute error (<= 3e-4, as in the append tests), which moves
+    # x / s by up to about 6e-4 / s (the key and the block's maximum both move)
+    s_ex = np.repeat(np.abs(kb).reshape(kb.shape[:-1] + (-1, 32)).max(-1) / 127.0, 32, axis=-1)
+    ratio = kb / np.where(s_ex > 0, s_ex, 1)
+    frac = np.abs(np.abs(ratio) % 1 - 0.5)
+    slack = 6e-4 / np.where(s_ex > 0, s_ex, 1) * (1 + np.abs(ratio) / 127)
+    assert (np.abs(dk) <= 1).all() and (frac[dk != 0] < slack[dk != 0]).all() and (dk != 0).mean() < 1e-3
     dv = gv.astype(int) - vq.astype(int)
     _, t = polykv.centroids_thresholds()
     u = polykv.rotate(vb) * np.sqrt(sh.head_dim) / np.linalg.norm(vb, axis=-1, keepdims=True)
