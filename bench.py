@@ -44,7 +44,7 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "all"
 ALL_WORKLOADS = ["shared_decode_llama8b", "prefill_chunk_llama8b", "long_decode_ministral8b",
-                 "long_decode_codec_ministral8b",
+                 "long_decode_codec_ministral8b", "prefill_chunk_codec_llama8b",
                  "mixed_batch_qwen3_1p7b", "prelr_decode_llama8b", "rebase_prefill_llama8b"]
 HEADLINE = "shared_decode_llama8b"
 PREFILL_HEADLINE = "prefill_chunk_llama8b"
@@ -122,7 +122,8 @@ def workload_model(case):
             flops += Hq * vis * (4 * D + 2 * R)          # QK^T + PV + P L_V
             flops += Hkv * L * 2 * R * D                  # K rebuild (once per key)
             flops += n * Hq * 2 * R * D                   # O_lr B_V
-            nbytes += L * (Hkv * D * 2 + 2 * R) * es + 2 * n * Hq * D * es
+            base_tok = Hkv * (23 * D + 64) // 16 if sh.kv_codec else Hkv * D * 2 * es
+            nbytes += L * (base_tok + 2 * R * es) + 2 * n * Hq * D * es
         out["prefill"] = {"bytes": nbytes, "flops": flops, "units": int(qs[-1]),
                           "unit_name": "prefill tokens", "pairs": pairs}
     T = sum(b - a for _, a, b in case.step_appends())

@@ -55,9 +55,8 @@
  *   A value row v decodes to v^ = (H/sqrt(d)) y^, with y^_j = c[code_j] ||v|| / sqrt(d)
  *   (H the Sylvester-Hadamard matrix, c the 8 Lloyd-Max centroids for N(0,1)
  *   in ascending order); code_j counts the Lloyd-Max thresholds below
- *   u_j = y_j sqrt(d) / ||v||, y = (H/sqrt(d)) v. Attention reads
- *   K_i = K^_base + RoPE(L_K B_K,i), V_i = V^_base + L_V B_V,i (decode only;
- *   prefill on a compressed pool returns LRKV_ERR_UNSUPPORTED).
+ *   u_j = y_j sqrt(d) / ||v||, y = (H/sqrt(d)) v. Decode and prefill read
+ *   K_i = K^_base + RoPE(L_K B_K,i), V_i = V^_base + L_V B_V,i.
  * - Block tables: int32 [rows][max_blocks] row-major.
  * - RoPE: rotate-half pairing (j, j + d/2), angle p * theta_j with
  *   theta_j = rope_base^(-2j/d), no frequency scaling. Queries arrive already

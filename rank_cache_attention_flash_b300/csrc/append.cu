@@ -98,19 +98,6 @@ __device__ __forceinline__ void q8_0_store(const float* x, int8_t* codes, __half
   *scale = __float2half_rn(s);
 }
 
-// In-register Walsh-Hadamard transform of 32 values (Sylvester order, unnormalised).
-__device__ __forceinline__ void fwht32(float* z) {
-#pragma unroll
-  for (int len = 1; len < 32; len <<= 1)
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if ((i & len) == 0) {
-        const float a = z[i], b = z[i + len];
-        z[i] = a + b;
-        z[i + len] = a - b;
-      }
-}
-
 // 3-bit code of u: the number of (ascending) thresholds below u, in three compares.
 __device__ __forceinline__ uint32_t code3(float u, const float* t) {
   const bool b2 = t[3] < u;

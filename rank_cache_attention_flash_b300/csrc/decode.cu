@@ -955,13 +955,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // own online softmax, and stores its own split partial (the combine merges
 // 2 x n_splits partials per query head). While one warpgroup waits on a tensor
 // or memory operation of its tile, the other works on the next tile.
-// sqrt(d) of the value rotation's scale, d = 64 or 128
-template <int D>
-constexpr float kSqrtD = D == 128 ? 11.313708498984760f : 8.0f;
-
-// Bits 0-3 of x moved to bits 0, 8, 16, 24 (x < 16).
-__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
-
 namespace rb {
 constexpr int kRows = 4;          // query rows per item (one query)
 constexpr uint32_t RY_COL = 0;     // [2][d]  Y of the pipeline's tile, fp32

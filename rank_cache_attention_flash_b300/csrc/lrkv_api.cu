@@ -424,7 +424,6 @@ lrkv_status lrkv_attn_prefill(const lrkv_config* cfg, const void* q, const int32
   if (st != LRKV_OK) return st;
   if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0 || n_adapters < 0)
     return LRKV_ERR_INVALID_ARG;
-  if (cfg->kv_codec != LRKV_CODEC_NONE) return LRKV_ERR_UNSUPPORTED;  // prefill reads bf16 base planes
   if (num_seqs == 0 || total_q == 0) return LRKV_OK;
   if (q == nullptr || q_start == nullptr || seq_lens == nullptr || adapter_ids == nullptr ||
       block_tables == nullptr || out == nullptr)

@@ -117,6 +117,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// In-register Walsh-Hadamard transform of 32 values (Sylvester order,
+// unnormalised). The d-point transform, d = 32 m, is H_m (x) H_32: group g of
+// H_d v is fwht32 of sum_k (-1)^popc(g & k) v[32 k .. 32 k + 31].
+__device__ __forceinline__ void fwht32(float* z) {
+#pragma unroll
+  for (int len = 1; len < 32; len <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((i & len) == 0) {
+        const float a = z[i], b = z[i + len];
+        z[i] = a + b;
+        z[i + len] = a - b;
+      }
+}
+
+// sqrt(d) of the compressed pool's value scale ||v|| / sqrt(d), d = 64 or 128
+template <int D>
+constexpr float kSqrtD = D == 128 ? 11.313708498984760f : 8.0f;
+
+// Bits 0-3 of x moved to bits 0, 8, 16, 24 (x < 16).
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+
 // Plain (untiled) bulk copy global -> shared: both addresses 16-byte aligned,
 // `bytes` a multiple of 16, completion counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -72,6 +72,8 @@ struct PrefillParams {
   int lr_groups;  // > 1: agent-specific A, adapter a's low-rank group at columns [a r, (a+1) r)
   int has_bk, has_bv;
   float scale_log2;
+  const uint8_t* cbase;  // compressed base pool (CODEC kernels): chunks of codec_chunk_bytes(D)
+  float vcent[8];        // value-code centroids (Lloyd-Max for N(0,1)), ascending
   RopeFreqs freqs;
 };
 
@@ -177,7 +179,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D, int R>
+template <int D, int R, bool CODEC>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p,
                    const __grid_constant__ CUtensorMap tm_base,
@@ -232,6 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const bool rebuild = p.has_bk && adapter >= 0;
   const bool use_lr = p.has_bv && adapter >= 0;
+  // compressed base pool: the rebuild warpgroup expands each tile's key codes
+  // to fp16 (scored in fp16 like a rebuilt K_a) and its value codes to bf16 in
+  // the rotated domain; the epilogue rotates the output back
+  const bool kconv = rebuild || CODEC;
   // agent-specific A: this sequence's adapter reads its own low-rank group
   const int lr_x = (p.lr_groups > 1 && adapter >= 0) ? adapter * R : 0;
   const int k_first = row0 / g;
@@ -303,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         uint4 u = sm_valid ? __ldg(reinterpret_cast<const uint4*>(qrow + 32 * c + 8 * x)) : make_uint4(0, 0, 0, 0);
-        v[4 * x + 0] = rebuild ? bf16x2_to_f16x2(u.x) : u.x;
-        v[4 * x + 1] = rebuild ? bf16x2_to_f16x2(u.y) : u.y;
-        v[4 * x + 2] = rebuild ? bf16x2_to_f16x2(u.z) : u.z;
-        v[4 * x + 3] = rebuild ? bf16x2_to_f16x2(u.w) : u.w;
+        v[4 * x + 0] = kconv ? bf16x2_to_f16x2(u.x) : u.x;
+        v[4 * x + 1] = kconv ? bf16x2_to_f16x2(u.y) : u.y;
+        v[4 * x + 2] = kconv ? bf16x2_to_f16x2(u.z) : u.z;
+        v[4 * x + 3] = kconv ? bf16x2_to_f16x2(u.w) : u.w;
       }
       tc::st_x16(tbase + lane_off + Q_COL + 16 * c, v);
     }
@@ -326,14 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ============================================================ producer
   if (warp == 0) {
     if (lane == 0) {
-      prefetch_tmap(&tm_base);
+      if (!CODEC) prefetch_tmap(&tm_base);
       prefetch_tmap(&tm_lk);
-      prefetch_tmap(&tm_base_run);
-      prefetch_tmap(&tm_lr_run);
+      if (!CODEC) {
+        prefetch_tmap(&tm_base_run);
+        prefetch_tmap(&tm_lr_run);
+      }
     }
     const int nblk_vis = pos_max / kBlock + 1;  // blocks holding a key some row sees
-    const uint32_t per_blk = 2u * kBlock * D * 2 + (use_lr ? kBlock * LSPAN : 0) +
-                             (rebuild ? kBlock * LSPAN : 0);
+    // per block: K and V (planes, or the compressed chunk's Kq|Ks and Vq|Vn), L_V, L_K
+    const uint32_t base_blk = CODEC ? codec_k_bytes(D) + codec_v_bytes(D) : 2u * kBlock * D * 2;
+    const uint32_t per_blk = base_blk + (use_lr ? kBlock * LSPAN : 0) + (rebuild ? kBlock * LSPAN : 0);
     const int32_t* bt_row = p.block_tables + static_cast<int64_t>(s_row) * p.max_blocks;
     // block ids of the next tile are fetched one tile ahead (lane b: block b)
     int id_next = (lane < NB && lane < nblk_vis) ? __ldg(bt_row + lane) : -1;
@@ -361,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t mask = __ballot_sync(0xffffffffu, blk >= 0);
       // one copy per plane when the tile's blocks are consecutive in the pool
       const int blk0 = __shfl_sync(0xffffffffu, blk, 0);
-      const bool run = mask == (1u << NB) - 1 && __all_sync(0xffffffffu, lane >= NB || blk == blk0 + lane);
+      const bool run = !CODEC && mask == (1u << NB) - 1 && __all_sync(0xffffffffu, lane >= NB || blk == blk0 + lane);
       if (lane == 0) {
         stage_mask[s] = static_cast<int>(mask);
         mbar_arrive_expect_tx(bar(B_FULL + s), __popc(mask) * per_blk);
@@ -380,12 +389,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rebuild) tma_load_4d(st + L::off_lk, &tm_lr_run, lr_x, 0, 0, blk0, fb);
         }
       } else if (blk >= 0) {
-        const int yk = ((blk * 2 + 0) * p.Hkv + head) * kBlock;
-        const int yv = ((blk * 2 + 1) * p.Hkv + head) * kBlock;
+        if (CODEC) {
+          // the block's codes, staged at the front of the tile's K and V buffers
+          const uint8_t* chunk = p.cbase + (static_cast<int64_t>(blk) * p.Hkv + head) * codec_chunk_bytes(D);
+          bulk_load(st + L::off_k + lane * codec_k_bytes(D), chunk, codec_k_bytes(D), fb);
+          bulk_load(st + L::off_v + lane * codec_v_bytes(D), chunk + codec_k_bytes(D), codec_v_bytes(D), fb);
+        } else {
+          const int yk = ((blk * 2 + 0) * p.Hkv + head) * kBlock;
+          const int yv = ((blk * 2 + 1) * p.Hkv + head) * kBlock;
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_2d(st + L::off_k + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yk, fb);
-          tma_load_2d(st + L::off_v + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yv, fb);
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_2d(st + L::off_k + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yk, fb);
+            tma_load_2d(st + L::off_v + h * (BN * 128) + lane * 2048, &tm_base, 64 * h, yv, fb);
+          }
         }
         if (use_lr) tma_load_2d(st + L::off_lv + lane * kBlock * LSPAN, &tm_lk, lr_x, (blk * 2 + 1) * kBlock, fb);
         if (rebuild) tma_load_2d(st + L::off_lk + lane * kBlock * LSPAN, &tm_lk, lr_x, (blk * 2 + 0) * kBlock, fb);
@@ -403,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // S(u) = Q K_a(u)^T into the single score buffer, once the rebuild has
   // written K_a(u) and the softmax has loaded S(u-1).
   if (warp == 1) {
-    const uint32_t idS = rebuild ? kIdS16 : kIdSbf;
+    const uint32_t idS = kconv ? kIdS16 : kIdSbf;
     const uint64_t bdesc0 = tc::sdesc(sbase + L::off_k, 16, 1024, 2);
     bool ok = true;
     for (int u = 0; u < U; ++u) {
@@ -653,7 +669,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32], z[32];
-        tc::ld_x32(tbase + lane_off + O_COL + 32 * c, v);
+        if (CODEC) {
+          // O_base = (H / sqrt(d)) O_rot: group c of H O_rot is fwht32 of
+          // sum_k (-1)^popc(c & k) O_rot[32 k ..]
+          float zr[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) zr[e] = 0.f;
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            uint32_t x[32];
+            tc::ld_x32(tbase + lane_off + O_COL + 32 * k, x);
+            tc::wait_ld();
+            const bool neg = (__popc(c & k) & 1) != 0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) zr[e] += neg ? -__uint_as_float(x[e]) : __uint_as_float(x[e]);
+          }
+          fwht32(zr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(zr[e] * (1.0f / kSqrtD<D>));
+        } else {
+          tc::ld_x32(tbase + lane_off + O_COL + 32 * c, v);
+        }
         if (use_lr) tc::ld_x32(tbase + lane_off + S_COL + 32 * c, z);
         tc::wait_ld();
         if (sm_valid) {
@@ -737,6 +773,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = j * BN + i;
       const bool key_ok = row_in && ((mask >> bb) & 1) && t < Ls;
       uint8_t* kbuf = smem + s * L::STAGE + L::off_k;  // this tile's K buffer
+      if (CODEC) {
+        // Expand the tile's codes in place. Keys: each quarter-warp reads one
+        // row's code bytes (contiguous: no bank conflicts), warp w the rows
+        // 32 w ..; values: each thread its own row's three bit planes and norm.
+        // Every code is read before any expanded row is written over them.
+        constexpr int PR = D / 16, RPI = 32 / PR, NP = 32 / RPI;
+        const int pc = lane % PR;
+        uint4 kc[NP];
+        float ksc[NP];
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          const int row = 32 * (warp & 3) + RPI * n + lane / PR;
+          kc[n] = make_uint4(0u, 0u, 0u, 0u);
+          ksc[n] = 0.f;
+          if (row < BN) {
+            const uint8_t* kb = kbuf + (row >> 4) * codec_k_bytes(D);
+            kc[n] = *reinterpret_cast<const uint4*>(kb + (row & 15) * D + 16 * pc);
+            ksc[n] = __half2float(reinterpret_cast<const __half*>(kb + 16 * D)[(row & 15) * (D / 32) + pc / 2]);
+          }
+        }
+        uint8_t* vbuf = smem + s * L::STAGE + L::off_v;
+        uint32_t pw[3][D / 32];
+        float nv = 0.f;
+#pragma unroll
+        for (int b = 0; b < 3; ++b)
+#pragma unroll
+          for (int gg = 0; gg < D / 32; ++gg) pw[b][gg] = 0u;
+        if (row_in) {
+          const uint8_t* vrow = vbuf + bb * codec_v_bytes(D);
+#pragma unroll
+          for (int b = 0; b < 3; ++b) {
+            const uint8_t* pp = vrow + (i & 15) * (3 * D / 8) + b * (D / 8);
+            if constexpr (D == 128) {
+              const uint4 x = *reinterpret_cast<const uint4*>(pp);
+              pw[b][0] = x.x;
+              pw[b][1] = x.y;
+              pw[b][2] = x.z;
+              pw[b][3] = x.w;
+            } else {
+              const uint2 x = *reinterpret_cast<const uint2*>(pp);
+              pw[b][0] = x.x;
+              pw[b][1] = x.y;
+            }
+          }
+          nv = *reinterpret_cast<const float*>(vrow + 6 * D + 4 * (i & 15));
+        }
+        named_bar_sync(3, 128);
+        // K^ = q s, fp16; the pieces of the second 64-dim half store their
+        // 16-byte halves in the other order (8 bank groups per quarter-warp)
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          const int row = 32 * (warp & 3) + RPI * n + lane / PR;
+          if (row < BN) {
+            const uint32_t w[4] = {kc[n].x, kc[n].y, kc[n].z, kc[n].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t x = w[e >> 1] >> (16 * (e & 1));
+              o[e] = pack_f16(static_cast<float>(static_cast<int8_t>(x & 0xffu)) * ksc[n],
+                              static_cast<float>(static_cast<int8_t>((x >> 8) & 0xffu)) * ksc[n]);
+            }
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+              const int hf = hp ^ ((pc >> 2) & 1);
+              const int dim = 16 * pc + 8 * hf;
+              *reinterpret_cast<uint4*>(kbuf + (dim / 64) * (BN * 128) + swz<128>(row, (dim % 64) * 2)) =
+                  hf ? make_uint4(o[4], o[5], o[6], o[7]) : make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+        // V^ of this row in the rotated domain: c[code] ||v|| / sqrt(d) as bf16
+        // (0 for keys outside the sequence or an unloaded block), by a
+        // byte-permute table of the 8 scaled centroids
+        if (row_in) {
+          const float vs = key_ok ? nv * (1.0f / kSqrtD<D>) : 0.f;
+          const uint32_t t0 = pack_bf16(p.vcent[0] * vs, p.vcent[1] * vs), t1 = pack_bf16(p.vcent[2] * vs, p.vcent[3] * vs);
+          const uint32_t t2 = pack_bf16(p.vcent[4] * vs, p.vcent[5] * vs), t3 = pack_bf16(p.vcent[6] * vs, p.vcent[7] * vs);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            uint32_t o[4];
+#pragma unroll
+            for (int h4 = 0; h4 < 2; ++h4) {
+              const int jd = 8 * c + 4 * h4, gw = jd >> 5, sh = jd & 31;
+              const uint32_t lo2 = spread4((pw[0][gw] >> sh) & 15u) | (spread4((pw[1][gw] >> sh) & 15u) << 1);
+              const uint32_t hi8 = spread4((pw[2][gw] >> sh) & 15u) * 0xffu;
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const uint32_t sel = 0x1010u + 0x22u * ((lo2 >> (16 * e)) & 0xffffu);
+                const uint32_t m = __byte_perm(hi8, 0u, e ? 0x3322u : 0x1100u);
+                o[2 * h4 + e] = (__byte_perm(t0, t1, sel) & ~m) | (__byte_perm(t2, t3, sel) & m);
+              }
+            }
+            *reinterpret_cast<uint4*>(vbuf + (c / 8) * (BN * 128) + swz<128>(i, (c % 8) * 16)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
       if (rebuild) {
         const float2* bt = btab + bb * HALF;
         // Rotates quarter q (pairs 16 q .. 16 q + 15: y[0..15] low dims, y[16..31]
@@ -765,8 +898,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float c = b2.x * cd - b2.y * sd;
                 const float sn = b2.y * cd + b2.x * sd;
                 const float yl = __uint_as_float(y[pp]), yh = __uint_as_float(y[16 + pp]);
-                const float bl = e ? bf16_hi(kl[w]) : bf16_lo(kl[w]);
-                const float bh = e ? bf16_hi(kh[w]) : bf16_lo(kh[w]);
+                // K_base as loaded (bf16), or K^ expanded above (fp16)
+                const float bl = CODEC ? (e ? f16_hi(kl[w]) : f16_lo(kl[w])) : (e ? bf16_hi(kl[w]) : bf16_lo(kl[w]));
+                const float bh = CODEC ? (e ? f16_hi(kh[w]) : f16_lo(kh[w])) : (e ? bf16_hi(kh[w]) : bf16_lo(kh[w]));
                 rl[e] = fmaf(yl, c, fmaf(-yh, sn, bl));
                 rh[e] = fmaf(yh, c, fmaf(yl, sn, bh));
               }
@@ -820,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* vbuf = smem + s * L::STAGE + L::off_v;
         uint8_t* lvbuf = smem + s * L::STAGE + L::off_lv;
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c)
+        for (int c = 0; c < (CODEC ? 0 : D / 8); ++c)  // a compressed tile's expansion wrote zeros already
           *reinterpret_cast<uint4*>(vbuf + (c / 8) * (BN * 128) + swz<128>(i, (c % 8) * 16)) = make_uint4(0, 0, 0, 0);
         if (use_lr) {
 #pragma unroll
@@ -908,12 +1042,16 @@ lrkv_status run(const lrkv_config& cfg, const PrefillArgs& a, cudaStream_t strea
   p.lr_groups = cfg.lr_groups;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   rope_freqs(cfg, &p.freqs);
-  CUtensorMap tb, tlk, tbr, tlr;
-  if (!make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
+  const bool codec = cfg.kv_codec == LRKV_CODEC_POLYKV;
+  p.cbase = static_cast<const uint8_t*>(a.base_pool);
+  for (int k = 0; k < 8; ++k) p.vcent[k] = polykv_codec().centroid[k];
+  CUtensorMap tb{}, tlk{}, tbr{}, tlr{};
+  // a compressed base pool is read with plain bulk copies, block by block (no tensor maps)
+  if (!codec && !make_pool_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
   if (!make_lr_map(cfg, a.lr_pool, a.num_blocks, PL<D, R>::RP, &tlk)) return LRKV_ERR_CUDA;
-  if (!make_run_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, PL<D, R>::NB, PL<D, R>::RP, &tbr, &tlr))
+  if (!codec && !make_run_maps(cfg, a.base_pool, a.lr_pool, a.num_blocks, PL<D, R>::NB, PL<D, R>::RP, &tbr, &tlr))
     return LRKV_ERR_CUDA;
-  auto kern = prefill_kernel<D, R>;
+  auto kern = codec ? prefill_kernel<D, R, true> : prefill_kernel<D, R, false>;
   constexpr int smem = PL<D, R>::total;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), smem)) return LRKV_ERR_CUDA;
   const int tiles = (a.max_q_len * p.g + BM - 1) / BM;

@@ -411,6 +411,26 @@ def codec_decode(seed: int = 0, n: int = 700, n_agents: int = 4, rank: int = 16,
     return case
 
 
+def codec_prefill_chunk(seed: int = 0, prefix: int = 16384, chunk: int = 512, n_agents: int = 4,
+                        rank: int = 16, first: int = 0) -> Case:
+    """The prefill-chunk workload (4 agents x 512 new tokens over a 16384-token
+    shared prefix) over a compressed base pool (PolyKV codec)."""
+    case = prefill_chunk(seed, prefix, chunk, n_agents, rank, first)
+    case.shape = dataclasses.replace(case.shape, kv_codec=1)
+    case.name = "prefill_chunk_codec_llama8b"
+    return case
+
+
+def codec_prefill(seed: int = 0, prefix: int = 96, chunk: int = 45, n_agents: int = 3, rank: int = 16,
+                  head_dim: int = 128) -> Case:
+    """The prefill-chunk workload at small sizes over a compressed base pool
+    (PolyKV codec): each agent's chunk over the shared prefix plus its own
+    chunk, the prefix blocks shared physically."""
+    shape = dataclasses.replace(shape_llama8b(rank, n_agents), head_dim=head_dim, kv_codec=1)
+    seqs = [Seq(0, prefix, 1 + a, prefix, chunk, a, "prefill") for a in range(n_agents)]
+    return _build("codec_prefill", shape, seed, seqs, [], list(range(n_agents)), False, (0, 0))
+
+
 def rebase_prefill(seed: int = 0, prefix: int = 16384, chunk: int = 512, n_agents: int = 4,
                    rank: int = 16, first: int = 0) -> Case:
     """The prefill-chunk workload with a re-based cache (PReCache, ReBaseShared):
@@ -444,6 +464,7 @@ SHARD_UNITS = {
     "prelr_decode_llama8b": 1,
     "rebase_prefill_llama8b": 1,
     "long_decode_codec_ministral8b": 16,
+    "prefill_chunk_codec_llama8b": 1,
 }
 
 
@@ -466,6 +487,7 @@ FULL = {
     "prelr_decode_llama8b": lambda seed=0, first=0: prelr_decode(seed, first=first),
     "rebase_prefill_llama8b": lambda seed=0, first=0: rebase_prefill(seed, first=first),
     "long_decode_codec_ministral8b": lambda seed=0, first=0: codec_long_decode(seed, first=first),
+    "prefill_chunk_codec_llama8b": lambda seed=0, first=0: codec_prefill_chunk(seed, first=first),
 }
 
 # Small variants: same layer shapes, lengths the oracle finishes in seconds,

@@ -109,6 +109,10 @@ def oracle_prefill_seq(case, p: int, q_rows: Optional[Iterable[int]] = None, w64
     L = X.shape[0]
     q = case.pre_q[a:b][q_rows].double().numpy()
     pos = np.array([L - n + k for k in q_rows])
-    out = oracle.attend(X, int(case.pre_adapter[p]), q, pos, w64, sh.n_kv_heads, sh.head_dim,
-                        sh.rope_base, scale, cache, X_lr)
+    if getattr(sh, "kv_codec", 0):
+        out = polykv.attend_codec(X, int(case.pre_adapter[p]), q, pos, w64, sh.n_kv_heads, sh.head_dim,
+                                  sh.rope_base, scale, "bf16" if cache == "bf16" else None)
+    else:
+        out = oracle.attend(X, int(case.pre_adapter[p]), q, pos, w64, sh.n_kv_heads, sh.head_dim,
+                            sh.rope_base, scale, cache, X_lr)
     return [a + k for k in q_rows], out

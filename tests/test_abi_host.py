@@ -129,9 +129,10 @@ def test_base_pool_block_bytes(lib):
     assert lrkv.base_pool_block_bytes(_cfg(kv_codec=3)) == 0
 
 
-def test_prefill_on_compressed_pool_unsupported(lib):
+def test_compressed_pool_arguments_checked(lib):
+    """A compressed pool goes through the same host checks (null seq_lens)."""
     cfg = _cfg(kv_codec=1)
     P = 1 << 20
-    pargs = [ctypes.byref(cfg), P, P, 1, 8, 8, P, 64, P, P, 4, P, P, 8, P, P, 2, 0.125, P, None, 0,
+    pargs = [ctypes.byref(cfg), P, P, 1, 8, 8, None, 64, P, P, 4, P, P, 8, P, P, 2, 0.125, P, None, 0,
              None, None]
-    assert lib.lrkv_attn_prefill(*pargs) == 2
+    assert lib.lrkv_attn_prefill(*pargs) == 1

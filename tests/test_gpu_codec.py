@@ -12,7 +12,7 @@ import oracle
 from oracle import polykv
 from rank_cache_attention_flash_b300 import inputs as I
 from rank_cache_attention_flash_b300.harness import GpuCase
-from tests.parity import BF16_TOL, _hidden, assert_close, oracle_decode_rows, weights64
+from tests.parity import BF16_TOL, _hidden, assert_close, oracle_decode_rows, oracle_prefill_seq, weights64
 
 pytestmark = pytest.mark.gpu
 NAN = float("nan")
@@ -150,12 +150,64 @@ def test_codec_decode_without_adapter_factors(cuda_lib, rank):
                      f"without {drop}")
 
 
-def test_codec_prefill_refused(cuda_lib):
-    case = I.codec_decode(rank=16, n=64)
-    g = GpuCase(case, pool_fill=0.0)
-    with pytest.raises(cuda_lib.LrkvError) as e:
-        cuda_lib.attn_prefill(g.cfg, g.dec_q[:1].contiguous(), torch.tensor([0, 1], dtype=torch.int32, device="cuda"), 1,
-                              torch.tensor([64], dtype=torch.int32, device="cuda"), 64,
-                              torch.tensor([0], dtype=torch.int32, device="cuda"), g.dec_bt, g.base_pool,
-                              g.lr_pool, g.B_K, g.B_V, g.scale)
-    assert e.value.code == 2
+@pytest.mark.parametrize("rank,d", [(16, 128), (64, 128), (8, 64), (32, 64)])
+def test_codec_prefill(cuda_lib, rank, d):
+    """Each agent's chunk over the shared prefix plus its own chunk, read from a
+    compressed pool: keys and values expanded in the rebuild warpgroup, the
+    output rotated back in the epilogue. Every row against the codec oracle."""
+    case = I.codec_prefill(prefix=160, chunk=45, n_agents=3, rank=rank, head_dim=d)
+    g = GpuCase(case, pool_fill=NAN)
+    g.setup()
+    res = g.step()
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    got, want = [], []
+    for p in range(g.n_pre):
+        rows, w = oracle_prefill_seq(case, p, cache="bf16")
+        got.append(res["prefill"][rows].double().cpu().numpy())
+        want.append(w)
+    assert_close(np.concatenate([x.reshape(-1) for x in got]), np.concatenate([x.reshape(-1) for x in want]),
+                 BF16_TOL, f"r={rank} d={d}")
+
+
+def test_codec_prefill_without_adapter_factors(cuda_lib):
+    """B_K = NULL: no rebuild; the expanded K^ is scored directly (fp16)."""
+    case = I.codec_prefill(prefix=64, chunk=33, n_agents=2, rank=16)
+    g = GpuCase(case, pool_fill=NAN)
+    g.setup()
+    g.step_append()  # the chunks' own tokens
+    w64 = weights64(case)
+    out = cuda_lib.attn_prefill(g.cfg, g.pre_q, g.pre_q_start, g.pre_max_q, g.pre_lens, g.pre_max_len,
+                                g.pre_adapter, g.pre_bt, g.base_pool, g.lr_pool, None, g.B_V, g.scale)
+    torch.cuda.synchronize()
+    w = dict(w64)
+    w["B_K"] = np.zeros_like(w["B_K"])
+    got, want = [], []
+    for p in range(g.n_pre):
+        rows, ww = oracle_prefill_seq(case, p, w64=w, cache="bf16")
+        got.append(out[rows].double().cpu().numpy())
+        want.append(ww)
+    assert_close(np.concatenate([x.reshape(-1) for x in got]), np.concatenate([x.reshape(-1) for x in want]),
+                 BF16_TOL, "without B_K")
+
+
+def test_codec_prefill_last_row_equals_decode(cuda_lib):
+    """The last row of a prefill chunk and a decode query at the same position
+    over the same compressed context agree (both read the same codes)."""
+    case = I.codec_prefill(prefix=208, chunk=17, n_agents=2, rank=16)
+    g = GpuCase(case, pool_fill=NAN)
+    g.setup()
+    res = g.step()
+    torch.cuda.synchronize()
+    for p in range(g.n_pre):
+        a, b = int(case.pre_q_start[p]), int(case.pre_q_start[p + 1])
+        q = case.pre_q[b - 1:b].to("cuda")
+        s = case.pre_seq[p]
+        L = case.seqs[s].total_len
+        dec = cuda_lib.attn_decode(g.cfg, q, torch.tensor([0, 1], dtype=torch.int32, device="cuda"),
+                                   case.pre_adapter[p:p + 1].to("cuda"), g.pre_bt[p:p + 1].contiguous(),
+                                   torch.tensor([L], dtype=torch.int32, device="cuda"), L, 1,
+                                   g.base_pool, g.lr_pool, g.B_K, g.B_V, g.scale)
+        torch.cuda.synchronize()
+        assert_close(dec.double().cpu().numpy(), res["prefill"][b - 1:b].double().cpu().numpy(), BF16_TOL,
+                     f"sequence {p}")

@@ -162,6 +162,24 @@ def test_full_codec_long_decode(cuda_lib):
     _whole([got], [want], case, "compressed long decode")
 
 
+def test_full_codec_prefill(cuda_lib):
+    """The prefill-chunk workload over a compressed base pool: all 512 rows of
+    each of the 4 agents' chunks against the codec oracle, gated per
+    configuration like the compressed long decode (per-sequence errors
+    reported)."""
+    case, g, res = _run("prefill_chunk_codec_llama8b")
+    assert case.shape.kv_codec == 1 and g.n_pre == 4
+    w64 = weights64(case)
+    got, want = [], []
+    for p in range(g.n_pre):
+        rows, w = oracle_prefill_seq(case, p, w64=w64)
+        got.append(res["prefill"][rows].double().cpu().numpy())
+        want.append(w)
+        mx, rf = errors(got[-1], want[-1])
+        print(f"prefill seq {p}: max_abs {mx:.3e} rel_fro {rf:.3e}")
+    _whole(got, want, case, "compressed prefill")
+
+
 def test_full_codec_codes(cuda_lib):
     """Every code of one 32768-token context of the compressed long decode
     against the codec oracle: keys and values, scales and norms. Codes are
