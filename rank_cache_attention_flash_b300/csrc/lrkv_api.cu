@@ -15,14 +15,23 @@
 namespace lrkv {
 
 void rope_freqs(const lrkv_config& cfg, RopeFreqs* f) {
-  std::memset(f, 0, sizeof(*f));
-  const int half = cfg.head_dim / 2;
-  for (int j = 0; j < half && j < 64; ++j) {
-    const double th = std::pow(static_cast<double>(cfg.rope_base), -2.0 * j / cfg.head_dim);
-    const float hi = static_cast<float>(th);
-    f->hi[j] = hi;
-    f->lo[j] = static_cast<float>(th - static_cast<double>(hi));
+  // the table of the last (base, d) seen by this host thread is reused
+  thread_local float last_base = 0.f;
+  thread_local int last_d = 0;
+  thread_local RopeFreqs last;
+  if (cfg.rope_base != last_base || cfg.head_dim != last_d) {
+    std::memset(&last, 0, sizeof(last));
+    const int half = cfg.head_dim / 2;
+    for (int j = 0; j < half && j < 64; ++j) {
+      const double th = std::pow(static_cast<double>(cfg.rope_base), -2.0 * j / cfg.head_dim);
+      const float hi = static_cast<float>(th);
+      last.hi[j] = hi;
+      last.lo[j] = static_cast<float>(th - static_cast<double>(hi));
+    }
+    last_base = cfg.rope_base;
+    last_d = cfg.head_dim;
   }
+  *f = last;
 }
 
 namespace {
@@ -32,9 +41,13 @@ std::atomic<int> g_decode_test_stall{0};
 int decode_test_stall() { return g_decode_test_stall.load(std::memory_order_relaxed); }
 
 int device_sm_count() {
+  thread_local int last_dev = -1, last_n = 0;
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev == last_dev) return last_n;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  last_dev = dev;
+  last_n = n;
   return n;
 }
 
@@ -49,14 +62,20 @@ bool ensure_smem_attr(const void* func, int bytes) {
   static std::mutex mu;
   static Entry done[256];
   static int n_done = 0;
+  thread_local Entry last{nullptr, -1, 0};  // this host thread's last success: no lock
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (last.func == func && last.dev == dev && last.bytes >= bytes) return true;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_done; ++i)
-    if (done[i].func == func && done[i].dev == dev && done[i].bytes >= bytes) return true;
+    if (done[i].func == func && done[i].dev == dev && done[i].bytes >= bytes) {
+      last = done[i];
+      return true;
+    }
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
     return false;
   if (n_done < 256) done[n_done++] = Entry{func, dev, bytes};
+  last = Entry{func, dev, bytes};
   return true;
 }
 
@@ -67,20 +86,74 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiled get_encoder() {
-  static EncodeTiled fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+EncodeTiled raw_encoder() {
+  static const EncodeTiled fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  }
+      return reinterpret_cast<EncodeTiled>(p);
+    return static_cast<EncodeTiled>(nullptr);
+  }();
   return fn;
 }
+
+// A tensor-map encoding is a pure function of its arguments, and every call
+// of an entry point encodes the same few maps again: each host thread keeps
+// its last 16 encodings and copies a match instead of encoding.
+CUresult encode_cached(CUtensorMap* map, CUtensorMapDataType dt, cuuint32_t rank, void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       const cuuint32_t* es, CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                       CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob) {
+  struct Key {
+    int dt, il, sw, l2, oob;
+    cuuint32_t rank;
+    const void* base;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], es[5];
+  };
+  struct Entry {
+    Key key;
+    CUtensorMap map;
+    bool valid;
+  };
+  thread_local Entry cache[16];
+  thread_local int next = 0;
+  const EncodeTiled enc = raw_encoder();
+  if (enc == nullptr) return CUDA_ERROR_NOT_INITIALIZED;
+  if (rank < 1 || rank > 5) return enc(map, dt, rank, base, dims, strides, box, es, il, sw, l2, oob);
+  Key k;
+  std::memset(&k, 0, sizeof(k));
+  k.dt = dt;
+  k.il = il;
+  k.sw = sw;
+  k.l2 = l2;
+  k.oob = oob;
+  k.rank = rank;
+  k.base = base;
+  for (cuuint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    k.es[i] = es[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  for (const Entry& e : cache)
+    if (e.valid && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
+      *map = e.map;
+      return CUDA_SUCCESS;
+    }
+  const CUresult r = enc(map, dt, rank, base, dims, strides, box, es, il, sw, l2, oob);
+  if (r == CUDA_SUCCESS) {
+    cache[next].key = k;
+    cache[next].map = *map;
+    cache[next].valid = true;
+    next = (next + 1) % 16;
+  }
+  return r;
+}
+
+EncodeTiled get_encoder() { return raw_encoder() != nullptr ? &encode_cached : nullptr; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }

@@ -296,9 +296,10 @@ def attn_decode(cfg: Config, q: torch.Tensor, ctx_q_start: torch.Tensor, adapter
     _check(out, "out", cfg.torch_dtype, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(cfg.head_dim)
-    need = decode_workspace_bytes(cfg, nq, num_ctx, max_ctx_len, max_q_per_ctx)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace is None:  # a workspace passed in is checked by the library (LRKV_ERR_WORKSPACE)
+        need = decode_workspace_bytes(cfg, nq, num_ctx, max_ctx_len, max_q_per_ctx)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     n_adapters = 0 if B_K is None and B_V is None else (B_K if B_K is not None else B_V).shape[0]
     code = lib.lrkv_attn_decode(
         ctypes.byref(cfg), _ptr(q), nq, _ptr(ctx_q_start), num_ctx, _ptr(adapter_ids),
