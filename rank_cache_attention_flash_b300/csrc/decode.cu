@@ -150,7 +150,8 @@ enum : int {
   B_PR = 14,     // [2] O^T and O_lr^T MMAs of that P buffer complete (two commits)
   B_DRAIN = 16,  // [4] per MMA warp, on abort: its MMAs have completed
   B_TEST = 20,   // test only: a barrier nothing arrives at (a bounded wait that must run out)
-  B_COUNT = 21
+  B_GK = 21,     // the item's B_K rows landed in the G rows (TMA bytes)
+  B_COUNT = 22
 };
 
 __device__ __forceinline__ uint32_t bar_count(int i) {
@@ -221,7 +222,8 @@ template <int D, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeParams p,
                   const __grid_constant__ CUtensorMap tm_base,
-                  const __grid_constant__ CUtensorMap tm_lr) {
+                  const __grid_constant__ CUtensorMap tm_lr,
+                  const __grid_constant__ CUtensorMap tm_bk) {
   using L = DL<D, R>;
   constexpr int HALF = D / 2;
   constexpr int KS = D / 16;  // k-steps over the head dims (and over u)
@@ -370,6 +372,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  // Warp 1 (lane = item row): each row's B_K rows of its adapter, R rows of
+  // d dims, by TMA straight into that row's G rows [r R, r R + R), 128-byte
+  // swizzle like G. G is then built in place from shared memory. A row with
+  // no adapter (or an id the combine reports as bad) gets a zero G row.
+  bool gk_issued = false;
+  if (warp == 1 && p.has_bk) {
+    const bool ld = lane < nrows && a_row >= 0 && a_row < p.n_adapters;
+    const uint32_t m = __ballot_sync(0xffffffffu, ld);
+    gk_issued = m != 0;
+    if (gk_issued) {
+      if (lane == 0) mbar_arrive_expect_tx(bar(B_GK), __popc(m) * (R * D * 2));
+      __syncwarp();
+      if (ld) {
+#pragma unroll
+        for (int c = 0; c < L::KATOMS; ++c)
+          tma_load_3d(sbase + L::off_g + c * L::GAMMA_ATOM + lane * (R * 128), &tm_bk, 64 * c, head, a_row * R,
+                      bar(B_GK));
+      }
+    }
+  }
+
   // ============================================================ producer
   // Items in the order K_0, K_1, V_0, K_2, V_1, ...: each K tile is requested
   // a tile ahead of the V tile before it, so V tiles (consumed last) do not
@@ -481,53 +504,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < kMaxRows; ++r) use_w |= row_ad[r] >= 0;
     const int nw = ((nrows * R + 15) / 16) * 16;
 
-    // G (fp16, K-major over u, 128-byte swizzle) for rows n = row * R + k < nw;
-    // one row per thread, its B_K row loaded in one burst
+    // G (fp16, K-major over u, 128-byte swizzle) for rows n = row * R + k < nw,
+    // one row per thread, in place over the B_K row that the TMA left there:
+    // chunk pair (jc, d/16 + jc) of the row becomes (G_c, G_s) of the same pair.
     if (use_w) {
       const int n = tid - 32;
       if (n < nw) {
-        const int r = n / R, k = n % R;
-        const int a = row_ad[r];
+        const int r = n / R;
         uint8_t* grow = smem + L::off_g + n * 128;
-        if (a >= 0) {
-          const uint4* brow = reinterpret_cast<const uint4*>(
-              p.B_K + ((static_cast<int64_t>(a) * R + k) * p.Hkv + head) * D);
-          const int gr = row0 + r;
-          const uint4* qrow = reinterpret_cast<const uint4*>(
-              p.q + (static_cast<int64_t>(qs + gr / p.g) * p.Hq + head * p.g + gr % p.g) * D);
-          uint4 bv[D / 8], qv2[D / 8];
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            bv[c] = __ldg(brow + c);
-            qv2[c] = __ldg(qrow + c);
+        bool have = row_ad[r] >= 0;
+        if (have && !wait_ab(bar(B_GK), 0, p.status, abort_flag)) {
+          *abort_flag = 1;
+          have = false;
+        }
+        const uint8_t* qrow = smem + L::off_q + r * 128;
+#pragma unroll 2
+        for (int jc = 0; jc < HALF / 8; ++jc) {
+          const int c2 = HALF / 8 + jc;
+          uint4* pa = reinterpret_cast<uint4*>(grow + (jc >> 3) * L::GAMMA_ATOM + (((jc & 7) ^ (n & 7)) << 4));
+          uint4* pb = reinterpret_cast<uint4*>(grow + (c2 >> 3) * L::GAMMA_ATOM + (((c2 & 7) ^ (n & 7)) << 4));
+          if (!have) {
+            *pa = make_uint4(0u, 0u, 0u, 0u);
+            *pb = make_uint4(0u, 0u, 0u, 0u);
+            continue;
           }
+          const uint4 q1 = *reinterpret_cast<const uint4*>(qrow + (jc >> 3) * (kMaxRows * 128) + (((jc & 7) ^ (r & 7)) << 4));
+          const uint4 q2 = *reinterpret_cast<const uint4*>(qrow + (c2 >> 3) * (kMaxRows * 128) + (((c2 & 7) ^ (r & 7)) << 4));
+          const uint4 b1 = *pa, b2 = *pb;
+          const uint32_t qa[4] = {q1.x, q1.y, q1.z, q1.w};
+          const uint32_t qb[4] = {q2.x, q2.y, q2.z, q2.w};
+          const uint32_t ba[4] = {b1.x, b1.y, b1.z, b1.w};
+          const uint32_t bb[4] = {b2.x, b2.y, b2.z, b2.w};
+          uint32_t gc[4], gs[4];
 #pragma unroll
-          for (int jc = 0; jc < HALF / 8; ++jc) {
-            const int c2 = HALF / 8 + jc;
-            const uint32_t qa[4] = {qv2[jc].x, qv2[jc].y, qv2[jc].z, qv2[jc].w};
-            const uint32_t qb[4] = {qv2[c2].x, qv2[c2].y, qv2[c2].z, qv2[c2].w};
-            const uint32_t ba[4] = {bv[jc].x, bv[jc].y, bv[jc].z, bv[jc].w};
-            const uint32_t bb[4] = {bv[c2].x, bv[c2].y, bv[c2].z, bv[c2].w};
-            uint32_t gc[4], gs[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float q1l = bf16_lo(qa[e]), q1h = bf16_hi(qa[e]);
-              const float q2l = bf16_lo(qb[e]), q2h = bf16_hi(qb[e]);
-              const float b1l = bf16_lo(ba[e]), b1h = bf16_hi(ba[e]);
-              const float b2l = bf16_lo(bb[e]), b2h = bf16_hi(bb[e]);
-              gc[e] = pack_f16(fmaf(q1l, b1l, q2l * b2l), fmaf(q1h, b1h, q2h * b2h));
-              gs[e] = pack_f16(fmaf(q2l, b1l, -(q1l * b2l)), fmaf(q2h, b1h, -(q1h * b2h)));
-            }
-            *reinterpret_cast<uint4*>(grow + (jc >> 3) * L::GAMMA_ATOM + (((jc & 7) ^ (n & 7)) << 4)) =
-                make_uint4(gc[0], gc[1], gc[2], gc[3]);
-            *reinterpret_cast<uint4*>(grow + (c2 >> 3) * L::GAMMA_ATOM + (((c2 & 7) ^ (n & 7)) << 4)) =
-                make_uint4(gs[0], gs[1], gs[2], gs[3]);
+          for (int e = 0; e < 4; ++e) {
+            const float q1l = bf16_lo(qa[e]), q1h = bf16_hi(qa[e]);
+            const float q2l = bf16_lo(qb[e]), q2h = bf16_hi(qb[e]);
+            const float b1l = bf16_lo(ba[e]), b1h = bf16_hi(ba[e]);
+            const float b2l = bf16_lo(bb[e]), b2h = bf16_hi(bb[e]);
+            gc[e] = pack_f16(fmaf(q1l, b1l, q2l * b2l), fmaf(q1h, b1h, q2h * b2h));
+            gs[e] = pack_f16(fmaf(q2l, b1l, -(q1l * b2l)), fmaf(q2h, b1h, -(q1h * b2h)));
           }
-        } else {
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c)
-            *reinterpret_cast<uint4*>(grow + (c >> 3) * L::GAMMA_ATOM + (((c & 7) ^ (n & 7)) << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
+          *pa = make_uint4(gc[0], gc[1], gc[2], gc[3]);
+          *pb = make_uint4(gs[0], gs[1], gs[2], gs[3]);
         }
       }
     }
@@ -936,6 +955,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before();
   __syncthreads();
   if (warp == 1) {
+    // no B_K copy may still be landing when the CTA leaves (an aborted item
+    // may have skipped its wait)
+    if (gk_issued && lane == 0) wait_ab(bar(B_GK), 0, p.status, nullptr);
+    __syncwarp();
     tc::fence_after();
     tc::dealloc(tbase, kTmemCols);
   }
@@ -1031,7 +1054,8 @@ template <int D, int R, bool CODEC>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_rb_kernel(const __grid_constant__ DecodeParams p,
                      const __grid_constant__ CUtensorMap tm_base,
-                     const __grid_constant__ CUtensorMap tm_lr) {
+                     const __grid_constant__ CUtensorMap tm_lr,
+                     const __grid_constant__ CUtensorMap /* B_K map: G mode only */) {
   using L = rb::Layout<D, R>;
   using namespace rb;
   constexpr int HALF = D / 2;
@@ -1953,15 +1977,17 @@ lrkv_status run(const lrkv_config& cfg, const DecodeArgs& a, const DecodePlan& p
   for (int k = 0; k < 8; ++k) p.vcent[k] = polykv_codec().centroid[k];
   rope_freqs(cfg, &p.freqs);
 
-  CUtensorMap tb{}, tl;
+  CUtensorMap tb{}, tl, tk{};
   // a compressed base pool is read with plain bulk copies (no tensor map)
   if (!p.codec && !make_pool_maps(cfg, a.base_pool, nullptr, a.num_blocks, &tb, nullptr)) return LRKV_ERR_CUDA;
   if (!make_lr_map(cfg, a.lr_pool, a.num_blocks, L::RP, &tl)) return LRKV_ERR_CUDA;
+  // G mode copies each item's B_K rows with a tensor map
+  if (!plan.rebuild && p.has_bk && !make_bk_map(cfg, a.B_K, a.n_adapters, &tk)) return LRKV_ERR_CUDA;
 
   if (plan.n_items > 0) {
     auto kern = !plan.rebuild ? decode_kernel<D, R> : p.codec ? decode_rb_kernel<D, R, true> : decode_rb_kernel<D, R, false>;
     if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), plan.smem_bytes)) return LRKV_ERR_CUDA;
-    kern<<<static_cast<unsigned>(plan.n_items), kThreads, plan.smem_bytes, stream>>>(p, tb, tl);
+    kern<<<static_cast<unsigned>(plan.n_items), kThreads, plan.smem_bytes, stream>>>(p, tb, tl, tk);
     if (cudaGetLastError() != cudaSuccess) return LRKV_ERR_CUDA;
   }
   CombineParams c{};

@@ -302,6 +302,20 @@ bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_bk_map(const lrkv_config& cfg, const void* B_K, int n_adapters, CUtensorMap* map) {
+  EncodeTiled enc = get_encoder();
+  if (enc == nullptr || n_adapters < 1) return false;
+  const cuuint64_t d = static_cast<cuuint64_t>(cfg.head_dim);
+  const cuuint64_t dims[3] = {d, static_cast<cuuint64_t>(cfg.n_kv_heads),
+                              static_cast<cuuint64_t>(n_adapters) * cfg.rank};
+  const cuuint64_t strides[2] = {d * 2, d * 2 * cfg.n_kv_heads};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(cfg.rank)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(B_K), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D maps that load a run of `nb` consecutive blocks of one (K|V, kv head)
 // chunk, or of one low-rank plane, in a single copy. Base pool dims: (d,
 // 16 rows, 2 * Hkv chunks of a block, blocks), box {64, 16, 1, nb}; low-rank

@@ -87,6 +87,10 @@ bool make_bf16_2d_map(const void* base, int64_t inner, int64_t rows, int64_t row
 // Low-rank pool map with a box of box_cols (>= rank) columns, zero-filled past the rank.
 bool make_lr_map(const lrkv_config& cfg, const void* lr_pool, int64_t num_blocks, int box_cols,
                  CUtensorMap* lr_map);
+// 3-D map over B_K [n_adapters][rank][Hkv][d] (bf16) with box {64, 1, rank}:
+// one copy brings one adapter's rank rows of one kv head, 64 dims wide, as
+// rank consecutive 128-byte rows with the 128-byte swizzle.
+bool make_bk_map(const lrkv_config& cfg, const void* B_K, int n_adapters, CUtensorMap* map);
 // 4-D maps copying a run of nb consecutive blocks per copy (base: one K|V
 // chunk of one kv head; low-rank: one plane), box width lr_cols for the
 // low-rank pool.
