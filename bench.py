@@ -7,7 +7,9 @@
 One step = one pass of the hot path over one batch of a workload, inputs
 already resident in HBM: for the decode workloads the decode call; for the
 prefill workload the append of the new chunk tokens plus the causal prefill;
-for the mixed batch append + decode + prefill. With ``--config all`` (the
+for the mixed batch the append, then the decode and the prefill in one
+``lrkv_attn_mixed`` call (the two run concurrently); its decode and prefill are
+also timed alone, in a second loop, for their rooflines. With ``--config all`` (the
 default) every bf16 workload is timed in turn in one process and reported under
 ``workloads.<name>``; the line's headline fields (value, roofline, e2e,
 cpu_baseline) are those of the shared-context decode (Llama-3.1-8B-shaped
@@ -452,30 +454,34 @@ def time_workload(name, args, world, rank, dev, pk):
     dominant = "decode" if "decode" in model else "prefill"
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    calls = {"append": g.step_append, "decode": g.decode, "prefill": g.prefill}
+    calls = {"append": g.step_append, "decode": g.decode, "prefill": g.prefill, "mixed": g.mixed}
+    # a step with both decode and prefill makes them one mixed call
+    mixed = "decode" in kinds and "prefill" in kinds
+    step_kinds = [k for k in kinds if not (mixed and k in ("decode", "prefill"))] + (["mixed"] if mixed else [])
+    alone = ["decode", "prefill"] if mixed else []
 
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
-        for k in kinds:
+        for k in step_kinds + alone:
             calls[k]()
     torch.cuda.synchronize()
     # Each part of the step is captured once into a CUDA graph and replayed in
     # the timed loop: the replay keeps host launch latency out of the device
     # timings (the kernels and their arguments are exactly the API call's).
     graphs = {}
-    for k in kinds:
+    for k in step_kinds + alone:
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr):
             calls[k]()
         graphs[k] = gr
     for i in range(3):
         flush.fill_(i & 0xFF)
-        for k in kinds:
+        for k in step_kinds + alone:
             graphs[k].replay()
     torch.cuda.synchronize()
     K = args.steps
-    evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in kinds}
-           for _ in range(K)]
+    evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for k in step_kinds + alone} for _ in range(K)]
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         import torch.distributed as dist
@@ -487,17 +493,26 @@ def time_workload(name, args, world, rank, dev, pk):
         for i in range(K):
             flush.fill_(i & 0xFF)
             step_ev[i][0].record(stream)
-            for k in kinds:
+            for k in step_kinds:
                 evs[i][k][0].record(stream)
                 graphs[k].replay()
                 evs[i][k][1].record(stream)
             step_ev[i][1].record(stream)
         torch.cuda.synchronize()
-    host_dt = time.perf_counter() - host_t0
+        host_dt = time.perf_counter() - host_t0
+        # the mixed call's two parts alone (each after its own flush), for
+        # their rooflines; not part of the step time
+        for i in range(K if alone else 0):
+            for k in alone:
+                flush.fill_(i & 0xFF)
+                evs[i][k][0].record(stream)
+                graphs[k].replay()
+                evs[i][k][1].record(stream)
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    part_ms = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in evs) / K for k in kinds}
+    part_ms = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in evs) / K for k in step_kinds + alone}
     ms_per_step = reduce_step_time(sum(step_ms), K, world, dev)
     status = g.device_status()
     del graphs
@@ -516,7 +531,7 @@ def time_workload(name, args, world, rank, dev, pk):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         g.upload_inputs()
-        for k in kinds:
+        for k in step_kinds:
             calls[k]()
         g.download_outputs()
         b.record(stream)
@@ -551,6 +566,10 @@ def time_workload(name, args, world, rank, dev, pk):
         if pk.get("bf16_tflops_sustained"):
             parts[k]["frac_tensor_sustained"] = parts[k]["TFLOP/s"] / pk["bf16_tflops_sustained"]
         parts[k]["roofline"] = part_roofline(k, name, m, ms, pk)
+    if mixed:
+        parts["mixed"] = {"ms": part_ms["mixed"], "decode_and_prefill_alone_ms": part_ms["decode"] + part_ms["prefill"],
+                          "note": "the step's decode and prefill in one lrkv_attn_mixed call, run concurrently; "
+                                  "the decode and prefill entries are the same calls timed alone"}
     roof = parts[dominant]["roofline"]
     sh = case.shape
     entry = {
@@ -564,6 +583,7 @@ def time_workload(name, args, world, rank, dev, pk):
                    "parallelism": f"weak x{world}: rank {rank} holds its own share of the contexts"},
         "roofline": roof, "parts": parts, "e2e": e2e,
         "gpu_launches": K * sum(LAUNCHES_PER_CALL[k] for k in kinds),
+        **({"gpu_launches_parts_alone": K * sum(LAUNCHES_PER_CALL[k] for k in alone)} if alone else {}),
         "clocks": clk.summary(), "device_status": status, "host_s": host_dt,
     }
     if args.no_bk:

@@ -279,6 +279,72 @@ size_t lrkv_prefill_workspace_bytes(const lrkv_config* cfg, int32_t num_seqs, in
                                     int32_t max_q_len, int32_t max_seq_len);
 
 /*
+ * lrkv_attn_mixed -- one call for a mixed batch: decode queries and causal
+ * prefill chunks over the same pools and adapters.
+ *
+ * Defines: Efficient Multi-Adapter LLM Serving via Cross-Model KV-Cache Reuse
+ * with Activated LoRA, "Builds on" (SARATHI: decodes piggybacked on chunked
+ * prefills in one batch); PReCache, Figure 4 (serving, where agents' prefills
+ * and decodes share the GPU). Each part computes exactly what
+ * lrkv_attn_decode and lrkv_attn_prefill compute for it: the result is
+ * bitwise that of the two calls made one after the other.
+ *
+ * The two parts run at the same time: the prefill on `stream`, the decode on
+ * a second stream of the library's own, forked from `stream` by an event and
+ * joined back to it by another before the call returns, so work queued on
+ * `stream` afterwards sees both outputs. The decode's CTAs then take the SMs
+ * the prefill grid leaves idle in its last wave. The second stream and the
+ * two events are created on the first mixed call of each host thread on each
+ * device and kept until the process exits. The call may be captured into a
+ * CUDA graph (the fork and the join become graph edges).
+ *
+ *   dec, pre   either may be NULL or describe an empty batch (num_queries or
+ *              num_ctx 0; num_seqs or total_q 0); with one part empty the
+ *              other runs on `stream` alone.
+ *   Fields of lrkv_decode_batch and lrkv_prefill_batch: as the arguments of
+ *   the same names of lrkv_attn_decode and lrkv_attn_prefill; the pools,
+ *   the adapter factors, n_adapters, scale and dev_status are shared.
+ *
+ * Errors: both parts are checked before anything is launched; the first
+ * failing check's status is returned (decode first) and nothing runs.
+ * LRKV_ERR_CUDA if the second stream or its events cannot be made.
+ */
+typedef struct lrkv_decode_batch {
+  const void* q;
+  int32_t num_queries;
+  const int32_t* ctx_q_start;
+  int32_t num_ctx;
+  const int32_t* adapter_ids;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* ctx_lens;
+  int32_t max_ctx_len;
+  int32_t max_q_per_ctx;
+  void* out;
+  void* workspace;
+  size_t workspace_bytes;
+} lrkv_decode_batch;
+
+typedef struct lrkv_prefill_batch {
+  const void* q;
+  const int32_t* q_start;
+  int32_t num_seqs;
+  int32_t total_q;
+  int32_t max_q_len;
+  const int32_t* seq_lens;
+  int32_t max_seq_len;
+  const int32_t* adapter_ids;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  void* out;
+} lrkv_prefill_batch;
+
+lrkv_status lrkv_attn_mixed(const lrkv_config* cfg, const lrkv_decode_batch* dec,
+                            const lrkv_prefill_batch* pre, const void* base_pool, const void* lr_pool,
+                            int64_t num_blocks, const void* B_K, const void* B_V, int32_t n_adapters,
+                            float scale, int32_t* dev_status, lrkv_stream_t stream);
+
+/*
  * lrkv_attn_decode_noalloc -- lrkv_attn_decode for callers that cannot
  * allocate device memory.
  *

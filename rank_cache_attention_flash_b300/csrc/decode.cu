@@ -811,12 +811,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tt < HALF / 2 && j + 2 < ntiles) btab[b * HALF + jb + tt] = rope_cos_sin_fast(t0 + 2 * kBT, th_hi, th_lo);
 
-        // ---- online softmax over the tile's tokens (log2 units), own rows
+        // ---- online softmax over the tile's tokens (log2 units), own rows.
+        // Rows past the item's last row read W columns past nw, which hold
+        // whatever an earlier kernel left in tensor memory: they are masked
+        // here, so that they take no part in the rescale vote.
         const bool tok_ok = ((vmask >> (tt >> 4)) & 1) != 0 && t0 + tt < len;
         bool need = false;
 #pragma unroll
         for (int r = 0; r < RH; ++r) {
-          sc[r] = tok_ok ? sc[r] * p.scale_log2 : -CUDART_INF_F;
+          sc[r] = (tok_ok && rb + r < nrows) ? sc[r] * p.scale_log2 : -CUDART_INF_F;
           need |= sc[r] > m_run[r] + kRescaleLog2;
         }
         if (*abort_flag != 0) failed = true;

@@ -375,7 +375,7 @@ const char* lrkv_status_string(lrkv_status s) {
   return "LRKV_UNKNOWN_STATUS";
 }
 
-int32_t lrkv_version(void) { return 20100; }
+int32_t lrkv_version(void) { return 20200; }
 
 size_t lrkv_base_pool_block_bytes(const lrkv_config* cfg) {
   if (check_config(cfg) != LRKV_OK) return 0;
@@ -445,14 +445,27 @@ size_t lrkv_decode_workspace_bytes(const lrkv_config* cfg, int32_t num_queries, 
   return plan.ws_bytes;
 }
 
-lrkv_status lrkv_attn_decode(const lrkv_config* cfg, const void* q, int32_t num_queries,
-                             const int32_t* ctx_q_start, int32_t num_ctx,
-                             const int32_t* adapter_ids, const int32_t* block_tables,
-                             int32_t max_blocks, const int32_t* ctx_lens, int32_t max_ctx_len,
-                             int32_t max_q_per_ctx, const void* base_pool, const void* lr_pool,
-                             int64_t num_blocks, const void* B_K, const void* B_V,
-                             int32_t n_adapters, float scale, void* out, void* workspace,
-                             size_t workspace_bytes, int32_t* dev_status, lrkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// A validated decode call, ready to launch (empty: nothing to do).
+struct DecodeCall {
+  bool empty = true;
+  bool fp32 = false;
+  DecodeArgs a{};
+  DecodePlan plan{};
+  int max_q_per_ctx = 0;
+  void* workspace = nullptr;
+};
+
+lrkv_status prepare_decode(const lrkv_config* cfg, const void* q, int32_t num_queries,
+                           const int32_t* ctx_q_start, int32_t num_ctx, const int32_t* adapter_ids,
+                           const int32_t* block_tables, int32_t max_blocks, const int32_t* ctx_lens,
+                           int32_t max_ctx_len, int32_t max_q_per_ctx, const void* base_pool,
+                           const void* lr_pool, int64_t num_blocks, const void* B_K, const void* B_V,
+                           int32_t n_adapters, float scale, void* out, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, DecodeCall* c) {
   lrkv_status st = check_config(cfg);
   if (st != LRKV_OK) return st;
   if (num_queries < 0 || num_ctx < 0 || n_adapters < 0 || max_ctx_len < 0 || max_q_per_ctx < 0)
@@ -472,19 +485,128 @@ lrkv_status lrkv_attn_decode(const lrkv_config* cfg, const void* q, int32_t num_
   if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
   if (static_cast<int64_t>(max_ctx_len) > static_cast<int64_t>(max_blocks) * kBlock)
     return LRKV_ERR_INVALID_ARG;
-  DecodeArgs a{q, num_queries, ctx_q_start, num_ctx, adapter_ids, block_tables, max_blocks,
-               ctx_lens, max_ctx_len, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters,
-               scale, out, dev_status};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cfg->dtype == LRKV_FP32) return launch_decode_fp32(*cfg, a, max_q_per_ctx, s);
-  const int sms = device_sm_count();
-  if (sms <= 0) return LRKV_ERR_CUDA;
-  DecodePlan plan;
-  if (!plan_decode_bf16(*cfg, num_queries, num_ctx, max_ctx_len, max_q_per_ctx, sms, &plan))
-    return LRKV_ERR_UNSUPPORTED;
-  if (workspace == nullptr || workspace_bytes < plan.ws_bytes || !aligned16(workspace))
-    return LRKV_ERR_WORKSPACE;
-  return launch_decode_bf16(*cfg, a, plan, workspace, s);
+  c->a = DecodeArgs{q, num_queries, ctx_q_start, num_ctx, adapter_ids, block_tables, max_blocks,
+                    ctx_lens, max_ctx_len, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters,
+                    scale, out, dev_status};
+  c->max_q_per_ctx = max_q_per_ctx;
+  c->fp32 = cfg->dtype == LRKV_FP32;
+  if (!c->fp32) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return LRKV_ERR_CUDA;
+    if (!plan_decode_bf16(*cfg, num_queries, num_ctx, max_ctx_len, max_q_per_ctx, sms, &c->plan))
+      return LRKV_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < c->plan.ws_bytes || !aligned16(workspace))
+      return LRKV_ERR_WORKSPACE;
+    c->workspace = workspace;
+  }
+  c->empty = false;
+  return LRKV_OK;
+}
+
+lrkv_status launch_decode_call(const lrkv_config& cfg, const DecodeCall& c, cudaStream_t s) {
+  if (c.empty) return LRKV_OK;
+  if (c.fp32) return launch_decode_fp32(cfg, c.a, c.max_q_per_ctx, s);
+  return launch_decode_bf16(cfg, c.a, c.plan, c.workspace, s);
+}
+
+// A validated prefill call, ready to launch (empty: nothing to do).
+struct PrefillCall {
+  bool empty = true;
+  bool fp32 = false;
+  PrefillArgs a{};
+};
+
+lrkv_status prepare_prefill(const lrkv_config* cfg, const void* q, const int32_t* q_start,
+                            int32_t num_seqs, int32_t total_q, int32_t max_q_len,
+                            const int32_t* seq_lens, int32_t max_seq_len, const int32_t* adapter_ids,
+                            const int32_t* block_tables, int32_t max_blocks, const void* base_pool,
+                            const void* lr_pool, int64_t num_blocks, const void* B_K, const void* B_V,
+                            int32_t n_adapters, float scale, void* out, int32_t* dev_status,
+                            PrefillCall* c) {
+  lrkv_status st = check_config(cfg);
+  if (st != LRKV_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0 || n_adapters < 0)
+    return LRKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return LRKV_OK;
+  if (q == nullptr || q_start == nullptr || seq_lens == nullptr || adapter_ids == nullptr ||
+      block_tables == nullptr || out == nullptr)
+    return LRKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(q_start) || !aligned4(seq_lens) ||
+      !aligned4(adapter_ids) || !aligned4(block_tables))
+    return LRKV_ERR_INVALID_ARG;
+  if ((B_K != nullptr && !aligned16(B_K)) || (B_V != nullptr && !aligned16(B_V)))
+    return LRKV_ERR_INVALID_ARG;
+  if ((B_K != nullptr || B_V != nullptr) && n_adapters == 0) return LRKV_ERR_INVALID_ARG;
+  if (cfg->lr_groups > 1 && n_adapters > cfg->lr_groups) return LRKV_ERR_INVALID_ARG;
+  if (max_q_len < 1 || max_seq_len < max_q_len || !(scale == scale)) return LRKV_ERR_INVALID_ARG;
+  if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * kBlock)
+    return LRKV_ERR_INVALID_ARG;
+  c->a = PrefillArgs{q, q_start, num_seqs, total_q, max_q_len, seq_lens, max_seq_len, adapter_ids,
+                     block_tables, max_blocks, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters,
+                     scale, out, dev_status};
+  c->fp32 = cfg->dtype == LRKV_FP32;
+  c->empty = false;
+  return LRKV_OK;
+}
+
+lrkv_status launch_prefill_call(const lrkv_config& cfg, const PrefillCall& c, cudaStream_t s) {
+  if (c.empty) return LRKV_OK;
+  if (c.fp32) return launch_prefill_fp32(cfg, c.a, s);
+  return launch_prefill_bf16(cfg, c.a, s);
+}
+
+// The second stream of a mixed call and its two events, one set per device
+// and host thread, created on first use and kept (a stream and two events of
+// each device this thread calls on).
+struct ForkJoin {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+};
+
+ForkJoin* fork_join() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  thread_local ForkJoin fj[64];
+  ForkJoin& f = fj[dev];
+  if (!f.ok) {
+    if (f.side == nullptr && cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) != cudaSuccess) {
+      f.side = nullptr;
+      return nullptr;
+    }
+    if (f.fork == nullptr && cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess) {
+      f.fork = nullptr;
+      return nullptr;
+    }
+    if (f.join == nullptr && cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess) {
+      f.join = nullptr;
+      return nullptr;
+    }
+    f.ok = true;
+  }
+  return &f;
+}
+
+}  // namespace
+
+extern "C" {
+
+lrkv_status lrkv_attn_decode(const lrkv_config* cfg, const void* q, int32_t num_queries,
+                             const int32_t* ctx_q_start, int32_t num_ctx,
+                             const int32_t* adapter_ids, const int32_t* block_tables,
+                             int32_t max_blocks, const int32_t* ctx_lens, int32_t max_ctx_len,
+                             int32_t max_q_per_ctx, const void* base_pool, const void* lr_pool,
+                             int64_t num_blocks, const void* B_K, const void* B_V,
+                             int32_t n_adapters, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, lrkv_stream_t stream) {
+  DecodeCall c;
+  const lrkv_status st = prepare_decode(cfg, q, num_queries, ctx_q_start, num_ctx, adapter_ids, block_tables,
+                                        max_blocks, ctx_lens, max_ctx_len, max_q_per_ctx, base_pool, lr_pool,
+                                        num_blocks, B_K, B_V, n_adapters, scale, out, workspace,
+                                        workspace_bytes, dev_status, &c);
+  if (st != LRKV_OK) return st;
+  return launch_decode_call(*cfg, c, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t lrkv_prefill_workspace_bytes(const lrkv_config* cfg, int32_t num_seqs, int32_t total_q,
@@ -507,31 +629,54 @@ lrkv_status lrkv_attn_prefill(const lrkv_config* cfg, const void* q, const int32
                               size_t workspace_bytes, int32_t* dev_status, lrkv_stream_t stream) {
   (void)workspace;
   (void)workspace_bytes;
+  PrefillCall c;
+  const lrkv_status st = prepare_prefill(cfg, q, q_start, num_seqs, total_q, max_q_len, seq_lens, max_seq_len,
+                                         adapter_ids, block_tables, max_blocks, base_pool, lr_pool, num_blocks,
+                                         B_K, B_V, n_adapters, scale, out, dev_status, &c);
+  if (st != LRKV_OK) return st;
+  return launch_prefill_call(*cfg, c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lrkv_status lrkv_attn_mixed(const lrkv_config* cfg, const lrkv_decode_batch* dec,
+                            const lrkv_prefill_batch* pre, const void* base_pool, const void* lr_pool,
+                            int64_t num_blocks, const void* B_K, const void* B_V, int32_t n_adapters,
+                            float scale, int32_t* dev_status, lrkv_stream_t stream) {
+  DecodeCall dc;
+  PrefillCall pc;
   lrkv_status st = check_config(cfg);
   if (st != LRKV_OK) return st;
-  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_seq_len < 0 || n_adapters < 0)
-    return LRKV_ERR_INVALID_ARG;
-  if (num_seqs == 0 || total_q == 0) return LRKV_OK;
-  if (q == nullptr || q_start == nullptr || seq_lens == nullptr || adapter_ids == nullptr ||
-      block_tables == nullptr || out == nullptr)
-    return LRKV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out) || !aligned4(q_start) || !aligned4(seq_lens) ||
-      !aligned4(adapter_ids) || !aligned4(block_tables))
-    return LRKV_ERR_INVALID_ARG;
-  if ((B_K != nullptr && !aligned16(B_K)) || (B_V != nullptr && !aligned16(B_V)))
-    return LRKV_ERR_INVALID_ARG;
-  if ((B_K != nullptr || B_V != nullptr) && n_adapters == 0) return LRKV_ERR_INVALID_ARG;
-  if (cfg->lr_groups > 1 && n_adapters > cfg->lr_groups) return LRKV_ERR_INVALID_ARG;
-  if (max_q_len < 1 || max_seq_len < max_q_len || !(scale == scale)) return LRKV_ERR_INVALID_ARG;
-  if ((st = check_pool(*cfg, base_pool, lr_pool, num_blocks, max_blocks)) != LRKV_OK) return st;
-  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks) * kBlock)
-    return LRKV_ERR_INVALID_ARG;
-  PrefillArgs a{q, q_start, num_seqs, total_q, max_q_len, seq_lens, max_seq_len, adapter_ids,
-                block_tables, max_blocks, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters,
-                scale, out, dev_status};
+  if (dec != nullptr &&
+      (st = prepare_decode(cfg, dec->q, dec->num_queries, dec->ctx_q_start, dec->num_ctx, dec->adapter_ids,
+                           dec->block_tables, dec->max_blocks, dec->ctx_lens, dec->max_ctx_len,
+                           dec->max_q_per_ctx, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters, scale,
+                           dec->out, dec->workspace, dec->workspace_bytes, dev_status, &dc)) != LRKV_OK)
+    return st;
+  if (pre != nullptr &&
+      (st = prepare_prefill(cfg, pre->q, pre->q_start, pre->num_seqs, pre->total_q, pre->max_q_len,
+                            pre->seq_lens, pre->max_seq_len, pre->adapter_ids, pre->block_tables,
+                            pre->max_blocks, base_pool, lr_pool, num_blocks, B_K, B_V, n_adapters, scale,
+                            pre->out, dev_status, &pc)) != LRKV_OK)
+    return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cfg->dtype == LRKV_FP32) return launch_prefill_fp32(*cfg, a, s);
-  return launch_prefill_bf16(*cfg, a, s);
+  if (dc.empty || pc.empty) {
+    if ((st = launch_prefill_call(*cfg, pc, s)) != LRKV_OK) return st;
+    return launch_decode_call(*cfg, dc, s);
+  }
+  // Both parts: the prefill on the caller's stream, the decode on a second
+  // stream forked from it and joined back, so that the decode's CTAs fill the
+  // SMs the prefill grid leaves idle (its last partial wave) instead of
+  // waiting for the whole prefill.
+  ForkJoin* fj = fork_join();
+  if (fj == nullptr) return LRKV_ERR_CUDA;
+  if (cudaEventRecord(fj->fork, s) != cudaSuccess || cudaStreamWaitEvent(fj->side, fj->fork, 0) != cudaSuccess)
+    return LRKV_ERR_CUDA;
+  const lrkv_status sp = launch_prefill_call(*cfg, pc, s);
+  const lrkv_status sd = launch_decode_call(*cfg, dc, fj->side);
+  // the join is recorded whatever the launches returned, so the caller's
+  // stream never runs ahead of work still queued on the second stream
+  if (cudaEventRecord(fj->join, fj->side) != cudaSuccess || cudaStreamWaitEvent(s, fj->join, 0) != cudaSuccess)
+    return LRKV_ERR_CUDA;
+  return sp != LRKV_OK ? sp : sd;
 }
 
 }  // extern "C"

@@ -201,9 +201,27 @@ class GpuCase:
                                  self.base_pool, self.lr_pool, self.attn_B_K, self.B_V, self.scale,
                                  out=self.pre_out, status=self.status, stream=stream)
 
+    def mixed(self, stream=None):
+        """The decode and the prefill of this step in one lrkv_attn_mixed call
+        (the two parts run concurrently on the GPU)."""
+        dec = pre = None
+        if self.n_dec:
+            dec = {"q": self.dec_q, "ctx_q_start": self.dec_q_start, "adapter_ids": self.dec_adapter,
+                   "block_tables": self.dec_bt, "ctx_lens": self.dec_lens, "max_ctx_len": self.dec_max_len,
+                   "max_q_per_ctx": self.dec_max_q, "out": self.dec_out, "workspace": self.dec_ws}
+        if self.n_pre:
+            pre = {"q": self.pre_q, "q_start": self.pre_q_start, "max_q_len": self.pre_max_q,
+                   "seq_lens": self.pre_lens, "max_seq_len": self.pre_max_len, "adapter_ids": self.pre_adapter,
+                   "block_tables": self.pre_bt, "out": self.pre_out}
+        return lrkv.attn_mixed(self.cfg, self.base_pool, self.lr_pool, self.attn_B_K, self.B_V, decode=dec,
+                               prefill=pre, scale=self.scale, status=self.status, stream=stream)
+
     def step(self) -> Dict[str, Optional[torch.Tensor]]:
         """One pass of the hot path: append the new tokens, then attend."""
         self.step_append()
+        if self.n_dec and self.n_pre:
+            d, p = self.mixed()
+            return {"decode": d, "prefill": p}
         return {"decode": self.decode(), "prefill": self.prefill()}
 
     def device_status(self) -> int:

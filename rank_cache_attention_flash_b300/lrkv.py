@@ -28,7 +28,8 @@ CODEC_NONE, CODEC_POLYKV = 0, 1
 
 EXPORTS = ("lrkv_append", "lrkv_append_rebase", "lrkv_attn_decode", "lrkv_decode_workspace_bytes", "lrkv_attn_prefill",
            "lrkv_prefill_workspace_bytes", "lrkv_status_string", "lrkv_version",
-           "lrkv_attn_decode_noalloc", "lrkv_testing_set_decode_stall", "lrkv_base_pool_block_bytes")
+           "lrkv_attn_decode_noalloc", "lrkv_testing_set_decode_stall", "lrkv_base_pool_block_bytes",
+           "lrkv_attn_mixed")
 NOALLOC_SCRATCH_BYTES = 16 << 20  # LRKV_NOALLOC_SCRATCH_BYTES in lrkv.h
 
 
@@ -62,6 +63,24 @@ class Config(ctypes.Structure):
     @property
     def n_cols(self) -> int:
         return 2 * self.n_kv_heads * self.head_dim + 2 * self.lr_width
+
+
+class DecodeBatch(ctypes.Structure):
+    """lrkv_decode_batch: the decode part of a mixed call."""
+    _fields_ = [("q", ctypes.c_void_p), ("num_queries", ctypes.c_int32), ("ctx_q_start", ctypes.c_void_p),
+                ("num_ctx", ctypes.c_int32), ("adapter_ids", ctypes.c_void_p),
+                ("block_tables", ctypes.c_void_p), ("max_blocks", ctypes.c_int32),
+                ("ctx_lens", ctypes.c_void_p), ("max_ctx_len", ctypes.c_int32),
+                ("max_q_per_ctx", ctypes.c_int32), ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class PrefillBatch(ctypes.Structure):
+    """lrkv_prefill_batch: the prefill part of a mixed call."""
+    _fields_ = [("q", ctypes.c_void_p), ("q_start", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
+                ("total_q", ctypes.c_int32), ("max_q_len", ctypes.c_int32), ("seq_lens", ctypes.c_void_p),
+                ("max_seq_len", ctypes.c_int32), ("adapter_ids", ctypes.c_void_p),
+                ("block_tables", ctypes.c_void_p), ("max_blocks", ctypes.c_int32), ("out", ctypes.c_void_p)]
 
 
 def make_config(hidden: int, n_q_heads: int, n_kv_heads: int, head_dim: int, rank: int,
@@ -105,6 +124,9 @@ def load() -> ctypes.CDLL:
     lib.lrkv_attn_decode_noalloc.argtypes = [cfgp, _P, _I32, _P, _I32, _P, _P, _I32, _P, _I32, _I32,
                                              _P, _P, _I64, _P, _P, _I32, _F, _P, _P, _P]
     lib.lrkv_attn_decode_noalloc.restype = ctypes.c_int
+    lib.lrkv_attn_mixed.argtypes = [cfgp, ctypes.POINTER(DecodeBatch), ctypes.POINTER(PrefillBatch), _P, _P,
+                                    _I64, _P, _P, _I32, _F, _P, _P]
+    lib.lrkv_attn_mixed.restype = ctypes.c_int
     lib.lrkv_status_string.argtypes = [ctypes.c_int]
     lib.lrkv_status_string.restype = ctypes.c_char_p
     lib.lrkv_version.argtypes = []
@@ -343,6 +365,67 @@ def attn_prefill(cfg: Config, q: torch.Tensor, q_start: torch.Tensor, max_q_len:
         _ptr(status), _stream(stream))
     _raise(code, "lrkv_attn_prefill")
     return out
+
+
+def attn_mixed(cfg: Config, base_pool: torch.Tensor, lr_pool: torch.Tensor, B_K: Optional[torch.Tensor],
+               B_V: Optional[torch.Tensor], decode: Optional[dict] = None, prefill: Optional[dict] = None,
+               scale: Optional[float] = None, status: Optional[torch.Tensor] = None, stream=None):
+    """lrkv_attn_mixed: a decode batch and a prefill batch in one call (the two
+    run concurrently on the GPU). ``decode`` holds the tensors and sizes of
+    attn_decode (q, ctx_q_start, adapter_ids, block_tables, ctx_lens,
+    max_ctx_len, max_q_per_ctx, out, workspace), ``prefill`` those of
+    attn_prefill (q, q_start, max_q_len, seq_lens, max_seq_len, adapter_ids,
+    block_tables, out); outputs and the decode workspace are allocated here
+    when missing. Returns (decode out or None, prefill out or None)."""
+    lib = load()
+    dev = base_pool.device
+    _check(B_K, "B_K", cfg.torch_dtype, dev)
+    _check(B_V, "B_V", cfg.torch_dtype, dev)
+    _check(status, "status", torch.int32, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+    dref = pref = None
+    d_out = p_out = None
+    keep = []
+    if decode is not None:
+        d = decode
+        _check(d["q"], "decode q", cfg.torch_dtype, dev)
+        for n in ("ctx_q_start", "adapter_ids", "block_tables", "ctx_lens"):
+            _check(d[n], "decode " + n, torch.int32, dev)
+        nq, num_ctx = d["q"].shape[0], d["ctx_lens"].numel()
+        d_out = d.get("out")
+        if d_out is None:
+            d_out = torch.empty_like(d["q"])
+        _check(d_out, "decode out", cfg.torch_dtype, dev)
+        ws = d.get("workspace")
+        if ws is None:
+            need = decode_workspace_bytes(cfg, nq, num_ctx, d["max_ctx_len"], d["max_q_per_ctx"])
+            if need > 0:
+                ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        keep.append(ws)
+        dref = ctypes.byref(DecodeBatch(
+            _ptr(d["q"]), nq, _ptr(d["ctx_q_start"]), num_ctx, _ptr(d["adapter_ids"]), _ptr(d["block_tables"]),
+            d["block_tables"].shape[1], _ptr(d["ctx_lens"]), d["max_ctx_len"], d["max_q_per_ctx"], _ptr(d_out),
+            _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size()))
+    if prefill is not None:
+        f = prefill
+        _check(f["q"], "prefill q", cfg.torch_dtype, dev)
+        for n in ("q_start", "seq_lens", "adapter_ids", "block_tables"):
+            _check(f[n], "prefill " + n, torch.int32, dev)
+        p_out = f.get("out")
+        if p_out is None:
+            p_out = torch.empty_like(f["q"])
+        _check(p_out, "prefill out", cfg.torch_dtype, dev)
+        pref = ctypes.byref(PrefillBatch(
+            _ptr(f["q"]), _ptr(f["q_start"]), f["seq_lens"].numel(), f["q"].shape[0], f["max_q_len"],
+            _ptr(f["seq_lens"]), f["max_seq_len"], _ptr(f["adapter_ids"]), _ptr(f["block_tables"]),
+            f["block_tables"].shape[1], _ptr(p_out)))
+    n_adapters = 0 if B_K is None and B_V is None else (B_K if B_K is not None else B_V).shape[0]
+    code = lib.lrkv_attn_mixed(ctypes.byref(cfg), dref, pref, _ptr(base_pool), _ptr(lr_pool), base_pool.shape[0],
+                               _ptr(B_K), _ptr(B_V), n_adapters, float(scale), _ptr(status), _stream(stream))
+    del keep
+    _raise(code, "lrkv_attn_mixed")
+    return d_out, p_out
 
 
 def attn_decode_noalloc(cfg: Config, q: torch.Tensor, ctx_q_start: torch.Tensor,

@@ -32,7 +32,7 @@ def declared_functions(headers=None):
 def test_header_declares_the_entry_points():
     names = declared_functions([HEADER])
     for n in ("lrkv_append", "lrkv_append_rebase", "lrkv_attn_decode", "lrkv_attn_prefill",
-              "lrkv_decode_workspace_bytes", "lrkv_attn_decode_noalloc"):
+              "lrkv_decode_workspace_bytes", "lrkv_attn_decode_noalloc", "lrkv_attn_mixed"):
         assert n in names
     assert "lrkv_testing_set_decode_stall" in declared_functions([os.path.join(INCLUDE, "lrkv_testing.h")])
 
@@ -108,6 +108,29 @@ def test_null_and_misaligned_pointers_rejected(lib):
     pargs2[6] = P
     pargs2[7] = 4
     assert lib.lrkv_attn_prefill(*pargs2) == 1
+
+
+def test_mixed_call_checks_both_parts_before_launch(lib):
+    """lrkv_attn_mixed: a bad field in either part is refused before anything
+    runs (these calls reach no CUDA call), and two empty parts are a no-op."""
+    cfg = _cfg()
+    P = 1 << 20  # a fake, 16-byte aligned address: never dereferenced on these paths
+    dec = lrkv.DecodeBatch(P, 2, P, 1, P, P, 4, P, 64, 2, P, P, 1 << 20)
+    pre = lrkv.PrefillBatch(P, P, 1, 8, 8, P, 64, P, P, 4, P)
+    call = lambda d, p: lib.lrkv_attn_mixed(ctypes.byref(cfg), d, p, P, P, 8, P, P, 2, 0.125, None, None)
+    empty_d = lrkv.DecodeBatch(None, 0, None, 0, None, None, 0, None, 0, 0, None, None, 0)
+    empty_p = lrkv.PrefillBatch(None, None, 0, 0, 0, None, 0, None, None, 0, None)
+    assert call(None, None) == 0
+    assert call(ctypes.byref(empty_d), ctypes.byref(empty_p)) == 0
+    bad_d = lrkv.DecodeBatch(None, 2, P, 1, P, P, 4, P, 64, 2, P, P, 1 << 20)  # null q
+    assert call(ctypes.byref(bad_d), ctypes.byref(pre)) == 1
+    bad_p = lrkv.PrefillBatch(P, P, 1, 8, 8, None, 64, P, P, 4, P)  # null seq_lens
+    assert call(None, ctypes.byref(bad_p)) == 1
+    bad_p2 = lrkv.PrefillBatch(P, P, 1, 8, 8, P, 4, P, P, 4, P)  # max_seq_len < max_q_len
+    assert call(ctypes.byref(empty_d), ctypes.byref(bad_p2)) == 1
+    bad_d2 = lrkv.DecodeBatch(P, 2, P, 1, P, P, 4, P, 4 * 16 + 1, 2, P, P, 1 << 20)  # past the block table
+    assert call(ctypes.byref(bad_d2), None) == 1
+    assert lib.lrkv_attn_mixed(None, None, None, P, P, 8, P, P, 2, 0.125, None, None) == 1
 
 
 def test_positions_limit_rejected(lib):
