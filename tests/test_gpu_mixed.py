@@ -100,3 +100,18 @@ def test_mixed_captured_in_a_graph(cuda_lib):
     assert g.device_status() == 0
     assert torch.equal(g.dec_out, want_d)
     assert torch.equal(g.pre_out, want_p)
+
+
+def test_decode_does_not_depend_on_earlier_kernels(cuda_lib):
+    """Tensor memory is not cleared between kernels: a decode run after a
+    prefill (which leaves its own accumulators there) must give the same bits
+    as one run before it. G-mode items with fewer rows than the tile's read W
+    columns past their last row; those rows are masked before the softmax."""
+    g = _case()
+    before = g.decode().clone()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.prefill()
+        after = g.decode().clone()
+        torch.cuda.synchronize()
+        assert torch.equal(after, before)
