@@ -554,57 +554,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(1, kThreads - 32);
 
     if (warp == 1) {
-      // ================================== W issuer, O_lr^T issuer
-      // Iteration j issues W_j = U_j G^T, then O_lr^T += L_V^T P^T of tile j - 1
-      // (two issuing warps share the P V work of a tile).
+      // ================================================ W issuer
+      // Iteration j issues W_j = U_j G^T once U_j is written and W_{j-1} read.
       const uint32_t idw = tc::idesc_f16(128, nw, false, false, false);
-      const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
       const uint64_t gdesc = tc::sdesc(sbase + L::off_g, 16, 1024, 2);
       bool ok = true;
       int issued = 0;
-      for (int j = 0; j <= ntiles; ++j) {
+      for (int j = 0; j < ntiles; ++j) {
         if (p.test_stall && j == 0) {
           // test only: a wait that runs out, then the abort path of every role
           ok = warp_all(wait_limited(bar(B_TEST), 0, p.status, kTestWaitCycles));
           if (!ok) break;
         }
-        if (use_w && j < ntiles) {
-          ok = warp_all(wait_ab(bar(B_UF), j & 1, p.status, abort_flag));
-          if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
-          if (!ok) break;
-          tc::fence_after();
-          if (tc::elect_one()) {
+        if (!use_w) break;
+        ok = warp_all(wait_ab(bar(B_UF), j & 1, p.status, abort_flag));
+        if (ok && j > 0) ok = warp_all(wait_ab(bar(B_WR), (j - 1) & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after();
+        if (tc::elect_one()) {
 #pragma unroll
-            for (int k = 0; k < KS; ++k)
-              tc::mma_ts(tbase + W_COL, tbase + U_COL + 8 * k,
-                         gdesc + (((k >> 2) * L::GAMMA_ATOM + (k & 3) * 32) >> 4), idw, k > 0 ? 1u : 0u);
-            tc::commit(bar(B_WF));
-          }
-          __syncwarp();
-          ++issued;
+          for (int k = 0; k < KS; ++k)
+            tc::mma_ts(tbase + W_COL, tbase + U_COL + 8 * k,
+                       gdesc + (((k >> 2) * L::GAMMA_ATOM + (k & 3) * 32) >> 4), idw, k > 0 ? 1u : 0u);
+          tc::commit(bar(B_WF));
         }
-        if (p.has_bv && j > 0) {
-          const int jj = j - 1, vi = vidx(jj, ntiles), v = vi % NS, b = jj & 1;
-          ok = warp_all(wait_ab(bar(B_FULL + v), (vi / NS) & 1, p.status, abort_flag));
-          if (ok) ok = warp_all(wait_ab(bar(B_PF + b), (jj >> 1) & 1, p.status, abort_flag));
-          if (!ok) break;
-          tc::fence_after();
-          if (tc::elect_one()) {
-            const uint32_t vst = sbase + L::off_ring + v * L::STAGE;
-            // L_V^T: M = rank (MN-major, swizzled by the row span), K = tokens
-            const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
-            const uint64_t pdesc = tc::sdesc(sbase + L::off_p + b * L::PB, 16, 1024, 2);
-#pragma unroll
-            for (int k = 0; k < kBT / 16; ++k)
-              tc::mma_ss(tbase + OL_COL, lvdesc + ((k * 16 * LSPAN) >> 4),
-                         pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
-                         (jj > 0 || k > 0) ? 1u : 0u);
-            tc::commit(bar(B_PR + b));
-            tc::commit(bar(B_EMPTY + v));
-          }
-          __syncwarp();
-          ++issued;
-        }
+        __syncwarp();
+        ++issued;
       }
       if (!ok) {
         if (lane == 0) *abort_flag = 1;
@@ -648,7 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 3) {
-      // ================================================ O^T issuer
+      // ================================= O^T issuer, O_lr^T issuer
+      // Both products of tile j read P_j: O^T += V_base^T P^T, then
+      // O_lr^T += L_V^T P^T; together they release the V slot and the P buffer.
       const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
       bool ok = true;
       int issued = 0;
@@ -668,12 +645,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_ss(tbase + OT_COL, vdesc + ((k * 16 * 128) >> 4),
                        pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
                        (j > 0 || k > 0) ? 1u : 0u);
+          if (p.has_bv) {
+            // L_V^T: M = rank (MN-major, swizzled by the row span), K = tokens
+            const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
+#pragma unroll
+            for (int k = 0; k < kBT / 16; ++k)
+              tc::mma_ss(tbase + OL_COL, lvdesc + ((k * 16 * LSPAN) >> 4),
+                         pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
+                         (j > 0 || k > 0) ? 1u : 0u);
+          }
+          // two arrivals on each (the P buffer's and the V slot's MMA counts)
           tc::commit(bar(B_PR + b));
           tc::commit(bar(B_EMPTY + v));
-          if (!p.has_bv) {  // no O_lr^T issuer: both arrivals from here
-            tc::commit(bar(B_PR + b));
-            tc::commit(bar(B_EMPTY + v));
-          }
+          tc::commit(bar(B_PR + b));
+          tc::commit(bar(B_EMPTY + v));
         }
         __syncwarp();
         ++issued;
