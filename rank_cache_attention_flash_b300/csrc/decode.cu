@@ -1307,50 +1307,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
 
     if (warp == 1) {
-      // ======================================== Y issuer, O_lr^T issuer
+      // ======================================================== Y issuer
       const uint32_t idy = tc::idesc_f16(128, D, true, false, false);
-      const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
       const uint64_t bdesc = tc::sdesc(sbase + L::off_bk, 16, 8 * LSPAN, L::SW_LR);
       bool ok = true;
       int issued = 0;
-      for (int j = 0; j <= ntiles; ++j) {
-        if (rebuild && j < ntiles) {
-          const int b = j & 1, i = j >> 1, ki = kidx(j, ntiles), s = ki % NS;
-          ok = warp_all(wait_ab(bar(FULL + s), (ki / NS) & 1, p.status, abort_flag));
-          if (ok && i > 0) ok = warp_all(wait_ab(bar(YR + b), (i - 1) & 1, p.status, abort_flag));
-          if (!ok) break;
-          tc::fence_after();
-          if (tc::elect_one()) {
-            const uint64_t ldesc = tc::sdesc(sbase + L::off_ring + s * L::STAGE, 16, 8 * LSPAN, L::SW_LR);
+      for (int j = 0; rebuild && j < ntiles; ++j) {
+        const int b = j & 1, i = j >> 1, ki = kidx(j, ntiles), s = ki % NS;
+        ok = warp_all(wait_ab(bar(FULL + s), (ki / NS) & 1, p.status, abort_flag));
+        if (ok && i > 0) ok = warp_all(wait_ab(bar(YR + b), (i - 1) & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after();
+        if (tc::elect_one()) {
+          const uint64_t ldesc = tc::sdesc(sbase + L::off_ring + s * L::STAGE, 16, 8 * LSPAN, L::SW_LR);
 #pragma unroll
-            for (int k = 0; k < L::RP / 16; ++k)
-              tc::mma_ss(tbase + RY_COL + b * D, ldesc + 2 * k, bdesc + 2 * k, idy, k > 0 ? 1u : 0u);
-            tc::commit(bar(YF + b));
-          }
-          __syncwarp();
-          ++issued;
+          for (int k = 0; k < L::RP / 16; ++k)
+            tc::mma_ss(tbase + RY_COL + b * D, ldesc + 2 * k, bdesc + 2 * k, idy, k > 0 ? 1u : 0u);
+          tc::commit(bar(YF + b));
         }
-        if (p.has_bv && j > 0) {
-          const int jj = j - 1, b = jj & 1, i = jj >> 1, vi = vidx(jj, ntiles), v = vi % NS;
-          ok = warp_all(wait_ab(bar(FULL + v), (vi / NS) & 1, p.status, abort_flag));
-          if (ok) ok = warp_all(wait_ab(bar(PF + b), i & 1, p.status, abort_flag));
-          if (!ok) break;
-          tc::fence_after();
-          if (tc::elect_one()) {
-            const uint32_t vst = sbase + L::off_ring + v * L::STAGE;
-            const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
-            const uint64_t pdesc = tc::sdesc(sbase + L::off_p + b * L::PB, 16, 1024, 2);
-#pragma unroll
-            for (int k = 0; k < kBT / 16; ++k)
-              tc::mma_ss(tbase + ROL_COL + 16 * b, lvdesc + ((k * 16 * LSPAN) >> 4),
-                         pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
-                         (i > 0 || k > 0) ? 1u : 0u);
-            tc::commit(bar(PR + b));
-            tc::commit(bar(EMPTY + v));
-          }
-          __syncwarp();
-          ++issued;
-        }
+        __syncwarp();
+        ++issued;
       }
       if (!ok) {
         if (lane == 0) *abort_flag = 1;
@@ -1395,7 +1371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp == 3) {
-      // ================================================ O^T issuer
+      // ================================= O^T issuer, O_lr^T issuer
+      // Both products of a tile read its P: O^T += V^T P^T, then O_lr^T += L_V^T P^T.
       const uint32_t ido = tc::idesc_f16(128, kMaxRows, true, true, false);
       bool ok = true;
       int issued = 0;
@@ -1415,12 +1392,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_ss(tbase + ROT_COL + 16 * b, vdesc + ((k * 16 * 128) >> 4),
                        pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
                        (i > 0 || k > 0) ? 1u : 0u);
+          if (p.has_bv) {
+            const uint64_t lvdesc = tc::sdesc(vst, L::LR_TILE, 8 * LSPAN, L::SW_LR);
+#pragma unroll
+            for (int k = 0; k < kBT / 16; ++k)
+              tc::mma_ss(tbase + ROL_COL + 16 * b, lvdesc + ((k * 16 * LSPAN) >> 4),
+                         pdesc + (((k >> 2) * (kMaxRows * 128) + (k & 3) * 32) >> 4), ido,
+                         (i > 0 || k > 0) ? 1u : 0u);
+          }
+          // two arrivals on each (the P buffer's and the V slot's MMA counts)
           tc::commit(bar(PR + b));
           tc::commit(bar(EMPTY + v));
-          if (!p.has_bv) {
-            tc::commit(bar(PR + b));
-            tc::commit(bar(EMPTY + v));
-          }
+          tc::commit(bar(PR + b));
+          tc::commit(bar(EMPTY + v));
         }
         __syncwarp();
         ++issued;
