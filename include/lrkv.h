@@ -295,8 +295,9 @@ size_t lrkv_prefill_workspace_bytes(const lrkv_config* cfg, int32_t num_seqs, in
  * `stream` afterwards sees both outputs. The decode's CTAs then take the SMs
  * the prefill grid leaves idle in its last wave. The second stream and the
  * two events are created on the first mixed call of each host thread on each
- * device and kept until the process exits. The call may be captured into a
- * CUDA graph (the fork and the join become graph edges).
+ * device and kept until the process exits; make that first call outside any
+ * stream capture. Later calls may be captured into a CUDA graph (the fork and
+ * the join become graph edges).
  *
  *   dec, pre   either may be NULL or describe an empty batch (num_queries or
  *              num_ctx 0; num_seqs or total_q 0); with one part empty the

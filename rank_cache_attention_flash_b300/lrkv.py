@@ -386,7 +386,7 @@ def attn_mixed(cfg: Config, base_pool: torch.Tensor, lr_pool: torch.Tensor, B_K:
         scale = 1.0 / math.sqrt(cfg.head_dim)
     dref = pref = None
     d_out = p_out = None
-    keep = []
+    ws = None
     if decode is not None:
         d = decode
         _check(d["q"], "decode q", cfg.torch_dtype, dev)
@@ -402,7 +402,6 @@ def attn_mixed(cfg: Config, base_pool: torch.Tensor, lr_pool: torch.Tensor, B_K:
             need = decode_workspace_bytes(cfg, nq, num_ctx, d["max_ctx_len"], d["max_q_per_ctx"])
             if need > 0:
                 ws = torch.empty(need, dtype=torch.uint8, device=dev)
-        keep.append(ws)
         dref = ctypes.byref(DecodeBatch(
             _ptr(d["q"]), nq, _ptr(d["ctx_q_start"]), num_ctx, _ptr(d["adapter_ids"]), _ptr(d["block_tables"]),
             d["block_tables"].shape[1], _ptr(d["ctx_lens"]), d["max_ctx_len"], d["max_q_per_ctx"], _ptr(d_out),
@@ -423,7 +422,6 @@ def attn_mixed(cfg: Config, base_pool: torch.Tensor, lr_pool: torch.Tensor, B_K:
     n_adapters = 0 if B_K is None and B_V is None else (B_K if B_K is not None else B_V).shape[0]
     code = lib.lrkv_attn_mixed(ctypes.byref(cfg), dref, pref, _ptr(base_pool), _ptr(lr_pool), base_pool.shape[0],
                                _ptr(B_K), _ptr(B_V), n_adapters, float(scale), _ptr(status), _stream(stream))
-    del keep
     _raise(code, "lrkv_attn_mixed")
     return d_out, p_out
 
