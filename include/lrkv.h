@@ -295,8 +295,8 @@ size_t lrkv_prefill_workspace_bytes(const lrkv_config* cfg, int32_t num_seqs, in
  * `stream` afterwards sees both outputs. The decode's CTAs then take the SMs
  * the prefill grid leaves idle in its last wave. The second stream and the
  * two events are created on the first mixed call of each host thread on each
- * device and kept until the process exits; make that first call outside any
- * stream capture. Later calls may be captured into a CUDA graph (the fork and
+ * device and kept until the process exits (also when that thread ends before
+ * it); make that first call outside any stream capture. Later calls may be captured into a CUDA graph (the fork and
  * the join become graph edges).
  *
  *   dec, pre   either may be NULL or describe an empty batch (num_queries or
