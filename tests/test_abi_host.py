@@ -133,6 +133,39 @@ def test_mixed_call_checks_both_parts_before_launch(lib):
     assert lib.lrkv_attn_mixed(None, None, None, P, P, 8, P, P, 2, 0.125, None, None) == 1
 
 
+def _header_struct_fields(name):
+    """(field, C type) pairs of a struct typedef in lrkv.h, in declaration order."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    m = re.search(r"typedef struct(?:\s+\w+)?\s*\{([^}]*)\}\s*" + name + r"\s*;", src)
+    assert m, name
+    out = []
+    for decl in m.group(1).split(";"):
+        decl = " ".join(decl.split())
+        if decl:
+            ctype, field = decl.rsplit(" ", 1)
+            out.append((field.lstrip("*"), ctype + ("*" if field.startswith("*") else "")))
+    return out
+
+
+def _ctypes_kind(ctype):
+    if ctype.endswith("*"):
+        return ctypes.c_void_p
+    return {"int32_t": ctypes.c_int32, "float": ctypes.c_float, "size_t": ctypes.c_size_t}[ctype]
+
+
+@pytest.mark.parametrize("cname,pyclass", [("lrkv_config", lrkv.Config), ("lrkv_decode_batch", lrkv.DecodeBatch),
+                                           ("lrkv_prefill_batch", lrkv.PrefillBatch)])
+def test_binding_structs_match_the_header(cname, pyclass):
+    """The ctypes structures the binding passes by pointer have the header's
+    fields, in its order, with types of the same size and kind."""
+    fields = _header_struct_fields(cname)
+    assert [f for f, _ in fields] == [f for f, _ in pyclass._fields_]
+    for (f, ctype), (_, pytype) in zip(fields, pyclass._fields_):
+        want = _ctypes_kind(ctype)
+        assert ctypes.sizeof(pytype) == ctypes.sizeof(want), (cname, f)
+        assert (pytype in (ctypes.c_float, ctypes.c_double)) == (want is ctypes.c_float), (cname, f)
+
+
 def test_positions_limit_rejected(lib):
     cfg = _cfg()
     P = 1 << 20
