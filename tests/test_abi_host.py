@@ -166,6 +166,51 @@ def test_binding_structs_match_the_header(cname, pyclass):
         assert (pytype in (ctypes.c_float, ctypes.c_double)) == (want is ctypes.c_float), (cname, f)
 
 
+def _header_prototypes():
+    """name -> list of parameter C types of every function declared in lrkv.h."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(lrkv_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+        params = " ".join(m.group(2).split())
+        if params in ("", "void"):
+            protos[m.group(1)] = []
+            continue
+        types = []
+        for p in params.split(","):
+            p = p.strip()
+            ptr = "*" in p
+            base = p.replace("*", " ").split()
+            base = [w for w in base if w != "const"]
+            types.append("ptr" if ptr or base[0] == "lrkv_stream_t" else base[0])
+        protos[m.group(1)] = types
+    return protos
+
+
+def test_binding_argtypes_match_the_header(lib):
+    """Every function the binding types has the header's parameter count, and
+    each parameter a ctypes type of the same size and kind (pointer, 32-bit
+    int, 64-bit int, size_t, float)."""
+    kinds = {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+             "float": ctypes.c_float, "lrkv_status": ctypes.c_int, "ptr": ctypes.c_void_p}
+    protos = _header_prototypes()
+    checked = 0
+    for name, params in protos.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert len(fn.argtypes) == len(params), name
+        for i, (have, want) in enumerate(zip(fn.argtypes, params)):
+            w = kinds[want]
+            if w is ctypes.c_void_p:
+                assert ctypes.sizeof(have) == ctypes.sizeof(ctypes.c_void_p) and have not in (
+                    ctypes.c_int64, ctypes.c_size_t, ctypes.c_double), (name, i)
+            else:
+                assert ctypes.sizeof(have) == ctypes.sizeof(w), (name, i, have, want)
+                assert (have in (ctypes.c_float, ctypes.c_double)) == (w is ctypes.c_float), (name, i)
+        checked += 1
+    assert checked >= 10
+
+
 def test_positions_limit_rejected(lib):
     cfg = _cfg()
     P = 1 << 20
